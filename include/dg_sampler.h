@@ -1,0 +1,209 @@
+/*
+ * dg_sampler.h -- C ABI of the GB300 (sm_103a) denoise-step library for the
+ * uniform-state discrete-diffusion sampler of DiffusionGemma.
+ *
+ * One denoising step ("tick") runs, for every active canvas:
+ *   1. the final RMSNorm of the residual stream, w * x * sqrt(D) / (||x||_2 + eps),
+ *      cast to bf16                 ("The Annotated DiffusionGemma", "RMSNorm")
+ *   2. the tied LM head z = h W_vocab^T, fp32 accumulate, never stored
+ *                                   (same page, "Complete DiffusionGemma model")
+ *   3. softmax(z / T) with the per-position entropy H (nats), log Z, the argmax
+ *      and one sampled token        (same page, "Apply temperature", "Compute
+ *                                    entropy")
+ *   4. the entropy-bounded commit: the uncommitted positions sorted by entropy,
+ *      the prefix whose exclusive entropy sum stays <= entropy_bound freezes to
+ *      its sampled tokens          (same page, "Keep a low-entropy prefix and
+ *                                    renoise the rest"; ComfyUI-DiffusionGemma,
+ *                                    "What it is")
+ *   5. the early-stop test (mean H < confidence and an unchanged argmax canvas)
+ *      and the uniform re-noise of every position still uncommitted
+ *                                   (same page, "Check for early stopping")
+ * with the temperature cooling T_s = t_max + (s/N)(t_min - t_max), s = 0..N-1
+ * ("Apply temperature"; DiffusionGemma Denoise node, "Inputs": t_min / t_max).
+ *
+ * Conventions for every entry point:
+ *   - "dev" pointers are CUDA device pointers, "host" pointers host memory.
+ *   - The library never allocates device memory.  The caller allocates one
+ *     workspace of dg_workspace_size() bytes and keeps it alive until
+ *     dg_destroy().  Device buffers passed in are borrowed, not owned.
+ *   - Work is enqueued on the stream given to dg_sampler_create().  Calls
+ *     marked "asynchronous" return before the GPU work ends; calls marked
+ *     "synchronizing" wait for the stream.
+ *   - Errors are returned as dg_status; no C++ exception crosses the ABI.  A
+ *     failed call leaves a message readable by dg_last_error().  A device-side
+ *     fault condition found by a kernel (non-finite logits, a bounded wait that
+ *     ran out) is latched on the device and reported by the next synchronizing
+ *     call.
+ *   - A sampler is not thread-safe; distinct samplers are independent.
+ */
+#ifndef DG_SAMPLER_H
+#define DG_SAMPLER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t.  NULL selects the legacy default stream. */
+typedef struct CUstream_st* dg_stream_t;
+
+typedef enum dg_status {
+  DG_OK = 0,
+  DG_ERR_ARG = 1,         /* an argument or config field is out of range          */
+  DG_ERR_ALIGN = 2,       /* a pointer lacks the alignment the kernels need        */
+  DG_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than dg_workspace_size()    */
+  DG_ERR_CUDA = 4,        /* a CUDA runtime call failed (message in dg_last_error) */
+  DG_ERR_STATE = 5,       /* call not valid in the sampler's state (e.g. all done) */
+  DG_ERR_NONFINITE = 6,   /* a kernel met a non-finite logit statistic             */
+  DG_ERR_UNSUPPORTED = 7, /* a valid request this build does not implement         */
+  DG_ERR_TIMEOUT = 8      /* a kernel's bounded wait ran out (pipeline stalled)    */
+} dg_status;
+
+/* Commit semantics.  DG_FREEZE: a committed position keeps its token for the
+ * rest of the block and only uncommitted positions enter each step's sort
+ * (ComfyUI-DiffusionGemma, "What it is": confident positions freeze). */
+typedef enum dg_mode { DG_FREEZE = 0 } dg_mode;
+
+/*
+ * Sampler configuration.  Field names follow the pages' knobs (DiffusionGemma
+ * Denoise node, "Inputs (11)"; TensorSharp DiffusionGemma doc, "3. Sampler
+ * contract"); defaults there: num_inference_steps 48, t_min 0.4, t_max 0.8,
+ * entropy_bound 0.1 nats, confidence 0.005, canvas length 256, stability 1.
+ */
+typedef struct dg_config {
+  int32_t vocab;               /* V >= 2 (the pages' model: 2^18)                                */
+  int32_t hidden;              /* d, a multiple of 8 (16-byte rows for TMA), <= 16384            */
+  int32_t canvas_len;          /* L positions per canvas, 1..1024 (pages: 256)                  */
+  int32_t n_canvases;          /* B >= 1 independent canvases                                    */
+  int32_t gen_blocks;          /* blocks per canvas, denoised one after another, >= 1           */
+  int32_t num_inference_steps; /* N, 1..1024: steps per block                                   */
+  float t_min;                 /* cold temperature endpoint, > 0                                 */
+  float t_max;                 /* hot temperature endpoint (step 0), > 0                         */
+  float entropy_bound;         /* per-step acceptance budget in nats, >= 0                       */
+  float confidence;            /* early stop when mean H (nats) falls below this, >= 0           */
+  int32_t stability;           /* steps the argmax canvas must stay unchanged; must be 1         */
+  float rms_eps;               /* RMSNorm epsilon, added to ||x||_2, >= 0                        */
+  int32_t mode;                /* dg_mode; DG_FREEZE                                             */
+  int32_t max_active;          /* most canvases active in one tick, 1..B (0 = B); sizes buffers  */
+  const uint64_t* seeds;       /* host [B]: per-canvas Philox key; NULL = seed c for canvas c    */
+  const int32_t* admit_tick;   /* host [B]: tick at which canvas c joins, >= 0; NULL = all at 0  */
+} dg_config;
+
+/* Per-canvas state, the layout of the device array returned by dg_slots().
+ * state: 0 waiting for admission, 1 active, 2 done (all blocks finished). */
+typedef struct dg_slot {
+  uint64_t seed;
+  int32_t admit_tick;
+  int32_t state;
+  int32_t block;            /* current block (gen_blocks - 1 after the last one)      */
+  int32_t step;             /* step of the current block the next tick runs           */
+  int32_t n_committed;      /* committed positions of the current block               */
+  int32_t steps_used;       /* steps run over all finished blocks                     */
+  int32_t converged_blocks; /* blocks ended by the early-stop test                    */
+  float temperature;        /* T the next tick applies to this canvas                 */
+  float mean_entropy;       /* mean H (nats) over the canvas at its last tick         */
+  int32_t reserved;
+} dg_slot;
+
+typedef struct dg_sampler dg_sampler;
+
+/* Bytes of device workspace a sampler with this config needs; 0 if the
+ * config is invalid (dg_sampler_create then reports why). */
+size_t dg_workspace_size(const dg_config* cfg);
+
+/*
+ * Create a sampler.  Synchronizing.
+ *   w_vocab   dev, bf16 [V, d] row-major, 16-byte aligned: the tied embedding /
+ *             LM-head matrix.  Borrowed; must stay valid and unchanged.
+ *   norm_w    dev, fp32 [d]: RMSNorm weight, or NULL for all ones.  Borrowed.
+ *   workspace dev, >= dg_workspace_size(cfg) bytes, 256-byte aligned.  Borrowed.
+ *   stream    stream all later work of this sampler is enqueued on.
+ * Canvases whose admit_tick is 0 receive their uniform initial canvas.
+ */
+dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const float* norm_w, void* workspace,
+                            size_t ws_bytes, dg_stream_t stream, dg_sampler** out);
+
+/*
+ * Run one tick (steps 1-5 above) for every active canvas.  Asynchronous: no
+ * host synchronization inside, so a tick can be captured in a CUDA graph.
+ *   resid  dev, fp32 [B, L, d]: the residual stream entering the final norm;
+ *          rows of canvases not active this tick are not read.
+ * Returns DG_ERR_STATE when the host can tell every canvas has finished.
+ */
+dg_status dg_denoise_step(dg_sampler* s, const float* resid);
+
+/*
+ * The same tick from host memory.  Synchronizing.  Copies resid_host
+ * (fp32 [B, L, d]; page-locked memory gives the fastest copy) into the
+ * workspace, runs the tick, and copies back the canvas after the tick
+ * (int32 [B, L], nullable) and this tick's entropies (fp32 [B, L], nullable).
+ */
+dg_status dg_denoise_step_host(dg_sampler* s, const float* resid_host, int32_t* canvas_host, float* entropy_host);
+
+/* Residual supplier for dg_run: the backbone's place in the loop.  Must fill
+ * resid_dev [B, L, d] for the active canvases of this tick from their current
+ * canvas_dev [B, L] and slots_dev [B], enqueueing work on `stream`.  Returns
+ * 0 on success; anything else stops dg_run with DG_ERR_ARG. */
+typedef int (*dg_resid_fn)(void* user, int32_t tick, const int32_t* canvas_dev, const dg_slot* slots_dev,
+                           float* resid_dev, dg_stream_t stream);
+
+/*
+ * Drive ticks until every canvas is done: fn, then dg_denoise_step, repeated.
+ * Synchronizes once every num_inference_steps ticks to test for completion.
+ *   resid_dev   dev, fp32 [B, L, d] scratch the callback writes
+ *   tokens_host host int32 [B, gen_blocks, L] final tokens, or NULL
+ *   slots_host  host dg_slot [B] final per-canvas readout, or NULL
+ */
+dg_status dg_run(dg_sampler* s, dg_resid_fn fn, void* user, float* resid_dev, int32_t* tokens_host,
+                 dg_slot* slots_host);
+
+/* Free the host-side sampler object (the workspace belongs to the caller).
+ * NULL-safe.  Waits for the sampler's stream first. */
+void dg_destroy(dg_sampler* s);
+
+/* Device views into the workspace, valid until dg_destroy.  [B, L] row-major. */
+const int32_t* dg_canvas(const dg_sampler* s);      /* current tokens                                 */
+const uint8_t* dg_committed(const dg_sampler* s);   /* 1 where frozen in the current block            */
+const int16_t* dg_commit_step(const dg_sampler* s); /* step at which each position froze, -1 if not  */
+const float* dg_entropy(const dg_sampler* s);       /* H (nats) from the last tick                    */
+const float* dg_logz(const dg_sampler* s);          /* log Z of softmax(z/T) from the last tick       */
+const int32_t* dg_sample(const dg_sampler* s);      /* sampled token from the last tick               */
+const int32_t* dg_argmax(const dg_sampler* s);      /* argmax token from the last tick                */
+const int32_t* dg_tokens_out(const dg_sampler* s);  /* [B, gen_blocks, L] tokens of finished blocks   */
+const dg_slot* dg_slots(const dg_sampler* s);       /* [B] per-canvas state                           */
+
+/* Copy the per-canvas state to host memory (dg_slot [B]).  Synchronizing;
+ * also reports a latched device fault. */
+dg_status dg_sync_info(dg_sampler* s, dg_slot* slots_host);
+
+/* Whole sampler state in host arrays ([B] and [B, L] row-major, [B, G, L] for
+ * tokens_out), for checkpoint and resume.  prev_argmax is the argmax canvas of
+ * each canvas's previous step (the early-stop test compares against it). */
+typedef struct dg_state {
+  int32_t tick;
+  dg_slot* slots;       /* [B]        */
+  int32_t* tokens;      /* [B, L]     */
+  uint8_t* committed;   /* [B, L]     */
+  int16_t* commit_step; /* [B, L]     */
+  int32_t* prev_argmax; /* [B, L]     */
+  int32_t* tokens_out;  /* [B, G, L]  */
+} dg_state;
+
+/* Copy out the state (synchronizing). */
+dg_status dg_get_state(dg_sampler* s, dg_state* host);
+
+/* Replace the state (synchronizing); the next tick resumes from it.  The
+ * active set is rebuilt from the slots' states; per-canvas seeds, admit ticks
+ * and temperatures are taken from the config and the slots' steps. */
+dg_status dg_set_state(dg_sampler* s, const dg_state* host);
+
+const char* dg_status_string(dg_status st);
+const char* dg_last_error(const dg_sampler* s); /* "" when none; s may be NULL (last create failure) */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_SAMPLER_H */

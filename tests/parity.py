@@ -1,0 +1,209 @@
+"""Parity harness: the CUDA path against the CPU oracle on the same seeded inputs.
+
+Inputs (W_vocab and the per-step residual rows) come from ``synth`` only.  For
+a teacher-forced tick the oracle's state before the tick is loaded into the
+CUDA sampler (dg_set_state), both sides run the tick on the same residual, and
+every output is compared:
+
+  entropy H       |H_gpu - H_oracle| <= 1e-3 nats            (task tolerance)
+  log Z           |dlogZ| <= 1e-3 |logZ|                      (task tolerance)
+  sample, argmax  bit-exact unless the oracle's top-2 gap < 1e-4 (flagged)
+  state after     tokens / committed / commit_step bit-exact except flagged
+                  positions (sample near-tie on an accepted position, or an
+                  entropy within 1e-3 nats of the other side of the accept
+                  boundary) and flagged canvases (a prefix sum within 1e-3 of
+                  the bound, or the early-stop test within 1e-3 of its
+                  threshold)
+
+Nothing the CUDA path produces is fed to the oracle.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+import oracle
+import synth
+from oracle.sampler import ACTIVE, OracleConfig, OracleSampler
+
+TOL_H = 1e-3
+TOL_LOGZ_REL = 1e-3
+
+
+def f32(x: float) -> float:
+    """The fp32 value the C ABI will hold for a config float."""
+    return float(np.float32(x))
+
+
+@dataclasses.dataclass
+class Case:
+    vocab: int
+    hidden: int
+    canvas_len: int
+    n_canvases: int = 1
+    gen_blocks: int = 1
+    steps: int = 48
+    t_min: float = 0.4
+    t_max: float = 0.8
+    bound: float = 0.1
+    conf: float = 0.005
+    sigma: float = 0.5
+    sigma_w: float = 0.02
+    w_seed: int = 0
+    seeds: tuple = None
+    admit: tuple = None
+    max_active: int = 0
+
+    def oracle_cfg(self) -> OracleConfig:
+        return OracleConfig(vocab=self.vocab, hidden=self.hidden, canvas_len=self.canvas_len,
+                            n_canvases=self.n_canvases, gen_blocks=self.gen_blocks, num_inference_steps=self.steps,
+                            t_min=f32(self.t_min), t_max=f32(self.t_max), entropy_bound=f32(self.bound),
+                            confidence=f32(self.conf), rms_eps=f32(1e-6),
+                            seeds=list(self.seeds) if self.seeds else list(range(self.n_canvases)),
+                            admit_tick=list(self.admit) if self.admit else None,
+                            max_active=self.max_active or None)
+
+    def gpu_cfg(self):
+        import uniform_state_discrete_gb300 as dg
+        return dg.make_config(self.vocab, self.hidden, self.canvas_len, n_canvases=self.n_canvases,
+                              gen_blocks=self.gen_blocks, num_inference_steps=self.steps, t_min=self.t_min,
+                              t_max=self.t_max, entropy_bound=self.bound, confidence=self.conf, rms_eps=1e-6,
+                              max_active=self.max_active,
+                              seeds=list(self.seeds) if self.seeds else list(range(self.n_canvases)),
+                              admit_tick=list(self.admit) if self.admit else None)
+
+
+def weights(case: Case) -> np.ndarray:
+    return synth.wvocab(case.w_seed, case.vocab, case.hidden, sigma_w=case.sigma_w)
+
+
+def resid_slots(case: Case, ocfg: OracleConfig, W: np.ndarray, canvases, blocks, steps, tokens) -> np.ndarray:
+    """Residual rows for the given canvases, placed in the [B, L, d] slot layout the ABI reads."""
+    full = np.zeros((case.n_canvases, case.canvas_len, case.hidden), np.float32)
+    rows = oracle.sampler.synth_resid_fn(ocfg, W, case.sigma)(np.asarray(canvases), np.asarray(blocks),
+                                                              np.asarray(steps), np.asarray(tokens))
+    full[np.asarray(canvases)] = rows.reshape(len(canvases), case.canvas_len, case.hidden)
+    return full
+
+
+def oracle_state_to_gpu(o: OracleSampler, case: Case) -> dict:
+    import uniform_state_discrete_gb300 as dg
+    B = case.n_canvases
+    slots = np.zeros(B, dg.SLOT_DTYPE)
+    slots["state"] = o.status
+    slots["block"] = o.block
+    slots["step"] = o.step_no
+    slots["n_committed"] = o.committed.sum(axis=1)
+    slots["steps_used"] = o.steps_used
+    slots["converged_blocks"] = o.converged_blocks
+    return {"tick": o.tick_no, "slots": slots, "tokens": o.x.astype(np.int32),
+            "committed": o.committed.astype(np.uint8), "commit_step": o.commit_step.astype(np.int16),
+            "prev_argmax": o.prev_amax.astype(np.int32), "tokens_out": o.tokens_out.astype(np.int32)}
+
+
+@dataclasses.dataclass
+class Report:
+    ticks: int = 0
+    positions: int = 0
+    max_dH: float = 0.0
+    max_dlogZ_rel: float = 0.0
+    y_mismatch: int = 0
+    y_flagged: int = 0
+    amax_mismatch: int = 0
+    amax_flagged: int = 0
+    state_mismatch_unflagged: int = 0
+    state_flagged_positions: int = 0
+    canvas_flagged: int = 0
+    errors: list = dataclasses.field(default_factory=list)
+
+    def ok(self) -> bool:
+        return not self.errors
+
+
+def teacher_forced(case: Case, ticks: int = 1 << 30, gpu=None, W=None, check_every: int = 1) -> Report:
+    """Run the oracle free; before each checked tick load its state into the CUDA sampler, run both
+    on the same residual and compare.  Returns a Report; ``errors`` lists every violation."""
+    import torch
+    import uniform_state_discrete_gb300 as dg
+    W = weights(case) if W is None else W
+    ocfg = case.oracle_cfg()
+    o = OracleSampler(ocfg, W)
+    dev = torch.device("cuda:0")
+    w_dev = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    s = gpu or dg.Sampler(case.gpu_cfg(), w_dev)
+    rep = Report()
+    L = case.canvas_len
+    t = 0
+    while not o.done() and t < ticks:
+        act = o.active()
+        check = (t % check_every == 0) or o.step_no[act].max(initial=0) >= case.steps - 1
+        resid = resid_slots(case, ocfg, W, act, o.block[act], o.step_no[act], o.x[act]) if act.size else None
+        if check and act.size:
+            s.set_state(oracle_state_to_gpu(o, case))
+            s.step(torch.from_numpy(resid).to(dev))
+        rec = o.tick(lambda canv, blocks, steps, tok: resid[canv].reshape(-1, case.hidden))
+        if check and rec is not None:
+            compare_tick(s, o, rec, case, rep)
+        t += 1
+    return rep
+
+
+def compare_tick(s, o: OracleSampler, rec, case: Case, rep: Report):
+    L = case.canvas_len
+    H = s.entropy().cpu().numpy()
+    lz = s.logz().cpu().numpy()
+    y = s.sample().cpu().numpy()
+    am = s.argmax().cpu().numpy()
+    gst = s.get_state()
+    rep.ticks += 1
+    for i, c in enumerate(rec.canvases):
+        st = rec.stats[i * L:(i + 1) * L]
+        rep.positions += L
+        dH = np.abs(H[c].astype(np.float64) - st["H"])
+        dZ = np.abs(lz[c].astype(np.float64) - st["logZ"]) / np.maximum(np.abs(st["logZ"]), 1e-30)
+        rep.max_dH = max(rep.max_dH, float(dH.max()))
+        rep.max_dlogZ_rel = max(rep.max_dlogZ_rel, float(dZ.max()))
+        if dH.max() > TOL_H:
+            rep.errors.append(f"tick {rec.tick} canvas {c}: |dH| {dH.max():.3g} > {TOL_H}")
+        if dZ.max() > TOL_LOGZ_REL:
+            rep.errors.append(f"tick {rec.tick} canvas {c}: |dlogZ|/|logZ| {dZ.max():.3g} > {TOL_LOGZ_REL}")
+        fy = rec.flag_y[i * L:(i + 1) * L]
+        fa = rec.flag_amax[i * L:(i + 1) * L]
+        ym = y[c] != st["y"]
+        amm = am[c] != st["amax"]
+        rep.y_mismatch += int(ym.sum())
+        rep.y_flagged += int(fy.sum())
+        rep.amax_mismatch += int(amm.sum())
+        rep.amax_flagged += int(fa.sum())
+        if np.any(ym & ~fy):
+            rep.errors.append(f"tick {rec.tick} canvas {c}: sample differs at unflagged positions "
+                              f"{np.nonzero(ym & ~fy)[0][:8].tolist()}")
+        if np.any(amm & ~fa):
+            rep.errors.append(f"tick {rec.tick} canvas {c}: argmax differs at unflagged positions "
+                              f"{np.nonzero(amm & ~fa)[0][:8].tolist()}")
+        if rec.flag_canvas[i]:
+            rep.canvas_flagged += 1
+            continue
+        # state after the tick
+        pos_flag = rec.flag_commit[i] | (rec.accepted[i] & fy)
+        rep.state_flagged_positions += int(pos_flag.sum())
+        for name, gv, ov in (("tokens", gst["tokens"][c], o.x[c]), ("committed", gst["committed"][c],
+                                                                     o.committed[c].astype(np.uint8)),
+                             ("commit_step", gst["commit_step"][c], o.commit_step[c])):
+            bad = (gv != ov) & ~pos_flag
+            if rec.final[i] and not np.any(pos_flag):
+                bad = gv != ov
+            if np.any(bad):
+                rep.state_mismatch_unflagged += int(bad.sum())
+                rep.errors.append(f"tick {rec.tick} canvas {c}: {name} differs at {np.nonzero(bad)[0][:8].tolist()}")
+        if not np.any(pos_flag):
+            gs, os_ = gst["slots"][c], o
+            for fld, ov in (("state", o.status[c]), ("block", o.block[c]), ("step", o.step_no[c]),
+                            ("steps_used", o.steps_used[c]), ("converged_blocks", o.converged_blocks[c])):
+                if int(gs[fld]) != int(ov):
+                    rep.errors.append(f"tick {rec.tick} canvas {c}: slot {fld} {int(gs[fld])} != oracle {int(ov)}")
+            if rec.final[i]:
+                b = rec.block[i]
+                if not np.array_equal(gst["tokens_out"][c, b], o.tokens_out[c, b]):
+                    rep.errors.append(f"tick {rec.tick} canvas {c}: finished block tokens differ")

@@ -1,0 +1,148 @@
+"""CUDA path vs CPU oracle, element by element, through the C ABI (GB300 only)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+from parity import Case, f32, oracle_state_to_gpu, resid_slots, teacher_forced, weights
+
+pytestmark = pytest.mark.gpu
+
+
+def _assert_report(rep, label):
+    print(f"\n[{label}] ticks={rep.ticks} positions={rep.positions} max|dH|={rep.max_dH:.3g} "
+          f"max|dlogZ|/|logZ|={rep.max_dlogZ_rel:.3g} y mismatch={rep.y_mismatch} (flagged {rep.y_flagged}) "
+          f"argmax mismatch={rep.amax_mismatch} (flagged {rep.amax_flagged}) "
+          f"flagged positions={rep.state_flagged_positions} flagged canvases={rep.canvas_flagged}")
+    assert rep.ticks > 0
+    assert rep.ok(), "\n".join(rep.errors[:20])
+
+
+def test_tiny_config_teacher_forced():
+    """1 canvas x 16 positions, V=2048, d=128, 8 steps (W drawn in fp32, rounded once to bf16)."""
+    rep = teacher_forced(Case(vocab=2048, hidden=128, canvas_len=16, steps=8))
+    _assert_report(rep, "tiny")
+    assert rep.max_dH < 1e-4
+
+
+def test_canvas256_v32k_teacher_forced():
+    """1 canvas x 256 positions, V=32768, d=1024, 48 steps, every tick checked."""
+    rep = teacher_forced(Case(vocab=32768, hidden=1024, canvas_len=256, steps=48))
+    _assert_report(rep, "V32k")
+    assert rep.max_dH < 1e-4
+
+
+def test_ragged_shapes_and_staggered_admission():
+    """V not a multiple of the 256-wide tile, d not a multiple of the 64-wide K stage, a canvas
+    length that splits M tiles, three canvases admitted at different ticks, two blocks each."""
+    case = Case(vocab=1000, hidden=200, canvas_len=37, n_canvases=3, gen_blocks=2, steps=5, seeds=(5, 6, 7),
+                admit=(0, 2, 3))
+    _assert_report(teacher_forced(case), "ragged")
+
+
+def test_single_position_canvases_capacity_limited():
+    case = Case(vocab=4096, hidden=64, canvas_len=1, n_canvases=5, steps=4, admit=(0, 0, 1, 1, 1), max_active=2)
+    _assert_report(teacher_forced(case), "L1")
+
+
+def test_low_entropy_multi_commit_and_early_stop():
+    """Peaked distributions: several positions fit the bound per step and the early-stop test fires."""
+    case = Case(vocab=512, hidden=256, canvas_len=32, steps=24, bound=1.0, sigma=0.1, sigma_w=0.1, w_seed=2,
+                seeds=(9,), gen_blocks=3)
+    rep = teacher_forced(case)
+    _assert_report(rep, "low-entropy")
+
+
+def test_hot_schedule_noise_driven_regime():
+    """t 1.5 -> 0.1 with large hidden noise: sampling ties get exercised."""
+    case = Case(vocab=2048, hidden=256, canvas_len=64, steps=12, t_max=1.5, t_min=0.1, sigma=2.0, bound=0.01,
+                n_canvases=2, seeds=(3, 4))
+    _assert_report(teacher_forced(case), "hot")
+
+
+def _gpu_free_run(case, W):
+    import torch
+    import uniform_state_discrete_gb300 as dg
+    dev = torch.device("cuda:0")
+    w_dev = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    s = dg.Sampler(case.gpu_cfg(), w_dev)
+    ocfg = case.oracle_cfg()
+    for _ in range(10000):
+        info = s.sync_info()
+        if np.all(info["state"] == dg.DONE):
+            break
+        act = np.nonzero(info["state"] == dg.ACTIVE)[0]
+        tok = s.canvas().cpu().numpy()
+        resid = resid_slots(case, ocfg, W, act, info["block"][act], info["step"][act], tok[act])
+        s.step(torch.from_numpy(resid).to(dev))
+    return s, s.tokens_out().cpu().numpy(), s.sync_info()
+
+
+def test_free_run_tiny_matches_oracle():
+    case = Case(vocab=2048, hidden=128, canvas_len=16, steps=8, n_canvases=2, seeds=(0, 1))
+    W = weights(case)
+    o = oracle.OracleSampler(case.oracle_cfg(), W)
+    o.run(oracle.sampler.synth_resid_fn(case.oracle_cfg(), W, case.sigma))
+    _, tok, info = _gpu_free_run(case, W)
+    assert np.array_equal(tok, o.tokens_out)
+    assert np.array_equal(info["steps_used"], o.steps_used)
+
+
+def test_batch_and_admission_invariance_bitwise():
+    """A canvas gives the same tokens and entropies alone or inside a staggered batch
+    (TensorSharp doc, "7. Test coverage": batched decode equals per-sequence decode)."""
+    base = dict(vocab=4096, hidden=256, canvas_len=64, steps=6)
+    W = weights(Case(**base))
+    _, alone, _ = _gpu_free_run(Case(**base, seeds=(21,)), W)
+    _, batch, _ = _gpu_free_run(Case(**base, n_canvases=3, seeds=(20, 21, 22), admit=(0, 2, 4)), W)
+    assert np.array_equal(batch[1], alone[0])
+
+
+def test_dg_run_callback_and_host_step():
+    import torch
+    import uniform_state_discrete_gb300 as dg
+    case = Case(vocab=2048, hidden=128, canvas_len=16, steps=8, n_canvases=2, seeds=(0, 1))
+    W = weights(case)
+    ocfg = case.oracle_cfg()
+    o = oracle.OracleSampler(ocfg, W)
+    o.run(oracle.sampler.synth_resid_fn(ocfg, W, case.sigma))
+    dev = torch.device("cuda:0")
+    w_dev = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    s = dg.Sampler(case.gpu_cfg(), w_dev)
+    resid_dev = torch.zeros(case.n_canvases, case.canvas_len, case.hidden, device=dev)
+
+    def cb(tick, canvas_ptr, slots_ptr, resid_ptr, stream_ptr):
+        info = s.sync_info()
+        act = np.nonzero(info["state"] == dg.ACTIVE)[0]
+        if act.size == 0:
+            return 0
+        tok = s.canvas().cpu().numpy()
+        r = resid_slots(case, ocfg, W, act, info["block"][act], info["step"][act], tok[act])
+        assert resid_ptr == resid_dev.data_ptr()
+        resid_dev.copy_(torch.from_numpy(r))
+        torch.cuda.synchronize()
+        return 0
+
+    tokens, slots = s.run(cb, resid_dev)
+    assert np.array_equal(tokens, o.tokens_out)
+    assert np.all(slots["state"] == dg.DONE)
+    # the host-buffer tick gives what the device tick gives
+    s2 = dg.Sampler(case.gpu_cfg(), w_dev)
+    s3 = dg.Sampler(case.gpu_cfg(), w_dev)
+    for _ in range(3):
+        info = s2.sync_info()
+        act = np.nonzero(info["state"] == dg.ACTIVE)[0]
+        r = resid_slots(case, ocfg, W, act, info["block"][act], info["step"][act], s2.canvas().cpu().numpy()[act])
+        canvas_h, ent_h = s2.step_host(r)
+        s3.step(torch.from_numpy(r).to(dev))
+        assert np.array_equal(canvas_h, s3.canvas().cpu().numpy())
+        assert np.array_equal(ent_h, s3.entropy().cpu().numpy())
+
+
+def test_model_scale_two_ticks():
+    """The pages' model shape in the launch configuration the benchmark times: 1 canvas x 256
+    positions, V=2^18, d=2816; every position of the first two ticks against the oracle."""
+    rep = teacher_forced(Case(vocab=262144, hidden=2816, canvas_len=256, steps=48), ticks=2)
+    _assert_report(rep, "model-scale")
+    assert rep.ticks == 2

@@ -1,0 +1,270 @@
+"""GB300 (sm_103a) denoise step of DiffusionGemma's uniform-state discrete-diffusion sampler.
+
+A thin ctypes binding over the C ABI in ``include/dg_sampler.h`` (library
+``_build/libdgsampler.so``): argument marshalling only, every step of the path
+runs in the library's CUDA kernels.  PyTorch supplies device memory and
+streams.  There is no CPU fallback: if the library is missing, importing the
+binding raises.
+
+Names match the C ABI (``dg_sampler_create``, ``dg_denoise_step``, ``dg_run``,
+``dg_destroy`` ...).  ``Sampler`` bundles them for Python callers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libdgsampler.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "dg_sampler.h")
+
+DG_OK, DG_ERR_ARG, DG_ERR_ALIGN, DG_ERR_WORKSPACE, DG_ERR_CUDA, DG_ERR_STATE, DG_ERR_NONFINITE, \
+    DG_ERR_UNSUPPORTED, DG_ERR_TIMEOUT = range(9)
+DG_FREEZE = 0
+WAITING, ACTIVE, DONE = 0, 1, 2
+
+
+class dg_config(ctypes.Structure):
+    _fields_ = [("vocab", ctypes.c_int32), ("hidden", ctypes.c_int32), ("canvas_len", ctypes.c_int32),
+                ("n_canvases", ctypes.c_int32), ("gen_blocks", ctypes.c_int32),
+                ("num_inference_steps", ctypes.c_int32), ("t_min", ctypes.c_float), ("t_max", ctypes.c_float),
+                ("entropy_bound", ctypes.c_float), ("confidence", ctypes.c_float), ("stability", ctypes.c_int32),
+                ("rms_eps", ctypes.c_float), ("mode", ctypes.c_int32), ("max_active", ctypes.c_int32),
+                ("seeds", ctypes.POINTER(ctypes.c_uint64)), ("admit_tick", ctypes.POINTER(ctypes.c_int32))]
+
+
+class dg_slot(ctypes.Structure):
+    _fields_ = [("seed", ctypes.c_uint64), ("admit_tick", ctypes.c_int32), ("state", ctypes.c_int32),
+                ("block", ctypes.c_int32), ("step", ctypes.c_int32), ("n_committed", ctypes.c_int32),
+                ("steps_used", ctypes.c_int32), ("converged_blocks", ctypes.c_int32),
+                ("temperature", ctypes.c_float), ("mean_entropy", ctypes.c_float), ("reserved", ctypes.c_int32)]
+
+
+SLOT_DTYPE = np.dtype([("seed", "u8"), ("admit_tick", "i4"), ("state", "i4"), ("block", "i4"), ("step", "i4"),
+                       ("n_committed", "i4"), ("steps_used", "i4"), ("converged_blocks", "i4"),
+                       ("temperature", "f4"), ("mean_entropy", "f4"), ("reserved", "i4")], align=True)
+assert SLOT_DTYPE.itemsize == ctypes.sizeof(dg_slot) == 48
+
+
+class dg_state(ctypes.Structure):
+    _fields_ = [("tick", ctypes.c_int32), ("slots", ctypes.c_void_p), ("tokens", ctypes.c_void_p),
+                ("committed", ctypes.c_void_p), ("commit_step", ctypes.c_void_p),
+                ("prev_argmax", ctypes.c_void_p), ("tokens_out", ctypes.c_void_p)]
+
+
+DG_RESID_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_void_p, ctypes.c_void_p)
+
+# exported name -> (restype, argtypes)
+_SIGS = {
+    "dg_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(dg_config)]),
+    "dg_sampler_create": (ctypes.c_int, [ctypes.POINTER(dg_config), ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                         ctypes.POINTER(ctypes.c_void_p)]),
+    "dg_denoise_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "dg_denoise_step_host": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "dg_run": (ctypes.c_int, [ctypes.c_void_p, DG_RESID_FN, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                              ctypes.c_void_p]),
+    "dg_destroy": (None, [ctypes.c_void_p]),
+    "dg_canvas": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_committed": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_commit_step": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_entropy": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_logz": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_sample": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_argmax": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_tokens_out": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_slots": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_sync_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "dg_get_state": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(dg_state)]),
+    "dg_set_state": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(dg_state)]),
+    "dg_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "dg_last_error": (ctypes.c_char_p, [ctypes.c_void_p]),
+}
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()'); "
+                          "there is no fallback path")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+class DGError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{lib.dg_status_string(status).decode()}: {msg}")
+        self.status = status
+
+
+def _check(st: int, handle=None):
+    if st != DG_OK:
+        raise DGError(st, (lib.dg_last_error(handle) or b"").decode())
+
+
+def make_config(vocab, hidden, canvas_len, n_canvases=1, gen_blocks=1, num_inference_steps=48, t_min=0.4,
+                t_max=0.8, entropy_bound=0.1, confidence=0.005, stability=1, rms_eps=1e-6, mode=DG_FREEZE,
+                max_active=0, seeds=None, admit_tick=None):
+    """Build a ``dg_config``; the returned object keeps the seed/admit arrays alive."""
+    cfg = dg_config(vocab, hidden, canvas_len, n_canvases, gen_blocks, num_inference_steps, t_min, t_max,
+                    entropy_bound, confidence, stability, rms_eps, mode, max_active)
+    keep = []
+    if seeds is not None:
+        a = (ctypes.c_uint64 * n_canvases)(*[int(s) for s in seeds])
+        cfg.seeds = ctypes.cast(a, ctypes.POINTER(ctypes.c_uint64))
+        keep.append(a)
+    if admit_tick is not None:
+        a = (ctypes.c_int32 * n_canvases)(*[int(t) for t in admit_tick])
+        cfg.admit_tick = ctypes.cast(a, ctypes.POINTER(ctypes.c_int32))
+        keep.append(a)
+    cfg._keep = keep
+    return cfg
+
+
+def dg_workspace_size(cfg: dg_config) -> int:
+    return int(lib.dg_workspace_size(ctypes.byref(cfg)))
+
+
+class Sampler:
+    """One sampler: owns its workspace (a torch uint8 CUDA tensor) and borrows ``w_vocab``."""
+
+    def __init__(self, cfg: dg_config, w_vocab, norm_w=None, stream=None):
+        import torch
+        assert w_vocab.is_cuda and w_vocab.dtype == torch.bfloat16 and w_vocab.is_contiguous()
+        self.cfg = cfg
+        self.device = w_vocab.device
+        self.w_vocab = w_vocab
+        self.norm_w = norm_w
+        self.B, self.L, self.d, self.V, self.G = (cfg.n_canvases, cfg.canvas_len, cfg.hidden, cfg.vocab,
+                                                  cfg.gen_blocks)
+        nbytes = dg_workspace_size(cfg)
+        if nbytes == 0:
+            h = ctypes.c_void_p()
+            st = lib.dg_sampler_create(ctypes.byref(cfg), None, None, None, 0, None, ctypes.byref(h))
+            _check(st if st != DG_OK else DG_ERR_ARG)
+        self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
+        off = (-self.workspace.data_ptr()) % 256
+        self._ws_off = off
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        h = ctypes.c_void_p()
+        st = lib.dg_sampler_create(ctypes.byref(cfg), ctypes.c_void_p(w_vocab.data_ptr()),
+                                   ctypes.c_void_p(norm_w.data_ptr()) if norm_w is not None else None,
+                                   ctypes.c_void_p(self.workspace.data_ptr() + off), nbytes,
+                                   ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(h))
+        _check(st)
+        self.handle = h
+
+    # --------------------------------------------------------------- calls
+    def dg_denoise_step(self, resid) -> int:
+        return lib.dg_denoise_step(self.handle, ctypes.c_void_p(resid.data_ptr()))
+
+    def step(self, resid):
+        _check(self.dg_denoise_step(resid), self.handle)
+
+    def step_host(self, resid_host: np.ndarray, want_canvas=True, want_entropy=True):
+        assert resid_host.dtype == np.float32 and resid_host.flags["C_CONTIGUOUS"]
+        canvas = np.empty((self.B, self.L), np.int32) if want_canvas else None
+        ent = np.empty((self.B, self.L), np.float32) if want_entropy else None
+        _check(lib.dg_denoise_step_host(self.handle, ctypes.c_void_p(resid_host.ctypes.data),
+                                        ctypes.c_void_p(canvas.ctypes.data) if canvas is not None else None,
+                                        ctypes.c_void_p(ent.ctypes.data) if ent is not None else None), self.handle)
+        return canvas, ent
+
+    def run(self, resid_fn, resid_dev=None):
+        """dg_run with a Python callback ``resid_fn(tick, canvas_ptr, slots_ptr, resid_ptr, stream_ptr) -> int``."""
+        cb = DG_RESID_FN(lambda user, tick, canvas, slots, resid, stream: int(resid_fn(tick, canvas, slots, resid,
+                                                                                          stream)))
+        tokens = np.empty((self.B, self.G, self.L), np.int32)
+        slots = np.empty(self.B, SLOT_DTYPE)
+        _check(lib.dg_run(self.handle, cb, None, ctypes.c_void_p(resid_dev.data_ptr()) if resid_dev is not None
+                          else None, ctypes.c_void_p(tokens.ctypes.data), ctypes.c_void_p(slots.ctypes.data)),
+               self.handle)
+        return tokens, slots
+
+    def sync_info(self) -> np.ndarray:
+        slots = np.empty(self.B, SLOT_DTYPE)
+        _check(lib.dg_sync_info(self.handle, ctypes.c_void_p(slots.ctypes.data)), self.handle)
+        return slots
+
+    def get_state(self) -> dict:
+        B, L, G = self.B, self.L, self.G
+        st = {"slots": np.empty(B, SLOT_DTYPE), "tokens": np.empty((B, L), np.int32),
+              "committed": np.empty((B, L), np.uint8), "commit_step": np.empty((B, L), np.int16),
+              "prev_argmax": np.empty((B, L), np.int32), "tokens_out": np.empty((B, G, L), np.int32)}
+        s = dg_state(0, *[ctypes.c_void_p(st[k].ctypes.data) for k in ("slots", "tokens", "committed", "commit_step",
+                                                                       "prev_argmax", "tokens_out")])
+        _check(lib.dg_get_state(self.handle, ctypes.byref(s)), self.handle)
+        st["tick"] = s.tick
+        return st
+
+    def set_state(self, st: dict):
+        arrs = {k: np.ascontiguousarray(st[k], dtype=dt) for k, dt in
+                (("slots", SLOT_DTYPE), ("tokens", np.int32), ("committed", np.uint8), ("commit_step", np.int16),
+                 ("prev_argmax", np.int32), ("tokens_out", np.int32))}
+        s = dg_state(int(st["tick"]), *[ctypes.c_void_p(arrs[k].ctypes.data) for k in
+                                        ("slots", "tokens", "committed", "commit_step", "prev_argmax", "tokens_out")])
+        _check(lib.dg_set_state(self.handle, ctypes.byref(s)), self.handle)
+
+    # --------------------------------------------------------------- views
+    def _view(self, fn, dtype, shape):
+        import torch
+        ptr = getattr(lib, fn)(self.handle)
+        off = ptr - self.workspace.data_ptr()
+        n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        return self.workspace[off:off + n].view(dtype).view(*shape)
+
+    def canvas(self):
+        import torch
+        return self._view("dg_canvas", torch.int32, (self.B, self.L))
+
+    def committed(self):
+        import torch
+        return self._view("dg_committed", torch.uint8, (self.B, self.L))
+
+    def commit_step(self):
+        import torch
+        return self._view("dg_commit_step", torch.int16, (self.B, self.L))
+
+    def entropy(self):
+        import torch
+        return self._view("dg_entropy", torch.float32, (self.B, self.L))
+
+    def logz(self):
+        import torch
+        return self._view("dg_logz", torch.float32, (self.B, self.L))
+
+    def sample(self):
+        import torch
+        return self._view("dg_sample", torch.int32, (self.B, self.L))
+
+    def argmax(self):
+        import torch
+        return self._view("dg_argmax", torch.int32, (self.B, self.L))
+
+    def tokens_out(self):
+        import torch
+        return self._view("dg_tokens_out", torch.int32, (self.B, self.G, self.L))
+
+    def slots_ptr(self) -> int:
+        return int(lib.dg_slots(self.handle))
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib.dg_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,169 @@
+// Internal declarations of the denoise-step library (sm_103a): workspace
+// view, device helpers and the PTX wrappers the kernels use.  Not part of the
+// public ABI (include/dg_sampler.h is).
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the driver entry point is looked up at run time)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dg_sampler.h"
+
+namespace dg {
+
+// ---------------------------------------------------------------- tiling
+// LM-head GEMM tile: 128 canvas positions (TMEM lanes) x 256 vocabulary rows
+// (TMEM columns) per accumulator, K staged 64 bf16 (one 128-byte swizzle row)
+// at a time.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kStageA = kBM * kBK * 2;  // 16 KB
+constexpr int kStageB = kBN * kBK * 2;  // 32 KB
+constexpr int kEpiWarps = 8;            // two per TMEM lane quadrant, each owning 128 of the 256 columns
+constexpr int kThreadsLM = 64 + 32 * kEpiWarps;
+constexpr int kTmemCols = 2 * kBN;      // double-buffered accumulator
+// The vocabulary is cut into this many chunks (fewer when V is small),
+// independent of how many canvases are active, so a position's statistics do
+// not depend on the batch it runs in.
+constexpr int kChunkTarget = 76;
+constexpr int kSubPerChunk = 2;         // one partial record per column half
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after 1 s
+
+// Philox counter "purpose" word (word 3); see the oracle's definition.
+enum : uint32_t { kPurposeInit = 2u, kPurposeGumbel = 3u, kPurposeRenoise = 4u };
+enum : int32_t { kWaiting = 0, kActive = 1, kDone = 2 };
+// Device error codes latched in Plan::err.
+enum : int32_t { kErrNone = 0, kErrNonFinite = 1, kErrTimeout = 2 };
+
+// Split-vocabulary partial statistics of one position over one column range,
+// in base-2 units: u = z * log2(e) / T.
+//   m = max u, S = sum 2^(u-m), A = sum 2^(u-m) (u-m),
+//   g = max (u - log2 E_v) with E_v the Exp(1) variate of the Gumbel draw.
+struct Partial {
+  float m, S, A, g;
+  int32_t amax, gidx, pad0, pad1;
+};
+static_assert(sizeof(Partial) == 32, "partial record is 32 bytes");
+
+struct Plan {
+  int32_t tick;
+  int32_t n_active;
+  uint32_t k4_counter;
+  int32_t err;
+  int32_t err_info[4];
+};
+
+// Everything a kernel needs, by value.
+struct Dev {
+  dg_slot* slots;       // [B]
+  Plan* plan;
+  int32_t* active;      // [B] active canvas ids, in canvas order
+  int32_t* x;           // [B, L]
+  uint8_t* committed;   // [B, L]
+  int16_t* commit_step; // [B, L]
+  int32_t* prev_amax;   // [B, L]
+  int32_t* tokens_out;  // [B, G, L]
+  float* H;             // [B, L]
+  float* logZ;          // [B, L]
+  int32_t* y;           // [B, L]
+  int32_t* amax;        // [B, L]
+  uint16_t* h;          // [rows_cap, d] bf16 bits, compact active rows
+  Partial* part;        // [rows_cap, n_sub]
+  float* resid_stage;   // [B, L, d]
+  const float* norm_w;  // [d] or null
+  int32_t V, d, L, B, G, N;
+  float t_min, t_max, bound, conf, eps;
+  int32_t n_vtiles, tiles_per_chunk, n_chunks, n_sub, rows_cap, max_active;
+};
+
+// ------------------------------------------------------------ Philox4x32-10
+// Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3"
+// (SC'11): ten rounds of two 32x32->64 multiplies, key bumped by the Weyl
+// constants between rounds.
+__device__ __forceinline__ uint4 philox(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// One word for a per-position draw (initial canvas, re-noise): counter
+// (0, p, (block<<16)|step, purpose), key = canvas seed, lane 0.
+__device__ __forceinline__ uint32_t draw_u32(uint64_t seed, uint32_t purpose, int block, int step, int p) {
+  return philox(make_uint4(0u, (uint32_t)p, ((uint32_t)block << 16) | (uint32_t)step, purpose), (uint32_t)seed,
+                (uint32_t)(seed >> 32)).x;
+}
+
+// Uniform token in [0, V): Lemire's multiply-shift.
+__device__ __forceinline__ int32_t uniform_token(uint32_t u, int32_t V) {
+  return (int32_t)(((uint64_t)u * (uint64_t)(uint32_t)V) >> 32);
+}
+
+// T_s = t_max + (s/N)(t_min - t_max), evaluated in fp64 without contraction,
+// rounded once to fp32.
+__device__ __forceinline__ float temperature(int s, int N, float t_min, float t_max) {
+  const double frac = __ddiv_rn((double)s, (double)N);
+  return __double2float_rn(__dadd_rn((double)t_max, __dmul_rn(frac, __dsub_rn((double)t_min, (double)t_max))));
+}
+
+// ------------------------------------------------------------ small PTX
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Merge two partial records (base-2 units).  Ties keep the lower vocabulary index.
+__device__ __forceinline__ Partial merge_partial(const Partial& a, const Partial& b) {
+  Partial r;
+  r.m = fmaxf(a.m, b.m);
+  const float fa = a.S > 0.f ? ex2_approx(a.m - r.m) : 0.f;
+  const float fb = b.S > 0.f ? ex2_approx(b.m - r.m) : 0.f;
+  r.S = fa * a.S + fb * b.S;
+  r.A = (a.S > 0.f ? fa * fmaf(a.m - r.m, a.S, a.A) : 0.f) + (b.S > 0.f ? fb * fmaf(b.m - r.m, b.S, b.A) : 0.f);
+  const bool ta = (a.m > b.m) || (a.m == b.m && a.amax < b.amax);
+  r.amax = ta ? a.amax : b.amax;
+  const bool ga = (a.g > b.g) || (a.g == b.g && a.gidx < b.gidx);
+  r.g = ga ? a.g : b.g;
+  r.gidx = ga ? a.gidx : b.gidx;
+  r.pad0 = r.pad1 = 0;
+  return r;
+}
+
+__device__ __forceinline__ Partial empty_partial() {
+  Partial p;
+  p.m = -INFINITY;
+  p.S = 0.f;
+  p.A = 0.f;
+  p.g = -INFINITY;
+  p.amax = 0x7FFFFFFF;
+  p.gidx = 0x7FFFFFFF;
+  p.pad0 = p.pad1 = 0;
+  return p;
+}
+
+// ------------------------------------------------------------- launchers
+// Implemented in dg_kernels.cu / dg_lmhead.cu; all enqueue on `st`.
+cudaError_t launch_rmsnorm(const Dev& dv, const float* resid, cudaStream_t st);
+cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
+                          cudaStream_t st);
+cudaError_t launch_combine(const Dev& dv, cudaStream_t st);
+cudaError_t launch_commit(const Dev& dv, cudaStream_t st);
+cudaError_t launch_plan(const Dev& dv, int tick, cudaStream_t st);
+cudaError_t launch_refresh_slots(const Dev& dv, cudaStream_t st);
+cudaError_t lmhead_configure();
+
+}  // namespace dg

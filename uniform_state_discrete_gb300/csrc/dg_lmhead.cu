@@ -1,0 +1,451 @@
+// K2: the tied LM head z = h W^T on the 5th-generation tensor cores, fused
+// with the temperature-softmax statistics and the Gumbel-max sample, so the
+// [positions x V] logits never leave the SM.
+//
+// Pages: "The Annotated DiffusionGemma" -- the tied LM head at the end of
+// "Complete DiffusionGemma model", the temperature divisor of "Apply
+// temperature", the entropy of "Compute entropy", the sample drawn in
+// "Denoise, stage, commit, and generate".  TensorSharp's DiffusionGemma doc
+// ("5. Acceleration status") fuses output-norm + lm-head and then reduces
+// per position on the device; here the reduction moves into the GEMM's own
+// epilogue so the logits are never written.
+//
+// Structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: A = h tile [128 x 64] and B = W tile [256 x 64]
+//               per stage, 128-byte swizzle, 4-stage mbarrier ring.
+//   warp 1      allocates 512 TMEM columns; one lane issues
+//               tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32,
+//               M=128, N=256, K=16) into one of two TMEM accumulators and
+//               commits stage release / accumulator-ready barriers.
+//   warps 2..9  epilogue: two warps per TMEM lane quadrant (rows), each
+//               owning 128 of the 256 columns; per element
+//                 u = z * log2(e)/T, running (max, sum 2^(u-m), sum 2^(u-m)(u-m)),
+//                 argmax, and the perturbed score u - log2 E_v of the
+//                 Gumbel draw (E_v = -ln U_v, U_v from Philox).
+// Work unit = (128-row M tile of active positions, vocabulary chunk); the
+// epilogue keeps its running statistics in registers across the chunk's
+// tiles and writes one 32-byte partial record per row and column half.
+// Every mbarrier wait is bounded (1 s); on expiry the CTA latches an error,
+// drains what it issued and frees TMEM.
+#include <cuda_runtime.h>
+
+#include "dg_internal.cuh"
+
+namespace dg {
+namespace {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `parity` to complete, giving up after kWaitLimitNs or
+// as soon as another role of this CTA gave up.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, Plan* plan) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0u) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicExch(&plan->err, kErrTimeout);
+        atomicExch(&plan->err_info[0], (int)blockIdx.x);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major tile stored with the
+// 128-byte swizzle (rows of 128 bytes, 8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address >> 4
+  d |= (uint64_t)1 << 16;                            // leading byte offset (unused with this swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                            // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                            // layout: 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
+constexpr uint32_t kIdesc = (1u << 4)                         // D format fp32
+                            | (1u << 7)                       // A format bf16
+                            | (1u << 10)                      // B format bf16
+                            | ((uint32_t)(kBN >> 3) << 17)    // N / 8
+                            | ((uint32_t)(kBM >> 4) << 24);   // M / 16
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane, waited in the same
+// statement so no use of the registers can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// -log2(E) for the Exp(1) variate E = -ln U of one Gumbel draw,
+// U = (r + 0.5) 2^-32.  For U < 3/4, E comes from lg2(U).  For U >= 3/4,
+// E = -ln(1 - q) with q = 1 - U taken exactly from the integer, through the
+// series -ln(1-q) = 2 atanh(s) = 2 (s + s^3/3 + s^5/5 + ...), s = q / (2 - q)
+// <= 1/7, truncated after s^9 (relative error < 4e-10), which keeps the large
+// Gumbel values (small E) accurate where lg2(U) would lose them.
+__device__ __forceinline__ float neg_log2_exp_variate(uint32_t r) {
+  float E;
+  if (r < 0xC0000000u) {
+    const float U = fmaf(__uint2float_rn(r), 0x1p-32f, 0x1p-33f);
+    E = -0.69314718055994531f * lg2_approx(U);
+  } else {
+    const float q = fmaf(__uint2float_rn(~r), 0x1p-32f, 0x1p-33f);
+    const float s = __fdividef(q, 2.0f - q);
+    const float s2 = s * s;
+    float t = fmaf(s2, 1.0f / 9.0f, 1.0f / 7.0f);
+    t = fmaf(s2, t, 1.0f / 5.0f);
+    t = fmaf(s2, t, 1.0f / 3.0f);
+    t = fmaf(s2, t, 1.0f);
+    E = 2.0f * s * t;
+  }
+  return -lg2_approx(E);
+}
+
+struct RowMeta {
+  uint32_t key0, key1, bs, p;
+  float scale;  // log2(e) / T
+  bool valid;
+};
+
+// Fold 32 columns [v0, v0+32) of one row into its running statistics.
+__device__ __forceinline__ void fold32(const float (&acc)[32], int v0, int V, const RowMeta& rm, Partial& st) {
+  float u[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) u[j] = acc[j] * rm.scale;
+  const bool full = (v0 + 32 <= V);
+  if (!full) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (v0 + j >= V) u[j] = -INFINITY;
+  }
+  // running max / argmax (first index on ties)
+  float cm = u[0];
+  int ci = 0;
+#pragma unroll
+  for (int j = 1; j < 32; ++j)
+    if (u[j] > cm) {
+      cm = u[j];
+      ci = j;
+    }
+  if (cm > st.m) {
+    const float f = ex2_approx(st.m - cm);
+    st.A = st.S > 0.f ? f * fmaf(st.m - cm, st.S, st.A) : 0.f;
+    st.S = f * st.S;
+    st.m = cm;
+    st.amax = v0 + ci;
+  }
+  if (cm == -INFINITY) return;  // a fully masked tail chunk
+  float S = 0.f, A = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float dlt = u[j] - st.m;
+    const float e = ex2_approx(dlt);
+    if (full || v0 + j < V) {
+      S += e;
+      A = fmaf(e, dlt, A);
+    }
+  }
+  st.S += S;
+  st.A += A;
+  // Gumbel-max: one Philox block per 4 consecutive vocabulary entries
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int vb = v0 + 4 * g;
+    const uint4 r = philox(make_uint4((uint32_t)vb >> 2, rm.p, rm.bs, kPurposeGumbel), rm.key0, rm.key1);
+    const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const float sc = u[4 * g + l] + neg_log2_exp_variate(rw[l]);
+      if (sc > st.g && (full || vb + l < V)) {
+        st.g = sc;
+        st.gidx = vb + l;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreadsLM, 1)
+    k_lmhead(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kStageA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kStageB);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_rows = dv.plan->n_active * dv.L;
+  const int n_mt = (n_rows + kBM - 1) / kBM;
+  const int n_units = n_mt * dv.n_chunks;
+  const int KB = (dv.d + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"((uint32_t)kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int issued_parity[kStages];
+      for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const int chunk = u / n_mt, mt = u - chunk * n_mt;
+        const int vt0 = chunk * dv.tiles_per_chunk;
+        const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
+        for (int vt = vt0; vt < vt1 && ok; ++vt) {
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&full[stage], (uint32_t)(kStageA + kStageB));
+            tma_load_2d(sA + stage * kStageA, &tmA, kb * kBK, mt * kBM, &full[stage]);
+            tma_load_2d(sB + stage * kStageB, &tmB, kb * kBK, vt * kBN, &full[stage]);
+            issued_parity[stage] = (int)phase;
+            if (++stage == (uint32_t)kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before shared memory is released
+        for (int s = 0; s < kStages; ++s) {
+          if (issued_parity[s] < 0) continue;
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(&full[s], (uint32_t)issued_parity[s]) && global_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, tcount = 0;
+      bool ok = true, any = false;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const int chunk = u / n_mt;
+        const int vt0 = chunk * dv.tiles_per_chunk;
+        const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
+        for (int vt = vt0; vt < vt1 && ok; ++vt, ++tcount) {
+          const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
+          if (!mbar_wait(&tempty[ab], aph ^ 1u, abort_flag, dv.plan)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + ab * (uint32_t)kBN;
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, dv.plan)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + stage * kStageA);
+            const uint32_t b0 = smem_u32(sB + stage * kStageB);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // advance K by 16 bf16 = 32 bytes inside the swizzled 128-byte row
+              mma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), (kb | kk) != 0 ? 1u : 0u);
+            }
+            mma_commit(&empty[stage]);
+            any = true;
+            if (++stage == (uint32_t)kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&tfull[ab]);
+        }
+      }
+      if (!ok && any) {
+        // wait (bounded) for the MMAs already issued before TMEM is freed
+        mma_commit(drain);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(drain, 0u) && global_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;             // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;   // which 128 of the 256 columns
+    uint32_t tcount = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int chunk = u / n_mt, mt = u - chunk * n_mt;
+      const int vt0 = chunk * dv.tiles_per_chunk;
+      const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
+      const int row = mt * kBM + q * 32 + lane;
+      RowMeta rm;
+      rm.valid = row < n_rows;
+      rm.key0 = rm.key1 = rm.bs = rm.p = 0u;
+      rm.scale = 0.f;
+      if (rm.valid) {
+        const int a = row / dv.L;
+        const int c = dv.active[a];
+        const dg_slot sl = dv.slots[c];
+        rm.p = (uint32_t)(row - a * dv.L);
+        rm.key0 = (uint32_t)sl.seed;
+        rm.key1 = (uint32_t)(sl.seed >> 32);
+        rm.bs = ((uint32_t)sl.block << 16) | (uint32_t)sl.step;
+        rm.scale = 1.4426950408889634f / sl.temperature;
+      }
+      Partial st = empty_partial();
+      for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
+        const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
+        int got = 0;
+        if (lane == 0) got = mbar_wait(&tfull[ab], aph, abort_flag, dv.plan) ? 1 : 0;
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(half * 128);
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          float acc[32];
+          __syncwarp();  // tcgen05.ld is .sync.aligned: the fold below may leave lanes diverged
+          tmem_ld32(tbase + (uint32_t)(cc * 32), acc);
+          if (rm.valid) fold32(acc, vt * kBN + half * 128 + cc * 32, dv.V, rm, st);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[ab]);
+      }
+      if (!ok) break;
+      if (rm.valid) dv.part[(size_t)row * dv.n_sub + chunk * kSubPerChunk + half] = st;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)kTmemCols)
+                 : "memory");
+  }
+}
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kStageA + kStageB) + 256;
+
+}  // namespace
+
+cudaError_t lmhead_configure() {
+  return cudaFuncSetAttribute(k_lmhead, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+}
+
+cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
+                          cudaStream_t st) {
+  // Persistent grid: one CTA per SM (the shared-memory ring keeps it at one),
+  // never more CTAs than the largest number of work units.
+  const int max_mt = (dv.max_active * dv.L + kBM - 1) / kBM;
+  int grid = max_mt * dv.n_chunks;
+  if (grid > num_sms) grid = num_sms;
+  if (grid < 1) grid = 1;
+  k_lmhead<<<grid, kThreadsLM, kSmemBytes, st>>>(*tmA, *tmB, dv);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,471 @@
+// Host side of the C ABI in include/dg_sampler.h: config validation,
+// workspace layout, TMA tensor maps, the per-tick launch sequence and state
+// transfer.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "dg_internal.cuh"
+
+struct dg_sampler {
+  dg_config cfg;
+  std::vector<uint64_t> seeds;
+  std::vector<int32_t> admit;
+  dg::Dev dv;
+  CUtensorMap tmA, tmB;
+  cudaStream_t stream;
+  int num_sms;
+  int64_t host_tick;
+  int64_t tick_bound;
+  void* ws;
+  size_t ws_bytes;
+  char err[512];
+};
+
+namespace {
+
+char g_create_err[512] = "";
+
+void set_err(char* buf, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, 512, fmt, ap);
+  va_end(ap);
+}
+
+struct Layout {
+  size_t slots, plan, active, x, committed, commit_step, prev_amax, tokens_out, H, logZ, y, amax, h, part, resid;
+  size_t total;
+  int rows_cap, n_vtiles, tiles_per_chunk, n_chunks, n_sub, max_active;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+bool validate(const dg_config* c, char* why) {
+  if (!c) return set_err(why, "config is NULL"), false;
+  if (c->vocab < 2) return set_err(why, "vocab must be >= 2 (got %d)", c->vocab), false;
+  if (c->hidden < 8 || c->hidden > 16384 || c->hidden % 8)
+    return set_err(why, "hidden must be a multiple of 8 in [8, 16384] (got %d)", c->hidden), false;
+  if (c->canvas_len < 1 || c->canvas_len > 1024)
+    return set_err(why, "canvas_len must be in [1, 1024] (got %d)", c->canvas_len), false;
+  if (c->n_canvases < 1) return set_err(why, "n_canvases must be >= 1"), false;
+  if (c->gen_blocks < 1 || c->gen_blocks > 65535) return set_err(why, "gen_blocks must be in [1, 65535]"), false;
+  if (c->num_inference_steps < 1 || c->num_inference_steps > 1024)
+    return set_err(why, "num_inference_steps must be in [1, 1024] (got %d)", c->num_inference_steps), false;
+  if (!(c->t_min > 0.f) || !(c->t_max > 0.f) || !std::isfinite(c->t_min) || !std::isfinite(c->t_max))
+    return set_err(why, "t_min and t_max must be finite and > 0"), false;
+  if (!(c->entropy_bound >= 0.f) || !std::isfinite(c->entropy_bound))
+    return set_err(why, "entropy_bound must be finite and >= 0"), false;
+  if (!(c->confidence >= 0.f) || !std::isfinite(c->confidence))
+    return set_err(why, "confidence must be finite and >= 0"), false;
+  if (!(c->rms_eps >= 0.f) || !std::isfinite(c->rms_eps)) return set_err(why, "rms_eps must be finite and >= 0"), false;
+  if (c->max_active < 0 || c->max_active > c->n_canvases)
+    return set_err(why, "max_active must be in [0, n_canvases]"), false;
+  if ((int64_t)c->n_canvases * c->canvas_len > (int64_t)1 << 24)
+    return set_err(why, "n_canvases * canvas_len must be <= 2^24"), false;
+  if (c->admit_tick)
+    for (int i = 0; i < c->n_canvases; ++i)
+      if (c->admit_tick[i] < 0) return set_err(why, "admit_tick[%d] is negative", i), false;
+  return true;
+}
+
+// Returns 1 ok, 0 invalid, -1 unsupported.
+int make_layout(const dg_config* c, Layout* L, char* why) {
+  if (!validate(c, why)) return 0;
+  if (c->stability != 1) return set_err(why, "only stability = 1 is implemented (got %d)", c->stability), -1;
+  if (c->mode != DG_FREEZE) return set_err(why, "only mode DG_FREEZE is implemented (got %d)", c->mode), -1;
+  const size_t B = c->n_canvases, Lc = c->canvas_len, d = c->hidden, G = c->gen_blocks;
+  L->max_active = c->max_active ? c->max_active : c->n_canvases;
+  const size_t rows = (size_t)L->max_active * Lc;
+  L->rows_cap = (int)((rows + 255) / 256 * 256);
+  L->n_vtiles = (c->vocab + dg::kBN - 1) / dg::kBN;
+  const int target = L->n_vtiles < dg::kChunkTarget ? L->n_vtiles : dg::kChunkTarget;
+  L->tiles_per_chunk = (L->n_vtiles + target - 1) / target;
+  L->n_chunks = (L->n_vtiles + L->tiles_per_chunk - 1) / L->tiles_per_chunk;
+  L->n_sub = L->n_chunks * dg::kSubPerChunk;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L->slots = take(sizeof(dg_slot) * B);
+  L->plan = take(sizeof(dg::Plan));
+  L->active = take(sizeof(int32_t) * B);
+  L->x = take(4 * B * Lc);
+  L->committed = take(B * Lc);
+  L->commit_step = take(2 * B * Lc);
+  L->prev_amax = take(4 * B * Lc);
+  L->tokens_out = take(4 * B * G * Lc);
+  L->H = take(4 * B * Lc);
+  L->logZ = take(4 * B * Lc);
+  L->y = take(4 * B * Lc);
+  L->amax = take(4 * B * Lc);
+  L->h = take(2 * (size_t)L->rows_cap * d);
+  L->part = take(sizeof(dg::Partial) * (size_t)L->rows_cap * L->n_sub);
+  L->resid = take(4 * B * Lc * d);
+  L->total = o;
+  return 1;
+}
+
+dg_status cuda_fail(char* buf, cudaError_t e, const char* what) {
+  set_err(buf, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+  return DG_ERR_CUDA;
+}
+
+#define DG_CUDA(s, call, what)                               \
+  do {                                                       \
+    cudaError_t e_ = (call);                                 \
+    if (e_ != cudaSuccess) return cuda_fail((s), e_, (what)); \
+  } while (0)
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode(char* why) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn) return fn;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p) {
+    set_err(why, "cuTensorMapEncodeTiled not available from the driver");
+    return nullptr;
+  }
+  fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box [box_rows, 64],
+// 128-byte swizzle (the layout the MMA descriptors expect), zero fill outside.
+bool encode_2d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, char* why) {
+  auto enc = get_encode(why);
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)dg::kBK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_err(why, "cuTensorMapEncodeTiled failed (CUresult %d) for a [%llu x %llu] matrix", (int)r,
+            (unsigned long long)rows, (unsigned long long)cols);
+    return false;
+  }
+  return true;
+}
+
+dg_status check_device_error(dg_sampler* s) {
+  dg::Plan pl;
+  DG_CUDA(s->err, cudaMemcpyAsync(&pl, s->dv.plan, sizeof pl, cudaMemcpyDeviceToHost, s->stream), "read plan");
+  DG_CUDA(s->err, cudaStreamSynchronize(s->stream), "synchronize");
+  if (pl.err == dg::kErrNonFinite) {
+    set_err(s->err, "non-finite logit statistics at position index %d", pl.err_info[1]);
+    return DG_ERR_NONFINITE;
+  }
+  if (pl.err == dg::kErrTimeout) {
+    set_err(s->err, "a bounded wait in the LM-head kernel expired (CTA %d)", pl.err_info[0]);
+    return DG_ERR_TIMEOUT;
+  }
+  return DG_OK;
+}
+
+dg_status tick(dg_sampler* s, const float* resid) {
+  if (s->host_tick >= s->tick_bound) {
+    set_err(s->err, "every canvas has finished (tick %lld)", (long long)s->host_tick);
+    return DG_ERR_STATE;
+  }
+  DG_CUDA(s->err, dg::launch_rmsnorm(s->dv, resid, s->stream), "launch rmsnorm");
+  DG_CUDA(s->err, dg::launch_lmhead(s->dv, &s->tmA, &s->tmB, s->num_sms, s->stream), "launch lm head");
+  DG_CUDA(s->err, dg::launch_combine(s->dv, s->stream), "launch combine");
+  DG_CUDA(s->err, dg::launch_commit(s->dv, s->stream), "launch commit");
+  ++s->host_tick;
+  return DG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dg_workspace_size(const dg_config* cfg) {
+  Layout L;
+  char why[512];
+  if (make_layout(cfg, &L, why) != 1) return 0;
+  return L.total;
+}
+
+dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const float* norm_w, void* workspace,
+                            size_t ws_bytes, dg_stream_t stream, dg_sampler** out) {
+  g_create_err[0] = 0;
+  if (!out) return set_err(g_create_err, "out is NULL"), DG_ERR_ARG;
+  *out = nullptr;
+  Layout L;
+  const int lr = make_layout(cfg, &L, g_create_err);
+  if (lr == 0) return DG_ERR_ARG;
+  if (lr < 0) return DG_ERR_UNSUPPORTED;
+  if (!w_vocab) return set_err(g_create_err, "w_vocab is NULL"), DG_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(w_vocab) % 16)
+    return set_err(g_create_err, "w_vocab must be 16-byte aligned"), DG_ERR_ALIGN;
+  if (norm_w && reinterpret_cast<uintptr_t>(norm_w) % 16)
+    return set_err(g_create_err, "norm_w must be 16-byte aligned"), DG_ERR_ALIGN;
+  if (!workspace || ws_bytes < L.total)
+    return set_err(g_create_err, "workspace needs %zu bytes (got %zu)", L.total, workspace ? ws_bytes : 0),
+           DG_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256)
+    return set_err(g_create_err, "workspace must be 256-byte aligned"), DG_ERR_ALIGN;
+
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(g_create_err, e, "query device");
+  if (major != 10 || minor != 3) {
+    set_err(g_create_err, "this library is built for sm_103a (GB300); device is sm_%d%d", major, minor);
+    return DG_ERR_UNSUPPORTED;
+  }
+
+  dg_sampler* s = new (std::nothrow) dg_sampler();
+  if (!s) return set_err(g_create_err, "out of host memory"), DG_ERR_ARG;
+  s->cfg = *cfg;
+  const int B = cfg->n_canvases;
+  s->seeds.resize(B);
+  s->admit.resize(B);
+  for (int c = 0; c < B; ++c) {
+    s->seeds[c] = cfg->seeds ? cfg->seeds[c] : (uint64_t)c;
+    s->admit[c] = cfg->admit_tick ? cfg->admit_tick[c] : 0;
+  }
+  s->cfg.seeds = nullptr;
+  s->cfg.admit_tick = nullptr;
+  s->stream = reinterpret_cast<cudaStream_t>(stream);
+  s->num_sms = sms;
+  s->ws = workspace;
+  s->ws_bytes = ws_bytes;
+  s->err[0] = 0;
+  s->host_tick = 0;
+  int32_t max_admit = 0;
+  for (int c = 0; c < B; ++c) max_admit = s->admit[c] > max_admit ? s->admit[c] : max_admit;
+  // every canvas has finished by then, even if it waited for a free slot behind all others
+  s->tick_bound = (int64_t)max_admit + (int64_t)cfg->gen_blocks * cfg->num_inference_steps * B;
+
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  dg::Dev& dv = s->dv;
+  dv.slots = reinterpret_cast<dg_slot*>(w + L.slots);
+  dv.plan = reinterpret_cast<dg::Plan*>(w + L.plan);
+  dv.active = reinterpret_cast<int32_t*>(w + L.active);
+  dv.x = reinterpret_cast<int32_t*>(w + L.x);
+  dv.committed = w + L.committed;
+  dv.commit_step = reinterpret_cast<int16_t*>(w + L.commit_step);
+  dv.prev_amax = reinterpret_cast<int32_t*>(w + L.prev_amax);
+  dv.tokens_out = reinterpret_cast<int32_t*>(w + L.tokens_out);
+  dv.H = reinterpret_cast<float*>(w + L.H);
+  dv.logZ = reinterpret_cast<float*>(w + L.logZ);
+  dv.y = reinterpret_cast<int32_t*>(w + L.y);
+  dv.amax = reinterpret_cast<int32_t*>(w + L.amax);
+  dv.h = reinterpret_cast<uint16_t*>(w + L.h);
+  dv.part = reinterpret_cast<dg::Partial*>(w + L.part);
+  dv.resid_stage = reinterpret_cast<float*>(w + L.resid);
+  dv.norm_w = norm_w;
+  dv.V = cfg->vocab;
+  dv.d = cfg->hidden;
+  dv.L = cfg->canvas_len;
+  dv.B = B;
+  dv.G = cfg->gen_blocks;
+  dv.N = cfg->num_inference_steps;
+  dv.t_min = cfg->t_min;
+  dv.t_max = cfg->t_max;
+  dv.bound = cfg->entropy_bound;
+  dv.conf = cfg->confidence;
+  dv.eps = cfg->rms_eps;
+  dv.n_vtiles = L.n_vtiles;
+  dv.tiles_per_chunk = L.tiles_per_chunk;
+  dv.n_chunks = L.n_chunks;
+  dv.n_sub = L.n_sub;
+  dv.rows_cap = L.rows_cap;
+  dv.max_active = L.max_active;
+
+  auto fail = [&](dg_status st) {
+    memcpy(g_create_err, s->err, sizeof g_create_err);
+    delete s;
+    return st;
+  };
+  if (!encode_2d(&s->tmA, dv.h, (uint64_t)L.rows_cap, (uint64_t)dv.d, dg::kBM, s->err)) return fail(DG_ERR_ARG);
+  if (!encode_2d(&s->tmB, w_vocab, (uint64_t)dv.V, (uint64_t)dv.d, dg::kBN, s->err)) return fail(DG_ERR_ARG);
+  cudaError_t ce = dg::lmhead_configure();
+  if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "configure lm-head kernel"));
+
+  std::vector<dg_slot> slots(B);
+  for (int c = 0; c < B; ++c) {
+    dg_slot& sl = slots[c];
+    memset(&sl, 0, sizeof sl);
+    sl.seed = s->seeds[c];
+    sl.admit_tick = s->admit[c];
+    sl.state = dg::kWaiting;
+    sl.temperature = cfg->t_max;
+  }
+  ce = cudaMemsetAsync(workspace, 0, L.total, s->stream);
+  if (ce == cudaSuccess)
+    ce = cudaMemcpyAsync(dv.slots, slots.data(), sizeof(dg_slot) * B, cudaMemcpyHostToDevice, s->stream);
+  if (ce == cudaSuccess) ce = dg::launch_plan(dv, 0, s->stream);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(s->stream);
+  if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "initialise sampler state"));
+  *out = s;
+  return DG_OK;
+}
+
+dg_status dg_denoise_step(dg_sampler* s, const float* resid) {
+  if (!s) return DG_ERR_ARG;
+  if (!resid) return set_err(s->err, "resid is NULL"), DG_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(resid) % 16) return set_err(s->err, "resid must be 16-byte aligned"), DG_ERR_ALIGN;
+  return tick(s, resid);
+}
+
+dg_status dg_denoise_step_host(dg_sampler* s, const float* resid_host, int32_t* canvas_host, float* entropy_host) {
+  if (!s) return DG_ERR_ARG;
+  if (!resid_host) return set_err(s->err, "resid_host is NULL"), DG_ERR_ARG;
+  const size_t BL = (size_t)s->dv.B * s->dv.L;
+  DG_CUDA(s->err,
+          cudaMemcpyAsync(s->dv.resid_stage, resid_host, BL * s->dv.d * sizeof(float), cudaMemcpyHostToDevice,
+                          s->stream),
+          "copy resid to device");
+  dg_status st = tick(s, s->dv.resid_stage);
+  if (st != DG_OK) return st;
+  if (canvas_host)
+    DG_CUDA(s->err, cudaMemcpyAsync(canvas_host, s->dv.x, BL * 4, cudaMemcpyDeviceToHost, s->stream), "copy canvas");
+  if (entropy_host)
+    DG_CUDA(s->err, cudaMemcpyAsync(entropy_host, s->dv.H, BL * 4, cudaMemcpyDeviceToHost, s->stream),
+            "copy entropy");
+  return check_device_error(s);
+}
+
+dg_status dg_sync_info(dg_sampler* s, dg_slot* slots_host) {
+  if (!s || !slots_host) return DG_ERR_ARG;
+  DG_CUDA(s->err,
+          cudaMemcpyAsync(slots_host, s->dv.slots, sizeof(dg_slot) * s->dv.B, cudaMemcpyDeviceToHost, s->stream),
+          "copy slots");
+  return check_device_error(s);
+}
+
+dg_status dg_run(dg_sampler* s, dg_resid_fn fn, void* user, float* resid_dev, int32_t* tokens_host,
+                 dg_slot* slots_host) {
+  if (!s || !fn) return DG_ERR_ARG;
+  float* resid = resid_dev ? resid_dev : s->dv.resid_stage;
+  if (reinterpret_cast<uintptr_t>(resid) % 16) return set_err(s->err, "resid_dev must be 16-byte aligned"), DG_ERR_ALIGN;
+  std::vector<dg_slot> sl(s->dv.B);
+  for (;;) {
+    for (int i = 0; i < s->dv.N && s->host_tick < s->tick_bound; ++i) {
+      if (fn(user, (int32_t)s->host_tick, s->dv.x, s->dv.slots, resid, reinterpret_cast<dg_stream_t>(s->stream)) != 0)
+        return set_err(s->err, "residual callback failed at tick %lld", (long long)s->host_tick), DG_ERR_ARG;
+      dg_status st = tick(s, resid);
+      if (st != DG_OK) return st;
+    }
+    dg_status st = dg_sync_info(s, sl.data());
+    if (st != DG_OK) return st;
+    bool done = true;
+    for (const dg_slot& x : sl) done = done && x.state == dg::kDone;
+    if (done || s->host_tick >= s->tick_bound) break;
+  }
+  if (tokens_host)
+    DG_CUDA(s->err,
+            cudaMemcpyAsync(tokens_host, s->dv.tokens_out, sizeof(int32_t) * s->dv.B * s->dv.G * s->dv.L,
+                            cudaMemcpyDeviceToHost, s->stream),
+            "copy tokens");
+  if (slots_host) memcpy(slots_host, sl.data(), sizeof(dg_slot) * s->dv.B);
+  return check_device_error(s);
+}
+
+dg_status dg_get_state(dg_sampler* s, dg_state* h) {
+  if (!s || !h) return DG_ERR_ARG;
+  const size_t B = s->dv.B, BL = B * s->dv.L;
+  dg::Plan pl;
+  struct {
+    void* dst;
+    const void* src;
+    size_t n;
+  } cp[] = {{h->slots, s->dv.slots, sizeof(dg_slot) * B},    {h->tokens, s->dv.x, 4 * BL},
+            {h->committed, s->dv.committed, BL},             {h->commit_step, s->dv.commit_step, 2 * BL},
+            {h->prev_argmax, s->dv.prev_amax, 4 * BL},       {h->tokens_out, s->dv.tokens_out, 4 * BL * s->dv.G},
+            {&pl, s->dv.plan, sizeof pl}};
+  for (auto& c : cp)
+    if (c.dst) DG_CUDA(s->err, cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, s->stream), "copy state");
+  DG_CUDA(s->err, cudaStreamSynchronize(s->stream), "synchronize");
+  h->tick = pl.tick;
+  return check_device_error(s);
+}
+
+dg_status dg_set_state(dg_sampler* s, const dg_state* h) {
+  if (!s || !h || !h->slots || !h->tokens || !h->committed || !h->commit_step || !h->prev_argmax)
+    return DG_ERR_ARG;
+  if (h->tick < 0) return set_err(s->err, "tick must be >= 0"), DG_ERR_ARG;
+  const size_t B = s->dv.B, BL = B * s->dv.L;
+  std::vector<dg_slot> sl(h->slots, h->slots + B);
+  int active = 0;
+  for (size_t c = 0; c < B; ++c) {
+    sl[c].seed = s->seeds[c];
+    sl[c].admit_tick = s->admit[c];
+    if (sl[c].state < dg::kWaiting || sl[c].state > dg::kDone || sl[c].block < 0 || sl[c].block >= s->dv.G ||
+        sl[c].step < 0 || sl[c].step >= s->dv.N)
+      return set_err(s->err, "slot %zu holds an invalid state/block/step", c), DG_ERR_ARG;
+    active += sl[c].state == dg::kActive;
+  }
+  if (active > s->dv.max_active) return set_err(s->err, "more active canvases than max_active"), DG_ERR_ARG;
+  for (size_t i = 0; i < BL; ++i)
+    if (h->tokens[i] < 0 || h->tokens[i] >= s->dv.V) return set_err(s->err, "token out of range"), DG_ERR_ARG;
+  struct {
+    void* dst;
+    const void* src;
+    size_t n;
+  } cp[] = {{s->dv.slots, sl.data(), sizeof(dg_slot) * B},  {s->dv.x, h->tokens, 4 * BL},
+            {s->dv.committed, h->committed, BL},            {s->dv.commit_step, h->commit_step, 2 * BL},
+            {s->dv.prev_amax, h->prev_argmax, 4 * BL},      {s->dv.tokens_out, h->tokens_out, 4 * BL * s->dv.G}};
+  for (auto& c : cp)
+    if (c.src) DG_CUDA(s->err, cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s->stream), "copy state");
+  DG_CUDA(s->err, dg::launch_plan(s->dv, h->tick, s->stream), "launch plan");
+  DG_CUDA(s->err, cudaStreamSynchronize(s->stream), "synchronize");
+  s->host_tick = h->tick;
+  int32_t max_admit = 0;
+  for (int32_t a : s->admit) max_admit = a > max_admit ? a : max_admit;
+  s->tick_bound = (int64_t)(h->tick > max_admit ? h->tick : max_admit) +
+                  (int64_t)s->dv.G * s->dv.N * (int64_t)s->dv.B;
+  return DG_OK;
+}
+
+void dg_destroy(dg_sampler* s) {
+  if (!s) return;
+  cudaStreamSynchronize(s->stream);
+  delete s;
+}
+
+const int32_t* dg_canvas(const dg_sampler* s) { return s ? s->dv.x : nullptr; }
+const uint8_t* dg_committed(const dg_sampler* s) { return s ? s->dv.committed : nullptr; }
+const int16_t* dg_commit_step(const dg_sampler* s) { return s ? s->dv.commit_step : nullptr; }
+const float* dg_entropy(const dg_sampler* s) { return s ? s->dv.H : nullptr; }
+const float* dg_logz(const dg_sampler* s) { return s ? s->dv.logZ : nullptr; }
+const int32_t* dg_sample(const dg_sampler* s) { return s ? s->dv.y : nullptr; }
+const int32_t* dg_argmax(const dg_sampler* s) { return s ? s->dv.amax : nullptr; }
+const int32_t* dg_tokens_out(const dg_sampler* s) { return s ? s->dv.tokens_out : nullptr; }
+const dg_slot* dg_slots(const dg_sampler* s) { return s ? s->dv.slots : nullptr; }
+
+const char* dg_status_string(dg_status st) {
+  switch (st) {
+    case DG_OK: return "DG_OK";
+    case DG_ERR_ARG: return "DG_ERR_ARG";
+    case DG_ERR_ALIGN: return "DG_ERR_ALIGN";
+    case DG_ERR_WORKSPACE: return "DG_ERR_WORKSPACE";
+    case DG_ERR_CUDA: return "DG_ERR_CUDA";
+    case DG_ERR_STATE: return "DG_ERR_STATE";
+    case DG_ERR_NONFINITE: return "DG_ERR_NONFINITE";
+    case DG_ERR_UNSUPPORTED: return "DG_ERR_UNSUPPORTED";
+    case DG_ERR_TIMEOUT: return "DG_ERR_TIMEOUT";
+  }
+  return "unknown dg_status";
+}
+
+const char* dg_last_error(const dg_sampler* s) { return s ? s->err : g_create_err; }
+
+}  // extern "C"
