@@ -26,7 +26,8 @@ enter the per-step sort; the prefix is exclusive and compared with <=; ties in
 H go to the lower position; the early-stop test is skipped at s = 0; the last
 step commits every remaining position to its sample; blocks of one canvas run
 one after another with a fresh uniform canvas each (DiffusionGemma Denoise
-node, "gen_length" input); canvas c joins at tick admit_tick[c].
+node, "gen_length" input); canvas c joins at the first tick >= admit_tick[c]
+with a free running slot (at most max_active canvases run at once).
 """
 from __future__ import annotations
 
@@ -78,6 +79,7 @@ class OracleConfig:
     rms_eps: float = 1e-6
     seeds: Optional[list] = None
     admit_tick: Optional[list] = None
+    max_active: Optional[int] = None  # most canvases running in one tick (None: all)
     # parity margins stated by the task for flagging near-ties
     margin_H: float = 1e-3
     margin_gap: float = 1e-4
@@ -147,10 +149,16 @@ class OracleSampler:
         self.step_no[c] = 0
 
     def _admit(self, tick: int):
+        """Canvases due by this tick join in canvas order while a running slot is free."""
+        cap = self.cfg.max_active if self.cfg.max_active is not None else self.cfg.n_canvases
+        running = int(np.sum(self.status == ACTIVE))
         for c in range(self.cfg.n_canvases):
-            if self.status[c] == WAITING and self.cfg.admit(c) == tick:
+            if running >= cap:
+                break
+            if self.status[c] == WAITING and self.cfg.admit(c) <= tick:
                 self._init_canvas(c, 0)
                 self.status[c] = ACTIVE
+                running += 1
 
     def active(self) -> np.ndarray:
         return np.nonzero(self.status == ACTIVE)[0].astype(np.int32)
