@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 denoise step: canvas positions denoised per second.
+
+One bench step is one tick of the whole hot path (RMSNorm -> tied LM head fused
+with softmax statistics and the Gumbel-max sample -> split-vocabulary combine ->
+entropy-bounded commit and uniform re-noise) over every active canvas, through
+the C ABI (dg_denoise_step).  Inputs are synthetic and seeded (``synth``):
+W_vocab ~ N(0, 0.02^2) in bf16 and, before every tick, the residual rows
+W[x_p] + N(0, 0.5^2) built on the device from the current canvas (the backbone
+stand-in, outside the timed kernels).
+
+Timing: CUDA events on the sampler's stream around the four kernels of each
+tick (device time); L2 is flushed by a 256 MB write before every timed tick,
+outside the events.  ``e2e`` repeats the metric through dg_denoise_step_host
+with the residual in pinned host memory: host->device copy, tick, and the
+device->host read of the canvas and entropies inside the host-clocked window.
+``roofline`` reports the LM-head kernel against the measured peaks;
+``cpu_baseline`` times the CPU oracle on a bounded sample of the same workload.
+
+``--impl reference`` times the CPU oracle as the reference arm (rank 0 only).
+Under torchrun each rank runs an independent replica (canvases seeded by rank);
+the timed region is bracketed by a barrier and the slowest rank's time counts.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "canvas positions denoised/sec (LM head+entropy+commit); % of bf16/HBM roofline"
+UNIT = "positions/s"
+L2_FLUSH_BYTES = 256 << 20
+
+# The workloads of the pages' sampler at the sizes this benchmark knows.  The
+# default is the single-canvas V=32768 case; the others are selectable.
+WORKLOADS = {
+    "canvas256_v32k": dict(vocab=32768, hidden=1024, canvas_len=256, n_canvases=1, steps=48,
+                           text="1 canvas x 256 positions, V=32768, d=1024, bf16 W_vocab N(0,0.02^2), hidden "
+                                "W[x_p]+N(0,0.5^2), 48 steps, T 0.8->0.4, entropy_bound 0.1, confidence 0.005"),
+    "canvas256_v262k": dict(vocab=262144, hidden=2816, canvas_len=256, n_canvases=1, steps=48,
+                            text="1 canvas x 256 positions, V=262144, d=2816 (model-scale LM head), same knobs"),
+    "tiny": dict(vocab=2048, hidden=128, canvas_len=16, n_canvases=1, steps=8,
+                 text="1 canvas x 16 positions, V=2048, d=128, 8 steps"),
+}
+SIGMA_HIDDEN = 0.5
+
+
+def kernel_source_digest() -> str:
+    """Digest of the LM-head kernel sources; a stored ncu traffic figure is valid only for this digest."""
+    h = hashlib.sha256()
+    for rel in ("uniform_state_discrete_gb300/csrc/dg_lmhead.cu", "uniform_state_discrete_gb300/csrc/dg_internal.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str):
+    """DRAM bytes per LM-head launch from the committed ncu summary, if it matches the current kernel."""
+    path = os.path.join(ROOT, "profiles", f"k_lmhead_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, out_path: str | None):
+        self.gpu = gpu_index
+        self.out_path = out_path
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        if self.out_path:
+            with open(self.out_path, "w") as f:
+                f.write(self.QUERY + "\n" + "\n".join(self.lines) + "\n")
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def oracle_positions_per_s(wl: dict, budget_s: float, seed_base: int, W16=None, max_ticks=None) -> dict:
+    """Time the CPU oracle, as it stands, on whole ticks of the workload until the budget is spent."""
+    import oracle
+    import synth
+    W16 = synth.wvocab(0, wl["vocab"], wl["hidden"]) if W16 is None else W16
+    cfg = oracle.OracleConfig(vocab=wl["vocab"], hidden=wl["hidden"], canvas_len=wl["canvas_len"],
+                              n_canvases=wl["n_canvases"], num_inference_steps=wl["steps"], gen_blocks=1 << 10,
+                              seeds=[seed_base + c for c in range(wl["n_canvases"])])
+    o = oracle.OracleSampler(cfg, W16)
+    fn = oracle.sampler.synth_resid_fn(cfg, W16, SIGMA_HIDDEN)
+    positions, busy, ticks = 0, 0.0, 0
+    while (ticks == 0 or busy < budget_s) and (max_ticks is None or ticks < max_ticks):
+        act = o.active()
+        r = fn(act, o.block[act], o.step_no[act], o.x[act])  # input generation is not timed
+        t0 = time.perf_counter()
+        o.tick(lambda *a: r)
+        busy += time.perf_counter() - t0
+        positions += act.size * wl["canvas_len"]
+        ticks += 1
+    return {"value": positions / busy, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{ticks} whole oracle ticks ({positions} positions) of the workload from tick 0, "
+                      f"fp64, OpenMP + BLAS on all cores; input generation untimed", "seconds": busy}
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    W16 = synth.wvocab(0, wl["vocab"], wl["hidden"])
+    # each bench step is one oracle tick restricted to a bounded sample of the canvas positions,
+    # sized so the whole --steps/--warmup run stays within a few minutes
+    probe = oracle_positions_per_s(wl, 0.0, 0, W16=W16, max_ticks=1)
+    per_pos = 1.0 / probe["value"]
+    budget = 120.0
+    n_pos = wl["canvas_len"] * wl["n_canvases"]
+    sample = max(1, min(n_pos, int(budget / max(1, args.steps + args.warmup) / per_pos)))
+    cfg = oracle.OracleConfig(vocab=wl["vocab"], hidden=wl["hidden"], canvas_len=wl["canvas_len"],
+                              n_canvases=wl["n_canvases"], num_inference_steps=wl["steps"], gen_blocks=1 << 10,
+                              seeds=list(range(wl["n_canvases"])))
+    o = oracle.OracleSampler(cfg, W16)
+    fn = oracle.sampler.synth_resid_fn(cfg, W16, SIGMA_HIDDEN)
+    rows = np.arange(sample)
+    busy = 0.0
+    for k in range(args.warmup + args.steps):
+        act = o.active()
+        r = fn(act, o.block[act], o.step_no[act], o.x[act])[rows]
+        s = int(o.step_no[act[0]])
+        t0 = time.perf_counter()
+        h = oracle.rmsnorm_bf16(r, cfg.rms_eps)
+        z = oracle.logits(h, W16)
+        T = oracle.temperature(s, cfg.num_inference_steps, cfg.t_min, cfg.t_max)
+        st = oracle.stats(z, T, cfg.seed(int(act[0])), int(o.block[act[0]]), s, rows)
+        oracle.sampler.entropy_bounded_accept(st["H"], range(sample), cfg.entropy_bound)
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            busy += dt
+        o.step_no[act] = (o.step_no[act] + 1) % cfg.num_inference_steps
+    value = sample * args.steps / busy
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * busy / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "description": wl["text"]},
+            "cpu_baseline": {"kind": "oracle", "cores": oracle.threads(), "value": value, "unit": UNIT,
+                             "sample": f"each step: {sample} of {n_pos} positions of one tick (RMSNorm, fp64 LM head, "
+                                       f"softmax statistics, Gumbel sample, acceptance), oracle as it stands"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_ours(args, wl, world, rank, local):
+    import torch
+    import synth
+    import uniform_state_discrete_gb300 as dg
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    V, d, L, B, N = wl["vocab"], wl["hidden"], wl["canvas_len"], wl["n_canvases"], wl["steps"]
+    W16 = synth.wvocab(0, V, d)
+    w_dev = torch.from_numpy(W16.view(np.int16)).to(dev).view(torch.bfloat16)
+    total_ticks = args.warmup + args.steps + args.e2e_steps
+    blocks = total_ticks // N + 2
+    seeds = [rank * B + c for c in range(B)]
+    cfg = dg.make_config(V, d, L, n_canvases=B, gen_blocks=blocks, num_inference_steps=N, seeds=seeds)
+    s = dg.Sampler(cfg, w_dev, stream=stream)
+    resid = torch.empty(B, L, d, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    slots_ptr = s.slots_ptr()
+    canvas_ptr = s.canvas().data_ptr()
+
+    def make_resid():
+        synth.resid_device(w_dev.data_ptr(), canvas_ptr, slots_ptr, B, L, d, SIGMA_HIDDEN, resid.data_ptr(),
+                           stream.cuda_stream)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for e5 in ev:  # torch creates the CUDA event on first record
+        for e in e5:
+            e.record(stream)
+    for _ in range(args.warmup):
+        make_resid()
+        flush.zero_()
+        s.step(resid)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
+        os.path.join(ROOT, "gpurun_out")) else None)
+    clocks.start()
+    time.sleep(0.3)
+    t_wall0 = time.perf_counter()
+    for k in range(args.steps):
+        make_resid()
+        flush.zero_()
+        s.set_timing_events(ev[k])
+        s.step(resid)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    s.set_timing_events(None)
+    info = s.sync_info()  # also surfaces a latched device fault
+
+    per_kernel = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in ev])  # ms, [K, 4]
+    tick_ms = np.array([e[0].elapsed_time(e[4]) for e in ev])
+    device_s = float(tick_ms.sum()) / 1e3
+    positions_per_tick = B * L
+    max_s = reduce_max(device_s, world)
+    value = positions_per_tick * args.steps * world / max_s
+
+    # roofline of the LM-head kernel (K2)
+    peaks = measured_peaks()
+    k2_s = float(per_kernel[:, 1].mean()) / 1e3
+    lay_chunks = math.ceil(math.ceil(V / 256) / math.ceil(math.ceil(V / 256) / min(math.ceil(V / 256), 76)))
+    n_sub = 2 * lay_chunks
+    P = positions_per_tick
+    alg_bytes = V * d * 2 + P * d * 2 + P * n_sub * 32
+    alg_flops = 2.0 * P * V * d
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg_flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": alg_bytes / k2_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": alg_flops / k2_s / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = stored_traffic(args.workload)
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "fallback"
+    roof["kernel"] = "k_lmhead"
+    roof["algorithmic_bytes_per_launch"] = alg_bytes
+    roof["algorithmic_flops_per_launch"] = alg_flops
+    roof["kernel_ms_mean"] = k2_s * 1e3
+    roof["tensor_frac"] = alg_flops / k2_s / 1e12 / peaks["bf16_tflops"]
+    roof["step_roofline_frac"] = max(t_hbm, t_tc) / (device_s / args.steps)
+
+    # e2e through the host-buffer entry point
+    e2e_steps = min(args.steps, args.e2e_steps)
+    host_resid = torch.empty(B, L, d, dtype=torch.float32).pin_memory()
+    hr = host_resid.numpy()
+    canvas_h = np.empty((B, L), np.int32)
+    e2e_s = 0.0
+    for k in range(e2e_steps):
+        info = s.sync_info()
+        act = np.nonzero(info["state"] == dg.ACTIVE)[0]
+        tok = s.canvas().cpu().numpy()
+        rows = synth.resid_rows(np.repeat(info["seed"][act], L), np.repeat(info["block"][act], L),
+                                np.repeat(info["step"][act], L), np.tile(np.arange(L), act.size),
+                                tok[act].reshape(-1), W16, SIGMA_HIDDEN)
+        hr[act] = rows.reshape(act.size, L, d)
+        t0 = time.perf_counter()
+        canvas_h, ent_h = s.step_host(hr)
+        e2e_s += time.perf_counter() - t0
+    e2e_max = reduce_max(e2e_s, world)
+    e2e = {"value": positions_per_tick * e2e_steps * world / e2e_max, "unit": UNIT,
+           "h2d_bytes_per_step": B * L * d * 4, "d2h_bytes_per_step": 2 * B * L * 4, "steps": e2e_steps,
+           "api": "dg_denoise_step_host"}
+
+    line = None
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": args.workload, "description": wl["text"],
+                           "positions_per_step": positions_per_tick,
+                           "l2": "flushed before every timed tick by a 256 MB device write (outside the events)",
+                           "parallelism": f"replicas x{world} (independent canvases per GPU)" if world > 1 else "1 GPU",
+                           "timing": "CUDA events around the 4 kernels of each tick on the sampler stream"},
+                "ms_per_kernel": {n: float(per_kernel[:, i].mean()) for i, n in
+                                  enumerate(("k_rmsnorm", "k_lmhead", "k_combine", "k_commit"))},
+                "tick_ms_p50": float(np.percentile(tick_ms, 50)), "tick_ms_p99": float(np.percentile(tick_ms, 99)),
+                "wall_s_timed_region": t_wall, "gpu_launches": args.steps * 5,
+                "gpu_launches_detail": "per step: 4 sampler kernels + 1 residual-generator kernel",
+                "roofline": roof, "e2e": e2e, "clocks": clk}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_positions_per_s(wl, args.cpu_budget, 0, W16=W16)
+        print(json.dumps(line), flush=True)
+    s.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="canvas256_v32k")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if world != args.gpus and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl, world, rank)
+    else:
+        run_ours(args, wl, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

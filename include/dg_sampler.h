@@ -174,6 +174,12 @@ const int32_t* dg_argmax(const dg_sampler* s);      /* argmax token from the las
 const int32_t* dg_tokens_out(const dg_sampler* s);  /* [B, gen_blocks, L] tokens of finished blocks   */
 const dg_slot* dg_slots(const dg_sampler* s);       /* [B] per-canvas state                           */
 
+/* Per-kernel timing: with events set (five cudaEvent_t created by the caller),
+ * every later tick records events[0] before the RMSNorm kernel and events[1..4]
+ * after the RMSNorm, LM-head, combine and commit kernels, on the sampler's
+ * stream.  NULL turns it off.  The events stay owned by the caller. */
+dg_status dg_set_timing_events(dg_sampler* s, void* const* events);
+
 /* Copy the per-canvas state to host memory (dg_slot [B]).  Synchronizing;
  * also reports a latched device fault. */
 dg_status dg_sync_info(dg_sampler* s, dg_slot* slots_host);

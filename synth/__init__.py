@@ -21,7 +21,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "libsynth.so")
+_SO_GPU = os.path.join(_BUILD, "libsynth_gpu.so")
 _lib = None
+_lib_gpu = None
 
 PURPOSE_W = 0
 PURPOSE_HIDDEN = 1
@@ -33,9 +35,41 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(src):
         os.makedirs(_BUILD, exist_ok=True)
         tmp = _SO + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", tmp, src, "-lm"], check=True)
+        subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-o", tmp, src, "-lm"], check=True)
         os.replace(tmp, _SO)
     return _SO
+
+
+def build_gpu(force: bool = False) -> str:
+    """Compile the device residual generator ``synth_gpu.cu`` (nvcc, sm_103a) into ``_build/libsynth_gpu.so``."""
+    src = os.path.join(_HERE, "synth_gpu.cu")
+    hdr = os.path.join(os.path.dirname(_HERE), "include", "dg_sampler.h")
+    if force or not os.path.exists(_SO_GPU) or os.path.getmtime(_SO_GPU) < max(os.path.getmtime(src),
+                                                                                   os.path.getmtime(hdr)):
+        os.makedirs(_BUILD, exist_ok=True)
+        tmp = _SO_GPU + f".tmp{os.getpid()}"
+        nvcc = os.environ.get("NVCC") or "/usr/local/cuda/bin/nvcc"
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-Xcompiler", "-fPIC",
+                        "-Xcompiler", "-ffp-contract=off", "-I", os.path.dirname(hdr), "-shared", "-o", tmp, src],
+                       check=True)
+        os.replace(tmp, _SO_GPU)
+    return _SO_GPU
+
+
+def resid_device(w_bf16_ptr: int, tokens_ptr: int, slots_ptr: int, B: int, L: int, d: int, sigma: float,
+                 out_ptr: int, stream_ptr: int) -> None:
+    """Device residual rows for every active canvas (same definition as ``resid_rows``), enqueued on a stream."""
+    global _lib_gpu
+    if _lib_gpu is None:
+        lib = ctypes.CDLL(build_gpu())
+        lib.synth_resid_device.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_double,
+                                                                                          ctypes.c_void_p,
+                                                                                          ctypes.c_void_p]
+        lib.synth_resid_device.restype = ctypes.c_int
+        _lib_gpu = lib
+    rc = _lib_gpu.synth_resid_device(w_bf16_ptr, tokens_ptr, slots_ptr, B, L, d, sigma, out_ptr, stream_ptr)
+    if rc != 0:
+        raise RuntimeError(f"synth_resid_device failed with CUDA error {rc}")
 
 
 def _load():

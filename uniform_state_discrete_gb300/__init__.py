@@ -79,6 +79,7 @@ _SIGS = {
     "dg_tokens_out": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_slots": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_sync_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "dg_set_timing_events": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "dg_get_state": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(dg_state)]),
     "dg_set_state": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(dg_state)]),
     "dg_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -190,6 +191,20 @@ class Sampler:
                           else None, ctypes.c_void_p(tokens.ctypes.data), ctypes.c_void_p(slots.ctypes.data)),
                self.handle)
         return tokens, slots
+
+    def set_timing_events(self, events):
+        """Five torch.cuda.Event(enable_timing=True) recorded around K1..K4 of every tick, or None."""
+        if events is None:
+            _check(lib.dg_set_timing_events(self.handle, None), self.handle)
+            self._timing = None
+            return
+        assert len(events) == 5
+        for e in events:
+            if not e.cuda_event:  # torch creates the CUDA event lazily, on first record
+                e.record(self.stream)
+        arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        self._timing = (events, arr)
+        _check(lib.dg_set_timing_events(self.handle, arr), self.handle)
 
     def sync_info(self) -> np.ndarray:
         slots = np.empty(self.B, SLOT_DTYPE)

@@ -26,6 +26,8 @@ struct dg_sampler {
   int64_t tick_bound;
   void* ws;
   size_t ws_bytes;
+  cudaEvent_t timing[5];
+  bool timed;
   char err[512];
 };
 
@@ -180,10 +182,16 @@ dg_status tick(dg_sampler* s, const float* resid) {
     set_err(s->err, "every canvas has finished (tick %lld)", (long long)s->host_tick);
     return DG_ERR_STATE;
   }
+  auto mark = [&](int i) { return s->timed ? cudaEventRecord(s->timing[i], s->stream) : cudaSuccess; };
+  DG_CUDA(s->err, mark(0), "record timing event");
   DG_CUDA(s->err, dg::launch_rmsnorm(s->dv, resid, s->stream), "launch rmsnorm");
+  DG_CUDA(s->err, mark(1), "record timing event");
   DG_CUDA(s->err, dg::launch_lmhead(s->dv, &s->tmA, &s->tmB, s->num_sms, s->stream), "launch lm head");
+  DG_CUDA(s->err, mark(2), "record timing event");
   DG_CUDA(s->err, dg::launch_combine(s->dv, s->stream), "launch combine");
+  DG_CUDA(s->err, mark(3), "record timing event");
   DG_CUDA(s->err, dg::launch_commit(s->dv, s->stream), "launch commit");
+  DG_CUDA(s->err, mark(4), "record timing event");
   ++s->host_tick;
   return DG_OK;
 }
@@ -341,6 +349,17 @@ dg_status dg_denoise_step_host(dg_sampler* s, const float* resid_host, int32_t* 
     DG_CUDA(s->err, cudaMemcpyAsync(entropy_host, s->dv.H, BL * 4, cudaMemcpyDeviceToHost, s->stream),
             "copy entropy");
   return check_device_error(s);
+}
+
+dg_status dg_set_timing_events(dg_sampler* s, void* const* events) {
+  if (!s) return DG_ERR_ARG;
+  s->timed = events != nullptr;
+  if (events)
+    for (int i = 0; i < 5; ++i) {
+      if (!events[i]) return s->timed = false, set_err(s->err, "timing event %d is NULL", i), DG_ERR_ARG;
+      s->timing[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+  return DG_OK;
 }
 
 dg_status dg_sync_info(dg_sampler* s, dg_slot* slots_host) {
