@@ -258,12 +258,13 @@ def run_ours(args, wl, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev)  # a capturable (non-default) stream owns the sampler's work
 
     V, d, L, B, N = wl["vocab"], wl["hidden"], wl["canvas_len"], wl["n_canvases"], wl["steps"]
     W16 = synth.wvocab(0, V, d)
     w_dev = torch.from_numpy(W16.view(np.int16)).to(dev).view(torch.bfloat16)
-    total_ticks = args.warmup + args.steps + args.e2e_steps
+    torch.cuda.synchronize(dev)
+    total_ticks = args.warmup + args.steps + args.kernel_steps + args.e2e_steps + 2
     blocks = total_ticks // N + 2
     seeds = [rank * B + c for c in range(B)]
     cfg = dg.make_config(V, d, L, n_canvases=B, gen_blocks=blocks, num_inference_steps=N, seeds=seeds)
@@ -277,37 +278,75 @@ def run_ours(args, wl, world, rank, local):
         synth.resid_device(w_dev.data_ptr(), canvas_ptr, slots_ptr, B, L, d, SIGMA_HIDDEN, resid.data_ptr(),
                            stream.cuda_stream)
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    for e5 in ev:  # torch creates the CUDA event on first record
-        for e in e5:
-            e.record(stream)
-    for _ in range(args.warmup):
-        make_resid()
-        flush.zero_()
-        s.step(resid)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
-        os.path.join(ROOT, "gpurun_out")) else None)
-    clocks.start()
-    time.sleep(0.3)
-    t_wall0 = time.perf_counter()
-    for k in range(args.steps):
-        make_resid()
-        flush.zero_()
-        s.set_timing_events(ev[k])
-        s.step(resid)
-    torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter() - t_wall0
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-    s.set_timing_events(None)
-    info = s.sync_info()  # also surfaces a latched device fault
+    def flush_l2():
+        # write a buffer twice the L2, then read it back, so L2 holds only clean lines of the
+        # flush buffer: the timed tick starts cold and pays no write-back of the flush
+        flush.fill_(1)
+        if args.flush == "writeread":
+            flush.sum(dtype=torch.int32)
 
-    per_kernel = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in ev])  # ms, [K, 4]
-    tick_ms = np.array([e[0].elapsed_time(e[4]) for e in ev])
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    t_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for e in ev + t_ev:  # torch creates the CUDA event on first record
+        e.record(stream)
+
+    def capture(timed_kernels: bool):
+        s.set_timing_events(ev if timed_kernels else None)
+        make_resid()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            s.step(resid)
+        return g
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            make_resid()
+            flush_l2()
+            s.step(resid)
+        graph = capture(False) if args.graph else None
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
+            os.path.join(ROOT, "gpurun_out")) else None)
+        clocks.start()
+        time.sleep(0.3)
+        # timed region: whole ticks only, so nothing separates the kernels of a tick
+        tick_ms = np.zeros(args.steps)
+        t_wall0 = time.perf_counter()
+        for k in range(args.steps):
+            make_resid()
+            flush_l2()
+            t_ev[0].record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                s.step(resid)
+            t_ev[1].record(stream)
+            t_ev[1].synchronize()
+            tick_ms[k] = t_ev[0].elapsed_time(t_ev[1])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        # per-kernel pass: the same ticks with events between the four kernels (which
+        # serialise them); its K2 mean is the roofline's launch duration
+        kgraph = capture(True) if args.graph else None
+        if kgraph is None:
+            s.set_timing_events(ev)
+        per_kernel = np.zeros((args.kernel_steps, 4))
+        for k in range(args.kernel_steps):
+            make_resid()
+            flush_l2()
+            if kgraph is not None:
+                kgraph.replay()
+            else:
+                s.step(resid)
+            ev[4].synchronize()
+            per_kernel[k] = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
+        s.set_timing_events(None)
+    info = s.sync_info()  # also surfaces a latched device fault
     device_s = float(tick_ms.sum()) / 1e3
     positions_per_tick = B * L
     max_s = reduce_max(device_s, world)
@@ -317,7 +356,7 @@ def run_ours(args, wl, world, rank, local):
     peaks = measured_peaks()
     k2_s = float(per_kernel[:, 1].mean()) / 1e3
     lay_chunks = math.ceil(math.ceil(V / 256) / math.ceil(math.ceil(V / 256) / min(math.ceil(V / 256), 76)))
-    n_sub = 2 * lay_chunks
+    n_sub = 4 * lay_chunks  # partial records per position: 4 column groups per vocabulary chunk
     P = positions_per_tick
     alg_bytes = V * d * 2 + P * d * 2 + P * n_sub * 32
     alg_flops = 2.0 * P * V * d
@@ -367,12 +406,16 @@ def run_ours(args, wl, world, rank, local):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": args.workload, "description": wl["text"],
                            "positions_per_step": positions_per_tick,
-                           "l2": "flushed before every timed tick by a 256 MB device write (outside the events)",
+                           "l2": "flushed before every timed tick: 256 MB device write, then read back (outside the "
+                                 "events)" if args.flush == "writeread" else "flushed by a 256 MB write",
+                           "graph": bool(args.graph),
                            "parallelism": f"replicas x{world} (independent canvases per GPU)" if world > 1 else "1 GPU",
-                           "timing": "CUDA events around the 4 kernels of each tick on the sampler stream"},
+                           "timing": "CUDA events around each whole tick on the sampler stream (timed region); "
+                                     "a second pass with events between the 4 kernels gives ms_per_kernel"},
                 "ms_per_kernel": {n: float(per_kernel[:, i].mean()) for i, n in
                                   enumerate(("k_rmsnorm", "k_lmhead", "k_combine", "k_commit"))},
                 "tick_ms_p50": float(np.percentile(tick_ms, 50)), "tick_ms_p99": float(np.percentile(tick_ms, 99)),
+                "kernel_pass_steps": args.kernel_steps,
                 "wall_s_timed_region": t_wall, "gpu_launches": args.steps * 5,
                 "gpu_launches_detail": "per step: 4 sampler kernels + 1 residual-generator kernel",
                 "roofline": roof, "e2e": e2e, "clocks": clk}
@@ -396,6 +439,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flush", choices=["write", "writeread"], default="writeread")
+    ap.add_argument("--graph", type=int, default=1, help="replay each tick as a captured CUDA graph")
+    ap.add_argument("--kernel-steps", type=int, default=200, help="ticks of the per-kernel timing pass")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

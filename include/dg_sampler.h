@@ -173,11 +173,15 @@ const int32_t* dg_sample(const dg_sampler* s);      /* sampled token from the la
 const int32_t* dg_argmax(const dg_sampler* s);      /* argmax token from the last tick                */
 const int32_t* dg_tokens_out(const dg_sampler* s);  /* [B, gen_blocks, L] tokens of finished blocks   */
 const dg_slot* dg_slots(const dg_sampler* s);       /* [B] per-canvas state                           */
+/* bf16 [rows, d] normalised hidden rows of the last tick (the LM head's input), one row per
+ * position of the active canvases in canvas order (active canvas a, position p -> row a*L + p). */
+const uint16_t* dg_normed(const dg_sampler* s);
 
 /* Per-kernel timing: with events set (five cudaEvent_t created by the caller),
  * every later tick records events[0] before the RMSNorm kernel and events[1..4]
  * after the RMSNorm, LM-head, combine and commit kernels, on the sampler's
- * stream.  NULL turns it off.  The events stay owned by the caller. */
+ * stream (as external event nodes when the tick is being captured into a CUDA
+ * graph).  NULL turns it off.  The events stay owned by the caller. */
 dg_status dg_set_timing_events(dg_sampler* s, void* const* events);
 
 /* Copy the per-canvas state to host memory (dg_slot [B]).  Synchronizing;

@@ -118,6 +118,12 @@ def wvocab(seed: int, V: int, d: int, sigma_w: float = 0.02, want_f32: bool = Fa
     return (w16, w32) if want_f32 else w16
 
 
+def norm_weight(seed: int, d: int, spread: float = 0.1) -> np.ndarray:
+    """An RMSNorm weight vector [d] in fp32: 1 + spread * N(0,1), drawn from the W stream of ``seed``."""
+    _, w32 = wvocab(seed, 1, d, sigma_w=spread, want_f32=True)
+    return (np.float32(1.0) + w32[0]).astype(np.float32)
+
+
 def resid_rows(seeds, block, step, pos, tok, w_bf16: np.ndarray, sigma: float, nthreads: int = 0) -> np.ndarray:
     """Residual rows r[i, :] = W[tok[i]] + sigma * N(0,1) noise keyed by (seed, block, step, pos)."""
     seeds = np.ascontiguousarray(np.asarray(seeds, dtype=np.uint64))

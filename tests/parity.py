@@ -54,6 +54,7 @@ class Case:
     seeds: tuple = None
     admit: tuple = None
     max_active: int = 0
+    norm_seed: int = None  # RMSNorm weight from synth.norm_weight, or all ones
 
     def oracle_cfg(self) -> OracleConfig:
         return OracleConfig(vocab=self.vocab, hidden=self.hidden, canvas_len=self.canvas_len,
@@ -76,6 +77,10 @@ class Case:
 
 def weights(case: Case) -> np.ndarray:
     return synth.wvocab(case.w_seed, case.vocab, case.hidden, sigma_w=case.sigma_w)
+
+
+def norm_w(case: Case):
+    return None if case.norm_seed is None else synth.norm_weight(case.norm_seed, case.hidden)
 
 
 def resid_slots(case: Case, ocfg: OracleConfig, W: np.ndarray, canvases, blocks, steps, tokens) -> np.ndarray:
@@ -128,10 +133,11 @@ def teacher_forced(case: Case, ticks: int = 1 << 30, gpu=None, W=None, check_eve
     import uniform_state_discrete_gb300 as dg
     W = weights(case) if W is None else W
     ocfg = case.oracle_cfg()
-    o = OracleSampler(ocfg, W)
+    nw = norm_w(case)
+    o = OracleSampler(ocfg, W, norm_w=nw)
     dev = torch.device("cuda:0")
     w_dev = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
-    s = gpu or dg.Sampler(case.gpu_cfg(), w_dev)
+    s = gpu or dg.Sampler(case.gpu_cfg(), w_dev, norm_w=None if nw is None else torch.from_numpy(nw).to(dev))
     rep = Report()
     L = case.canvas_len
     t = 0

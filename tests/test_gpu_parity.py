@@ -41,6 +41,36 @@ def test_ragged_shapes_and_staggered_admission():
     _assert_report(teacher_forced(case), "ragged")
 
 
+def test_rmsnorm_weight_vector():
+    """A non-trivial RMSNorm weight w (the pages' rms(x, w) with w != 1)."""
+    case = Case(vocab=4096, hidden=512, canvas_len=64, steps=4, norm_seed=17, seeds=(2,))
+    rep = teacher_forced(case)
+    _assert_report(rep, "norm-weight")
+
+
+@pytest.mark.parametrize("hidden,norm_seed,sigma", [(1024, None, 0.5), (2816, 5, 0.5), (200, None, 2.0),
+                                                    (512, 7, 1e-3)])
+def test_rmsnorm_bf16_bit_exact(hidden, norm_seed, sigma):
+    """K1's bf16 rows equal the oracle's RMSNorm bit for bit (both round the exact quotient)."""
+    import torch
+    import uniform_state_discrete_gb300 as dg
+    from parity import norm_w
+    case = Case(vocab=1024, hidden=hidden, canvas_len=96, n_canvases=3, steps=4, sigma=sigma, norm_seed=norm_seed)
+    W = weights(case)
+    ocfg = case.oracle_cfg()
+    nw = norm_w(case)
+    o = oracle.OracleSampler(ocfg, W, norm_w=nw)
+    dev = torch.device("cuda:0")
+    s = dg.Sampler(case.gpu_cfg(), torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16),
+                   norm_w=None if nw is None else torch.from_numpy(nw).to(dev))
+    act = o.active()
+    resid = resid_slots(case, ocfg, W, act, o.block[act], o.step_no[act], o.x[act])
+    s.step(torch.from_numpy(resid).to(dev))
+    got = s.normed(act.size * case.canvas_len).cpu().numpy().view(np.uint16)
+    want = oracle.rmsnorm_bf16(resid[act].reshape(-1, hidden), ocfg.rms_eps, nw)
+    assert np.array_equal(got, want), f"{int((got != want).sum())} of {got.size} bf16 values differ"
+
+
 def test_single_position_canvases_capacity_limited():
     case = Case(vocab=4096, hidden=64, canvas_len=1, n_canvases=5, steps=4, admit=(0, 0, 1, 1, 1), max_active=2)
     _assert_report(teacher_forced(case), "L1")

@@ -78,6 +78,7 @@ _SIGS = {
     "dg_argmax": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_tokens_out": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_slots": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_normed": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_sync_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "dg_set_timing_events": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "dg_get_state": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(dg_state)]),
@@ -269,6 +270,11 @@ class Sampler:
     def tokens_out(self):
         import torch
         return self._view("dg_tokens_out", torch.int32, (self.B, self.G, self.L))
+
+    def normed(self, n_rows: int):
+        """bf16 bit patterns (int16) of the first n_rows normalised hidden rows of the last tick."""
+        import torch
+        return self._view("dg_normed", torch.int16, (n_rows, self.d))
 
     def slots_ptr(self) -> int:
         return int(lib.dg_slots(self.handle))

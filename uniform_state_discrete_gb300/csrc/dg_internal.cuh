@@ -21,14 +21,16 @@ constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kStageA = kBM * kBK * 2;  // 16 KB
 constexpr int kStageB = kBN * kBK * 2;  // 32 KB
-constexpr int kEpiWarps = 8;            // two per TMEM lane quadrant, each owning 128 of the 256 columns
+constexpr int kEpiWarps = 16;           // four per TMEM lane quadrant, each owning 64 of the 256 columns
 constexpr int kThreadsLM = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 2 * kBN;      // double-buffered accumulator
 // The vocabulary is cut into this many chunks (fewer when V is small),
 // independent of how many canvases are active, so a position's statistics do
 // not depend on the batch it runs in.
 constexpr int kChunkTarget = 76;
-constexpr int kSubPerChunk = 2;         // one partial record per column half
+constexpr int kColGroups = kEpiWarps / 4;
+constexpr int kColsPerWarp = kBN / kColGroups;  // 64
+constexpr int kSubPerChunk = kColGroups;        // one partial record per column group
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after 1 s
 
@@ -86,11 +88,10 @@ struct Dev {
 __device__ __forceinline__ uint4 philox(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;  // one 32x32->64 multiply each
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ (k0 + (uint32_t)r * 0x9E3779B9u), (uint32_t)p1,
+                   (uint32_t)(p0 >> 32) ^ c.w ^ (k1 + (uint32_t)r * 0xBB67AE85u), (uint32_t)p0);
   }
   return c;
 }
@@ -125,6 +126,14 @@ __device__ __forceinline__ float lg2_approx(float x) {
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor in the stream still runs;
+// pdl_wait() blocks until that predecessor has completed and its memory is
+// visible (it returns at once when there is none), pdl_allow_next() lets the
+// successor begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Merge two partial records (base-2 units).  Ties keep the lower vocabulary index.
 __device__ __forceinline__ Partial merge_partial(const Partial& a, const Partial& b) {

@@ -3,51 +3,50 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <utility>
+
 #include "dg_internal.cuh"
 
 namespace dg {
 namespace {
 
-// Round a double to the nearest bfloat16, ties to even, from its bit pattern:
-// keep the top 7 fraction bits and round on the 45 bits below (normal range),
-// or on the bits below the 2^-133 quantum (subnormal range).
-__device__ __forceinline__ uint16_t bf16_rne(double x) {
-  const uint64_t b = (uint64_t)__double_as_longlong(x);
-  const uint32_t sign = (uint32_t)(b >> 63) << 15;
-  const int e = (int)((b >> 52) & 0x7FF);
-  const uint64_t frac = b & 0xFFFFFFFFFFFFFull;
-  if (e == 0x7FF) return (uint16_t)(sign | (frac ? 0x7FC0u : 0x7F80u));
-  if (e == 0) return (uint16_t)sign;  // zero or a double subnormal (far below the bf16 range)
-  int E = e - 1023 + 127;
-  if (E >= 1) {
-    uint32_t m7 = (uint32_t)(frac >> 45);
-    const uint64_t rem = frac & ((1ull << 45) - 1);
-    const uint64_t halfway = 1ull << 44;
-    if (rem > halfway || (rem == halfway && (m7 & 1u))) {
-      if (++m7 == 128u) {
-        m7 = 0;
-        ++E;
-      }
-    }
-    if (E >= 255) return (uint16_t)(sign | 0x7F80u);
-    return (uint16_t)(sign | ((uint32_t)E << 7) | m7);
-  }
-  // value = sig * 2^(e-1075); in quanta of 2^-133 that is sig >> (942 - e)
-  const uint64_t sig = frac | (1ull << 52);
-  const int shift = 942 - e;
-  if (shift >= 64) return (uint16_t)sign;
-  uint64_t m = sig >> shift;
-  const uint64_t rem = sig & ((1ull << shift) - 1);
-  const uint64_t halfway = 1ull << (shift - 1);
-  if (rem > halfway || (rem == halfway && (m & 1ull))) ++m;
-  return (uint16_t)(sign | (uint32_t)m);  // m == 128 rolls into the smallest normal
+// ------------------------------------------------------------------- K1
+// Error-free transformations in fp32 (the fp64 pipe of this part is slow):
+// Knuth's TwoSum gives a + b = s + e exactly; an FMA gives x*y = p + e exactly
+// (Dekker's product).  Carried as unevaluated pairs (hi, lo) they hold the sum
+// of squares and the scaled value to ~2^-46 relative accuracy.  __f*_rn
+// intrinsics keep the compiler from contracting the steps into other FMAs.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float z = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
 }
 
-// ------------------------------------------------------------------- K1
+// bf16 nearest-even of the exact value hi + lo, where hi = fl(hi + lo) (so
+// |lo| <= half an fp32 ulp of hi): hi's own rounding decides unless hi sits
+// exactly on a bf16 midpoint, where the sign of lo decides and 0 means a tie.
+__device__ __forceinline__ uint32_t bf16_rne_pair(float hi, float lo) {
+  const uint32_t b = __float_as_uint(hi);
+  const uint32_t rem = b & 0xFFFFu;
+  uint32_t up;
+  if (rem != 0x8000u) {
+    up = rem > 0x8000u ? 1u : 0u;
+  } else if (lo == 0.f) {
+    up = (b >> 16) & 1u;
+  } else {
+    up = ((lo > 0.f) == (hi > 0.f)) ? 1u : 0u;  // lo moves |value| above the midpoint
+  }
+  return (b >> 16) + up;
+}
+
 // h = bf16( w * r * sqrt(d) / (||r||_2 + eps) ) per active row, one warp per
-// row.  The norm and the scaling are carried in fp64 so the bf16 rounding of
-// every element is the one the exact quotient gives.
+// row.  The rounding of every element is the one the exact quotient gives
+// (up to ~2^-46 relative): sum of squares in TwoSum pairs, the per-row
+// scale sqrt(d) / (norm + eps) in fp64 (two operations per row), split into
+// an fp32 pair, and each product carried exactly before the bf16 rounding.
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ resid, const Dev dv) {
+  pdl_wait();
+  pdl_allow_next();
   const int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   const int n_rows = dv.plan->n_active * dv.L;
@@ -56,30 +55,50 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ resid
   const int c = dv.active[a];
   const float4* r4 = reinterpret_cast<const float4*>(resid + ((size_t)c * dv.L + p) * dv.d);
   const int n4 = dv.d >> 2;
-  double ss = 0.0;
+  float sh = 0.f, sl = 0.f;
   for (int i = lane; i < n4; i += 32) {
     const float4 v = __ldg(r4 + i);
-    ss = fma((double)v.x, (double)v.x, ss);
-    ss = fma((double)v.y, (double)v.y, ss);
-    ss = fma((double)v.z, (double)v.z, ss);
-    ss = fma((double)v.w, (double)v.w, ss);
+    const float xs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float sq = __fmul_rn(xs[j], xs[j]);
+      const float sq_err = fmaf(xs[j], xs[j], -sq);
+      float e;
+      two_sum(sh, sq, sh, e);
+      sl = __fadd_rn(sl, __fadd_rn(e, sq_err));
+    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-  const double inv = sqrt((double)dv.d) / (sqrt(ss) + (double)dv.eps);
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xFFFFFFFFu, sh, o);
+    const float ol = __shfl_xor_sync(0xFFFFFFFFu, sl, o);
+    float e;
+    two_sum(sh, oh, sh, e);
+    sl = __fadd_rn(__fadd_rn(sl, ol), e);
+  }
+  const double inv = sqrt((double)dv.d) / (sqrt((double)sh + (double)sl) + (double)dv.eps);
+  const float inv_hi = __double2float_rn(inv);
+  const float inv_lo = __double2float_rn(inv - (double)inv_hi);
   uint2* out = reinterpret_cast<uint2*>(dv.h + (size_t)row * dv.d);
+  const float4* w4 = reinterpret_cast<const float4*>(dv.norm_w);
   for (int i = lane; i < n4; i += 32) {
     const float4 v = __ldg(r4 + i);
-    double w0 = 1.0, w1 = 1.0, w2 = 1.0, w3 = 1.0;
-    if (dv.norm_w) {
-      w0 = dv.norm_w[4 * i];
-      w1 = dv.norm_w[4 * i + 1];
-      w2 = dv.norm_w[4 * i + 2];
-      w3 = dv.norm_w[4 * i + 3];
+    const float4 w = w4 ? __ldg(w4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
+    const float xs[4] = {v.x, v.y, v.z, v.w};
+    const float ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t hb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float xw = __fmul_rn(ws[j], xs[j]);            // w x = xw + xw_err exactly
+      const float xw_err = fmaf(ws[j], xs[j], -xw);
+      const float ph = __fmul_rn(xw, inv_hi);               // (w x) inv ~= ph + pl
+      const float pe = fmaf(xw, inv_hi, -ph);
+      const float pl = fmaf(xw, inv_lo, fmaf(xw_err, inv_hi, pe));
+      const float hi = __fadd_rn(ph, pl);                   // renormalise: |lo| <= ulp(hi)/2
+      const float lo = __fsub_rn(pl, __fsub_rn(hi, ph));
+      hb[j] = bf16_rne_pair(hi, lo) & 0xFFFFu;
     }
-    const uint32_t h0 = bf16_rne(w0 * (double)v.x * inv), h1 = bf16_rne(w1 * (double)v.y * inv);
-    const uint32_t h2 = bf16_rne(w2 * (double)v.z * inv), h3 = bf16_rne(w3 * (double)v.w * inv);
-    out[i] = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
+    out[i] = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
   }
 }
 
@@ -101,6 +120,8 @@ __device__ __forceinline__ Partial shfl_partial(const Partial& a, int o) {
 // the sample is the index of the largest perturbed score, the argmax the index
 // of the largest logit.  One warp per position.
 __global__ void __launch_bounds__(256) k_combine(const Dev dv) {
+  pdl_wait();
+  pdl_allow_next();
   const int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   const int n_rows = dv.plan->n_active * dv.L;
@@ -117,7 +138,7 @@ __global__ void __launch_bounds__(256) k_combine(const Dev dv) {
     const float H = 0.69314718055994531f * (l2S - acc.A / acc.S);
     const float lz = 0.69314718055994531f * (acc.m + l2S);
     const size_t o = (size_t)c * dv.L + p;
-    dv.H[o] = fmaxf(H, 0.f);
+    dv.H[o] = H > 0.f ? H : 0.f;  // +0 for rounding below zero (and never -0: its bits would sort last)
     dv.logZ[o] = lz;
     dv.y[o] = acc.gidx;
     dv.amax[o] = acc.amax;
@@ -190,34 +211,85 @@ __device__ void plan_tick(const Dev& dv, int tick) {
   __syncthreads();
 }
 
-__device__ __forceinline__ double block_sum_double(double v, double* scratch) {
+// Block-wide helpers for the commit kernel (blockDim.x = kCommitThreads).
+__device__ __forceinline__ float block_sum_f32(float v, float* scratch) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
   if (lane == 0) scratch[w] = v;
   __syncthreads();
-  double t = 0.0;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += scratch[i];
-    scratch[32] = t;
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < kCommitThreads / 32; ++i) t += scratch[i];
+  return t;
+}
+
+__device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v, unsigned long long* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = w < v ? w : v;
   }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
-  return scratch[32];
+  if (lane == 0) scratch[w] = v;
+  __syncthreads();
+  unsigned long long t = ~0ull;
+#pragma unroll
+  for (int i = 0; i < kCommitThreads / 32; ++i) t = scratch[i] < t ? scratch[i] : t;
+  return t;
+}
+
+// Sort 32 keys held one per lane, ascending (bitonic network over shuffles).
+__device__ __forceinline__ unsigned long long warp_sort_u64(unsigned long long key) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, key, stride);
+      const bool keep_min = ((lane & stride) == 0) == ((lane & size) == 0);
+      key = keep_min ? (other < key ? other : key) : (other > key ? other : key);
+    }
+  }
+  return key;
+}
+
+// Accepted entries among `n` ascending keys (H bits << 32 | p): the walk sums
+// the entropies in fp64, in order; entry j is accepted while the sum of the
+// entries before it is <= bound.  fp64 sums of non-negative terms never
+// decrease, so the first refusal ends the walk.
+__device__ __forceinline__ int accept_walk(const unsigned long long* keys, int n, float bound) {
+  double E = 0.0;
+  int k = 0;
+  for (int j = 0; j < n; ++j) {
+    if (keys[j] == ~0ull || !(E <= (double)bound)) break;
+    ++k;
+    E += (double)__uint_as_float((unsigned)(keys[j] >> 32));
+  }
+  return k;
 }
 
 // One CTA per active canvas:
 //  (i)   early stop: s >= 1, mean_p H < confidence and argmax == previous argmax at every p;
-//  (ii)  otherwise sort the uncommitted positions by (H, p) and accept the prefix whose
-//        exclusive entropy sums (fp64) stay <= entropy_bound; accepted take the sample;
+//  (ii)  otherwise order the uncommitted positions by (H, p) and accept the prefix whose
+//        exclusive entropy sums stay <= entropy_bound; accepted positions take their sample;
 //  (iii) on early stop or at s = N-1 every uncommitted position takes its sample and the
 //        block ends (tokens copied out, next block or done);
 //  (iv)  every other uncommitted position is re-noised to a uniform token.
+// Only entries whose entropy is <= bound, plus the smallest one above it, can be
+// accepted, so the common case sorts at most 32 candidates in one warp; more than
+// 31 entropies within the bound fall back to a bitonic sort of the canvas.
 // The CTA that finishes last plans the next tick.
 __global__ void __launch_bounds__(kCommitThreads) k_commit(const Dev dv) {
   __shared__ unsigned long long keys[kMaxL];
-  __shared__ double red[33];
-  __shared__ int s_k;
+  __shared__ float redf[kCommitThreads / 32];
+  __shared__ unsigned long long redk[kCommitThreads / 32];
+  __shared__ unsigned long long cand[32];
+  __shared__ int s_cnt, s_k;
+  pdl_wait();
+  pdl_allow_next();
   const int n_active = dv.plan->n_active;
   const int a = blockIdx.x;
   const int L = dv.L;
@@ -227,64 +299,82 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(const Dev dv) {
     const dg_slot sl = dv.slots[c];
     const int s = sl.step, b = sl.block;
     const size_t base = (size_t)c * L;
+    const float bound = dv.bound;
 
-    // (i) early-stop test
-    double hsum = 0.0;
+    // (i) early-stop test, and the keys of the uncommitted positions
+    float hsum = 0.f, n_le = 0.f;
     int stable = 1;
+    unsigned long long kmin_above = ~0ull;
     for (int p = threadIdx.x; p < L; p += blockDim.x) {
-      hsum += (double)dv.H[base + p];
+      const float H = dv.H[base + p];
+      hsum += H;
       stable &= (dv.amax[base + p] == dv.prev_amax[base + p]) ? 1 : 0;
+      if (!dv.committed[base + p]) {
+        const unsigned long long k = ((unsigned long long)__float_as_uint(H) << 32) | (unsigned)p;
+        if (H <= bound) n_le += 1.f;
+        else kmin_above = k < kmin_above ? k : kmin_above;
+      }
     }
-    const double mean_H = block_sum_double(hsum, red) / (double)L;
+    const float mean_H = block_sum_f32(hsum, redf) / (float)L;
+    const int count_le = (int)block_sum_f32(n_le, redf);
+    kmin_above = block_min_u64(kmin_above, redk);
     stable = __syncthreads_and(stable);
-    const bool converged = (s >= 1) && (mean_H < (double)dv.conf) && stable;
+    const bool converged = (s >= 1) && (mean_H < dv.conf) && stable;
     const bool final_step = converged || (s == dv.N - 1);
 
     int n_acc = 0;
     if (!final_step) {
-      // (ii) keys (H bits, p) for uncommitted positions, all-ones padding otherwise; H >= 0 so
-      // the float bit pattern orders like the value
-      int n2 = 1;
-      while (n2 < L) n2 <<= 1;
-      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-        unsigned long long k = ~0ull;
-        if (i < L && !dv.committed[base + i])
-          k = ((unsigned long long)__float_as_uint(dv.H[base + i]) << 32) | (unsigned)i;
-        keys[i] = k;
-      }
-      __syncthreads();
-      // bitonic sort, ascending
-      for (int size = 2; size <= n2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          for (int t = threadIdx.x; t < (n2 >> 1); t += blockDim.x) {
-            const int i = 2 * t - (t & (stride - 1));
-            const int j = i + stride;
-            const bool up = ((i & size) == 0);
-            const unsigned long long ki = keys[i], kj = keys[j];
-            if ((ki > kj) == up) {
-              keys[i] = kj;
-              keys[j] = ki;
+      // (ii) the accepted prefix of the (H, p) order
+      if (count_le < 32) {
+        if (threadIdx.x == 0) s_cnt = 0;
+        __syncthreads();
+        for (int p = threadIdx.x; p < L; p += blockDim.x) {
+          const float H = dv.H[base + p];
+          if (!dv.committed[base + p] && H <= bound)
+            cand[atomicAdd(&s_cnt, 1)] = ((unsigned long long)__float_as_uint(H) << 32) | (unsigned)p;
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+          const int lane = threadIdx.x;
+          unsigned long long k = lane < count_le ? cand[lane] : (lane == count_le ? kmin_above : ~0ull);
+          k = warp_sort_u64(k);
+          cand[lane] = k;
+          __syncwarp();
+          if (lane == 0) s_k = accept_walk(cand, 32, bound);
+        }
+        __syncthreads();
+        n_acc = s_k;
+        for (int j = threadIdx.x; j < n_acc; j += blockDim.x) keys[j] = cand[j];
+      } else {
+        int n2 = 1;
+        while (n2 < L) n2 <<= 1;
+        for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+          unsigned long long k = ~0ull;
+          if (i < L && !dv.committed[base + i])
+            k = ((unsigned long long)__float_as_uint(dv.H[base + i]) << 32) | (unsigned)i;
+          keys[i] = k;
+        }
+        __syncthreads();
+        for (int size = 2; size <= n2; size <<= 1) {
+          for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = threadIdx.x; t < (n2 >> 1); t += blockDim.x) {
+              const int i = 2 * t - (t & (stride - 1));
+              const int j = i + stride;
+              const bool up = ((i & size) == 0);
+              const unsigned long long ki = keys[i], kj = keys[j];
+              if ((ki > kj) == up) {
+                keys[i] = kj;
+                keys[j] = ki;
+              }
             }
+            __syncthreads();
           }
-          __syncthreads();
         }
-      }
-      // walk the sorted entries in order, summing their entropies in fp64: entry j is
-      // accepted while the sum of the entries before it is <= entropy_bound.  fp64
-      // sums of non-negative terms never decrease, so the first refusal ends the walk.
-      if (threadIdx.x == 0) {
-        double E = 0.0;
-        int k = 0;
-        for (int j = 0; j < n2; ++j) {
-          const unsigned long long kj = keys[j];
-          if (kj == ~0ull || !(E <= (double)dv.bound)) break;
-          ++k;
-          E += (double)__uint_as_float((unsigned)(kj >> 32));
-        }
-        s_k = k;
+        if (threadIdx.x == 0) s_k = accept_walk(keys, n2, bound);
+        __syncthreads();
+        n_acc = s_k;
       }
       __syncthreads();
-      n_acc = s_k;
       for (int j = threadIdx.x; j < n_acc; j += blockDim.x) {
         const int p = (int)(keys[j] & 0xFFFFFFFFu);
         dv.x[base + p] = dv.y[base + p];
@@ -302,7 +392,7 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(const Dev dv) {
         dg_slot& so = dv.slots[c];
         so.step = s + 1;
         so.n_committed = sl.n_committed + n_acc;
-        so.mean_entropy = (float)mean_H;
+        so.mean_entropy = mean_H;
       }
     } else {
       // (iii) finish the block
@@ -322,7 +412,7 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(const Dev dv) {
         dg_slot& so = dv.slots[c];
         so.steps_used = sl.steps_used + s + 1;
         so.converged_blocks = sl.converged_blocks + (converged ? 1 : 0);
-        so.mean_entropy = (float)mean_H;
+        so.mean_entropy = mean_H;
         if (more) {
           so.block = b + 1;
           so.step = 0;
@@ -351,22 +441,35 @@ __global__ void __launch_bounds__(kCommitThreads) k_plan(const Dev dv, int tick)
 
 }  // namespace
 
+// Launch with programmatic stream serialization (see pdl_wait / pdl_allow_next).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_rmsnorm(const Dev& dv, const float* resid, cudaStream_t st) {
   const int rows = dv.max_active * dv.L;
-  const int blocks = (rows + 7) / 8;
-  k_rmsnorm<<<blocks, 256, 0, st>>>(resid, dv);
-  return cudaGetLastError();
+  return launch_pdl(k_rmsnorm, dim3((rows + 7) / 8), dim3(256), 0, st, resid, dv);
 }
 
 cudaError_t launch_combine(const Dev& dv, cudaStream_t st) {
   const int rows = dv.max_active * dv.L;
-  k_combine<<<(rows + 7) / 8, 256, 0, st>>>(dv);
-  return cudaGetLastError();
+  return launch_pdl(k_combine, dim3((rows + 7) / 8), dim3(256), 0, st, dv);
 }
 
 cudaError_t launch_commit(const Dev& dv, cudaStream_t st) {
-  k_commit<<<dv.max_active, kCommitThreads, 0, st>>>(dv);
-  return cudaGetLastError();
+  return launch_pdl(k_commit, dim3(dv.max_active), dim3(kCommitThreads), 0, st, dv);
 }
 
 cudaError_t launch_plan(const Dev& dv, int tick, cudaStream_t st) {

@@ -10,21 +10,21 @@
 // per position on the device; here the reduction moves into the GEMM's own
 // epilogue so the logits are never written.
 //
-// Structure (one persistent CTA per SM, 320 threads):
+// Structure (one persistent CTA per SM, 576 threads):
 //   warp 0      TMA producer: A = h tile [128 x 64] and B = W tile [256 x 64]
 //               per stage, 128-byte swizzle, 4-stage mbarrier ring.
 //   warp 1      allocates 512 TMEM columns; one lane issues
 //               tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32,
 //               M=128, N=256, K=16) into one of two TMEM accumulators and
 //               commits stage release / accumulator-ready barriers.
-//   warps 2..9  epilogue: two warps per TMEM lane quadrant (rows), each
-//               owning 128 of the 256 columns; per element
+//   warps 2..17 epilogue: four warps per TMEM lane quadrant (rows), each
+//               owning 64 of the 256 columns; per element
 //                 u = z * log2(e)/T, running (max, sum 2^(u-m), sum 2^(u-m)(u-m)),
 //                 argmax, and the perturbed score u - log2 E_v of the
 //                 Gumbel draw (E_v = -ln U_v, U_v from Philox).
 // Work unit = (128-row M tile of active positions, vocabulary chunk); the
 // epilogue keeps its running statistics in registers across the chunk's
-// tiles and writes one 32-byte partial record per row and column half.
+// tiles and writes one 32-byte partial record per row and column group.
 // Every mbarrier wait is bounded (1 s); on expiry the CTA latches an error,
 // drains what it issued and frees TMEM.
 #include <cuda_runtime.h>
@@ -172,61 +172,81 @@ struct RowMeta {
   bool valid;
 };
 
+// Screen factor K = 2^(m - g + 32) (with 0.2 % slack): a Gumbel draw can raise the
+// best perturbed score g only if q < 2^(u - g) = e * 2^(m - g), e = 2^(u - m) being
+// the element's softmax weight, i.e. only if float(~r) < e * K.  The slack covers
+// the rounding of e, K and float(~r).  g = -inf lets every element through.
+__device__ __forceinline__ float screen_factor(float m, float g) {
+  return g == -INFINITY ? INFINITY : 1.002f * ex2_approx(m - g + 32.f);
+}
+
 // Fold 32 columns [v0, v0+32) of one row into its running statistics.
-__device__ __forceinline__ void fold32(const float (&acc)[32], int v0, int V, const RowMeta& rm, Partial& st) {
-  float u[32];
+//
+// Softmax statistics in base 2: u = z log2(e)/T, running max m, S = sum 2^(u-m),
+// A = sum 2^(u-m)(u-m); the argmax index is looked up only when the chunk
+// raises the running max.
+//
+// Gumbel-max sample: the perturbed score is u - log2 E with E = -ln U the
+// Exp(1) variate of the element's Philox word r.  Since -ln U >= 1 - U = q =
+// (~r + 0.5) 2^-32, the element can beat the running best g only if
+// q < 2^(u - g); that test costs one multiply of the softmax weight already
+// computed (see screen_factor).  Elements failing it cannot win and skip the
+// exact transform, so the result equals the unscreened maximum.
+__device__ __forceinline__ void fold32(float (&u)[32], int v0, int V, const RowMeta& rm, Partial& st, float& kscr) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) u[j] = acc[j] * rm.scale;
+  for (int j = 0; j < 32; ++j) u[j] *= rm.scale;
   const bool full = (v0 + 32 <= V);
   if (!full) {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (v0 + j >= V) u[j] = -INFINITY;
   }
-  // running max / argmax (first index on ties)
   float cm = u[0];
-  int ci = 0;
 #pragma unroll
-  for (int j = 1; j < 32; ++j)
-    if (u[j] > cm) {
-      cm = u[j];
-      ci = j;
-    }
+  for (int j = 1; j < 32; ++j) cm = fmaxf(cm, u[j]);
+  if (cm == -INFINITY) return;  // a fully masked tail chunk
   if (cm > st.m) {
     const float f = ex2_approx(st.m - cm);
     st.A = st.S > 0.f ? f * fmaf(st.m - cm, st.S, st.A) : 0.f;
     st.S = f * st.S;
     st.m = cm;
-    st.amax = v0 + ci;
-  }
-  if (cm == -INFINITY) return;  // a fully masked tail chunk
-  float S = 0.f, A = 0.f;
+    int ci = 31;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float dlt = u[j] - st.m;
-    const float e = ex2_approx(dlt);
-    if (full || v0 + j < V) {
-      S += e;
-      A = fmaf(e, dlt, A);
-    }
+    for (int j = 31; j >= 0; --j)
+      if (u[j] == cm) ci = j;  // first index holding the maximum
+    st.amax = v0 + ci;
+    kscr = screen_factor(st.m, st.g);
   }
-  st.S += S;
-  st.A += A;
-  // Gumbel-max: one Philox block per 4 consecutive vocabulary entries
+  float S = 0.f, A = 0.f;
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
     const int vb = v0 + 4 * g;
+    float e[4];
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const float dlt = u[4 * g + l] - st.m;
+      e[l] = ex2_approx(dlt);
+      if (full || vb + l < V) {
+        S += e[l];
+        A = fmaf(e[l], dlt, A);
+      }
+    }
     const uint4 r = philox(make_uint4((uint32_t)vb >> 2, rm.p, rm.bs, kPurposeGumbel), rm.key0, rm.key1);
     const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
-      const float sc = u[4 * g + l] + neg_log2_exp_variate(rw[l]);
-      if (sc > st.g && (full || vb + l < V)) {
-        st.g = sc;
-        st.gidx = vb + l;
+      if (__uint2float_rz(~rw[l]) < e[l] * kscr) {
+        const float sc = u[4 * g + l] + neg_log2_exp_variate(rw[l]);
+        if (sc > st.g && (full || vb + l < V)) {
+          st.g = sc;
+          st.gidx = vb + l;
+          kscr = screen_factor(st.m, st.g);
+        }
       }
     }
   }
+  st.S += S;
+  st.A += A;
 }
 
 __global__ void __launch_bounds__(kThreadsLM, 1)
@@ -244,9 +264,6 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_rows = dv.plan->n_active * dv.L;
-  const int n_mt = (n_rows + kBM - 1) / kBM;
-  const int n_units = n_mt * dv.n_chunks;
   const int KB = (dv.d + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
@@ -276,6 +293,12 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything above overlaps the previous kernel; the normalised rows and the plan are read below
+  pdl_wait();
+  pdl_allow_next();
+  const int n_rows = dv.plan->n_active * dv.L;
+  const int n_mt = (n_rows + kBM - 1) / kBM;
+  const int n_units = n_mt * dv.n_chunks;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -368,8 +391,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;             // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;   // which 128 of the 256 columns
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int cg = (warp - 2) >> 2;         // which 64 of the 256 columns
     uint32_t tcount = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -392,6 +415,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         rm.scale = 1.4426950408889634f / sl.temperature;
       }
       Partial st = empty_partial();
+      float kscr = INFINITY;
       for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
         const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
         int got = 0;
@@ -402,20 +426,24 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(half * 128);
+        const uint32_t tbase =
+            tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(cg * kColsPerWarp);
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < kColsPerWarp / 32; ++cc) {
           float acc[32];
           __syncwarp();  // tcgen05.ld is .sync.aligned: the fold below may leave lanes diverged
           tmem_ld32(tbase + (uint32_t)(cc * 32), acc);
-          if (rm.valid) fold32(acc, vt * kBN + half * 128 + cc * 32, dv.V, rm, st);
+          if (cc == kColsPerWarp / 32 - 1) {
+            // the accumulator is in registers: hand the buffer back to the MMA warp early
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ab]);
+          }
+          if (rm.valid) fold32(acc, vt * kBN + cg * kColsPerWarp + cc * 32, dv.V, rm, st, kscr);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[ab]);
       }
       if (!ok) break;
-      if (rm.valid) dv.part[(size_t)row * dv.n_sub + chunk * kSubPerChunk + half] = st;
+      if (rm.valid) dv.part[(size_t)row * dv.n_sub + chunk * kSubPerChunk + cg] = st;
     }
   }
 
@@ -444,8 +472,17 @@ cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorM
   int grid = max_mt * dv.n_chunks;
   if (grid > num_sms) grid = num_sms;
   if (grid < 1) grid = 1;
-  k_lmhead<<<grid, kThreadsLM, kSmemBytes, st>>>(*tmA, *tmB, dv);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreadsLM);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_lmhead, *tmA, *tmB, dv);
 }
 
 }  // namespace dg

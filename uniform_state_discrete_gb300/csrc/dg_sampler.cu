@@ -182,7 +182,13 @@ dg_status tick(dg_sampler* s, const float* resid) {
     set_err(s->err, "every canvas has finished (tick %lld)", (long long)s->host_tick);
     return DG_ERR_STATE;
   }
-  auto mark = [&](int i) { return s->timed ? cudaEventRecord(s->timing[i], s->stream) : cudaSuccess; };
+  // external event nodes when the tick is captured in a CUDA graph, plain records otherwise
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (s->timed) DG_CUDA(s->err, cudaStreamIsCapturing(s->stream, &cap), "query stream capture");
+  const unsigned rec_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+  auto mark = [&](int i) {
+    return s->timed ? cudaEventRecordWithFlags(s->timing[i], s->stream, rec_flags) : cudaSuccess;
+  };
   DG_CUDA(s->err, mark(0), "record timing event");
   DG_CUDA(s->err, dg::launch_rmsnorm(s->dv, resid, s->stream), "launch rmsnorm");
   DG_CUDA(s->err, mark(1), "record timing event");
@@ -469,6 +475,7 @@ const int32_t* dg_sample(const dg_sampler* s) { return s ? s->dv.y : nullptr; }
 const int32_t* dg_argmax(const dg_sampler* s) { return s ? s->dv.amax : nullptr; }
 const int32_t* dg_tokens_out(const dg_sampler* s) { return s ? s->dv.tokens_out : nullptr; }
 const dg_slot* dg_slots(const dg_sampler* s) { return s ? s->dv.slots : nullptr; }
+const uint16_t* dg_normed(const dg_sampler* s) { return s ? s->dv.h : nullptr; }
 
 const char* dg_status_string(dg_status st) {
   switch (st) {
