@@ -285,7 +285,7 @@ def run_ours(args, wl, world, rank, local):
         if args.flush == "writeread":
             flush.sum(dtype=torch.int32)
 
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     t_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     for e in ev + t_ev:  # torch creates the CUDA event on first record
         e.record(stream)
@@ -330,12 +330,12 @@ def run_ours(args, wl, world, rank, local):
         barrier(world)
         torch.cuda.synchronize(dev)
         clk = clocks.stop()
-        # per-kernel pass: the same ticks with events between the four kernels (which
-        # serialise them); its K2 mean is the roofline's launch duration
+        # per-kernel pass: the same ticks with events between the three kernels (which
+        # serialise them); the LM-head kernel's mean is the roofline's launch duration
         kgraph = capture(True) if args.graph else None
         if kgraph is None:
             s.set_timing_events(ev)
-        per_kernel = np.zeros((args.kernel_steps, 4))
+        per_kernel = np.zeros((args.kernel_steps, 3))
         for k in range(args.kernel_steps):
             make_resid()
             flush_l2()
@@ -343,8 +343,8 @@ def run_ours(args, wl, world, rank, local):
                 kgraph.replay()
             else:
                 s.step(resid)
-            ev[4].synchronize()
-            per_kernel[k] = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
+            ev[3].synchronize()
+            per_kernel[k] = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
         s.set_timing_events(None)
     info = s.sync_info()  # also surfaces a latched device fault
     device_s = float(tick_ms.sum()) / 1e3
@@ -356,7 +356,7 @@ def run_ours(args, wl, world, rank, local):
     peaks = measured_peaks()
     k2_s = float(per_kernel[:, 1].mean()) / 1e3
     lay_chunks = math.ceil(math.ceil(V / 256) / math.ceil(math.ceil(V / 256) / min(math.ceil(V / 256), 76)))
-    n_sub = 4 * lay_chunks  # partial records per position: 4 column groups per vocabulary chunk
+    n_sub = lay_chunks  # partial records per position: one per vocabulary chunk
     P = positions_per_tick
     alg_bytes = V * d * 2 + P * d * 2 + P * n_sub * 32
     alg_flops = 2.0 * P * V * d
@@ -411,13 +411,15 @@ def run_ours(args, wl, world, rank, local):
                            "graph": bool(args.graph),
                            "parallelism": f"replicas x{world} (independent canvases per GPU)" if world > 1 else "1 GPU",
                            "timing": "CUDA events around each whole tick on the sampler stream (timed region); "
-                                     "a second pass with events between the 4 kernels gives ms_per_kernel"},
+                                     "a second pass with events between the 3 kernels gives ms_per_kernel"},
                 "ms_per_kernel": {n: float(per_kernel[:, i].mean()) for i, n in
-                                  enumerate(("k_rmsnorm", "k_lmhead", "k_combine", "k_commit"))},
+                                  enumerate(("k_rmsnorm", "k_lmhead", "k_finish"))},
                 "tick_ms_p50": float(np.percentile(tick_ms, 50)), "tick_ms_p99": float(np.percentile(tick_ms, 99)),
                 "kernel_pass_steps": args.kernel_steps,
-                "wall_s_timed_region": t_wall, "gpu_launches": args.steps * 5,
-                "gpu_launches_detail": "per step: 4 sampler kernels + 1 residual-generator kernel",
+                "wall_s_timed_region": t_wall, "gpu_launches": args.steps * 4,
+                "gpu_launches_detail": "per step: 3 sampler kernels (RMSNorm; LM head fused with softmax "
+                                       "statistics and sample; combine + commit + re-noise + plan) + 1 residual "
+                                       "generator",
                 "roofline": roof, "e2e": e2e, "clocks": clk}
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_positions_per_s(wl, args.cpu_budget, 0, W16=W16)

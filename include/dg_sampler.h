@@ -177,11 +177,13 @@ const dg_slot* dg_slots(const dg_sampler* s);       /* [B] per-canvas state     
  * position of the active canvases in canvas order (active canvas a, position p -> row a*L + p). */
 const uint16_t* dg_normed(const dg_sampler* s);
 
-/* Per-kernel timing: with events set (five cudaEvent_t created by the caller),
- * every later tick records events[0] before the RMSNorm kernel and events[1..4]
- * after the RMSNorm, LM-head, combine and commit kernels, on the sampler's
- * stream (as external event nodes when the tick is being captured into a CUDA
- * graph).  NULL turns it off.  The events stay owned by the caller. */
+/* Per-kernel timing: with events set (four cudaEvent_t created by the caller),
+ * every later tick records events[0] before the RMSNorm kernel, events[1] after
+ * it, events[2] after the LM-head kernel (LM head fused with the softmax
+ * statistics and the sample) and events[3] after the finishing kernel (combine,
+ * commit, re-noise, next-tick plan), on the sampler's stream (as external event
+ * nodes when the tick is being captured into a CUDA graph).  NULL turns it off.
+ * The events stay owned by the caller. */
 dg_status dg_set_timing_events(dg_sampler* s, void* const* events);
 
 /* Copy the per-canvas state to host memory (dg_slot [B]).  Synchronizing;

@@ -194,16 +194,17 @@ class Sampler:
         return tokens, slots
 
     def set_timing_events(self, events):
-        """Five torch.cuda.Event(enable_timing=True) recorded around K1..K4 of every tick, or None."""
+        """Four torch.cuda.Event(enable_timing=True) recorded on every tick: before the RMSNorm kernel,
+        after it, after the LM-head kernel and after the finishing kernel; or None."""
         if events is None:
             _check(lib.dg_set_timing_events(self.handle, None), self.handle)
             self._timing = None
             return
-        assert len(events) == 5
+        assert len(events) == 4
         for e in events:
             if not e.cuda_event:  # torch creates the CUDA event lazily, on first record
                 e.record(self.stream)
-        arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
         self._timing = (events, arr)
         _check(lib.dg_set_timing_events(self.handle, arr), self.handle)
 

@@ -30,7 +30,7 @@ constexpr int kTmemCols = 2 * kBN;      // double-buffered accumulator
 constexpr int kChunkTarget = 76;
 constexpr int kColGroups = kEpiWarps / 4;
 constexpr int kColsPerWarp = kBN / kColGroups;  // 64
-constexpr int kSubPerChunk = kColGroups;        // one partial record per column group
+constexpr int kSubPerChunk = 1;                 // column groups are merged in the CTA before writing
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after 1 s
 
@@ -53,7 +53,7 @@ static_assert(sizeof(Partial) == 32, "partial record is 32 bytes");
 struct Plan {
   int32_t tick;
   int32_t n_active;
-  uint32_t k4_counter;
+  uint32_t commits;  // canvases committed so far this tick
   int32_t err;
   int32_t err_info[4];
 };
@@ -74,6 +74,7 @@ struct Dev {
   int32_t* amax;        // [B, L]
   uint16_t* h;          // [rows_cap, d] bf16 bits, compact active rows
   Partial* part;        // [rows_cap, n_sub]
+  uint32_t* canvas_rows;// [B] rows combined per canvas this tick
   float* resid_stage;   // [B, L, d]
   const float* norm_w;  // [d] or null
   int32_t V, d, L, B, G, N;
@@ -169,10 +170,8 @@ __device__ __forceinline__ Partial empty_partial() {
 cudaError_t launch_rmsnorm(const Dev& dv, const float* resid, cudaStream_t st);
 cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
                           cudaStream_t st);
-cudaError_t launch_combine(const Dev& dv, cudaStream_t st);
-cudaError_t launch_commit(const Dev& dv, cudaStream_t st);
+cudaError_t launch_finish(const Dev& dv, cudaStream_t st);
 cudaError_t launch_plan(const Dev& dv, int tick, cudaStream_t st);
-cudaError_t launch_refresh_slots(const Dev& dv, cudaStream_t st);
 cudaError_t lmhead_configure();
 
 }  // namespace dg

@@ -1,11 +1,12 @@
-// K1 RMSNorm, K3 split-vocabulary combine, K4 entropy-bounded commit +
-// uniform re-noise + schedule advance, and the tick planner.
+// K1 RMSNorm, the finishing kernel (split-vocabulary combine, entropy-bounded
+// commit, re-noise and next-tick plan) and the stand-alone tick planner.
 #include <cuda_runtime.h>
 #include <math.h>
 
 #include <utility>
 
 #include "dg_internal.cuh"
+#include "dg_tail.cuh"
 
 namespace dg {
 namespace {
@@ -102,344 +103,105 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ resid
   }
 }
 
-// ------------------------------------------------------------------- K3
-__device__ __forceinline__ Partial shfl_partial(const Partial& a, int o) {
-  Partial b;
-  b.m = __shfl_xor_sync(0xFFFFFFFFu, a.m, o);
-  b.S = __shfl_xor_sync(0xFFFFFFFFu, a.S, o);
-  b.A = __shfl_xor_sync(0xFFFFFFFFu, a.A, o);
-  b.g = __shfl_xor_sync(0xFFFFFFFFu, a.g, o);
-  b.amax = __shfl_xor_sync(0xFFFFFFFFu, a.amax, o);
-  b.gidx = __shfl_xor_sync(0xFFFFFFFFu, a.gidx, o);
-  b.pad0 = b.pad1 = 0;
-  return b;
-}
+// Finishing kernel of a tick.  Each warp combines the split-vocabulary partial
+// records of one active position: log2 Z = m + log2 S, H = ln 2 (log2 S - A/S)
+// (= log Z - E_p[z/T] in nats), the sample is the index of the largest
+// perturbed score and the argmax the index of the largest logit.  Each CTA then
+// credits its positions to their canvases; the CTA that completes a canvas
+// commits it (dg_tail.cuh), and the last commit plans the next tick.  No CTA
+// waits for another: the last arrival at a counter does the work.
+constexpr int kFinishRows = 8;  // positions (warps) per CTA
 
-// Combine the split-vocabulary partials of each active position:
-// log2 Z = m + log2 S,  H = ln 2 (log2 S - A / S)  (= log Z - E_p[z/T] in nats),
-// the sample is the index of the largest perturbed score, the argmax the index
-// of the largest logit.  One warp per position.
-__global__ void __launch_bounds__(256) k_combine(const Dev dv) {
+__global__ void __launch_bounds__(256) k_finish(const Dev dv) {
+  __shared__ TailScratch sc;
   pdl_wait();
   pdl_allow_next();
-  const int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
+  const Group g{(int)threadIdx.x, (int)blockDim.x, 0};
   const int n_rows = dv.plan->n_active * dv.L;
-  if (row >= n_rows) return;
-  Partial acc = empty_partial();
-  const Partial* src = dv.part + (size_t)row * dv.n_sub;
-  for (int i = lane; i < dv.n_sub; i += 32) acc = merge_partial(acc, src[i]);
+  if (n_rows == 0) {
+    if (blockIdx.x == 0) plan_tick(dv, dv.plan->tick + 1, g, &sc);
+    return;
+  }
+  const int row0 = blockIdx.x * kFinishRows;
+  if (row0 >= n_rows) return;
+  const int row1 = min(row0 + kFinishRows, n_rows);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = row0 + warp;
+  if (row < row1) {
+    Partial acc = empty_partial();
+    const Partial* src = dv.part + (size_t)row * dv.n_sub;
+    for (int i = lane; i < dv.n_sub; i += 32) acc = merge_partial(acc, src[i]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc = merge_partial(acc, shfl_partial(acc, o));
-  if (lane == 0) {
-    const int a = row / dv.L, p = row - a * dv.L;
-    const int c = dv.active[a];
-    const float l2S = log2f(acc.S);
-    const float H = 0.69314718055994531f * (l2S - acc.A / acc.S);
-    const float lz = 0.69314718055994531f * (acc.m + l2S);
-    const size_t o = (size_t)c * dv.L + p;
-    dv.H[o] = H > 0.f ? H : 0.f;  // +0 for rounding below zero (and never -0: its bits would sort last)
-    dv.logZ[o] = lz;
-    dv.y[o] = acc.gidx;
-    dv.amax[o] = acc.amax;
-    if (!isfinite(H) || !isfinite(lz) || !isfinite(acc.g) || acc.gidx < 0 || acc.gidx >= dv.V) {
-      if (atomicCAS(&dv.plan->err, kErrNone, kErrNonFinite) == kErrNone) dv.plan->err_info[1] = (int)o;
+    for (int o = 16; o > 0; o >>= 1) {
+      Partial b;
+      b.m = __shfl_xor_sync(0xFFFFFFFFu, acc.m, o);
+      b.S = __shfl_xor_sync(0xFFFFFFFFu, acc.S, o);
+      b.A = __shfl_xor_sync(0xFFFFFFFFu, acc.A, o);
+      b.g = __shfl_xor_sync(0xFFFFFFFFu, acc.g, o);
+      b.amax = __shfl_xor_sync(0xFFFFFFFFu, acc.amax, o);
+      b.gidx = __shfl_xor_sync(0xFFFFFFFFu, acc.gidx, o);
+      b.pad0 = b.pad1 = 0;
+      acc = merge_partial(acc, b);
     }
-  }
-}
-
-// ------------------------------------------------------------------- K4
-constexpr int kCommitThreads = 256;
-constexpr int kMaxL = 1024;
-
-__device__ void init_canvas(const Dev& dv, int c, int block) {
-  const uint64_t seed = dv.slots[c].seed;
-  for (int p = threadIdx.x; p < dv.L; p += blockDim.x) {
-    const size_t o = (size_t)c * dv.L + p;
-    dv.x[o] = uniform_token(draw_u32(seed, kPurposeInit, block, 0, p), dv.V);
-    dv.committed[o] = 0;
-    dv.commit_step[o] = -1;
-    dv.prev_amax[o] = 0;
-  }
-}
-
-// Admit the canvases due by `tick` (admit_tick <= tick), in canvas order, while
-// fewer than max_active are running; refresh temperatures; rebuild the active
-// list in canvas order.  Run by every thread of one CTA.
-__device__ void plan_tick(const Dev& dv, int tick) {
-  __shared__ int s_running;
-  // Slots were written by other CTAs of this grid: read them at L2 (ld.global.cg), not L1.
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int c = 0; c < dv.B; ++c) n += (__ldcg(&dv.slots[c].state) == kActive) ? 1 : 0;
-    s_running = n;
-  }
-  __syncthreads();
-  int running = s_running;
-  for (int c = 0; c < dv.B && running < dv.max_active; ++c) {
-    const int state = __ldcg(&dv.slots[c].state);
-    const int admit = __ldcg(&dv.slots[c].admit_tick);
-    if (state == kWaiting && admit <= tick) {
-      init_canvas(dv, c, 0);
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        dg_slot& s = dv.slots[c];
-        s.state = kActive;
-        s.block = 0;
-        s.step = 0;
-        s.n_committed = 0;
-      }
-      ++running;
-      __syncthreads();
-    }
-  }
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int c = 0; c < dv.B; ++c) {
-      dg_slot& s = dv.slots[c];
-      if (__ldcg(&s.state) == kActive) {
-        s.temperature = temperature(__ldcg(&s.step), dv.N, dv.t_min, dv.t_max);
-        if (n < dv.max_active) dv.active[n] = c;
-        ++n;
-      }
-    }
-    if (n > dv.max_active) n = dv.max_active;  // only reachable through an inconsistent dg_set_state
-    dv.plan->n_active = n;
-    dv.plan->tick = tick;
-    dv.plan->k4_counter = 0u;
-  }
-  __syncthreads();
-}
-
-// Block-wide helpers for the commit kernel (blockDim.x = kCommitThreads).
-__device__ __forceinline__ float block_sum_f32(float v, float* scratch) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) scratch[w] = v;
-  __syncthreads();
-  float t = 0.f;
-#pragma unroll
-  for (int i = 0; i < kCommitThreads / 32; ++i) t += scratch[i];
-  return t;
-}
-
-__device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v, unsigned long long* scratch) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    v = w < v ? w : v;
-  }
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) scratch[w] = v;
-  __syncthreads();
-  unsigned long long t = ~0ull;
-#pragma unroll
-  for (int i = 0; i < kCommitThreads / 32; ++i) t = scratch[i] < t ? scratch[i] : t;
-  return t;
-}
-
-// Sort 32 keys held one per lane, ascending (bitonic network over shuffles).
-__device__ __forceinline__ unsigned long long warp_sort_u64(unsigned long long key) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, key, stride);
-      const bool keep_min = ((lane & stride) == 0) == ((lane & size) == 0);
-      key = keep_min ? (other < key ? other : key) : (other > key ? other : key);
-    }
-  }
-  return key;
-}
-
-// Accepted entries among `n` ascending keys (H bits << 32 | p): the walk sums
-// the entropies in fp64, in order; entry j is accepted while the sum of the
-// entries before it is <= bound.  fp64 sums of non-negative terms never
-// decrease, so the first refusal ends the walk.
-__device__ __forceinline__ int accept_walk(const unsigned long long* keys, int n, float bound) {
-  double E = 0.0;
-  int k = 0;
-  for (int j = 0; j < n; ++j) {
-    if (keys[j] == ~0ull || !(E <= (double)bound)) break;
-    ++k;
-    E += (double)__uint_as_float((unsigned)(keys[j] >> 32));
-  }
-  return k;
-}
-
-// One CTA per active canvas:
-//  (i)   early stop: s >= 1, mean_p H < confidence and argmax == previous argmax at every p;
-//  (ii)  otherwise order the uncommitted positions by (H, p) and accept the prefix whose
-//        exclusive entropy sums stay <= entropy_bound; accepted positions take their sample;
-//  (iii) on early stop or at s = N-1 every uncommitted position takes its sample and the
-//        block ends (tokens copied out, next block or done);
-//  (iv)  every other uncommitted position is re-noised to a uniform token.
-// Only entries whose entropy is <= bound, plus the smallest one above it, can be
-// accepted, so the common case sorts at most 32 candidates in one warp; more than
-// 31 entropies within the bound fall back to a bitonic sort of the canvas.
-// The CTA that finishes last plans the next tick.
-__global__ void __launch_bounds__(kCommitThreads) k_commit(const Dev dv) {
-  __shared__ unsigned long long keys[kMaxL];
-  __shared__ float redf[kCommitThreads / 32];
-  __shared__ unsigned long long redk[kCommitThreads / 32];
-  __shared__ unsigned long long cand[32];
-  __shared__ int s_cnt, s_k;
-  pdl_wait();
-  pdl_allow_next();
-  const int n_active = dv.plan->n_active;
-  const int a = blockIdx.x;
-  const int L = dv.L;
-
-  if (a < n_active) {
-    const int c = dv.active[a];
-    const dg_slot sl = dv.slots[c];
-    const int s = sl.step, b = sl.block;
-    const size_t base = (size_t)c * L;
-    const float bound = dv.bound;
-
-    // (i) early-stop test, and the keys of the uncommitted positions
-    float hsum = 0.f, n_le = 0.f;
-    int stable = 1;
-    unsigned long long kmin_above = ~0ull;
-    for (int p = threadIdx.x; p < L; p += blockDim.x) {
-      const float H = dv.H[base + p];
-      hsum += H;
-      stable &= (dv.amax[base + p] == dv.prev_amax[base + p]) ? 1 : 0;
-      if (!dv.committed[base + p]) {
-        const unsigned long long k = ((unsigned long long)__float_as_uint(H) << 32) | (unsigned)p;
-        if (H <= bound) n_le += 1.f;
-        else kmin_above = k < kmin_above ? k : kmin_above;
-      }
-    }
-    const float mean_H = block_sum_f32(hsum, redf) / (float)L;
-    const int count_le = (int)block_sum_f32(n_le, redf);
-    kmin_above = block_min_u64(kmin_above, redk);
-    stable = __syncthreads_and(stable);
-    const bool converged = (s >= 1) && (mean_H < dv.conf) && stable;
-    const bool final_step = converged || (s == dv.N - 1);
-
-    int n_acc = 0;
-    if (!final_step) {
-      // (ii) the accepted prefix of the (H, p) order
-      if (count_le < 32) {
-        if (threadIdx.x == 0) s_cnt = 0;
-        __syncthreads();
-        for (int p = threadIdx.x; p < L; p += blockDim.x) {
-          const float H = dv.H[base + p];
-          if (!dv.committed[base + p] && H <= bound)
-            cand[atomicAdd(&s_cnt, 1)] = ((unsigned long long)__float_as_uint(H) << 32) | (unsigned)p;
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) {
-          const int lane = threadIdx.x;
-          unsigned long long k = lane < count_le ? cand[lane] : (lane == count_le ? kmin_above : ~0ull);
-          k = warp_sort_u64(k);
-          cand[lane] = k;
-          __syncwarp();
-          if (lane == 0) s_k = accept_walk(cand, 32, bound);
-        }
-        __syncthreads();
-        n_acc = s_k;
-        for (int j = threadIdx.x; j < n_acc; j += blockDim.x) keys[j] = cand[j];
-      } else {
-        int n2 = 1;
-        while (n2 < L) n2 <<= 1;
-        for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-          unsigned long long k = ~0ull;
-          if (i < L && !dv.committed[base + i])
-            k = ((unsigned long long)__float_as_uint(dv.H[base + i]) << 32) | (unsigned)i;
-          keys[i] = k;
-        }
-        __syncthreads();
-        for (int size = 2; size <= n2; size <<= 1) {
-          for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int t = threadIdx.x; t < (n2 >> 1); t += blockDim.x) {
-              const int i = 2 * t - (t & (stride - 1));
-              const int j = i + stride;
-              const bool up = ((i & size) == 0);
-              const unsigned long long ki = keys[i], kj = keys[j];
-              if ((ki > kj) == up) {
-                keys[i] = kj;
-                keys[j] = ki;
-              }
-            }
-            __syncthreads();
-          }
-        }
-        if (threadIdx.x == 0) s_k = accept_walk(keys, n2, bound);
-        __syncthreads();
-        n_acc = s_k;
-      }
-      __syncthreads();
-      for (int j = threadIdx.x; j < n_acc; j += blockDim.x) {
-        const int p = (int)(keys[j] & 0xFFFFFFFFu);
-        dv.x[base + p] = dv.y[base + p];
-        dv.committed[base + p] = 1;
-        dv.commit_step[base + p] = (int16_t)s;
-      }
-      __syncthreads();
-      // (iv) uniform re-noise of everything still uncommitted; keep the argmax canvas
-      for (int p = threadIdx.x; p < L; p += blockDim.x) {
-        if (!dv.committed[base + p]) dv.x[base + p] = uniform_token(draw_u32(sl.seed, kPurposeRenoise, b, s, p), dv.V);
-        dv.prev_amax[base + p] = dv.amax[base + p];
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        dg_slot& so = dv.slots[c];
-        so.step = s + 1;
-        so.n_committed = sl.n_committed + n_acc;
-        so.mean_entropy = mean_H;
-      }
-    } else {
-      // (iii) finish the block
-      for (int p = threadIdx.x; p < L; p += blockDim.x) {
-        if (!dv.committed[base + p]) {
-          dv.x[base + p] = dv.y[base + p];
-          dv.committed[base + p] = 1;
-          dv.commit_step[base + p] = (int16_t)s;
-        }
-        dv.tokens_out[((size_t)c * dv.G + b) * L + p] = dv.x[base + p];
-      }
-      __syncthreads();
-      const bool more = (b + 1 < dv.G);
-      if (more) init_canvas(dv, c, b + 1);
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        dg_slot& so = dv.slots[c];
-        so.steps_used = sl.steps_used + s + 1;
-        so.converged_blocks = sl.converged_blocks + (converged ? 1 : 0);
-        so.mean_entropy = mean_H;
-        if (more) {
-          so.block = b + 1;
-          so.step = 0;
-          so.n_committed = 0;
-        } else {
-          so.n_committed = L;
-          so.state = kDone;
-        }
+    if (lane == 0) {
+      const int a = row / dv.L, p = row - a * dv.L;
+      const int c = dv.active[a];
+      const float l2S = log2f(acc.S);
+      const float H = 0.69314718055994531f * (l2S - acc.A / acc.S);
+      const float lz = 0.69314718055994531f * (acc.m + l2S);
+      const size_t o = (size_t)c * dv.L + p;
+      dv.H[o] = H > 0.f ? H : 0.f;  // +0 for rounding below zero (and never -0: its bits would sort last)
+      dv.logZ[o] = lz;
+      dv.y[o] = acc.gidx;
+      dv.amax[o] = acc.amax;
+      if (!isfinite(H) || !isfinite(lz) || !isfinite(acc.g) || acc.gidx < 0 || acc.gidx >= dv.V) {
+        if (atomicCAS(&dv.plan->err, kErrNone, kErrNonFinite) == kErrNone) dv.plan->err_info[1] = (int)o;
       }
     }
   }
-
-  // last CTA to finish plans the next tick
-  __shared__ int s_last;
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&dv.plan->k4_counter, 1u) == gridDim.x - 1) ? 1 : 0;
+  if (threadIdx.x == 0) {
+    int nd = 0;
+    for (int a = row0 / dv.L; a * dv.L < row1; ++a) {
+      const int lo = max(a * dv.L, row0), hi = min((a + 1) * dv.L, row1);
+      const int c = dv.active[a];
+      const unsigned old = atomicAdd(&dv.canvas_rows[c], (unsigned)(hi - lo));
+      if (old + (unsigned)(hi - lo) == (unsigned)dv.L) {
+        dv.canvas_rows[c] = 0u;  // every row of this canvas is combined: reset for the next tick
+        sc.done_list[nd++] = c;
+      }
+    }
+    sc.flags[3] = nd;
+  }
   __syncthreads();
-  if (s_last) {
+  const int nd = sc.flags[3];
+  for (int i = 0; i < nd; ++i) {
+    const int c = sc.done_list[i];
     __threadfence();
-    plan_tick(dv, __ldcg(&dv.plan->tick) + 1);
+    commit_canvas(dv, c, g, &sc);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+      sc.flags[1] = (atomicAdd(&dv.plan->commits, 1u) == (unsigned)(__ldcg(&dv.plan->n_active) - 1)) ? 1 : 0;
+    __syncthreads();
+    const int plan_now = sc.flags[1];
+    __syncthreads();
+    if (plan_now) {
+      __threadfence();
+      plan_tick(dv, __ldcg(&dv.plan->tick) + 1, g, &sc);
+    }
   }
 }
 
-__global__ void __launch_bounds__(kCommitThreads) k_plan(const Dev dv, int tick) { plan_tick(dv, tick); }
-
-}  // namespace
+// Planner kernel (sampler creation and dg_set_state): clears the tick's
+// counters, which an interrupted tick may have left behind, then plans `tick`.
+__global__ void __launch_bounds__(256) k_plan(const Dev dv, int tick) {
+  __shared__ TailScratch sc;
+  for (int i = threadIdx.x; i < dv.B; i += blockDim.x) dv.canvas_rows[i] = 0u;
+  __syncthreads();
+  plan_tick(dv, tick, Group{(int)threadIdx.x, (int)blockDim.x, 0}, &sc);
+}
 
 // Launch with programmatic stream serialization (see pdl_wait / pdl_allow_next).
 template <typename... KArgs, typename... Args>
@@ -458,22 +220,20 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+}  // namespace
+
 cudaError_t launch_rmsnorm(const Dev& dv, const float* resid, cudaStream_t st) {
   const int rows = dv.max_active * dv.L;
   return launch_pdl(k_rmsnorm, dim3((rows + 7) / 8), dim3(256), 0, st, resid, dv);
 }
 
-cudaError_t launch_combine(const Dev& dv, cudaStream_t st) {
+cudaError_t launch_finish(const Dev& dv, cudaStream_t st) {
   const int rows = dv.max_active * dv.L;
-  return launch_pdl(k_combine, dim3((rows + 7) / 8), dim3(256), 0, st, dv);
-}
-
-cudaError_t launch_commit(const Dev& dv, cudaStream_t st) {
-  return launch_pdl(k_commit, dim3(dv.max_active), dim3(kCommitThreads), 0, st, dv);
+  return launch_pdl(k_finish, dim3((rows + kFinishRows - 1) / kFinishRows), dim3(256), 0, st, dv);
 }
 
 cudaError_t launch_plan(const Dev& dv, int tick, cudaStream_t st) {
-  k_plan<<<1, kCommitThreads, 0, st>>>(dv, tick);
+  k_plan<<<1, 256, 0, st>>>(dv, tick);
   return cudaGetLastError();
 }
 

@@ -262,6 +262,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // column-group merge area: the four warps of a row quadrant leave their records here
+  Partial* mrg = reinterpret_cast<Partial*>(reinterpret_cast<uint8_t*>(sB + kStages * kStageB) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = (dv.d + kBK - 1) / kBK;
@@ -394,12 +396,13 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
     const int cg = (warp - 2) >> 2;         // which 64 of the 256 columns
     uint32_t tcount = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    bool aborted = false;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const int chunk = u / n_mt, mt = u - chunk * n_mt;
       const int vt0 = chunk * dv.tiles_per_chunk;
       const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
-      const int row = mt * kBM + q * 32 + lane;
+      const int rl = q * 32 + lane;         // row within the tile
+      const int row = mt * kBM + rl;
       RowMeta rm;
       rm.valid = row < n_rows;
       rm.key0 = rm.key1 = rm.bs = rm.p = 0u;
@@ -417,13 +420,14 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       Partial st = empty_partial();
       float kscr = INFINITY;
       for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
+        if (aborted) continue;
         const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
         int got = 0;
         if (lane == 0) got = mbar_wait(&tfull[ab], aph, abort_flag, dv.plan) ? 1 : 0;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
         if (!got) {
-          ok = false;
-          break;
+          aborted = true;
+          continue;
         }
         tc_fence_after();
         const uint32_t tbase =
@@ -442,8 +446,18 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
           if (rm.valid) fold32(acc, vt * kBN + cg * kColsPerWarp + cc * 32, dv.V, rm, st, kscr);
         }
       }
-      if (!ok) break;
-      if (rm.valid) dv.part[(size_t)row * dv.n_sub + chunk * kSubPerChunk + cg] = st;
+      // merge the four column groups of each row; one record per row and chunk.  Every
+      // epilogue warp reaches both barriers once per unit, aborted or not (named barrier 1,
+      // the 512 epilogue threads).
+      mrg[cg * kBM + rl] = st;
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+      if (cg == 0 && rm.valid) {
+        Partial m = st;
+#pragma unroll
+        for (int k = 1; k < kColGroups; ++k) m = merge_partial(m, mrg[k * kBM + rl]);
+        dv.part[(size_t)row * dv.n_sub + chunk] = m;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
     }
   }
 
@@ -456,7 +470,9 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   }
 }
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kStageA + kStageB) + 256;
+constexpr size_t kSmemBytes =
+    1024 + (size_t)kStages * (kStageA + kStageB) + 256 + sizeof(Partial) * kColGroups * kBM;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 }  // namespace
 

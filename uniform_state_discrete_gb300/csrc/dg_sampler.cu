@@ -26,7 +26,7 @@ struct dg_sampler {
   int64_t tick_bound;
   void* ws;
   size_t ws_bytes;
-  cudaEvent_t timing[5];
+  cudaEvent_t timing[4];
   bool timed;
   char err[512];
 };
@@ -43,7 +43,8 @@ void set_err(char* buf, const char* fmt, ...) {
 }
 
 struct Layout {
-  size_t slots, plan, active, x, committed, commit_step, prev_amax, tokens_out, H, logZ, y, amax, h, part, resid;
+  size_t slots, plan, active, x, committed, commit_step, prev_amax, tokens_out, H, logZ, y, amax, h, part, resid,
+      canvas_rows;
   size_t total;
   int rows_cap, n_vtiles, tiles_per_chunk, n_chunks, n_sub, max_active;
 };
@@ -113,6 +114,7 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
   L->h = take(2 * (size_t)L->rows_cap * d);
   L->part = take(sizeof(dg::Partial) * (size_t)L->rows_cap * L->n_sub);
   L->resid = take(4 * B * Lc * d);
+  L->canvas_rows = take(4 * B);
   L->total = o;
   return 1;
 }
@@ -194,10 +196,8 @@ dg_status tick(dg_sampler* s, const float* resid) {
   DG_CUDA(s->err, mark(1), "record timing event");
   DG_CUDA(s->err, dg::launch_lmhead(s->dv, &s->tmA, &s->tmB, s->num_sms, s->stream), "launch lm head");
   DG_CUDA(s->err, mark(2), "record timing event");
-  DG_CUDA(s->err, dg::launch_combine(s->dv, s->stream), "launch combine");
+  DG_CUDA(s->err, dg::launch_finish(s->dv, s->stream), "launch finish");
   DG_CUDA(s->err, mark(3), "record timing event");
-  DG_CUDA(s->err, dg::launch_commit(s->dv, s->stream), "launch commit");
-  DG_CUDA(s->err, mark(4), "record timing event");
   ++s->host_tick;
   return DG_OK;
 }
@@ -284,6 +284,7 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.h = reinterpret_cast<uint16_t*>(w + L.h);
   dv.part = reinterpret_cast<dg::Partial*>(w + L.part);
   dv.resid_stage = reinterpret_cast<float*>(w + L.resid);
+  dv.canvas_rows = reinterpret_cast<uint32_t*>(w + L.canvas_rows);
   dv.norm_w = norm_w;
   dv.V = cfg->vocab;
   dv.d = cfg->hidden;
@@ -361,7 +362,7 @@ dg_status dg_set_timing_events(dg_sampler* s, void* const* events) {
   if (!s) return DG_ERR_ARG;
   s->timed = events != nullptr;
   if (events)
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < 4; ++i) {
       if (!events[i]) return s->timed = false, set_err(s->err, "timing event %d is NULL", i), DG_ERR_ARG;
       s->timing[i] = static_cast<cudaEvent_t>(events[i]);
     }
