@@ -71,6 +71,20 @@ def test_rmsnorm_bf16_bit_exact(hidden, norm_seed, sigma):
     assert np.array_equal(got, want), f"{int((got != want).sum())} of {got.size} bf16 values differ"
 
 
+def test_pair_tiles_ragged_rows_and_tails():
+    """>= 256 rows per tick selects the SM-pair LM head: 3 canvases x 100 positions (a second,
+    partly empty 256-row pair tile), V and d not multiples of the tile sizes, staggered admission."""
+    case = Case(vocab=1000, hidden=200, canvas_len=100, n_canvases=3, gen_blocks=2, steps=4, seeds=(1, 2, 3),
+                admit=(0, 1, 2))
+    _assert_report(teacher_forced(case), "pair-ragged")
+
+
+def test_pair_tiles_many_canvases():
+    """Five 256-position canvases in one tick: five pair tiles per vocabulary chunk."""
+    case = Case(vocab=4096, hidden=256, canvas_len=256, n_canvases=5, steps=3, seeds=(11, 12, 13, 14, 15))
+    _assert_report(teacher_forced(case), "pair-many")
+
+
 def test_single_position_canvases_capacity_limited():
     case = Case(vocab=4096, hidden=64, canvas_len=1, n_canvases=5, steps=4, admit=(0, 0, 1, 1, 1), max_active=2)
     _assert_report(teacher_forced(case), "L1")

@@ -170,6 +170,8 @@ __device__ __forceinline__ Partial empty_partial() {
 cudaError_t launch_rmsnorm(const Dev& dv, const float* resid, cudaStream_t st);
 cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
                           cudaStream_t st);
+cudaError_t launch_lmhead_pair(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
+                               cudaStream_t st);
 cudaError_t launch_finish(const Dev& dv, cudaStream_t st);
 cudaError_t launch_plan(const Dev& dv, int tick, cudaStream_t st);
 cudaError_t lmhead_configure();

@@ -249,6 +249,54 @@ __device__ __forceinline__ void fold32(float (&u)[32], int v0, int V, const RowM
   st.A += A;
 }
 
+// ---------------------------------------------------------------- CTA pairs
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory object in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is signalled on the
+// barrier at `bar_cluster_addr`, which may live in the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* tm, int x, int y,
+                                                 uint32_t bar_cluster_addr) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster_addr)
+      : "memory");
+}
+// Instruction descriptor for the pair MMA: D fp32, A and B bf16, K-major, M = 256, N = 256.
+constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                                ((uint32_t)(256 >> 4) << 24);
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdescPair), "r"(accumulate)
+      : "memory");
+}
+// Commit the issuing thread's outstanding pair MMAs to the barrier at the same
+// offset in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                   "r"(smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+
 __global__ void __launch_bounds__(kThreadsLM, 1)
     k_lmhead(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv) {
   extern __shared__ uint8_t smem_raw[];
@@ -470,6 +518,245 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   }
 }
 
+// The same LM head on SM pairs: a cluster of two CTAs computes M = 256 rows x
+// N = 256 vocabulary entries per tcgen05.mma.cta_group::2 instruction, issued
+// by one thread of the leader CTA (rank 0).  Each CTA stages its own 128 rows
+// of A and its own 128-row half of the W tile (32 KB per stage, 6 stages), so
+// a pair streams W once for 256 rows; the accumulator of each CTA's 128 rows
+// lands in its own TMEM, and each CTA runs the same epilogue on its rows.
+//   full[s]   (leader)  both CTAs' TMA bytes; the leader arms it with the total
+//   empty[s]  (both)    released by the leader's commit, multicast to the pair
+//   tfull[b]  (both)    accumulator ready, multicast from the leader's commit
+//   tempty[b] (leader)  both CTAs' 16 epilogue warps release the accumulator
+constexpr int kStagesPair = 6;
+constexpr int kStagePairA = kBM * kBK * 2;        // this CTA's 128 rows of h
+constexpr int kStagePairB = (kBN / 2) * kBK * 2;  // this CTA's 128 rows of the W tile
+
+__global__ void __launch_bounds__(kThreadsLM, 1)
+    k_lmhead_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStagesPair * kStagePairA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStagesPair * kStagePairB);
+  uint64_t* empty = full + kStagesPair;
+  uint64_t* tfull = empty + kStagesPair;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  Partial* mrg = reinterpret_cast<Partial*>(reinterpret_cast<uint8_t*>(sB + kStagesPair * kStagePairB) + 256);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int KB = (dv.d + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesPair; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 1) {
+    // one warp of each CTA of the pair allocates together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"((uint32_t)kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before anything arrives on them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_allow_next();
+  const int n_rows = dv.plan->n_active * dv.L;
+  const int n_mt = (n_rows + 2 * kBM - 1) / (2 * kBM);  // 256-row pair tiles
+  const int n_units = n_mt * dv.n_chunks;
+  const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      int issued = 0;
+      for (int u = cid; u < n_units && ok; u += n_clusters) {
+        const int chunk = u / n_mt, mt = u - chunk * n_mt;
+        const int vt0 = chunk * dv.tiles_per_chunk;
+        const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
+        for (int vt = vt0; vt < vt1 && ok; ++vt) {
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full_leader = peer_addr(smem_u32(&full[stage]), 0);
+            if (leader) mbar_expect_tx(&full[stage], (uint32_t)(2 * (kStagePairA + kStagePairB)));
+            tma_load_2d_pair(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM, full_leader);
+            tma_load_2d_pair(sB + stage * kStagePairB, &tmB, kb * kBK, vt * kBN + (int)rank * (kBN / 2), full_leader);
+            ++issued;
+            if (++stage == (uint32_t)kStagesPair) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // drain: one more lap of the ring's waits covers the releases of the last
+      // kStagesPair loads (laps before the first load pass at once), so no copy or
+      // release is still in flight toward this CTA when the pair exits
+      (void)issued;
+      for (int i = 0; i < kStagesPair; ++i) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) break;
+        if (++stage == (uint32_t)kStagesPair) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer (leader)
+    if (lane == 0 && leader) {
+      uint32_t stage = 0, phase = 0, tcount = 0;
+      bool ok = true, any = false;
+      for (int u = cid; u < n_units && ok; u += n_clusters) {
+        const int chunk = u / n_mt;
+        const int vt0 = chunk * dv.tiles_per_chunk;
+        const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
+        for (int vt = vt0; vt < vt1 && ok; ++vt, ++tcount) {
+          const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
+          if (!mbar_wait(&tempty[ab], aph ^ 1u, abort_flag, dv.plan)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + ab * (uint32_t)kBN;
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, dv.plan)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + stage * kStagePairA);
+            const uint32_t b0 = smem_u32(sB + stage * kStagePairB);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_pair(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), (kb | kk) != 0 ? 1u : 0u);
+            mma_commit_pair(&empty[stage], (uint16_t)0x3);
+            any = true;
+            if (++stage == (uint32_t)kStagesPair) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit_pair(&tfull[ab], (uint16_t)0x3);
+        }
+      }
+      if (!ok && any) {
+        mma_commit_pair(drain, (uint16_t)0x1);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(drain, 0u) && global_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int cg = (warp - 2) >> 2;
+    const uint32_t tempty_leader[2] = {peer_addr(smem_u32(&tempty[0]), 0), peer_addr(smem_u32(&tempty[1]), 0)};
+    uint32_t tcount = 0;
+    bool aborted = false;
+    for (int u = cid; u < n_units; u += n_clusters) {
+      const int chunk = u / n_mt, mt = u - chunk * n_mt;
+      const int vt0 = chunk * dv.tiles_per_chunk;
+      const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
+      const int rl = q * 32 + lane;
+      const int row = mt * 2 * kBM + (int)rank * kBM + rl;
+      RowMeta rm;
+      rm.valid = row < n_rows;
+      rm.key0 = rm.key1 = rm.bs = rm.p = 0u;
+      rm.scale = 0.f;
+      if (rm.valid) {
+        const int a = row / dv.L;
+        const int c = dv.active[a];
+        const dg_slot sl = dv.slots[c];
+        rm.p = (uint32_t)(row - a * dv.L);
+        rm.key0 = (uint32_t)sl.seed;
+        rm.key1 = (uint32_t)(sl.seed >> 32);
+        rm.bs = ((uint32_t)sl.block << 16) | (uint32_t)sl.step;
+        rm.scale = 1.4426950408889634f / sl.temperature;
+      }
+      Partial st = empty_partial();
+      float kscr = INFINITY;
+      for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
+        if (aborted) continue;
+        const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
+        int got = 0;
+        if (lane == 0) got = mbar_wait(&tfull[ab], aph, abort_flag, dv.plan) ? 1 : 0;
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) {
+          aborted = true;
+          continue;
+        }
+        tc_fence_after();
+        const uint32_t tbase =
+            tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(cg * kColsPerWarp);
+#pragma unroll 1
+        for (int cc = 0; cc < kColsPerWarp / 32; ++cc) {
+          float acc[32];
+          __syncwarp();  // tcgen05.ld is .sync.aligned: the fold below may leave lanes diverged
+          tmem_ld32(tbase + (uint32_t)(cc * 32), acc);
+          if (cc == kColsPerWarp / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader[ab]);
+          }
+          if (rm.valid) fold32(acc, vt * kBN + cg * kColsPerWarp + cc * 32, dv.V, rm, st, kscr);
+        }
+      }
+      mrg[cg * kBM + rl] = st;
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+      if (cg == 0 && rm.valid) {
+        Partial m = st;
+#pragma unroll
+        for (int k = 1; k < kColGroups; ++k) m = merge_partial(m, mrg[k * kBM + rl]);
+        dv.part[(size_t)row * dv.n_sub + chunk] = m;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs are done with the pair's TMEM and barriers
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)kTmemCols)
+                 : "memory");
+  }
+}
+
+constexpr size_t kSmemBytesPair =
+    1024 + (size_t)kStagesPair * (kStagePairA + kStagePairB) + 256 + sizeof(Partial) * kColGroups * kBM;
+static_assert(kSmemBytesPair <= 232448, "shared memory per CTA");
+
 constexpr size_t kSmemBytes =
     1024 + (size_t)kStages * (kStageA + kStageB) + 256 + sizeof(Partial) * kColGroups * kBM;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -477,7 +764,34 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 }  // namespace
 
 cudaError_t lmhead_configure() {
-  return cudaFuncSetAttribute(k_lmhead, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(k_lmhead, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_lmhead_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesPair);
+  return e;
+}
+
+cudaError_t launch_lmhead_pair(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
+                               cudaStream_t st) {
+  // persistent grid of CTA pairs, never more pairs than the largest number of work units
+  const int max_mt = (dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM);
+  int pairs = max_mt * dv.n_chunks;
+  if (pairs > num_sms / 2) pairs = num_sms / 2;
+  if (pairs < 1) pairs = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kThreadsLM);
+  cfg.dynamicSmemBytes = kSmemBytesPair;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_lmhead_pair, *tmA, *tmB, dv);
 }
 
 cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,

@@ -20,6 +20,7 @@ struct dg_sampler {
   std::vector<int32_t> admit;
   dg::Dev dv;
   CUtensorMap tmA, tmB;
+  bool pair;  // LM head on CTA pairs (tcgen05 cta_group::2), chosen when a tick can hold >= 256 rows
   cudaStream_t stream;
   int num_sms;
   int64_t host_tick;
@@ -194,7 +195,10 @@ dg_status tick(dg_sampler* s, const float* resid) {
   DG_CUDA(s->err, mark(0), "record timing event");
   DG_CUDA(s->err, dg::launch_rmsnorm(s->dv, resid, s->stream), "launch rmsnorm");
   DG_CUDA(s->err, mark(1), "record timing event");
-  DG_CUDA(s->err, dg::launch_lmhead(s->dv, &s->tmA, &s->tmB, s->num_sms, s->stream), "launch lm head");
+  DG_CUDA(s->err,
+          s->pair ? dg::launch_lmhead_pair(s->dv, &s->tmA, &s->tmB, s->num_sms, s->stream)
+                  : dg::launch_lmhead(s->dv, &s->tmA, &s->tmB, s->num_sms, s->stream),
+          "launch lm head");
   DG_CUDA(s->err, mark(2), "record timing event");
   DG_CUDA(s->err, dg::launch_finish(s->dv, s->stream), "launch finish");
   DG_CUDA(s->err, mark(3), "record timing event");
@@ -310,7 +314,9 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
     return st;
   };
   if (!encode_2d(&s->tmA, dv.h, (uint64_t)L.rows_cap, (uint64_t)dv.d, dg::kBM, s->err)) return fail(DG_ERR_ARG);
-  if (!encode_2d(&s->tmB, w_vocab, (uint64_t)dv.V, (uint64_t)dv.d, dg::kBN, s->err)) return fail(DG_ERR_ARG);
+  s->pair = (int64_t)L.max_active * cfg->canvas_len >= 2 * dg::kBM && sms >= 2;
+  if (!encode_2d(&s->tmB, w_vocab, (uint64_t)dv.V, (uint64_t)dv.d, s->pair ? dg::kBN / 2 : dg::kBN, s->err))
+    return fail(DG_ERR_ARG);
   cudaError_t ce = dg::lmhead_configure();
   if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "configure lm-head kernel"));
 
