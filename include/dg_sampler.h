@@ -214,6 +214,61 @@ dg_status dg_set_state(dg_sampler* s, const dg_state* host);
 const char* dg_status_string(dg_status st);
 const char* dg_last_error(const dg_sampler* s); /* "" when none; s may be NULL (last create failure) */
 
+/*
+ * Stateless LM-head statistics without any workspace.  The paper has no
+ * counterpart: this is a library convenience, not a step of the method.
+ *
+ * Computes steps 1-3 above for the positions of ONE canvas -- RMSNorm, tied LM
+ * head, and at temperature T the entropy H (nats), log Z, the sampled token
+ * and the argmax of every position -- exactly as a sampler tick computes them
+ * for an active canvas with this seed, block, step and temperature (position
+ * p is row p of resid).  Nothing is committed or re-noised and no sampler is
+ * needed.
+ *
+ * Who it is for: callers that cannot allocate device memory at the point of
+ * the call, such as engines that reserve the whole device for their own pool
+ * at start-up (a later cudaMalloc fails), or code that must not allocate
+ * because cudaMalloc/cudaFree would synchronize the device.  The scratch this
+ * call needs (the normalised rows and the split-vocabulary partial records)
+ * is one fixed array in device global memory inside the library, about
+ * 2.7 MB on each device the library is loaded on, held until the process
+ * exits.  Nothing is allocated per call, by this function or by anything it
+ * calls.
+ *
+ * Limits: 1 <= rows <= DG_STATIC_MAX_ROWS; hidden a multiple of 8 and
+ * <= DG_STATIC_MAX_HIDDEN; vocab >= 2; temperature > 0; block and step in
+ * [0, 65535].  Larger sizes are rejected with DG_ERR_ARG and a message saying
+ * which limit was passed; nothing is launched then.
+ *
+ *   resid     dev, fp32 [rows, hidden], 16-byte aligned.
+ *   w_vocab   dev, bf16 [vocab, hidden] row-major, 16-byte aligned.
+ *   norm_w    dev, fp32 [hidden] (16-byte aligned), or NULL for all ones.
+ *   entropy, logz      dev, fp32 [rows] outputs.
+ *   sample, argmax     dev, int32 [rows] outputs.
+ *   stream    the work is enqueued on this stream, then the call waits for it.
+ *   err       host buffer of err_len bytes for a message on failure, or NULL.
+ *
+ * Synchronizing: it returns after the stream has finished the work and
+ * reports a non-finite statistic (DG_ERR_NONFINITE) or an expired bounded
+ * wait (DG_ERR_TIMEOUT) found on the device.
+ *
+ * The first call on each device (with that device current) does a one-time
+ * set-up: it looks up the scratch array's device address and sets the
+ * kernels' shared-memory limits.  Make that first call before capturing any
+ * stream, e.g. once at start-up.
+ *
+ * Every call on a device shares the one scratch array, and each call resets
+ * the parts of it that must start cleared.  Calls that overlap in time --
+ * from two host threads, or on two streams -- race on it and give wrong
+ * results: serialize them.  The sampler entry points do not use this array.
+ */
+#define DG_STATIC_MAX_ROWS 256
+#define DG_STATIC_MAX_HIDDEN 4096
+dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, const void* w_vocab, int32_t vocab,
+                                 int32_t hidden, const float* norm_w, float rms_eps, float temperature,
+                                 uint64_t seed, int32_t block, int32_t step, float* entropy, float* logz,
+                                 int32_t* sample, int32_t* argmax, dg_stream_t stream, char* err, size_t err_len);
+
 #ifdef __cplusplus
 }
 #endif

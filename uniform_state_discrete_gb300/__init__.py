@@ -85,6 +85,11 @@ _SIGS = {
     "dg_set_state": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(dg_state)]),
     "dg_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dg_last_error": (ctypes.c_char_p, [ctypes.c_void_p]),
+    "dg_lmhead_stats_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_void_p, ctypes.c_float, ctypes.c_float,
+                                              ctypes.c_uint64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_char_p, ctypes.c_size_t]),
 }
 
 
@@ -135,6 +140,26 @@ def make_config(vocab, hidden, canvas_len, n_canvases=1, gen_blocks=1, num_infer
 
 def dg_workspace_size(cfg: dg_config) -> int:
     return int(lib.dg_workspace_size(ctypes.byref(cfg)))
+
+
+def dg_lmhead_stats_static(resid, w_vocab, norm_w, rms_eps, temperature, seed, block, step, entropy, logz, sample,
+                           argmax, stream=None):
+    """LM-head statistics of one canvas into caller-provided outputs, with no device allocation.
+
+    ``resid`` fp32 [rows, d], ``w_vocab`` bf16 [V, d], ``norm_w`` fp32 [d] or None; ``entropy``/``logz`` fp32
+    [rows] and ``sample``/``argmax`` int32 [rows] are written.  Raises ``DGError`` with the library's message.
+    """
+    import torch
+    rows, d = resid.shape
+    st = stream if stream is not None else torch.cuda.current_stream(resid.device)
+    msg = ctypes.create_string_buffer(512)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    status = lib.dg_lmhead_stats_static(ptr(resid), rows, ptr(w_vocab), w_vocab.shape[0], d, ptr(norm_w),
+                                        float(rms_eps), float(temperature), int(seed), int(block), int(step),
+                                        ptr(entropy), ptr(logz), ptr(sample), ptr(argmax),
+                                        ctypes.c_void_p(st.cuda_stream), msg, len(msg))
+    if status != DG_OK:
+        raise DGError(status, msg.value.decode())
 
 
 class Sampler:
