@@ -60,7 +60,8 @@ SIGMA_HIDDEN = 0.5
 def kernel_source_digest() -> str:
     """Digest of the LM-head kernel sources; a stored ncu traffic figure is valid only for this digest."""
     h = hashlib.sha256()
-    for rel in ("uniform_state_discrete_gb300/csrc/dg_lmhead.cu", "uniform_state_discrete_gb300/csrc/dg_internal.cuh"):
+    for rel in ("uniform_state_discrete_gb300/csrc/dg_lmhead.cu", "uniform_state_discrete_gb300/csrc/dg_internal.cuh",
+                "uniform_state_discrete_gb300/csrc/dg_gumbel.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -286,8 +287,7 @@ def run_ours(args, wl, world, rank, local):
             flush.sum(dtype=torch.int32)
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    t_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    for e in ev + t_ev:  # torch creates the CUDA event on first record
+    for e in ev:  # torch creates the CUDA event on first record
         e.record(stream)
 
     def capture(timed_kernels: bool):
@@ -311,22 +311,28 @@ def run_ours(args, wl, world, rank, local):
             os.path.join(ROOT, "gpurun_out")) else None)
         clocks.start()
         time.sleep(0.3)
-        # timed region: whole ticks only, so nothing separates the kernels of a tick
-        tick_ms = np.zeros(args.steps)
+        # timed region: whole ticks only, so nothing separates the kernels of a tick.  The
+        # ticks are enqueued back to back, as a serving loop would issue them, and every
+        # tick is bracketed by its own pair of events; the host reads them at the end.
+        tick_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+        for a, b in tick_ev:
+            a.record(stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
         t_wall0 = time.perf_counter()
         for k in range(args.steps):
             make_resid()
             flush_l2()
-            t_ev[0].record(stream)
+            tick_ev[k][0].record(stream)
             if graph is not None:
                 graph.replay()
             else:
                 s.step(resid)
-            t_ev[1].record(stream)
-            t_ev[1].synchronize()
-            tick_ms[k] = t_ev[0].elapsed_time(t_ev[1])
+            tick_ev[k][1].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
+        tick_ms = np.array([a.elapsed_time(b) for a, b in tick_ev])
         barrier(world)
         torch.cuda.synchronize(dev)
         clk = clocks.stop()
@@ -410,8 +416,9 @@ def run_ours(args, wl, world, rank, local):
                                  "events)" if args.flush == "writeread" else "flushed by a 256 MB write",
                            "graph": bool(args.graph),
                            "parallelism": f"replicas x{world} (independent canvases per GPU)" if world > 1 else "1 GPU",
-                           "timing": "CUDA events around each whole tick on the sampler stream (timed region); "
-                                     "a second pass with events between the 3 kernels gives ms_per_kernel"},
+                           "timing": "CUDA events around each whole tick on the sampler stream, ticks enqueued back "
+                                     "to back without host synchronisation (timed region); a second pass with events "
+                                     "between the 3 kernels gives ms_per_kernel"},
                 "ms_per_kernel": {n: float(per_kernel[:, i].mean()) for i, n in
                                   enumerate(("k_rmsnorm", "k_lmhead", "k_finish"))},
                 "tick_ms_p50": float(np.percentile(tick_ms, 50)), "tick_ms_p99": float(np.percentile(tick_ms, 99)),

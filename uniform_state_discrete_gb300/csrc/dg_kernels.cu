@@ -40,33 +40,85 @@ __device__ __forceinline__ uint32_t bf16_rne_pair(float hi, float lo) {
   return (b >> 16) + up;
 }
 
-// h = bf16( w * r * sqrt(d) / (||r||_2 + eps) ) per active row, one warp per
-// row.  The rounding of every element is the one the exact quotient gives
-// (up to ~2^-46 relative): sum of squares in TwoSum pairs, the per-row
-// scale sqrt(d) / (norm + eps) in fp64 (two operations per row), split into
-// an fp32 pair, and each product carried exactly before the bf16 rounding.
-__global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ resid, const Dev dv) {
+// Accumulate x^2 into the unevaluated pair (sh, sl): the square is split
+// exactly by an FMA, its high part added by TwoSum, all low parts summed.
+__device__ __forceinline__ void acc_square(float x, float& sh, float& sl) {
+  const float sq = __fmul_rn(x, x);
+  const float sq_err = fmaf(x, x, -sq);
+  float e;
+  two_sum(sh, sq, sh, e);
+  sl = __fadd_rn(sl, __fadd_rn(e, sq_err));
+}
+
+// bf16 bits of w x (inv_hi + inv_lo), rounded as the exact product would be.
+__device__ __forceinline__ uint32_t scaled_bf16(float x, float w, float inv_hi, float inv_lo) {
+  const float xw = __fmul_rn(w, x);  // w x = xw + xw_err exactly
+  const float xw_err = fmaf(w, x, -xw);
+  const float ph = __fmul_rn(xw, inv_hi);  // (w x) inv ~= ph + pl
+  const float pe = fmaf(xw, inv_hi, -ph);
+  const float pl = fmaf(xw, inv_lo, fmaf(xw_err, inv_hi, pe));
+  const float hi = __fadd_rn(ph, pl);  // renormalise: |lo| <= ulp(hi)/2
+  const float lo = __fsub_rn(pl, __fsub_rn(hi, ph));
+  return bf16_rne_pair(hi, lo) & 0xFFFFu;
+}
+
+// h = bf16( w * r * sqrt(d) / (||r||_2 + eps) ) per active row.  The rounding
+// of every element is the one the exact quotient gives (up to ~2^-46
+// relative): sum of squares in TwoSum pairs, the per-row scale sqrt(d) /
+// (norm + eps) in fp64 (two operations per row), split into an fp32 pair, and
+// each product carried exactly before the bf16 rounding.
+//
+// Layout for latency: one CTA of kNormThreads (eight warps) per row.  A row
+// of up to kNormThreads * kNormVec float4 (d <= 4096) is loaded into
+// registers with every load issued before the first use, so the kernel costs
+// about one memory round trip; longer rows are read twice.  At most 40
+// registers a thread, so a CTA fits on an SM beside a resident LM-head CTA
+// that was launched early.
+constexpr int kNormThreads = 256;
+constexpr int kNormVec = 4;
+
+__global__ void __launch_bounds__(kNormThreads, 6) k_rmsnorm(const float* __restrict__ resid, const Dev dv) {
+  __shared__ float red[kNormThreads / 32][2];
+  __shared__ float scale[2];
   pdl_wait();
   pdl_allow_next();
-  const int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
   const int n_rows = dv.plan->n_active * dv.L;
-  if (row >= n_rows) return;
-  const int a = row / dv.L, p = row - a * dv.L;
-  const int c = dv.active[a];
-  const float4* r4 = reinterpret_cast<const float4*>(resid + ((size_t)c * dv.L + p) * dv.d);
+  if ((int)blockIdx.x >= n_rows) return;  // uniform per CTA
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int row = blockIdx.x;
   const int n4 = dv.d >> 2;
+  const bool in_regs = n4 <= kNormThreads * kNormVec;
+  const int a = row / dv.L, p = row - a * dv.L;
+  const float4* r4 = reinterpret_cast<const float4*>(resid + ((size_t)dv.active[a] * dv.L + p) * dv.d);
+  float4 v[kNormVec];
   float sh = 0.f, sl = 0.f;
-  for (int i = lane; i < n4; i += 32) {
-    const float4 v = __ldg(r4 + i);
-    const float xs[4] = {v.x, v.y, v.z, v.w};
+  if (in_regs) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float sq = __fmul_rn(xs[j], xs[j]);
-      const float sq_err = fmaf(xs[j], xs[j], -sq);
-      float e;
-      two_sum(sh, sq, sh, e);
-      sl = __fadd_rn(sl, __fadd_rn(e, sq_err));
+    for (int k = 0; k < kNormVec; ++k) {
+      const int i = t + k * kNormThreads;
+      v[k] = i < n4 ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kNormVec; ++k) {
+      acc_square(v[k].x, sh, sl);
+      acc_square(v[k].y, sh, sl);
+      acc_square(v[k].z, sh, sl);
+      acc_square(v[k].w, sh, sl);
+    }
+  } else {
+    for (int i0 = t; i0 < n4; i0 += kNormThreads * kNormVec) {
+#pragma unroll
+      for (int k = 0; k < kNormVec; ++k) {
+        const int i = i0 + k * kNormThreads;
+        v[k] = i < n4 ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kNormVec; ++k) {
+        acc_square(v[k].x, sh, sl);
+        acc_square(v[k].y, sh, sl);
+        acc_square(v[k].z, sh, sl);
+        acc_square(v[k].w, sh, sl);
+      }
     }
   }
 #pragma unroll
@@ -77,29 +129,45 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ resid
     two_sum(sh, oh, sh, e);
     sl = __fadd_rn(__fadd_rn(sl, ol), e);
   }
-  const double inv = sqrt((double)dv.d) / (sqrt((double)sh + (double)sl) + (double)dv.eps);
-  const float inv_hi = __double2float_rn(inv);
-  const float inv_lo = __double2float_rn(inv - (double)inv_hi);
+  if (lane == 0) {
+    red[warp][0] = sh;
+    red[warp][1] = sl;
+  }
+  __syncthreads();
+  if (t == 0) {
+    float h = red[0][0], l = red[0][1];
+#pragma unroll
+    for (int w = 1; w < kNormThreads / 32; ++w) {
+      float e;
+      two_sum(h, red[w][0], h, e);
+      l = __fadd_rn(__fadd_rn(l, red[w][1]), e);
+    }
+    const double inv = sqrt((double)dv.d) / (sqrt((double)h + (double)l) + (double)dv.eps);
+    const float inv_hi = __double2float_rn(inv);
+    scale[0] = inv_hi;
+    scale[1] = __double2float_rn(inv - (double)inv_hi);
+  }
+  __syncthreads();
+  const float inv_hi = scale[0], inv_lo = scale[1];
   uint2* out = reinterpret_cast<uint2*>(dv.h + (size_t)row * dv.d);
   const float4* w4 = reinterpret_cast<const float4*>(dv.norm_w);
-  for (int i = lane; i < n4; i += 32) {
-    const float4 v = __ldg(r4 + i);
-    const float4 w = w4 ? __ldg(w4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
-    const float xs[4] = {v.x, v.y, v.z, v.w};
-    const float ws[4] = {w.x, w.y, w.z, w.w};
-    uint32_t hb[4];
+  if (in_regs) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float xw = __fmul_rn(ws[j], xs[j]);            // w x = xw + xw_err exactly
-      const float xw_err = fmaf(ws[j], xs[j], -xw);
-      const float ph = __fmul_rn(xw, inv_hi);               // (w x) inv ~= ph + pl
-      const float pe = fmaf(xw, inv_hi, -ph);
-      const float pl = fmaf(xw, inv_lo, fmaf(xw_err, inv_hi, pe));
-      const float hi = __fadd_rn(ph, pl);                   // renormalise: |lo| <= ulp(hi)/2
-      const float lo = __fsub_rn(pl, __fsub_rn(hi, ph));
-      hb[j] = bf16_rne_pair(hi, lo) & 0xFFFFu;
+    for (int k = 0; k < kNormVec; ++k) {
+      const int i = t + k * kNormThreads;
+      if (i < n4) {
+        const float4 w = w4 ? __ldg(w4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
+        out[i] = make_uint2(scaled_bf16(v[k].x, w.x, inv_hi, inv_lo) | (scaled_bf16(v[k].y, w.y, inv_hi, inv_lo) << 16),
+                            scaled_bf16(v[k].z, w.z, inv_hi, inv_lo) | (scaled_bf16(v[k].w, w.w, inv_hi, inv_lo) << 16));
+      }
     }
-    out[i] = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+  } else {
+    for (int i = t; i < n4; i += kNormThreads) {
+      const float4 x = __ldg(r4 + i);
+      const float4 w = w4 ? __ldg(w4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
+      out[i] = make_uint2(scaled_bf16(x.x, w.x, inv_hi, inv_lo) | (scaled_bf16(x.y, w.y, inv_hi, inv_lo) << 16),
+                          scaled_bf16(x.z, w.z, inv_hi, inv_lo) | (scaled_bf16(x.w, w.w, inv_hi, inv_lo) << 16));
+    }
   }
 }
 
@@ -224,7 +292,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 cudaError_t launch_rmsnorm(const Dev& dv, const float* resid, cudaStream_t st) {
   const int rows = dv.max_active * dv.L;
-  return launch_pdl(k_rmsnorm, dim3((rows + 7) / 8), dim3(256), 0, st, resid, dv);
+  return launch_pdl(k_rmsnorm, dim3(rows), dim3(kNormThreads), 0, st, resid, dv);
 }
 
 cudaError_t launch_finish(const Dev& dv, cudaStream_t st) {

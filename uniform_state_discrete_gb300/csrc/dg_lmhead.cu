@@ -29,6 +29,7 @@
 // drains what it issued and frees TMEM.
 #include <cuda_runtime.h>
 
+#include "dg_gumbel.cuh"
 #include "dg_internal.cuh"
 
 namespace dg {
@@ -41,6 +42,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// Raise the barrier's expected transaction bytes without arriving on it.
+__device__ __forceinline__ void mbar_expect_tx_only(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cluster.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -142,6 +148,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
 // -log2(E) for the Exp(1) variate E = -ln U of one Gumbel draw,
 // U = (r + 0.5) 2^-32.  For U < 3/4, E comes from lg2(U).  For U >= 3/4,
 // E = -ln(1 - q) with q = 1 - U taken exactly from the integer, through the
@@ -167,86 +187,142 @@ __device__ __forceinline__ float neg_log2_exp_variate(uint32_t r) {
 }
 
 struct RowMeta {
-  uint32_t key0, key1, bs, p;
-  float scale;  // log2(e) / T
+  GumbelStream gs;  // this position's Philox stream of Gumbel words
+  float scale;      // log2(e) / T
   bool valid;
 };
 
-// Screen factor K = 2^(m - g + 32) (with 0.2 % slack): a Gumbel draw can raise the
-// best perturbed score g only if q < 2^(u - g) = e * 2^(m - g), e = 2^(u - m) being
-// the element's softmax weight, i.e. only if float(~r) < e * K.  The slack covers
-// the rounding of e, K and float(~r).  g = -inf lets every element through.
-__device__ __forceinline__ float screen_factor(float m, float g) {
-  return g == -INFINITY ? INFINITY : 1.002f * ex2_approx(m - g + 32.f);
+// Meta data of TMEM lane `row` of the current unit: the position's canvas
+// seed, block, step and temperature.
+__device__ __forceinline__ RowMeta row_meta(const Dev& dv, int row, int n_rows) {
+  RowMeta rm;
+  rm.valid = row < n_rows;
+  rm.scale = 0.f;
+  if (rm.valid) {
+    const int a = row / dv.L;
+    const dg_slot sl = dv.slots[dv.active[a]];
+    rm.gs.init(sl.seed, (uint32_t)(row - a * dv.L), ((uint32_t)sl.block << 16) | (uint32_t)sl.step,
+               kPurposeGumbel);
+    rm.scale = 1.4426950408889634f / sl.temperature;
+  } else {
+    rm.gs.init(0ull, 0u, 0u, kPurposeGumbel);
+  }
+  return rm;
 }
 
-// Fold 32 columns [v0, v0+32) of one row into its running statistics.
+// Screen factor K ~ 2^(m - g).  A Gumbel draw can raise the best perturbed
+// score g only if q < 2^(u - g) = e 2^(m - g), where q = 1 - U <= -ln U = E and
+// e = 2^(u - m) is the element's softmax weight.  The factor carries 0.2 %
+// slack for the approximate exponentials and logarithms, plus the rounding of
+// scores of magnitude up to |m| + 64, so the screen never drops an element
+// that could win.
+__device__ __forceinline__ float screen_factor(float m, float g) {
+  return ex2_approx(m - g) * fmaf(fabsf(m) + 64.f, 0x1p-20f, 1.002f);
+}
+
+// Pass test of the screen without an integer-to-float conversion: with
+// Ut = (r >> 9) 2^-23 <= U, f = 1 + Ut is built by one funnel shift, and
+// q < e K implies f > 2 - e K - 2^-22; the threshold below leaves a further
+// 2^-22 for its own rounding.
+__device__ __forceinline__ float screen_word(uint32_t r) { return __uint_as_float(__funnelshift_r(r, 0x7Fu, 9)); }
+__device__ __forceinline__ float screen_threshold(float e, float K) { return fmaf(-e, K, 2.f - 0x1p-21f); }
+
+__device__ __forceinline__ uint32_t pick4(const uint32_t (&w)[4], uint32_t i) {
+  uint32_t r = w[0];
+  r = i == 1u ? w[1] : r;
+  r = i == 2u ? w[2] : r;
+  r = i == 3u ? w[3] : r;
+  return r;
+}
+
+// Fold 32 columns [v0, v0+32) of one row (raw fp32 logits z) into its running
+// statistics.  kTail: some of the columns lie at or beyond V.
 //
-// Softmax statistics in base 2: u = z log2(e)/T, running max m, S = sum 2^(u-m),
-// A = sum 2^(u-m)(u-m); the argmax index is looked up only when the chunk
-// raises the running max.
+// Softmax statistics in base 2 with u = z log2(e)/T: running max m, S = sum
+// 2^(u-m), A = sum 2^(u-m)(u-m), formed from d = u - m = fma(z, log2(e)/T, -m).
+// The argmax index is looked up only when the fold raises the running max.
 //
-// Gumbel-max sample: the perturbed score is u - log2 E with E = -ln U the
-// Exp(1) variate of the element's Philox word r.  Since -ln U >= 1 - U = q =
-// (~r + 0.5) 2^-32, the element can beat the running best g only if
-// q < 2^(u - g); that test costs one multiply of the softmax weight already
-// computed (see screen_factor).  Elements failing it cannot win and skip the
-// exact transform, so the result equals the unscreened maximum.
-__device__ __forceinline__ void fold32(float (&u)[32], int v0, int V, const RowMeta& rm, Partial& st, float& kscr) {
+// Gumbel-max sample: the perturbed score of an element is (m + d) - log2 E
+// with E = -ln U the Exp(1) variate of its Philox word.  The first fold that
+// sets the maximum seeds the best score with the maximum element's own draw,
+// so later elements face a finite screen at once; elements that pass the
+// screen (checked four at a time, one branch per Philox block) are scored
+// exactly, so the result equals the unscreened maximum.  Equal scores keep
+// the lower index.
+template <bool kTail>
+__device__ __forceinline__ void fold32(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, float& K) {
+  if (kTail) {
+    if (v0 >= V) return;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) u[j] *= rm.scale;
-  const bool full = (v0 + 32 <= V);
-  if (!full) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (v0 + j >= V) u[j] = -INFINITY;
+    for (int j = 0; j < 16; ++j)
+      if (v0 + j >= V) z[j] = -INFINITY;
   }
-  float cm = u[0];
+  float cmz = z[0];
 #pragma unroll
-  for (int j = 1; j < 32; ++j) cm = fmaxf(cm, u[j]);
-  if (cm == -INFINITY) return;  // a fully masked tail chunk
+  for (int j = 1; j < 16; ++j) cmz = fmaxf(cmz, z[j]);
+  const float cm = cmz * rm.scale;
   if (cm > st.m) {
     const float f = ex2_approx(st.m - cm);
     st.A = st.S > 0.f ? f * fmaf(st.m - cm, st.S, st.A) : 0.f;
     st.S = f * st.S;
     st.m = cm;
-    int ci = 31;
+    int ci = 15;
 #pragma unroll
-    for (int j = 31; j >= 0; --j)
-      if (u[j] == cm) ci = j;  // first index holding the maximum
+    for (int j = 15; j >= 0; --j)
+      if (z[j] == cmz) ci = j;  // first index holding the maximum
     st.amax = v0 + ci;
-    kscr = screen_factor(st.m, st.g);
-  }
-  float S = 0.f, A = 0.f;
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    const int vb = v0 + 4 * g;
-    float e[4];
-#pragma unroll
-    for (int l = 0; l < 4; ++l) {
-      const float dlt = u[4 * g + l] - st.m;
-      e[l] = ex2_approx(dlt);
-      if (full || vb + l < V) {
-        S += e[l];
-        A = fmaf(e[l], dlt, A);
-      }
+    if (st.g == -INFINITY) {
+      uint32_t w[4];
+      rm.gs.draw((uint32_t)(v0 + ci) >> 2, w);
+      st.g = (cm + fmaf(cmz, rm.scale, -cm)) + neg_log2_exp_variate(pick4(w, (uint32_t)ci & 3u));
+      st.gidx = v0 + ci;
     }
-    const uint4 r = philox(make_uint4((uint32_t)vb >> 2, rm.p, rm.bs, kPurposeGumbel), rm.key0, rm.key1);
-    const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+    K = screen_factor(st.m, st.g);
+  }
+  const float m = st.m, nm = -st.m;
+  float S[4] = {0.f, 0.f, 0.f, 0.f}, A[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int vb = v0 + 4 * g;
+    uint32_t w[4];
+    rm.gs.draw((uint32_t)vb >> 2, w);
+    float d[4];
+    bool pl[4];
+    bool any = false;
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
-      if (__uint2float_rz(~rw[l]) < e[l] * kscr) {
-        const float sc = u[4 * g + l] + neg_log2_exp_variate(rw[l]);
-        if (sc > st.g && (full || vb + l < V)) {
-          st.g = sc;
-          st.gidx = vb + l;
-          kscr = screen_factor(st.m, st.g);
+      const bool ok = !kTail || vb + l < V;
+      d[l] = fmaf(z[4 * g + l], rm.scale, nm);
+      const float e = ex2_approx(d[l]);  // +0 for a masked column (d = -inf)
+      S[l] += e;
+      if (ok) A[l] = fmaf(e, d[l], A[l]);
+      pl[l] = ok && screen_word(w[l]) > screen_threshold(e, K);
+      any |= pl[l];
+    }
+    if (any) {
+#pragma unroll
+      for (int l = 0; l < 4; ++l) {
+        if (pl[l]) {
+          const float sc = (m + d[l]) + neg_log2_exp_variate(w[l]);
+          if (sc > st.g || (sc == st.g && vb + l < st.gidx)) {
+            st.g = sc;
+            st.gidx = vb + l;
+            K = screen_factor(m, st.g);
+          }
         }
       }
     }
   }
-  st.S += S;
-  st.A += A;
+  st.S += (S[0] + S[1]) + (S[2] + S[3]);
+  st.A += (A[0] + A[1]) + (A[2] + A[3]);
+}
+
+// The two 32-column folds of this warp's 64 columns of one accumulator tile.
+__device__ __forceinline__ void fold_cols(float (&acc)[16], int v0, int V, const RowMeta& rm, Partial& st, float& K) {
+  if (v0 + 16 <= V)
+    fold32<false>(acc, v0, V, rm, st, K);
+  else
+    fold32<true>(acc, v0, V, rm, st, K);
 }
 
 // ---------------------------------------------------------------- CTA pairs
@@ -451,20 +527,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
       const int rl = q * 32 + lane;         // row within the tile
       const int row = mt * kBM + rl;
-      RowMeta rm;
-      rm.valid = row < n_rows;
-      rm.key0 = rm.key1 = rm.bs = rm.p = 0u;
-      rm.scale = 0.f;
-      if (rm.valid) {
-        const int a = row / dv.L;
-        const int c = dv.active[a];
-        const dg_slot sl = dv.slots[c];
-        rm.p = (uint32_t)(row - a * dv.L);
-        rm.key0 = (uint32_t)sl.seed;
-        rm.key1 = (uint32_t)(sl.seed >> 32);
-        rm.bs = ((uint32_t)sl.block << 16) | (uint32_t)sl.step;
-        rm.scale = 1.4426950408889634f / sl.temperature;
-      }
+      const RowMeta rm = row_meta(dv, row, n_rows);
       Partial st = empty_partial();
       float kscr = INFINITY;
       for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
@@ -481,17 +544,17 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         const uint32_t tbase =
             tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(cg * kColsPerWarp);
 #pragma unroll 1
-        for (int cc = 0; cc < kColsPerWarp / 32; ++cc) {
-          float acc[32];
+        for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
+          float acc[16];
           __syncwarp();  // tcgen05.ld is .sync.aligned: the fold below may leave lanes diverged
-          tmem_ld32(tbase + (uint32_t)(cc * 32), acc);
-          if (cc == kColsPerWarp / 32 - 1) {
+          tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
+          if (cc == kColsPerWarp / 16 - 1) {
             // the accumulator is in registers: hand the buffer back to the MMA warp early
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
           }
-          if (rm.valid) fold32(acc, vt * kBN + cg * kColsPerWarp + cc * 32, dv.V, rm, st, kscr);
+          if (rm.valid) fold_cols(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, kscr);
         }
       }
       // merge the four column groups of each row; one record per row and chunk.  Every
@@ -581,12 +644,32 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   cluster_sync();  // the peer's barriers are initialised before anything arrives on them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+  // W does not depend on the previous kernel, so its first stages are loaded
+  // before the wait below.  This needs the pair's first unit to be known
+  // already, which holds when one 256-row pair tile covers every position the
+  // sampler can hold: the unit is then vocabulary chunk `cid` whenever any
+  // canvas is active.  The leader raises the stage's expected bytes by the W
+  // halves now and arrives, with the h halves, after the wait.
+  int pre = 0;
+  if ((dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM) == 1 && cid < dv.n_chunks) {
+    const int vt0 = cid * dv.tiles_per_chunk;
+    pre = min(kStagesPair, KB * (min(vt0 + dv.tiles_per_chunk, dv.n_vtiles) - vt0));
+    if (warp == 0 && lane == 0) {
+      for (int it = 0; it < pre; ++it) {
+        const int vt = vt0 + it / KB, kb = it % KB;
+        if (leader) mbar_expect_tx_only(&full[it], (uint32_t)(2 * kStagePairB));
+        tma_load_2d_pair(sB + it * kStagePairB, &tmB, kb * kBK, vt * kBN + (int)rank * (kBN / 2),
+                         peer_addr(smem_u32(&full[it]), 0));
+      }
+    }
+  }
   pdl_wait();
   pdl_allow_next();
   const int n_rows = dv.plan->n_active * dv.L;
   const int n_mt = (n_rows + 2 * kBM - 1) / (2 * kBM);  // 256-row pair tiles
   const int n_units = n_mt * dv.n_chunks;
-  const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -600,19 +683,37 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
         for (int vt = vt0; vt < vt1 && ok; ++vt) {
           for (int kb = 0; kb < KB; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
-              ok = false;
-              break;
-            }
             const uint32_t full_leader = peer_addr(smem_u32(&full[stage]), 0);
-            if (leader) mbar_expect_tx(&full[stage], (uint32_t)(2 * (kStagePairA + kStagePairB)));
-            tma_load_2d_pair(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM, full_leader);
-            tma_load_2d_pair(sB + stage * kStagePairB, &tmB, kb * kBK, vt * kBN + (int)rank * (kBN / 2), full_leader);
+            if (issued < pre) {
+              // first lap, W half already in flight: the h half and the leader's arrival
+              if (leader) mbar_expect_tx(&full[stage], (uint32_t)(2 * kStagePairA));
+              tma_load_2d_pair(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
+                               full_leader);
+            } else {
+              if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
+                ok = false;
+                break;
+              }
+              if (leader) mbar_expect_tx(&full[stage], (uint32_t)(2 * (kStagePairA + kStagePairB)));
+              tma_load_2d_pair(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
+                               full_leader);
+              tma_load_2d_pair(sB + stage * kStagePairB, &tmB, kb * kBK, vt * kBN + (int)rank * (kBN / 2),
+                               full_leader);
+            }
             ++issued;
             if (++stage == (uint32_t)kStagesPair) {
               stage = 0;
               phase ^= 1u;
             }
+          }
+        }
+      }
+      if (issued == 0 && pre > 0 && leader) {
+        // no active canvas: close the preloaded stages and let their copies land
+        for (int it = 0; it < pre; ++it) {
+          mbar_arrive(&full[it]);
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(&full[it], 0u) && global_ns() - t0 < kWaitLimitNs) {
           }
         }
       }
@@ -689,20 +790,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
       const int rl = q * 32 + lane;
       const int row = mt * 2 * kBM + (int)rank * kBM + rl;
-      RowMeta rm;
-      rm.valid = row < n_rows;
-      rm.key0 = rm.key1 = rm.bs = rm.p = 0u;
-      rm.scale = 0.f;
-      if (rm.valid) {
-        const int a = row / dv.L;
-        const int c = dv.active[a];
-        const dg_slot sl = dv.slots[c];
-        rm.p = (uint32_t)(row - a * dv.L);
-        rm.key0 = (uint32_t)sl.seed;
-        rm.key1 = (uint32_t)(sl.seed >> 32);
-        rm.bs = ((uint32_t)sl.block << 16) | (uint32_t)sl.step;
-        rm.scale = 1.4426950408889634f / sl.temperature;
-      }
+      const RowMeta rm = row_meta(dv, row, n_rows);
       Partial st = empty_partial();
       float kscr = INFINITY;
       for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
@@ -719,16 +807,16 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         const uint32_t tbase =
             tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(cg * kColsPerWarp);
 #pragma unroll 1
-        for (int cc = 0; cc < kColsPerWarp / 32; ++cc) {
-          float acc[32];
+        for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
+          float acc[16];
           __syncwarp();  // tcgen05.ld is .sync.aligned: the fold below may leave lanes diverged
-          tmem_ld32(tbase + (uint32_t)(cc * 32), acc);
-          if (cc == kColsPerWarp / 32 - 1) {
+          tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
+          if (cc == kColsPerWarp / 16 - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader[ab]);
           }
-          if (rm.valid) fold32(acc, vt * kBN + cg * kColsPerWarp + cc * 32, dv.V, rm, st, kscr);
+          if (rm.valid) fold_cols(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, kscr);
         }
       }
       mrg[cg * kBM + rl] = st;
