@@ -77,6 +77,7 @@ struct Dev {
   uint32_t* canvas_rows;// [B] rows combined per canvas this tick
   float* resid_stage;   // [B, L, d]
   const float* norm_w;  // [d] or null
+  const float* temps;   // [N] temperature of each step, T_s = t_max + (s/N)(t_min - t_max)
   int32_t V, d, L, B, G, N;
   float t_min, t_max, bound, conf, eps;
   int32_t n_vtiles, tiles_per_chunk, n_chunks, n_sub, rows_cap, max_active;
@@ -107,13 +108,6 @@ __device__ __forceinline__ uint32_t draw_u32(uint64_t seed, uint32_t purpose, in
 // Uniform token in [0, V): Lemire's multiply-shift.
 __device__ __forceinline__ int32_t uniform_token(uint32_t u, int32_t V) {
   return (int32_t)(((uint64_t)u * (uint64_t)(uint32_t)V) >> 32);
-}
-
-// T_s = t_max + (s/N)(t_min - t_max), evaluated in fp64 without contraction,
-// rounded once to fp32.
-__device__ __forceinline__ float temperature(int s, int N, float t_min, float t_max) {
-  const double frac = __ddiv_rn((double)s, (double)N);
-  return __double2float_rn(__dadd_rn((double)t_max, __dmul_rn(frac, __dsub_rn((double)t_min, (double)t_max))));
 }
 
 // ------------------------------------------------------------ small PTX

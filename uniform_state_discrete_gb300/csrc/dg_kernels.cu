@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   const Group g{(int)threadIdx.x, (int)blockDim.x, 0};
   const int n_rows = dv.plan->n_active * dv.L;
   if (n_rows == 0) {
-    if (blockIdx.x == 0) plan_tick(dv, dv.plan->tick + 1, g, &sc);
+    if (blockIdx.x == 0) plan_tick(dv, dv.plan->tick + 1, g, &sc, false);
     return;
   }
   const int row0 = blockIdx.x * kFinishRows;
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
     __syncthreads();
     if (plan_now) {
       __threadfence();
-      plan_tick(dv, __ldcg(&dv.plan->tick) + 1, g, &sc);
+      plan_tick(dv, __ldcg(&dv.plan->tick) + 1, g, &sc, false);
     }
   }
 }
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(256) k_plan(const Dev dv, int tick) {
   __shared__ TailScratch sc;
   for (int i = threadIdx.x; i < dv.B; i += blockDim.x) dv.canvas_rows[i] = 0u;
   __syncthreads();
-  plan_tick(dv, tick, Group{(int)threadIdx.x, (int)blockDim.x, 0}, &sc);
+  plan_tick(dv, tick, Group{(int)threadIdx.x, (int)blockDim.x, 0}, &sc, true);
 }
 
 // Launch with programmatic stream serialization (see pdl_wait / pdl_allow_next).

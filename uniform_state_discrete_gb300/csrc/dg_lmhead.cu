@@ -227,15 +227,56 @@ __device__ __forceinline__ float screen_factor(float m, float g) {
 __device__ __forceinline__ float screen_word(uint32_t r) { return __uint_as_float(__funnelshift_r(r, 0x7Fu, 9)); }
 __device__ __forceinline__ float screen_threshold(float e, float K) { return fmaf(-e, K, 2.f - 0x1p-21f); }
 
-__device__ __forceinline__ uint32_t pick4(const uint32_t (&w)[4], uint32_t i) {
-  uint32_t r = w[0];
-  r = i == 1u ? w[1] : r;
-  r = i == 2u ? w[2] : r;
-  r = i == 3u ? w[3] : r;
-  return r;
+// The same transform without branches (both branches evaluated, one kept), so
+// a warp scores one candidate per lane in lockstep.  Same results.
+__device__ __forceinline__ float neg_log2_exp_variate_nb(uint32_t r) {
+  const float U = fmaf(__uint2float_rn(r), 0x1p-32f, 0x1p-33f);
+  const float Eu = -0.69314718055994531f * lg2_approx(U);
+  const float q = fmaf(__uint2float_rn(~r), 0x1p-32f, 0x1p-33f);
+  const float sq = __fdividef(q, 2.0f - q);
+  const float s2 = sq * sq;
+  float t = fmaf(s2, 1.0f / 9.0f, 1.0f / 7.0f);
+  t = fmaf(s2, t, 1.0f / 5.0f);
+  t = fmaf(s2, t, 1.0f / 3.0f);
+  t = fmaf(s2, t, 1.0f);
+  const float Eq = 2.0f * sq * t;
+  return -lg2_approx(r < 0xC0000000u ? Eu : Eq);
 }
 
-// Fold 32 columns [v0, v0+32) of one row (raw fp32 logits z) into its running
+// z[j] and w[j] for a lane-varying j, by a four-level select tree (registers
+// cannot be indexed).
+__device__ __forceinline__ void select16(const float (&z)[16], const uint32_t (&w)[16], uint32_t j, float& zj,
+                                         uint32_t& wj) {
+  float a[8];
+  uint32_t b[8];
+  const bool b0 = j & 1u, b1 = j & 2u, b2 = j & 4u, b3 = j & 8u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    a[i] = b0 ? z[2 * i + 1] : z[2 * i];
+    b[i] = b0 ? w[2 * i + 1] : w[2 * i];
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a[i] = b1 ? a[2 * i + 1] : a[2 * i];
+    b[i] = b1 ? b[2 * i + 1] : b[2 * i];
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    a[i] = b2 ? a[2 * i + 1] : a[2 * i];
+    b[i] = b2 ? b[2 * i + 1] : b[2 * i];
+  }
+  zj = b3 ? a[1] : a[0];
+  wj = b3 ? b[1] : b[0];
+}
+
+// Order-preserving int image of a float (for atomicMax on shared scores).
+__device__ __forceinline__ int ord_key(float f) {
+  const int b = __float_as_int(f);
+  return b >= 0 ? b : (b ^ 0x7FFFFFFF);
+}
+__device__ __forceinline__ float key_ord(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF)); }
+
+// Fold 16 columns [v0, v0+16) of one row (raw fp32 logits z) into its running
 // statistics.  kTail: some of the columns lie at or beyond V.
 //
 // Softmax statistics in base 2 with u = z log2(e)/T: running max m, S = sum
@@ -243,23 +284,37 @@ __device__ __forceinline__ uint32_t pick4(const uint32_t (&w)[4], uint32_t i) {
 // The argmax index is looked up only when the fold raises the running max.
 //
 // Gumbel-max sample: the perturbed score of an element is (m + d) - log2 E
-// with E = -ln U the Exp(1) variate of its Philox word.  The first fold that
-// sets the maximum seeds the best score with the maximum element's own draw,
-// so later elements face a finite screen at once; elements that pass the
-// screen (checked four at a time, one branch per Philox block) are scored
-// exactly, so the result equals the unscreened maximum.  Equal scores keep
-// the lower index.
+// with E = -ln U the Exp(1) variate of its Philox word.  The screen compares
+// each element against the best score known for the row: this stream's own,
+// seeded with the maximum element's draw by the first fold that sets the
+// maximum, or a better one another column group of the CTA found for the same
+// row (`best`, shared memory).  Either is the score of a real element, so the
+// row's winner always passes the screen, and candidates are scored exactly:
+// the result equals the unscreened maximum.  Candidates are scored one per lane
+// per round, all lanes of the warp together.  Equal scores keep the lower
+// index.
 template <bool kTail>
-__device__ __forceinline__ void fold32(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, float& K) {
+__device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, int* best) {
   if (kTail) {
     if (v0 >= V) return;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       if (v0 + j >= V) z[j] = -INFINITY;
   }
-  float cmz = z[0];
+  uint32_t w[16];
 #pragma unroll
-  for (int j = 1; j < 16; ++j) cmz = fmaxf(cmz, z[j]);
+  for (int g = 0; g < 4; ++g) {
+    uint32_t t4[4];
+    rm.gs.draw(((uint32_t)v0 >> 2) + (uint32_t)g, t4);
+#pragma unroll
+    for (int l = 0; l < 4; ++l) w[4 * g + l] = t4[l];
+  }
+  float t8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) t8[i] = fmaxf(z[i], z[i + 8]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t8[i] = fmaxf(t8[i], t8[i + 4]);
+  const float cmz = fmaxf(fmaxf(t8[0], t8[2]), fmaxf(t8[1], t8[3]));
   const float cm = cmz * rm.scale;
   if (cm > st.m) {
     const float f = ex2_approx(st.m - cm);
@@ -272,57 +327,54 @@ __device__ __forceinline__ void fold32(float (&z)[16], int v0, int V, const RowM
       if (z[j] == cmz) ci = j;  // first index holding the maximum
     st.amax = v0 + ci;
     if (st.g == -INFINITY) {
-      uint32_t w[4];
-      rm.gs.draw((uint32_t)(v0 + ci) >> 2, w);
-      st.g = (cm + fmaf(cmz, rm.scale, -cm)) + neg_log2_exp_variate(pick4(w, (uint32_t)ci & 3u));
+      float zc;
+      uint32_t wc;
+      select16(z, w, (uint32_t)ci, zc, wc);
+      st.g = (cm + fmaf(cmz, rm.scale, -cm)) + neg_log2_exp_variate_nb(wc);
       st.gidx = v0 + ci;
+      atomicMax(best, ord_key(st.g));
     }
-    K = screen_factor(st.m, st.g);
   }
   const float m = st.m, nm = -st.m;
+  const float K = screen_factor(m, fmaxf(st.g, key_ord(*(volatile int*)best)));
   float S[4] = {0.f, 0.f, 0.f, 0.f}, A[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t mask = 0u;
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    const int vb = v0 + 4 * g;
-    uint32_t w[4];
-    rm.gs.draw((uint32_t)vb >> 2, w);
-    float d[4];
-    bool pl[4];
-    bool any = false;
-#pragma unroll
-    for (int l = 0; l < 4; ++l) {
-      const bool ok = !kTail || vb + l < V;
-      d[l] = fmaf(z[4 * g + l], rm.scale, nm);
-      const float e = ex2_approx(d[l]);  // +0 for a masked column (d = -inf)
-      S[l] += e;
-      if (ok) A[l] = fmaf(e, d[l], A[l]);
-      pl[l] = ok && screen_word(w[l]) > screen_threshold(e, K);
-      any |= pl[l];
-    }
-    if (any) {
-#pragma unroll
-      for (int l = 0; l < 4; ++l) {
-        if (pl[l]) {
-          const float sc = (m + d[l]) + neg_log2_exp_variate(w[l]);
-          if (sc > st.g || (sc == st.g && vb + l < st.gidx)) {
-            st.g = sc;
-            st.gidx = vb + l;
-            K = screen_factor(m, st.g);
-          }
-        }
-      }
+  for (int j = 0; j < 16; ++j) {
+    const float d = fmaf(z[j], rm.scale, nm);
+    const float e = ex2_approx(d);  // +0 for a masked column (d = -inf)
+    S[j & 3] += e;
+    if (!kTail || v0 + j < V) A[j & 3] = fmaf(e, d, A[j & 3]);
+    if (screen_word(w[j]) > screen_threshold(e, K) && (!kTail || v0 + j < V)) mask |= 1u << j;
+  }
+  const unsigned act = __activemask();
+  bool improved = false;
+  while (__any_sync(act, mask != 0u)) {
+    const bool has = mask != 0u;
+    const uint32_t j = has ? (uint32_t)(__ffs(mask) - 1) : 0u;
+    mask &= mask - 1u;
+    float zj;
+    uint32_t wj;
+    select16(z, w, j, zj, wj);
+    const float sc = (m + fmaf(zj, rm.scale, nm)) + neg_log2_exp_variate_nb(wj);
+    const int idx = v0 + (int)j;
+    if (has && (sc > st.g || (sc == st.g && idx < st.gidx))) {
+      st.g = sc;
+      st.gidx = idx;
+      improved = true;
     }
   }
+  if (improved) atomicMax(best, ord_key(st.g));
   st.S += (S[0] + S[1]) + (S[2] + S[3]);
   st.A += (A[0] + A[1]) + (A[2] + A[3]);
 }
 
-// The two 32-column folds of this warp's 64 columns of one accumulator tile.
-__device__ __forceinline__ void fold_cols(float (&acc)[16], int v0, int V, const RowMeta& rm, Partial& st, float& K) {
+// The fold of this warp's 16 columns of one accumulator tile.
+__device__ __forceinline__ void fold_cols(float (&acc)[16], int v0, int V, const RowMeta& rm, Partial& st, int* best) {
   if (v0 + 16 <= V)
-    fold32<false>(acc, v0, V, rm, st, K);
+    fold16<false>(acc, v0, V, rm, st, best);
   else
-    fold32<true>(acc, v0, V, rm, st, K);
+    fold16<true>(acc, v0, V, rm, st, best);
 }
 
 // ---------------------------------------------------------------- CTA pairs
@@ -388,6 +440,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // column-group merge area: the four warps of a row quadrant leave their records here
   Partial* mrg = reinterpret_cast<Partial*>(reinterpret_cast<uint8_t*>(sB + kStages * kStageB) + 256);
+  int* gbest = reinterpret_cast<int*>(mrg + kColGroups * kBM);  // best score per row, shared by the column groups
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = (dv.d + kBK - 1) / kBK;
@@ -403,6 +456,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    for (int i = 0; i < kBM; ++i) gbest[i] = ord_key(-INFINITY);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
@@ -529,7 +583,6 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       const int row = mt * kBM + rl;
       const RowMeta rm = row_meta(dv, row, n_rows);
       Partial st = empty_partial();
-      float kscr = INFINITY;
       for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
         if (aborted) continue;
         const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
@@ -554,7 +607,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
           }
-          if (rm.valid) fold_cols(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, kscr);
+          if (rm.valid) fold_cols(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, gbest + rl);
         }
       }
       // merge the four column groups of each row; one record per row and chunk.  Every
@@ -568,6 +621,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         for (int k = 1; k < kColGroups; ++k) m = merge_partial(m, mrg[k * kBM + rl]);
         dv.part[(size_t)row * dv.n_sub + chunk] = m;
       }
+      if (cg == 0) gbest[rl] = ord_key(-INFINITY);  // the next unit may hold other rows
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
     }
   }
@@ -609,6 +663,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   Partial* mrg = reinterpret_cast<Partial*>(reinterpret_cast<uint8_t*>(sB + kStagesPair * kStagePairB) + 256);
+  int* gbest = reinterpret_cast<int*>(mrg + kColGroups * kBM);  // best score per row, shared by the column groups
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -626,6 +681,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    for (int i = 0; i < kBM; ++i) gbest[i] = ord_key(-INFINITY);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
@@ -792,7 +848,6 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       const int row = mt * 2 * kBM + (int)rank * kBM + rl;
       const RowMeta rm = row_meta(dv, row, n_rows);
       Partial st = empty_partial();
-      float kscr = INFINITY;
       for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
         if (aborted) continue;
         const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
@@ -816,7 +871,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader[ab]);
           }
-          if (rm.valid) fold_cols(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, kscr);
+          if (rm.valid) fold_cols(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, gbest + rl);
         }
       }
       mrg[cg * kBM + rl] = st;
@@ -827,6 +882,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         for (int k = 1; k < kColGroups; ++k) m = merge_partial(m, mrg[k * kBM + rl]);
         dv.part[(size_t)row * dv.n_sub + chunk] = m;
       }
+      if (cg == 0) gbest[rl] = ord_key(-INFINITY);  // the next unit may hold other rows
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
     }
   }
@@ -841,12 +897,12 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   }
 }
 
-constexpr size_t kSmemBytesPair =
-    1024 + (size_t)kStagesPair * (kStagePairA + kStagePairB) + 256 + sizeof(Partial) * kColGroups * kBM;
+constexpr size_t kSmemBytesPair = 1024 + (size_t)kStagesPair * (kStagePairA + kStagePairB) + 256 +
+                                  sizeof(Partial) * kColGroups * kBM + sizeof(int) * kBM;
 static_assert(kSmemBytesPair <= 232448, "shared memory per CTA");
 
 constexpr size_t kSmemBytes =
-    1024 + (size_t)kStages * (kStageA + kStageB) + 256 + sizeof(Partial) * kColGroups * kBM;
+    1024 + (size_t)kStages * (kStageA + kStageB) + 256 + sizeof(Partial) * kColGroups * kBM + sizeof(int) * kBM;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 }  // namespace

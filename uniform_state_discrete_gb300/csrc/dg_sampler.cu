@@ -45,7 +45,7 @@ void set_err(char* buf, const char* fmt, ...) {
 
 struct Layout {
   size_t slots, plan, active, x, committed, commit_step, prev_amax, tokens_out, H, logZ, y, amax, h, part, resid,
-      canvas_rows;
+      canvas_rows, temps;
   size_t total;
   int rows_cap, n_vtiles, tiles_per_chunk, n_chunks, n_sub, max_active;
 };
@@ -116,6 +116,7 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
   L->part = take(sizeof(dg::Partial) * (size_t)L->rows_cap * L->n_sub);
   L->resid = take(4 * B * Lc * d);
   L->canvas_rows = take(4 * B);
+  L->temps = take(4 * (size_t)c->num_inference_steps);
   L->total = o;
   return 1;
 }
@@ -290,6 +291,7 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.resid_stage = reinterpret_cast<float*>(w + L.resid);
   dv.canvas_rows = reinterpret_cast<uint32_t*>(w + L.canvas_rows);
   dv.norm_w = norm_w;
+  dv.temps = reinterpret_cast<const float*>(w + L.temps);
   dv.V = cfg->vocab;
   dv.d = cfg->hidden;
   dv.L = cfg->canvas_len;
@@ -329,9 +331,20 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
     sl.state = dg::kWaiting;
     sl.temperature = cfg->t_max;
   }
+  // T_s = t_max + (s/N)(t_min - t_max) for every step: fp64, one IEEE operation at a time
+  // (this file is compiled without contraction), rounded once to fp32
+  std::vector<float> temps(cfg->num_inference_steps);
+  for (int st = 0; st < cfg->num_inference_steps; ++st) {
+    const double frac = (double)st / (double)cfg->num_inference_steps;
+    const double span = (double)cfg->t_min - (double)cfg->t_max;
+    const double prod = frac * span;
+    temps[st] = (float)((double)cfg->t_max + prod);
+  }
   ce = cudaMemsetAsync(workspace, 0, L.total, s->stream);
   if (ce == cudaSuccess)
     ce = cudaMemcpyAsync(dv.slots, slots.data(), sizeof(dg_slot) * B, cudaMemcpyHostToDevice, s->stream);
+  if (ce == cudaSuccess)
+    ce = cudaMemcpyAsync(w + L.temps, temps.data(), 4 * temps.size(), cudaMemcpyHostToDevice, s->stream);
   if (ce == cudaSuccess) ce = dg::launch_plan(dv, 0, s->stream);
   if (ce == cudaSuccess) ce = cudaStreamSynchronize(s->stream);
   if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "initialise sampler state"));

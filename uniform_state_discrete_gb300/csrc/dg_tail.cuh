@@ -21,48 +21,20 @@ struct Group {
 };
 
 constexpr int kMaxL = 1024;
-constexpr int kTailMaxThreads = 1024;
+constexpr int kTailThreads = 256;               // threads of every group that runs the tail
+constexpr int kTailPer = kMaxL / kTailThreads;  // canvas positions per thread
 
 // Shared-memory scratch of the tail.
 struct TailScratch {
-  unsigned long long keys[kMaxL];
+  unsigned long long keys[kMaxL];  // (H bits << 32 | p) of each uncommitted position, ~0 otherwise
+  unsigned char acc[kMaxL];        // accepted this tick
   unsigned long long cand[32];
-  unsigned long long redk[kTailMaxThreads / 32];
-  float redf[kTailMaxThreads / 32];
+  unsigned long long redk[kTailThreads / 32];
+  float redf[kTailThreads / 32][2];
+  int redi[kTailThreads / 32][2];
   int flags[4];
   int done_list[64];  // canvases completed by one CTA's rows (at most 8 / L + 2)
 };
-
-__device__ __forceinline__ float group_sum_f32(float v, const Group& g, TailScratch* sc) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  const int w = g.tid >> 5, lane = g.tid & 31;
-  g.sync();
-  if (lane == 0) sc->redf[w] = v;
-  g.sync();
-  float t = 0.f;
-  for (int i = 0; i < g.n / 32; ++i) t += sc->redf[i];
-  return t;
-}
-
-__device__ __forceinline__ unsigned long long group_min_u64(unsigned long long v, const Group& g, TailScratch* sc) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    v = w < v ? w : v;
-  }
-  const int w = g.tid >> 5, lane = g.tid & 31;
-  g.sync();
-  if (lane == 0) sc->redk[w] = v;
-  g.sync();
-  unsigned long long t = ~0ull;
-  for (int i = 0; i < g.n / 32; ++i) t = sc->redk[i] < t ? sc->redk[i] : t;
-  return t;
-}
-
-__device__ __forceinline__ int group_and(int v, const Group& g, TailScratch* sc) {
-  return group_sum_f32(v ? 0.f : 1.f, g, sc) == 0.f ? 1 : 0;
-}
 
 // Sort 32 keys held one per lane, ascending (bitonic network over shuffles).
 __device__ __forceinline__ unsigned long long warp_sort_u64(unsigned long long key) {
@@ -106,46 +78,88 @@ __device__ __forceinline__ void init_canvas(const Dev& dv, int c, int block, con
 }
 
 // Admit the canvases due by `tick` (admit_tick <= tick), in canvas order, while
-// fewer than max_active are running; refresh temperatures; rebuild the active
-// list in canvas order; reset the tick's counters.  Slots may have been written
-// by other CTAs of the grid, so they are read at L2 (ld.global.cg).
-static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailScratch* sc) {
-  if (g.tid == 0) {
-    int n = 0;
-    for (int c = 0; c < dv.B; ++c) n += (__ldcg(&dv.slots[c].state) == kActive) ? 1 : 0;
-    sc->flags[0] = n;
+// fewer than max_active are running; rebuild the active list in canvas order;
+// reset the tick's counters.  A canvas's temperature is written by whoever
+// writes its step (the commit, an admission); `refresh_temps` rewrites it for
+// every active canvas, for a state loaded from the host.  Slots may have been
+// written by other CTAs of the grid, so they are read at L2 (ld.global.cg).
+// The group has kTailThreads threads; with at most that many canvases the
+// slots are read once.
+static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailScratch* sc, bool refresh_temps) {
+  const int lane = g.tid & 31, w = g.tid >> 5;
+  int st0 = kDone;  // state of canvas g.tid (first round)
+  int run = 0, due = 0;
+  for (int c = g.tid; c < dv.B; c += g.n) {
+    const int st = __ldcg(&dv.slots[c].state);
+    if (c == g.tid) st0 = st;
+    run += st == kActive ? 1 : 0;
+    due |= (st == kWaiting && __ldcg(&dv.slots[c].admit_tick) <= tick) ? 1 : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    run += __shfl_xor_sync(0xFFFFFFFFu, run, o);
+    due |= __shfl_xor_sync(0xFFFFFFFFu, due, o);
+  }
+  if (lane == 0) {
+    sc->redi[w][0] = run;
+    sc->redi[w][1] = due;
   }
   g.sync();
-  int running = sc->flags[0];
-  for (int c = 0; c < dv.B && running < dv.max_active; ++c) {
-    const int state = __ldcg(&dv.slots[c].state);
-    const int admit = __ldcg(&dv.slots[c].admit_tick);
-    if (state == kWaiting && admit <= tick) {
-      init_canvas(dv, c, 0, g);
-      g.sync();
-      if (g.tid == 0) {
-        dg_slot& s = dv.slots[c];
-        s.state = kActive;
-        s.block = 0;
-        s.step = 0;
-        s.n_committed = 0;
+  int running = 0, any_due = 0;
+  for (int k = 0; k < kTailThreads / 32; ++k) {
+    running += sc->redi[k][0];
+    any_due |= sc->redi[k][1];
+  }
+  bool admitted = false;
+  if (any_due) {
+    for (int c = 0; c < dv.B && running < dv.max_active; ++c) {
+      const int state = __ldcg(&dv.slots[c].state);
+      const int admit = __ldcg(&dv.slots[c].admit_tick);
+      if (state == kWaiting && admit <= tick) {
+        init_canvas(dv, c, 0, g);
+        g.sync();
+        if (g.tid == 0) {
+          dg_slot& s = dv.slots[c];
+          s.state = kActive;
+          s.block = 0;
+          s.step = 0;
+          s.n_committed = 0;
+          s.temperature = dv.temps[0];
+        }
+        ++running;
+        admitted = true;
+        g.sync();
       }
-      ++running;
-      g.sync();
     }
   }
-  if (g.tid == 0) {
-    int n = 0;
-    for (int c = 0; c < dv.B; ++c) {
-      dg_slot& s = dv.slots[c];
-      if (__ldcg(&s.state) == kActive) {
-        s.temperature = temperature(__ldcg(&s.step), dv.N, dv.t_min, dv.t_max);
-        if (n < dv.max_active) dv.active[n] = c;
-        ++n;
+  // active list in canvas order
+  int base = 0;
+  for (int c0 = 0; c0 < dv.B; c0 += g.n) {
+    const int c = c0 + g.tid;
+    bool act = false;
+    if (c < dv.B) act = (c0 == 0 && !admitted ? st0 : __ldcg(&dv.slots[c].state)) == kActive;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, act);
+    g.sync();  // the previous round's counts have been read
+    if (lane == 0) sc->redi[w][0] = __popc(bal);
+    g.sync();
+    int off = base, tot = 0;
+    for (int k = 0; k < kTailThreads / 32; ++k) {
+      off += k < w ? sc->redi[k][0] : 0;
+      tot += sc->redi[k][0];
+    }
+    if (act) {
+      const int idx = off + __popc(bal & ((1u << lane) - 1u));
+      if (idx < dv.max_active) dv.active[idx] = c;
+      if (refresh_temps) {
+        int st = __ldcg(&dv.slots[c].step);
+        st = st < 0 ? 0 : (st >= dv.N ? dv.N - 1 : st);
+        dv.slots[c].temperature = dv.temps[st];
       }
     }
-    if (n > dv.max_active) n = dv.max_active;  // only reachable through an inconsistent dg_set_state
-    dv.plan->n_active = n;
+    base += tot;
+  }
+  if (g.tid == 0) {
+    dv.plan->n_active = base < dv.max_active ? base : dv.max_active;  // above it only after an inconsistent dg_set_state
     dv.plan->tick = tick;
     dv.plan->commits = 0u;
   }
@@ -162,64 +176,105 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
 // Only entries whose entropy is <= bound, plus the smallest one above it, can be
 // accepted, so the common case sorts at most 32 candidates in one warp; more than
 // 31 entropies within the bound fall back to a bitonic sort of the canvas.
-// Per-position data of this tick were written by other CTAs: read at L2.
+// Every per-position input is read once, up front, into registers (this tick's
+// values were written by other CTAs: read at L2); the group has kTailThreads
+// threads, so each holds at most kTailPer positions.
 static __device__ void commit_canvas(const Dev& dv, int c, const Group& g, TailScratch* sc) {
   const int L = dv.L;
   const dg_slot sl = dv.slots[c];
   const int s = sl.step, b = sl.block;
   const size_t base = (size_t)c * L;
   const float bound = dv.bound;
+  const int lane = g.tid & 31, w = g.tid >> 5;
 
+  const float t_next = dv.temps[s + 1 < dv.N ? s + 1 : dv.N - 1], t_first = dv.temps[0];
+  float Hv[kTailPer];
+  int yv[kTailPer], av[kTailPer], pv[kTailPer], xv[kTailPer];
+  bool cm[kTailPer];
+#pragma unroll
+  for (int i = 0; i < kTailPer; ++i) {
+    const int p = g.tid + i * kTailThreads;
+    if (p < L) {
+      Hv[i] = __ldcg(dv.H + base + p);
+      yv[i] = __ldcg(dv.y + base + p);
+      av[i] = __ldcg(dv.amax + base + p);
+      pv[i] = dv.prev_amax[base + p];
+      xv[i] = dv.x[base + p];
+      cm[i] = dv.committed[base + p] != 0;
+    }
+  }
   float hsum = 0.f, n_le = 0.f;
   int stable = 1;
   unsigned long long kmin_above = ~0ull;
-  for (int p = g.tid; p < L; p += g.n) {
-    const float H = __ldcg(dv.H + base + p);
-    hsum += H;
-    stable &= (__ldcg(dv.amax + base + p) == dv.prev_amax[base + p]) ? 1 : 0;
-    if (!dv.committed[base + p]) {
-      const unsigned long long k = ((unsigned long long)__float_as_uint(H) << 32) | (unsigned)p;
-      if (H <= bound) n_le += 1.f;
-      else kmin_above = k < kmin_above ? k : kmin_above;
+#pragma unroll
+  for (int i = 0; i < kTailPer; ++i) {
+    const int p = g.tid + i * kTailThreads;
+    if (p < L) {
+      hsum += Hv[i];
+      stable &= av[i] == pv[i] ? 1 : 0;
+      const unsigned long long k = ((unsigned long long)__float_as_uint(Hv[i]) << 32) | (unsigned)p;
+      sc->keys[p] = cm[i] ? ~0ull : k;
+      sc->acc[p] = 0;
+      if (!cm[i]) {
+        if (Hv[i] <= bound) n_le += 1.f;
+        else kmin_above = k < kmin_above ? k : kmin_above;
+      }
     }
   }
-  const float mean_H = group_sum_f32(hsum, g, sc) / (float)L;
-  const int count_le = (int)group_sum_f32(n_le, g, sc);
-  kmin_above = group_min_u64(kmin_above, g, sc);
-  stable = group_and(stable, g, sc);
+  // the four canvas-wide reductions share one exchange through shared memory
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    hsum += __shfl_xor_sync(0xFFFFFFFFu, hsum, o);
+    n_le += __shfl_xor_sync(0xFFFFFFFFu, n_le, o);
+    stable &= __shfl_xor_sync(0xFFFFFFFFu, stable, o);
+    const unsigned long long ko = __shfl_xor_sync(0xFFFFFFFFu, kmin_above, o);
+    kmin_above = ko < kmin_above ? ko : kmin_above;
+  }
+  if (lane == 0) {
+    sc->redf[w][0] = hsum;
+    sc->redf[w][1] = n_le;
+    sc->redi[w][0] = stable;
+    sc->redk[w] = kmin_above;
+  }
+  if (g.tid == 0) sc->flags[1] = 0;
+  g.sync();
+  float tot_h = 0.f, tot_le = 0.f;
+  for (int k = 0; k < kTailThreads / 32; ++k) {
+    tot_h += sc->redf[k][0];
+    tot_le += sc->redf[k][1];
+    stable &= sc->redi[k][0];
+    kmin_above = sc->redk[k] < kmin_above ? sc->redk[k] : kmin_above;
+  }
+  const float mean_H = tot_h / (float)L;
+  const int count_le = (int)tot_le;
   const bool converged = (s >= 1) && (mean_H < dv.conf) && stable;
   const bool final_step = converged || (s == dv.N - 1);
 
   if (!final_step) {
     int n_acc;
     if (count_le < 32) {
-      if (g.tid == 0) sc->flags[1] = 0;
-      g.sync();
-      for (int p = g.tid; p < L; p += g.n) {
-        const float H = __ldcg(dv.H + base + p);
-        if (!dv.committed[base + p] && H <= bound)
-          sc->cand[atomicAdd(&sc->flags[1], 1)] = ((unsigned long long)__float_as_uint(H) << 32) | (unsigned)p;
+#pragma unroll
+      for (int i = 0; i < kTailPer; ++i) {
+        const int p = g.tid + i * kTailThreads;
+        if (p < L && !cm[i] && Hv[i] <= bound)
+          sc->cand[atomicAdd(&sc->flags[1], 1)] = ((unsigned long long)__float_as_uint(Hv[i]) << 32) | (unsigned)p;
       }
       g.sync();
       if (g.tid < 32) {
-        const int lane = g.tid;
         unsigned long long k = lane < count_le ? sc->cand[lane] : (lane == count_le ? kmin_above : ~0ull);
         k = warp_sort_u64(k);
-        sc->keys[lane] = k;
+        sc->cand[lane] = k;
         __syncwarp();
-        if (lane == 0) sc->flags[2] = accept_walk(sc->keys, 32, bound);
+        const int na = accept_walk(sc->cand, 32, bound);  // every lane walks the same keys
+        if (lane < na) sc->acc[(unsigned)(k & 0xFFFFFFFFu)] = 1;
+        if (lane == 0) sc->flags[2] = na;
       }
       g.sync();
       n_acc = sc->flags[2];
     } else {
       int n2 = 1;
       while (n2 < L) n2 <<= 1;
-      for (int i = g.tid; i < n2; i += g.n) {
-        unsigned long long k = ~0ull;
-        if (i < L && !dv.committed[base + i])
-          k = ((unsigned long long)__float_as_uint(__ldcg(dv.H + base + i)) << 32) | (unsigned)i;
-        sc->keys[i] = k;
-      }
+      for (int i = L + g.tid; i < n2; i += g.n) sc->keys[i] = ~0ull;
       g.sync();
       for (int size = 2; size <= n2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -239,33 +294,46 @@ static __device__ void commit_canvas(const Dev& dv, int c, const Group& g, TailS
       if (g.tid == 0) sc->flags[2] = accept_walk(sc->keys, n2, bound);
       g.sync();
       n_acc = sc->flags[2];
+      for (int j = g.tid; j < n_acc; j += g.n) sc->acc[(unsigned)(sc->keys[j] & 0xFFFFFFFFu)] = 1;
+      g.sync();
     }
-    for (int j = g.tid; j < n_acc; j += g.n) {
-      const int p = (int)(sc->keys[j] & 0xFFFFFFFFu);
-      dv.x[base + p] = __ldcg(dv.y + base + p);
-      dv.committed[base + p] = 1;
-      dv.commit_step[base + p] = (int16_t)s;
+#pragma unroll
+    for (int i = 0; i < kTailPer; ++i) {
+      const int p = g.tid + i * kTailThreads;
+      if (p < L) {
+        if (!cm[i]) {
+          if (sc->acc[p]) {
+            dv.x[base + p] = yv[i];
+            dv.committed[base + p] = 1;
+            dv.commit_step[base + p] = (int16_t)s;
+          } else {
+            dv.x[base + p] = uniform_token(draw_u32(sl.seed, kPurposeRenoise, b, s, p), dv.V);
+          }
+        }
+        dv.prev_amax[base + p] = av[i];
+      }
     }
-    g.sync();
-    for (int p = g.tid; p < L; p += g.n) {
-      if (!dv.committed[base + p]) dv.x[base + p] = uniform_token(draw_u32(sl.seed, kPurposeRenoise, b, s, p), dv.V);
-      dv.prev_amax[base + p] = __ldcg(dv.amax + base + p);
-    }
-    g.sync();
     if (g.tid == 0) {
       dg_slot& so = dv.slots[c];
       so.step = s + 1;
+      so.temperature = t_next;
       so.n_committed = sl.n_committed + n_acc;
       so.mean_entropy = mean_H;
     }
   } else {
-    for (int p = g.tid; p < L; p += g.n) {
-      if (!dv.committed[base + p]) {
-        dv.x[base + p] = __ldcg(dv.y + base + p);
-        dv.committed[base + p] = 1;
-        dv.commit_step[base + p] = (int16_t)s;
+#pragma unroll
+    for (int i = 0; i < kTailPer; ++i) {
+      const int p = g.tid + i * kTailThreads;
+      if (p < L) {
+        int xo = xv[i];
+        if (!cm[i]) {
+          xo = yv[i];
+          dv.x[base + p] = xo;
+          dv.committed[base + p] = 1;
+          dv.commit_step[base + p] = (int16_t)s;
+        }
+        dv.tokens_out[((size_t)c * dv.G + b) * L + p] = xo;
       }
-      dv.tokens_out[((size_t)c * dv.G + b) * L + p] = dv.x[base + p];
     }
     g.sync();
     const bool more = (b + 1 < dv.G);
@@ -279,6 +347,7 @@ static __device__ void commit_canvas(const Dev& dv, int c, const Group& g, TailS
       if (more) {
         so.block = b + 1;
         so.step = 0;
+        so.temperature = t_first;
         so.n_committed = 0;
       } else {
         so.n_committed = L;
