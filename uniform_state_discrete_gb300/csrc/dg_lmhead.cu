@@ -70,8 +70,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Wait for the phase of `parity` to complete, giving up after kWaitLimitNs or
 // as soon as another role of this CTA gave up.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, Plan* plan) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, Plan* plan) {
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -85,6 +84,11 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile 
       }
     }
   }
+}
+
+// The common case -- the phase has already completed -- without a call.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, Plan* plan) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, plan);
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
@@ -522,6 +526,9 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      // descriptors of stage 0; a stage or K offset adds its 16-byte count to the
+      // start-address field, which stays below 2^14 for any shared-memory address
+      const uint64_t adesc0 = sw128_desc(smem_u32(sA)), bdesc0 = sw128_desc(smem_u32(sB));
       uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true, any = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -542,12 +549,12 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + stage * kStageA);
-            const uint32_t b0 = smem_u32(sB + stage * kStageB);
+            const uint64_t ad = adesc0 + (uint64_t)((stage * kStageA) >> 4);
+            const uint64_t bd = bdesc0 + (uint64_t)((stage * kStageB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               // advance K by 16 bf16 = 32 bytes inside the swizzled 128-byte row
-              mma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), (kb | kk) != 0 ? 1u : 0u);
+              mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), (kb | kk) != 0 ? 1u : 0u);
             }
             mma_commit(&empty[stage]);
             any = true;
@@ -789,6 +796,9 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer (leader)
     if (lane == 0 && leader) {
+      // descriptors of stage 0; a stage or K offset adds its 16-byte count to the
+      // start-address field, which stays below 2^14 for any shared-memory address
+      const uint64_t adesc0 = sw128_desc(smem_u32(sA)), bdesc0 = sw128_desc(smem_u32(sB));
       uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true, any = false;
       for (int u = cid; u < n_units && ok; u += n_clusters) {
@@ -809,11 +819,11 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + stage * kStagePairA);
-            const uint32_t b0 = smem_u32(sB + stage * kStagePairB);
+            const uint64_t ad = adesc0 + (uint64_t)((stage * kStagePairA) >> 4);
+            const uint64_t bd = bdesc0 + (uint64_t)((stage * kStagePairB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_bf16_pair(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), (kb | kk) != 0 ? 1u : 0u);
+              mma_bf16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), (kb | kk) != 0 ? 1u : 0u);
             mma_commit_pair(&empty[stage], (uint16_t)0x3);
             any = true;
             if (++stage == (uint32_t)kStagesPair) {
