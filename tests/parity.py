@@ -55,12 +55,13 @@ class Case:
     admit: tuple = None
     max_active: int = 0
     norm_seed: int = None  # RMSNorm weight from synth.norm_weight, or all ones
+    rms_eps: float = 1e-6
 
     def oracle_cfg(self) -> OracleConfig:
         return OracleConfig(vocab=self.vocab, hidden=self.hidden, canvas_len=self.canvas_len,
                             n_canvases=self.n_canvases, gen_blocks=self.gen_blocks, num_inference_steps=self.steps,
                             t_min=f32(self.t_min), t_max=f32(self.t_max), entropy_bound=f32(self.bound),
-                            confidence=f32(self.conf), rms_eps=f32(1e-6),
+                            confidence=f32(self.conf), rms_eps=f32(self.rms_eps),
                             seeds=list(self.seeds) if self.seeds else list(range(self.n_canvases)),
                             admit_tick=list(self.admit) if self.admit else None,
                             max_active=self.max_active or None)
@@ -69,7 +70,7 @@ class Case:
         import uniform_state_discrete_gb300 as dg
         return dg.make_config(self.vocab, self.hidden, self.canvas_len, n_canvases=self.n_canvases,
                               gen_blocks=self.gen_blocks, num_inference_steps=self.steps, t_min=self.t_min,
-                              t_max=self.t_max, entropy_bound=self.bound, confidence=self.conf, rms_eps=1e-6,
+                              t_max=self.t_max, entropy_bound=self.bound, confidence=self.conf, rms_eps=self.rms_eps,
                               max_active=self.max_active,
                               seeds=list(self.seeds) if self.seeds else list(range(self.n_canvases)),
                               admit_tick=list(self.admit) if self.admit else None)

@@ -62,11 +62,38 @@ __device__ __forceinline__ uint32_t scaled_bf16(float x, float w, float inv_hi, 
   return bf16_rne_pair(hi, lo) & 0xFFFFu;
 }
 
+// sqrt(d) / (sqrt(h + l) + eps) as an unevaluated fp32 pair, to ~2^-46
+// relative, in double-float arithmetic (Dekker 1971): a square root and a
+// quotient rounded in fp32 and corrected by their exact FMA residues.
+__device__ __forceinline__ void row_scale(float h, float l, int d, float eps, float& inv_hi, float& inv_lo) {
+  // norm = sqrt(h + l): r = fl(sqrt(h)), then r + (h + l - r^2) / (2r)
+  const float r = __fsqrt_rn(h);
+  const float p = __fmul_rn(r, r);
+  const float pe = fmaf(r, r, -p);  // r^2 = p + pe exactly
+  const float r_lo = __fdiv_rn(__fadd_rn(__fsub_rn(__fsub_rn(h, p), pe), l), __fmul_rn(2.f, r));
+  // den = norm + eps, renormalised
+  float dh, de;
+  two_sum(r, eps, dh, de);
+  de = __fadd_rn(de, r_lo);
+  const float den_hi = __fadd_rn(dh, de);
+  const float den_lo = __fsub_rn(de, __fsub_rn(den_hi, dh));
+  // sqrt(d) = sd + sd_lo (d is an integer, exact in fp32)
+  const float fd = (float)d;
+  const float sd = __fsqrt_rn(fd);
+  const float sd_lo = __fdiv_rn(fmaf(-sd, sd, fd), __fmul_rn(2.f, sd));
+  // quotient: q = fl(sd / den_hi), remainder sd - q den_hi exact by FMA
+  const float q = __fdiv_rn(sd, den_hi);
+  const float rem = __fadd_rn(fmaf(-q, den_hi, sd), fmaf(-q, den_lo, sd_lo));
+  const float q_lo = __fdiv_rn(rem, den_hi);
+  inv_hi = __fadd_rn(q, q_lo);
+  inv_lo = __fsub_rn(q_lo, __fsub_rn(inv_hi, q));
+}
+
 // h = bf16( w * r * sqrt(d) / (||r||_2 + eps) ) per active row.  The rounding
 // of every element is the one the exact quotient gives (up to ~2^-46
 // relative): sum of squares in TwoSum pairs, the per-row scale sqrt(d) /
-// (norm + eps) in fp64 (two operations per row), split into an fp32 pair, and
-// each product carried exactly before the bf16 rounding.
+// (norm + eps) as a double-float fp32 pair (row_scale), and each product
+// carried exactly before the bf16 rounding.
 //
 // Layout for latency: one CTA of kNormThreads (eight warps) per row.  A row
 // of up to kNormThreads * kNormVec float4 (d <= 4096) is loaded into
@@ -79,7 +106,6 @@ constexpr int kNormVec = 4;
 
 __global__ void __launch_bounds__(kNormThreads, 6) k_rmsnorm(const float* __restrict__ resid, const Dev dv) {
   __shared__ float red[kNormThreads / 32][2];
-  __shared__ float scale[2];
   pdl_wait();
   pdl_allow_next();
   const int n_rows = dv.plan->n_active * dv.L;
@@ -134,21 +160,16 @@ __global__ void __launch_bounds__(kNormThreads, 6) k_rmsnorm(const float* __rest
     red[warp][1] = sl;
   }
   __syncthreads();
-  if (t == 0) {
-    float h = red[0][0], l = red[0][1];
+  // every thread forms the row's sum of squares and scale itself
+  float h = red[0][0], l = red[0][1];
 #pragma unroll
-    for (int w = 1; w < kNormThreads / 32; ++w) {
-      float e;
-      two_sum(h, red[w][0], h, e);
-      l = __fadd_rn(__fadd_rn(l, red[w][1]), e);
-    }
-    const double inv = sqrt((double)dv.d) / (sqrt((double)h + (double)l) + (double)dv.eps);
-    const float inv_hi = __double2float_rn(inv);
-    scale[0] = inv_hi;
-    scale[1] = __double2float_rn(inv - (double)inv_hi);
+  for (int w = 1; w < kNormThreads / 32; ++w) {
+    float e;
+    two_sum(h, red[w][0], h, e);
+    l = __fadd_rn(__fadd_rn(l, red[w][1]), e);
   }
-  __syncthreads();
-  const float inv_hi = scale[0], inv_lo = scale[1];
+  float inv_hi, inv_lo;
+  row_scale(h, l, dv.d, dv.eps, inv_hi, inv_lo);
   uint2* out = reinterpret_cast<uint2*>(dv.h + (size_t)row * dv.d);
   const float4* w4 = reinterpret_cast<const float4*>(dv.norm_w);
   if (in_regs) {
@@ -250,8 +271,11 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
     commit_canvas(dv, c, g, &sc);
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0)
-      sc.flags[1] = (atomicAdd(&dv.plan->commits, 1u) == (unsigned)(__ldcg(&dv.plan->n_active) - 1)) ? 1 : 0;
+    if (threadIdx.x == 0) {
+      // the last commit of the tick plans the next; alone, this one is the last
+      const int na = __ldcg(&dv.plan->n_active);
+      sc.flags[1] = (na == 1 || atomicAdd(&dv.plan->commits, 1u) == (unsigned)(na - 1)) ? 1 : 0;
+    }
     __syncthreads();
     const int plan_now = sc.flags[1];
     __syncthreads();
