@@ -135,6 +135,19 @@ def test_free_run_tiny_matches_oracle():
     assert np.array_equal(info["steps_used"], o.steps_used)
 
 
+def test_idle_ticks_before_admission_pair_kernel():
+    """256 positions of one canvas admitted at tick 2: the SM-pair LM head loads its first W stages
+    before it knows whether any canvas is active, so on ticks 0 and 1 it must let those copies land
+    with nothing to consume them; the run must then match the oracle."""
+    case = Case(vocab=4096, hidden=256, canvas_len=256, steps=5, seeds=(3,), admit=(2,))
+    W = weights(case)
+    o = oracle.OracleSampler(case.oracle_cfg(), W)
+    o.run(oracle.sampler.synth_resid_fn(case.oracle_cfg(), W, case.sigma))
+    _, tok, info = _gpu_free_run(case, W)
+    assert np.array_equal(tok, o.tokens_out)
+    assert np.array_equal(info["steps_used"], o.steps_used)
+
+
 def test_batch_and_admission_invariance_bitwise():
     """A canvas gives the same tokens and entropies alone or inside a staggered batch
     (TensorSharp doc, "7. Test coverage": batched decode equals per-sequence decode)."""
