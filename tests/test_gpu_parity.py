@@ -50,7 +50,7 @@ def test_rmsnorm_weight_vector():
 
 @pytest.mark.parametrize("hidden,norm_seed,sigma,eps", [(1024, None, 0.5, 1e-6), (2816, 5, 0.5, 1e-6),
                                                         (200, None, 2.0, 1e-6), (512, 7, 1e-3, 1e-6),
-                                                        (1024, 3, 0.05, 0.25)])
+                                                        (1024, 3, 0.05, 0.25), (4096, 9, 0.5, 1e-6)])
 def test_rmsnorm_bf16_bit_exact(hidden, norm_seed, sigma, eps):
     """K1's bf16 rows equal the oracle's RMSNorm bit for bit (both round the exact quotient)."""
     import torch

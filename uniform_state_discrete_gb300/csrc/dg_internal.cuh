@@ -75,6 +75,9 @@ struct Dev {
   uint16_t* h;          // [rows_cap, d] bf16 bits, compact active rows
   Partial* part;        // [rows_cap, n_sub]
   uint32_t* canvas_rows;// [B] rows combined per canvas this tick
+  uint32_t* rows_ready; // normalised rows written this tick (K1 -> K2)
+  uint32_t* fin_started;// K3 CTAs that have read this tick's plan
+  uint32_t* slab_done;  // [rows_cap / 128] LM-head units finished per 128-row slab (K2 -> K3)
   float* resid_stage;   // [B, L, d]
   const float* norm_w;  // [d] or null
   const float* temps;   // [N] temperature of each step, T_s = t_max + (s/N)(t_min - t_max)
@@ -130,6 +133,32 @@ __device__ __forceinline__ float lg2_approx(float x) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Counters that hand data from one kernel of a tick to the next without
+// waiting for the whole previous grid: the writer makes its stores visible
+// (fence after a CTA barrier) and adds to the counter; the reader spins on an
+// acquire load until the count it needs is reached, giving up after
+// kWaitLimitNs.  The planner of the next tick resets them.
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait until *cnt >= target; false if kWaitLimitNs passed first.
+__device__ __forceinline__ bool wait_count(const uint32_t* cnt, uint32_t target) {
+  if (ld_acquire(cnt) >= target) return true;
+  const uint64_t t0 = now_ns();
+  while (ld_acquire(cnt) < target) {
+    if (now_ns() - t0 > kWaitLimitNs) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
 // Merge two partial records (base-2 units).  Ties keep the lower vocabulary index.
 __device__ __forceinline__ Partial merge_partial(const Partial& a, const Partial& b) {
   Partial r;
@@ -144,6 +173,22 @@ __device__ __forceinline__ Partial merge_partial(const Partial& a, const Partial
   r.g = ga ? a.g : b.g;
   r.gidx = ga ? a.gidx : b.gidx;
   r.pad0 = r.pad1 = 0;
+  return r;
+}
+
+// A partial record written by another kernel, read at L2.
+__device__ __forceinline__ Partial load_partial(const Partial* p) {
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
+  const int4 b = __ldcg(reinterpret_cast<const int4*>(p) + 1);
+  Partial r;
+  r.m = a.x;
+  r.S = a.y;
+  r.A = a.z;
+  r.g = a.w;
+  r.amax = b.x;
+  r.gidx = b.y;
+  r.pad0 = b.z;
+  r.pad1 = b.w;
   return r;
 }
 

@@ -95,16 +95,16 @@ __device__ __forceinline__ void row_scale(float h, float l, int d, float eps, fl
 // (norm + eps) as a double-float fp32 pair (row_scale), and each product
 // carried exactly before the bf16 rounding.
 //
-// Layout for latency: one CTA of kNormThreads (eight warps) per row.  A row
-// of up to kNormThreads * kNormVec float4 (d <= 4096) is loaded into
+// Layout for latency: one CTA of kNormThreads (four warps) per row.  A row
+// of up to kNormThreads * kNormVec float4 (d <= 3072) is loaded into
 // registers with every load issued before the first use, so the kernel costs
 // about one memory round trip; longer rows are read twice.  At most 40
-// registers a thread, so a CTA fits on an SM beside a resident LM-head CTA
-// that was launched early.
-constexpr int kNormThreads = 256;
-constexpr int kNormVec = 4;
+// registers a thread: two of these CTAs fit on an SM beside an LM-head CTA, so
+// the LM head starts, and loads its first W stages, while the rows are formed.
+constexpr int kNormThreads = 128;
+constexpr int kNormVec = 6;
 
-__global__ void __launch_bounds__(kNormThreads, 6) k_rmsnorm(const float* __restrict__ resid, const Dev dv) {
+__global__ void __launch_bounds__(kNormThreads, 12) k_rmsnorm(const float* __restrict__ resid, const Dev dv) {
   __shared__ float red[kNormThreads / 32][2];
   pdl_wait();
   pdl_allow_next();
@@ -190,6 +190,12 @@ __global__ void __launch_bounds__(kNormThreads, 6) k_rmsnorm(const float* __rest
                           scaled_bf16(x.z, w.z, inv_hi, inv_lo) | (scaled_bf16(x.w, w.w, inv_hi, inv_lo) << 16));
     }
   }
+  // the row is written: count it for the LM head, which waits for all rows
+  __syncthreads();
+  if (t == 0) {
+    __threadfence();
+    atomicAdd(dv.rows_ready, 1u);
+  }
 }
 
 // Finishing kernel of a tick.  Each warp combines the split-vocabulary partial
@@ -201,25 +207,53 @@ __global__ void __launch_bounds__(kNormThreads, 6) k_rmsnorm(const float* __rest
 // waits for another: the last arrival at a counter does the work.
 constexpr int kFinishRows = 8;  // positions (warps) per CTA
 
+// The planner of k_finish: waits (bounded) until every CTA of the grid has read
+// this tick's plan, then plans the next tick.
+__device__ __forceinline__ void plan_next_tick(const Dev& dv, int tick, const Group& g, TailScratch* sc) {
+  if (g.tid == 0) {
+    if (!wait_count(dv.fin_started, gridDim.x) && atomicCAS(&dv.plan->err, kErrNone, kErrTimeout) == kErrNone)
+      dv.plan->err_info[0] = -2;
+  }
+  g.sync();
+  plan_tick(dv, tick + 1, g, sc, false);
+}
+
+// It does not wait for the whole LM-head grid: each CTA waits for the LM-head
+// units of its rows' 128-row slab (dv.slab_done), so it starts combining as
+// soon as the last partial record of those rows is written.  Data of earlier
+// kernels is read at L2.
 __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   __shared__ TailScratch sc;
-  pdl_wait();
-  pdl_allow_next();
   const Group g{(int)threadIdx.x, (int)blockDim.x, 0};
-  const int n_rows = dv.plan->n_active * dv.L;
+  // Each CTA reads the tick's plan, then counts itself as started; the planner of
+  // the next tick rewrites the plan only once every CTA of this grid has started,
+  // so a CTA that starts late cannot mistake the next tick's plan for this one's.
+  const int n_rows = __ldcg(&dv.plan->n_active) * dv.L;
+  const int tick = __ldcg(&dv.plan->tick);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(dv.fin_started, 1u);
+  }
+  pdl_allow_next();
   if (n_rows == 0) {
-    if (blockIdx.x == 0) plan_tick(dv, dv.plan->tick + 1, g, &sc, false);
+    if (blockIdx.x == 0) plan_next_tick(dv, tick, g, &sc);
     return;
   }
   const int row0 = blockIdx.x * kFinishRows;
   if (row0 >= n_rows) return;
+  if (threadIdx.x == 0) {
+    const bool ok = wait_count(dv.slab_done + row0 / 128, (uint32_t)dv.n_chunks);
+    if (!ok && atomicCAS(&dv.plan->err, kErrNone, kErrTimeout) == kErrNone) dv.plan->err_info[0] = -1 - (int)blockIdx.x;
+  }
+  __syncthreads();
   const int row1 = min(row0 + kFinishRows, n_rows);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = row0 + warp;
   if (row < row1) {
     Partial acc = empty_partial();
     const Partial* src = dv.part + (size_t)row * dv.n_sub;
-    for (int i = lane; i < dv.n_sub; i += 32) acc = merge_partial(acc, src[i]);
+    for (int i = lane; i < dv.n_sub; i += 32) acc = merge_partial(acc, load_partial(src + i));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       Partial b;
@@ -234,7 +268,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
     }
     if (lane == 0) {
       const int a = row / dv.L, p = row - a * dv.L;
-      const int c = dv.active[a];
+      const int c = __ldcg(dv.active + a);
       const float l2S = log2f(acc.S);
       const float H = 0.69314718055994531f * (l2S - acc.A / acc.S);
       const float lz = 0.69314718055994531f * (acc.m + l2S);
@@ -254,7 +288,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
     int nd = 0;
     for (int a = row0 / dv.L; a * dv.L < row1; ++a) {
       const int lo = max(a * dv.L, row0), hi = min((a + 1) * dv.L, row1);
-      const int c = dv.active[a];
+      const int c = __ldcg(dv.active + a);
       const unsigned old = atomicAdd(&dv.canvas_rows[c], (unsigned)(hi - lo));
       if (old + (unsigned)(hi - lo) == (unsigned)dv.L) {
         dv.canvas_rows[c] = 0u;  // every row of this canvas is combined: reset for the next tick
@@ -281,7 +315,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
     __syncthreads();
     if (plan_now) {
       __threadfence();
-      plan_tick(dv, __ldcg(&dv.plan->tick) + 1, g, &sc, false);
+      plan_next_tick(dv, tick, g, &sc);
     }
   }
 }

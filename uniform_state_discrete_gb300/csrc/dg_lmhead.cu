@@ -204,10 +204,10 @@ __device__ __forceinline__ RowMeta row_meta(const Dev& dv, int row, int n_rows) 
   rm.scale = 0.f;
   if (rm.valid) {
     const int a = row / dv.L;
-    const dg_slot sl = dv.slots[dv.active[a]];
-    rm.gs.init(sl.seed, (uint32_t)(row - a * dv.L), ((uint32_t)sl.block << 16) | (uint32_t)sl.step,
-               kPurposeGumbel);
-    rm.scale = 1.4426950408889634f / sl.temperature;
+    const dg_slot* sl = dv.slots + __ldcg(dv.active + a);
+    rm.gs.init(__ldcg(&sl->seed), (uint32_t)(row - a * dv.L),
+               ((uint32_t)__ldcg(&sl->block) << 16) | (uint32_t)__ldcg(&sl->step), kPurposeGumbel);
+    rm.scale = 1.4426950408889634f / __ldcg(&sl->temperature);
   } else {
     rm.gs.init(0ull, 0u, 0u, kPurposeGumbel);
   }
@@ -429,6 +429,20 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask) {
                : "memory");
 }
 
+// Before the first h copy: wait until RMSNorm has counted every active row as
+// written, then order those generic-proxy stores before this thread's TMA
+// (async-proxy) reads.  On expiry the CTA latches DG_ERR_TIMEOUT and aborts.
+__device__ __forceinline__ bool rows_written(const Dev& dv, int n_rows, volatile int* abort_flag) {
+  if (!wait_count(dv.rows_ready, (uint32_t)n_rows)) {
+    *abort_flag = 1;
+    atomicExch(&dv.plan->err, kErrTimeout);
+    atomicExch(&dv.plan->err_info[0], (int)blockIdx.x);
+    return false;
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreadsLM, 1)
     k_lmhead(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv) {
   extern __shared__ uint8_t smem_raw[];
@@ -477,10 +491,13 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // everything above overlaps the previous kernel; the normalised rows and the plan are read below
-  pdl_wait();
+  // everything above overlaps the previous kernel.  There is no wait for the whole
+  // RMSNorm grid: the producer waits for the count of written rows instead, and
+  // data of earlier kernels is read at L2.
+  // the plan is read before the next kernel may launch, so its planner cannot have
+  // rewritten it for the next tick yet
+  const int n_rows = __ldcg(&dv.plan->n_active) * dv.L;
   pdl_allow_next();
-  const int n_rows = dv.plan->n_active * dv.L;
   const int n_mt = (n_rows + kBM - 1) / kBM;
   const int n_units = n_mt * dv.n_chunks;
 
@@ -490,7 +507,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       uint32_t stage = 0, phase = 0;
       int issued_parity[kStages];
       for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
-      bool ok = true;
+      bool ok = rows_written(dv, n_rows, abort_flag);
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int chunk = u / n_mt, mt = u - chunk * n_mt;
         const int vt0 = chunk * dv.tiles_per_chunk;
@@ -630,6 +647,10 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       }
       if (cg == 0) gbest[rl] = ord_key(-INFINITY);  // the next unit may hold other rows
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+      if (warp == 2 && lane == 0 && mt * kBM < n_rows) {
+        __threadfence();  // this unit's partial records of the slab are written
+        atomicAdd(dv.slab_done + mt, 1u);
+      }
     }
   }
 
@@ -728,9 +749,10 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       }
     }
   }
-  pdl_wait();
+  // no wait for the whole RMSNorm grid (see rows_written); the plan is read before
+  // the next kernel may launch, so its planner cannot have rewritten it yet
+  const int n_rows = __ldcg(&dv.plan->n_active) * dv.L;
   pdl_allow_next();
-  const int n_rows = dv.plan->n_active * dv.L;
   const int n_mt = (n_rows + 2 * kBM - 1) / (2 * kBM);  // 256-row pair tiles
   const int n_units = n_mt * dv.n_chunks;
 
@@ -738,7 +760,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      bool ok = true;
+      bool ok = rows_written(dv, n_rows, abort_flag);
       int issued = 0;
       for (int u = cid; u < n_units && ok; u += n_clusters) {
         const int chunk = u / n_mt, mt = u - chunk * n_mt;
@@ -894,6 +916,10 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       }
       if (cg == 0) gbest[rl] = ord_key(-INFINITY);  // the next unit may hold other rows
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+      if (warp == 2 && lane == 0 && (mt * 2 + (int)rank) * kBM < n_rows) {
+        __threadfence();  // this unit's partial records of the slab are written
+        atomicAdd(dv.slab_done + mt * 2 + (int)rank, 1u);
+      }
     }
   }
 

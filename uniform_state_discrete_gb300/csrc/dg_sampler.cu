@@ -45,7 +45,7 @@ void set_err(char* buf, const char* fmt, ...) {
 
 struct Layout {
   size_t slots, plan, active, x, committed, commit_step, prev_amax, tokens_out, H, logZ, y, amax, h, part, resid,
-      canvas_rows, temps;
+      canvas_rows, temps, sync;
   size_t total;
   int rows_cap, n_vtiles, tiles_per_chunk, n_chunks, n_sub, max_active;
 };
@@ -117,6 +117,7 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
   L->resid = take(4 * B * Lc * d);
   L->canvas_rows = take(4 * B);
   L->temps = take(4 * (size_t)c->num_inference_steps);
+  L->sync = take(4 * (2 + (size_t)L->rows_cap / 128));  // rows_ready, fin_started, slab_done[rows_cap / 128]
   L->total = o;
   return 1;
 }
@@ -290,6 +291,9 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.part = reinterpret_cast<dg::Partial*>(w + L.part);
   dv.resid_stage = reinterpret_cast<float*>(w + L.resid);
   dv.canvas_rows = reinterpret_cast<uint32_t*>(w + L.canvas_rows);
+  dv.rows_ready = reinterpret_cast<uint32_t*>(w + L.sync);
+  dv.fin_started = dv.rows_ready + 1;
+  dv.slab_done = dv.rows_ready + 2;
   dv.norm_w = norm_w;
   dv.temps = reinterpret_cast<const float*>(w + L.temps);
   dv.V = cfg->vocab;
@@ -320,7 +324,7 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   if (!encode_2d(&s->tmB, w_vocab, (uint64_t)dv.V, (uint64_t)dv.d, s->pair ? dg::kBN / 2 : dg::kBN, s->err))
     return fail(DG_ERR_ARG);
   cudaError_t ce = dg::lmhead_configure();
-  if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "configure lm-head kernel"));
+  if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "configure kernels"));
 
   std::vector<dg_slot> slots(B);
   for (int c = 0; c < B; ++c) {

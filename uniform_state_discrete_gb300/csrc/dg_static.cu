@@ -30,6 +30,7 @@ namespace {
 constexpr size_t kOffSlot = 0;
 constexpr size_t kOffPlan = 256;
 constexpr size_t kOffActive = 512;
+constexpr size_t kOffSync = 768;  // rows written by RMSNorm, (unused here), LM-head units per 128-row slab (2)
 constexpr size_t kOffH = 1024;
 constexpr size_t kBytesH = (size_t)2 * DG_STATIC_MAX_ROWS * DG_STATIC_MAX_HIDDEN;
 constexpr size_t kOffPart = kOffH + kBytesH;
@@ -80,6 +81,8 @@ __global__ void k_static_prep(unsigned char* base, uint64_t seed, int block, int
   pl->err = dg::kErrNone;
   for (int i = 0; i < 4; ++i) pl->err_info[i] = 0;
   active[0] = 0;
+  uint32_t* sync = reinterpret_cast<uint32_t*>(base + kOffSync);
+  for (int i = 0; i < 4; ++i) sync[i] = 0u;
 }
 
 // One warp per position: merge its split-vocabulary partial records into the
@@ -204,7 +207,7 @@ extern "C" dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, co
       e = cudaGetSymbolAddress(&ptr, g_static_scratch);
       if (e != cudaSuccess || !ptr) return cuda_err(e, "cudaGetSymbolAddress of the static scratch", err, err_len);
       e = dg::lmhead_configure();
-      if (e != cudaSuccess) return cuda_err(e, "configure lm-head kernel", err, err_len);
+      if (e != cudaSuccess) return cuda_err(e, "configure kernels", err, err_len);
       g_setup[dev].base = static_cast<unsigned char*>(ptr);
       g_setup[dev].num_sms = sms;
       g_setup[dev].ready = true;
@@ -225,6 +228,9 @@ extern "C" dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, co
   dv.slots = reinterpret_cast<dg_slot*>(su.base + kOffSlot);
   dv.plan = reinterpret_cast<dg::Plan*>(su.base + kOffPlan);
   dv.active = reinterpret_cast<int32_t*>(su.base + kOffActive);
+  dv.rows_ready = reinterpret_cast<uint32_t*>(su.base + kOffSync);
+  dv.fin_started = dv.rows_ready + 1;
+  dv.slab_done = dv.rows_ready + 2;
   dv.h = reinterpret_cast<uint16_t*>(su.base + kOffH);
   dv.part = reinterpret_cast<dg::Partial*>(su.base + kOffPart);
   dv.norm_w = norm_w;

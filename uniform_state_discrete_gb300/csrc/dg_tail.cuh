@@ -67,7 +67,7 @@ __device__ __forceinline__ int accept_walk(const unsigned long long* keys, int n
 }
 
 __device__ __forceinline__ void init_canvas(const Dev& dv, int c, int block, const Group& g) {
-  const uint64_t seed = dv.slots[c].seed;
+  const uint64_t seed = __ldcg(&dv.slots[c].seed);
   for (int p = g.tid; p < dv.L; p += g.n) {
     const size_t o = (size_t)c * dv.L + p;
     dv.x[o] = uniform_token(draw_u32(seed, kPurposeInit, block, 0, p), dv.V);
@@ -158,6 +158,8 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
     }
     base += tot;
   }
+  // the tick's hand-off counters: every kernel that waited on them is past its wait
+  for (int i = g.tid; i < 2 + dv.rows_cap / 128; i += g.n) dv.rows_ready[i] = 0u;  // and fin_started, slab_done
   if (g.tid == 0) {
     dv.plan->n_active = base < dv.max_active ? base : dv.max_active;  // above it only after an inconsistent dg_set_state
     dv.plan->tick = tick;
@@ -181,7 +183,13 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
 // threads, so each holds at most kTailPer positions.
 static __device__ void commit_canvas(const Dev& dv, int c, const Group& g, TailScratch* sc) {
   const int L = dv.L;
-  const dg_slot sl = dv.slots[c];
+  dg_slot sl;
+  sl.seed = __ldcg(&dv.slots[c].seed);
+  sl.step = __ldcg(&dv.slots[c].step);
+  sl.block = __ldcg(&dv.slots[c].block);
+  sl.n_committed = __ldcg(&dv.slots[c].n_committed);
+  sl.steps_used = __ldcg(&dv.slots[c].steps_used);
+  sl.converged_blocks = __ldcg(&dv.slots[c].converged_blocks);
   const int s = sl.step, b = sl.block;
   const size_t base = (size_t)c * L;
   const float bound = dv.bound;
@@ -198,9 +206,9 @@ static __device__ void commit_canvas(const Dev& dv, int c, const Group& g, TailS
       Hv[i] = __ldcg(dv.H + base + p);
       yv[i] = __ldcg(dv.y + base + p);
       av[i] = __ldcg(dv.amax + base + p);
-      pv[i] = dv.prev_amax[base + p];
-      xv[i] = dv.x[base + p];
-      cm[i] = dv.committed[base + p] != 0;
+      pv[i] = __ldcg(dv.prev_amax + base + p);
+      xv[i] = __ldcg(dv.x + base + p);
+      cm[i] = __ldcg(dv.committed + base + p) != 0;
     }
   }
   float hsum = 0.f, n_le = 0.f;
