@@ -24,7 +24,11 @@ struct GumbelStream {
   uint32_t k0[8], k1[8];  // round keys of rounds 2..9
 
   __host__ __device__ __forceinline__ static uint32_t mulhi(uint32_t a, uint32_t b) {
+#ifdef __CUDA_ARCH__
+    return __umulhi(a, b);
+#else
     return (uint32_t)(((uint64_t)a * b) >> 32);
+#endif
   }
 
   __host__ __device__ __forceinline__ void init(uint64_t seed, uint32_t p, uint32_t bs, uint32_t purpose) {
@@ -44,19 +48,18 @@ struct GumbelStream {
     }
   }
 
+  // The high and low halves of each product are formed by two 32-bit
+  // multiplies rather than one 64-bit product: the same words, fewer issue
+  // cycles on the integer multiplier.
   __host__ __device__ __forceinline__ void draw(uint32_t x, uint32_t (&out)[4]) const {
-    const uint64_t p0 = (uint64_t)kM0 * x;
-    const uint32_t z1 = (uint32_t)(p0 >> 32) ^ c1, w1 = (uint32_t)p0;
-    const uint64_t p1 = (uint64_t)kM1 * z1;
-    uint32_t a = (uint32_t)(p1 >> 32) ^ d2, b = (uint32_t)p1, c = w1 ^ e2, d = f2;
+    const uint32_t z1 = mulhi(kM0, x) ^ c1, w1 = kM0 * x;
+    uint32_t a = mulhi(kM1, z1) ^ d2, b = kM1 * z1, c = w1 ^ e2, d = f2;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      const uint64_t q0 = (uint64_t)kM0 * a;
-      const uint64_t q1 = (uint64_t)kM1 * c;
-      const uint32_t na = (uint32_t)(q1 >> 32) ^ b ^ k0[r];
-      const uint32_t nc = (uint32_t)(q0 >> 32) ^ d ^ k1[r];
-      b = (uint32_t)q1;
-      d = (uint32_t)q0;
+      const uint32_t na = mulhi(kM1, c) ^ b ^ k0[r];
+      const uint32_t nc = mulhi(kM0, a) ^ d ^ k1[r];
+      b = kM1 * c;
+      d = kM0 * a;
       a = na;
       c = nc;
     }
