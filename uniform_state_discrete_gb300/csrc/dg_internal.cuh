@@ -132,6 +132,12 @@ __device__ __forceinline__ float lg2_approx(float x) {
 // successor begin launching.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// The same, issued only once `v` is in a register: a value read from the plan
+// before this call has arrived, so a dependent kernel that rewrites the plan
+// cannot change what this thread saw.
+__device__ __forceinline__ void pdl_allow_next_after(int v) {
+  asm volatile("griddepcontrol.launch_dependents;" ::"r"(v) : "memory");
+}
 
 // Counters that hand data from one kernel of a tick to the next without
 // waiting for the whole previous grid: the writer makes its stores visible
@@ -209,7 +215,7 @@ __device__ __forceinline__ Partial empty_partial() {
 cudaError_t launch_rmsnorm(const Dev& dv, const float* resid, cudaStream_t st);
 cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
                           cudaStream_t st);
-cudaError_t launch_lmhead_pair(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
+cudaError_t launch_lmhead_pair(const Dev& dv, const float* resid, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
                                cudaStream_t st);
 cudaError_t launch_finish(const Dev& dv, cudaStream_t st);
 cudaError_t launch_plan(const Dev& dv, int tick, cudaStream_t st);

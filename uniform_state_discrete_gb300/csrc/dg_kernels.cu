@@ -6,193 +6,33 @@
 #include <utility>
 
 #include "dg_internal.cuh"
+#include "dg_norm.cuh"
 #include "dg_tail.cuh"
 
 namespace dg {
 namespace {
 
 // ------------------------------------------------------------------- K1
-// Error-free transformations in fp32 (the fp64 pipe of this part is slow):
-// Knuth's TwoSum gives a + b = s + e exactly; an FMA gives x*y = p + e exactly
-// (Dekker's product).  Carried as unevaluated pairs (hi, lo) they hold the sum
-// of squares and the scaled value to ~2^-46 relative accuracy.  __f*_rn
-// intrinsics keep the compiler from contracting the steps into other FMAs.
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  const float z = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
-}
-
-// bf16 nearest-even of the exact value hi + lo, where hi = fl(hi + lo) (so
-// |lo| <= half an fp32 ulp of hi): hi's own rounding decides unless hi sits
-// exactly on a bf16 midpoint, where the sign of lo decides and 0 means a tie.
-__device__ __forceinline__ uint32_t bf16_rne_pair(float hi, float lo) {
-  const uint32_t b = __float_as_uint(hi);
-  const uint32_t rem = b & 0xFFFFu;
-  uint32_t up;
-  if (rem != 0x8000u) {
-    up = rem > 0x8000u ? 1u : 0u;
-  } else if (lo == 0.f) {
-    up = (b >> 16) & 1u;
-  } else {
-    up = ((lo > 0.f) == (hi > 0.f)) ? 1u : 0u;  // lo moves |value| above the midpoint
-  }
-  return (b >> 16) + up;
-}
-
-// Accumulate x^2 into the unevaluated pair (sh, sl): the square is split
-// exactly by an FMA, its high part added by TwoSum, all low parts summed.
-__device__ __forceinline__ void acc_square(float x, float& sh, float& sl) {
-  const float sq = __fmul_rn(x, x);
-  const float sq_err = fmaf(x, x, -sq);
-  float e;
-  two_sum(sh, sq, sh, e);
-  sl = __fadd_rn(sl, __fadd_rn(e, sq_err));
-}
-
-// bf16 bits of w x (inv_hi + inv_lo), rounded as the exact product would be.
-__device__ __forceinline__ uint32_t scaled_bf16(float x, float w, float inv_hi, float inv_lo) {
-  const float xw = __fmul_rn(w, x);  // w x = xw + xw_err exactly
-  const float xw_err = fmaf(w, x, -xw);
-  const float ph = __fmul_rn(xw, inv_hi);  // (w x) inv ~= ph + pl
-  const float pe = fmaf(xw, inv_hi, -ph);
-  const float pl = fmaf(xw, inv_lo, fmaf(xw_err, inv_hi, pe));
-  const float hi = __fadd_rn(ph, pl);  // renormalise: |lo| <= ulp(hi)/2
-  const float lo = __fsub_rn(pl, __fsub_rn(hi, ph));
-  return bf16_rne_pair(hi, lo) & 0xFFFFu;
-}
-
-// sqrt(d) / (sqrt(h + l) + eps) as an unevaluated fp32 pair, to ~2^-46
-// relative, in double-float arithmetic (Dekker 1971): a square root and a
-// quotient rounded in fp32 and corrected by their exact FMA residues.
-__device__ __forceinline__ void row_scale(float h, float l, int d, float eps, float& inv_hi, float& inv_lo) {
-  // norm = sqrt(h + l): r = fl(sqrt(h)), then r + (h + l - r^2) / (2r)
-  const float r = __fsqrt_rn(h);
-  const float p = __fmul_rn(r, r);
-  const float pe = fmaf(r, r, -p);  // r^2 = p + pe exactly
-  const float r_lo = __fdiv_rn(__fadd_rn(__fsub_rn(__fsub_rn(h, p), pe), l), __fmul_rn(2.f, r));
-  // den = norm + eps, renormalised
-  float dh, de;
-  two_sum(r, eps, dh, de);
-  de = __fadd_rn(de, r_lo);
-  const float den_hi = __fadd_rn(dh, de);
-  const float den_lo = __fsub_rn(de, __fsub_rn(den_hi, dh));
-  // sqrt(d) = sd + sd_lo (d is an integer, exact in fp32)
-  const float fd = (float)d;
-  const float sd = __fsqrt_rn(fd);
-  const float sd_lo = __fdiv_rn(fmaf(-sd, sd, fd), __fmul_rn(2.f, sd));
-  // quotient: q = fl(sd / den_hi), remainder sd - q den_hi exact by FMA
-  const float q = __fdiv_rn(sd, den_hi);
-  const float rem = __fadd_rn(fmaf(-q, den_hi, sd), fmaf(-q, den_lo, sd_lo));
-  const float q_lo = __fdiv_rn(rem, den_hi);
-  inv_hi = __fadd_rn(q, q_lo);
-  inv_lo = __fsub_rn(q_lo, __fsub_rn(inv_hi, q));
-}
-
-// h = bf16( w * r * sqrt(d) / (||r||_2 + eps) ) per active row.  The rounding
-// of every element is the one the exact quotient gives (up to ~2^-46
-// relative): sum of squares in TwoSum pairs, the per-row scale sqrt(d) /
-// (norm + eps) as a double-float fp32 pair (row_scale), and each product
-// carried exactly before the bf16 rounding.
-//
-// Layout for latency: one CTA of kNormThreads (four warps) per row.  A row
-// of up to kNormThreads * kNormVec float4 (d <= 3072) is loaded into
-// registers with every load issued before the first use, so the kernel costs
-// about one memory round trip; longer rows are read twice.  At most 40
-// registers a thread: two of these CTAs fit on an SM beside an LM-head CTA, so
-// the LM head starts, and loads its first W stages, while the rows are formed.
+// RMSNorm per active row, for the single-CTA LM head (the kernel on SM pairs
+// forms its rows itself).  Layout for latency: one CTA of kNormThreads (four
+// warps) per row; a row of up to kNormThreads * kNormVec float4 (d <= 3072)
+// is held in registers, so the kernel costs about one memory round trip.
 constexpr int kNormThreads = 128;
 constexpr int kNormVec = 6;
 
-__global__ void __launch_bounds__(kNormThreads, 12) k_rmsnorm(const float* __restrict__ resid, const Dev dv) {
+__global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float* __restrict__ resid, const Dev dv) {
   __shared__ float red[kNormThreads / 32][2];
   pdl_wait();
   pdl_allow_next();
   const int n_rows = dv.plan->n_active * dv.L;
   if ((int)blockIdx.x >= n_rows) return;  // uniform per CTA
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int row = blockIdx.x;
-  const int n4 = dv.d >> 2;
-  const bool in_regs = n4 <= kNormThreads * kNormVec;
   const int a = row / dv.L, p = row - a * dv.L;
-  const float4* r4 = reinterpret_cast<const float4*>(resid + ((size_t)dv.active[a] * dv.L + p) * dv.d);
-  float4 v[kNormVec];
-  float sh = 0.f, sl = 0.f;
-  if (in_regs) {
-#pragma unroll
-    for (int k = 0; k < kNormVec; ++k) {
-      const int i = t + k * kNormThreads;
-      v[k] = i < n4 ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int k = 0; k < kNormVec; ++k) {
-      acc_square(v[k].x, sh, sl);
-      acc_square(v[k].y, sh, sl);
-      acc_square(v[k].z, sh, sl);
-      acc_square(v[k].w, sh, sl);
-    }
-  } else {
-    for (int i0 = t; i0 < n4; i0 += kNormThreads * kNormVec) {
-#pragma unroll
-      for (int k = 0; k < kNormVec; ++k) {
-        const int i = i0 + k * kNormThreads;
-        v[k] = i < n4 ? __ldg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int k = 0; k < kNormVec; ++k) {
-        acc_square(v[k].x, sh, sl);
-        acc_square(v[k].y, sh, sl);
-        acc_square(v[k].z, sh, sl);
-        acc_square(v[k].w, sh, sl);
-      }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float oh = __shfl_xor_sync(0xFFFFFFFFu, sh, o);
-    const float ol = __shfl_xor_sync(0xFFFFFFFFu, sl, o);
-    float e;
-    two_sum(sh, oh, sh, e);
-    sl = __fadd_rn(__fadd_rn(sl, ol), e);
-  }
-  if (lane == 0) {
-    red[warp][0] = sh;
-    red[warp][1] = sl;
-  }
-  __syncthreads();
-  // every thread forms the row's sum of squares and scale itself
-  float h = red[0][0], l = red[0][1];
-#pragma unroll
-  for (int w = 1; w < kNormThreads / 32; ++w) {
-    float e;
-    two_sum(h, red[w][0], h, e);
-    l = __fadd_rn(__fadd_rn(l, red[w][1]), e);
-  }
-  float inv_hi, inv_lo;
-  row_scale(h, l, dv.d, dv.eps, inv_hi, inv_lo);
-  uint2* out = reinterpret_cast<uint2*>(dv.h + (size_t)row * dv.d);
-  const float4* w4 = reinterpret_cast<const float4*>(dv.norm_w);
-  if (in_regs) {
-#pragma unroll
-    for (int k = 0; k < kNormVec; ++k) {
-      const int i = t + k * kNormThreads;
-      if (i < n4) {
-        const float4 w = w4 ? __ldg(w4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
-        out[i] = make_uint2(scaled_bf16(v[k].x, w.x, inv_hi, inv_lo) | (scaled_bf16(v[k].y, w.y, inv_hi, inv_lo) << 16),
-                            scaled_bf16(v[k].z, w.z, inv_hi, inv_lo) | (scaled_bf16(v[k].w, w.w, inv_hi, inv_lo) << 16));
-      }
-    }
-  } else {
-    for (int i = t; i < n4; i += kNormThreads) {
-      const float4 x = __ldg(r4 + i);
-      const float4 w = w4 ? __ldg(w4 + i) : make_float4(1.f, 1.f, 1.f, 1.f);
-      out[i] = make_uint2(scaled_bf16(x.x, w.x, inv_hi, inv_lo) | (scaled_bf16(x.y, w.y, inv_hi, inv_lo) << 16),
-                          scaled_bf16(x.z, w.z, inv_hi, inv_lo) | (scaled_bf16(x.w, w.w, inv_hi, inv_lo) << 16));
-    }
-  }
+  norm_row<kNormThreads, kNormVec>(resid + ((size_t)dv.active[a] * dv.L + p) * dv.d, dv.norm_w,
+                                   dv.h + (size_t)row * dv.d, dv.d, dv.eps, (int)threadIdx.x, red,
+                                   [] { __syncthreads(); });
   // the row is written: count it for the LM head, which waits for all rows
-  __syncthreads();
-  if (t == 0) {
+  if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(dv.rows_ready, 1u);
   }

@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 
 #include "dg_gumbel.cuh"
+#include "dg_norm.cuh"
 #include "dg_internal.cuh"
 
 namespace dg {
@@ -678,8 +679,10 @@ constexpr int kStagePairA = kBM * kBK * 2;        // this CTA's 128 rows of h
 constexpr int kStagePairB = (kBN / 2) * kBK * 2;  // this CTA's 128 rows of the W tile
 
 __global__ void __launch_bounds__(kThreadsLM, 1)
-    k_lmhead_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv) {
+    k_lmhead_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv,
+                  const float* __restrict__ resid) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ float red_norm[2][8][2];  // RMSNorm reductions of the two row groups
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStagesPair * kStagePairA;
@@ -697,6 +700,24 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
   const int KB = (dv.d + kBK - 1) / kBK;
+
+  // The epilogue warps start the loads of the RMSNorm phase below before the
+  // set-up, so their latency overlaps it: the norm weights (constant), then,
+  // once the previous kernel of the stream (the last tick's planner) has
+  // completed, the plan, the canvas of the group's first row and an L2
+  // prefetch of that row as it lies when canvas k is the k-th active one.
+  const int et = (int)threadIdx.x - 64, grp = et >> 8, r_first = (int)blockIdx.x + grp * (int)gridDim.x;
+  int n_active = 0, c_first = 0;
+  if (warp >= 2) {
+    if (dv.norm_w) prefetch_row<256>(dv.norm_w, dv.d >> 2, et & 255);
+    pdl_wait();
+    n_active = __ldcg(&dv.plan->n_active);
+    if (r_first < dv.max_active * dv.L) {
+      const int a = r_first / dv.L;
+      c_first = __ldcg(dv.active + a);
+      prefetch_row<256>(resid + (size_t)r_first * dv.d, dv.d >> 2, et & 255);
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesPair; ++s) {
@@ -749,12 +770,42 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       }
     }
   }
-  // no wait for the whole RMSNorm grid (see rows_written); the plan is read before
-  // the next kernel may launch, so its planner cannot have rewritten it yet
-  const int n_rows = __ldcg(&dv.plan->n_active) * dv.L;
-  pdl_allow_next();
+  // The previous kernel of the stream (the last tick's planner) has completed:
+  // the plan, the active list and the slots are current.  The plan is read
+  // before the next kernel may launch, so its planner cannot rewrite it first.
+  if (warp < 2) {
+    pdl_wait();
+    n_active = __ldcg(&dv.plan->n_active);
+  }
+  const int n_rows = n_active * dv.L;
+  pdl_allow_next_after(n_rows);
   const int n_mt = (n_rows + 2 * kBM - 1) / (2 * kBM);  // 256-row pair tiles
   const int n_units = n_mt * dv.n_chunks;
+
+  if (warp >= 2) {
+    // RMSNorm: the epilogue warps form rows blockIdx.x + j * gridDim.x of h, two
+    // at a time (eight warps a row), and count them; every CTA's producer then
+    // waits for all rows (rows_written).  The grid is at most one CTA per SM, so
+    // all of its CTAs can be resident at once; one kept waiting for an SM longer
+    // than the bounded wait fails the tick with a timeout instead of hanging it.
+    for (int r = r_first; r < n_rows; r += 2 * (int)gridDim.x) {
+      const int a = r / dv.L, p = r - a * dv.L;
+      const int c = r == r_first ? c_first : __ldcg(dv.active + a);
+      norm_row<256, 4>(resid + ((size_t)c * dv.L + p) * dv.d, dv.norm_w, dv.h + (size_t)r * dv.d,
+                       dv.d, dv.eps, et & 255, red_norm[grp],
+                       [grp] {
+                         if (grp == 0)
+                           asm volatile("bar.sync 2, 256;" ::: "memory");
+                         else
+                           asm volatile("bar.sync 3, 256;" ::: "memory");
+                       });
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+    if (warp == 2 && lane == 0 && n_rows > (int)blockIdx.x) {
+      __threadfence();  // this CTA's rows are written
+      atomicAdd(dv.rows_ready, (unsigned)((n_rows - 1 - (int)blockIdx.x) / (int)gridDim.x + 1));
+    }
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -950,8 +1001,8 @@ cudaError_t lmhead_configure() {
   return e;
 }
 
-cudaError_t launch_lmhead_pair(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
-                               cudaStream_t st) {
+cudaError_t launch_lmhead_pair(const Dev& dv, const float* resid, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                               int num_sms, cudaStream_t st) {
   // persistent grid of CTA pairs, never more pairs than the largest number of work units
   const int max_mt = (dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM);
   int pairs = max_mt * dv.n_chunks;
@@ -971,7 +1022,7 @@ cudaError_t launch_lmhead_pair(const Dev& dv, const CUtensorMap* tmA, const CUte
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_lmhead_pair, *tmA, *tmB, dv);
+  return cudaLaunchKernelEx(&cfg, k_lmhead_pair, *tmA, *tmB, dv, resid);
 }
 
 cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,

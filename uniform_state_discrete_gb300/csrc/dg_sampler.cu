@@ -195,10 +195,11 @@ dg_status tick(dg_sampler* s, const float* resid) {
     return s->timed ? cudaEventRecordWithFlags(s->timing[i], s->stream, rec_flags) : cudaSuccess;
   };
   DG_CUDA(s->err, mark(0), "record timing event");
-  DG_CUDA(s->err, dg::launch_rmsnorm(s->dv, resid, s->stream), "launch rmsnorm");
+  // the LM head on SM pairs forms the RMSNorm rows itself
+  if (!s->pair) DG_CUDA(s->err, dg::launch_rmsnorm(s->dv, resid, s->stream), "launch rmsnorm");
   DG_CUDA(s->err, mark(1), "record timing event");
   DG_CUDA(s->err,
-          s->pair ? dg::launch_lmhead_pair(s->dv, &s->tmA, &s->tmB, s->num_sms, s->stream)
+          s->pair ? dg::launch_lmhead_pair(s->dv, resid, &s->tmA, &s->tmB, s->num_sms, s->stream)
                   : dg::launch_lmhead(s->dv, &s->tmA, &s->tmB, s->num_sms, s->stream),
           "launch lm head");
   DG_CUDA(s->err, mark(2), "record timing event");

@@ -260,9 +260,10 @@ extern "C" dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, co
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   k_static_prep<<<1, 32, 0, st>>>(su.base, seed, (int)block, (int)step, temperature);
   e = cudaGetLastError();
-  if (e == cudaSuccess) e = dg::launch_rmsnorm(dv, resid, st);
+  if (e == cudaSuccess && !pair) e = dg::launch_rmsnorm(dv, resid, st);  // the pair kernel forms its rows itself
   if (e == cudaSuccess)
-    e = pair ? dg::launch_lmhead_pair(dv, &tmA, &tmB, su.num_sms, st) : dg::launch_lmhead(dv, &tmA, &tmB, su.num_sms, st);
+    e = pair ? dg::launch_lmhead_pair(dv, resid, &tmA, &tmB, su.num_sms, st)
+             : dg::launch_lmhead(dv, &tmA, &tmB, su.num_sms, st);
   if (e == cudaSuccess) {
     k_static_combine<<<(rows + 7) / 8, 256, 0, st>>>(dv, rows, entropy, logz, sample, argmax);
     e = cudaGetLastError();
