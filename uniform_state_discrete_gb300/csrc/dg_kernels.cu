@@ -47,15 +47,20 @@ __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float* __restric
 // waits for another: the last arrival at a counter does the work.
 constexpr int kFinishRows = 8;  // positions (warps) per CTA
 
+static_assert(kFinishRows <= (int)(sizeof(TailScratch::row_canvas) / sizeof(int)), "row_canvas holds a CTA's rows");
+
 // The planner of k_finish: waits (bounded) until every CTA of the grid has read
-// this tick's plan, then plans the next tick.
-__device__ __forceinline__ void plan_next_tick(const Dev& dv, int tick, const Group& g, TailScratch* sc) {
-  if (g.tid == 0) {
+// this tick's plan, then plans the next tick.  `started` says that thread 0
+// already saw every CTA counted (a load the caller ordered by a fence since),
+// so no wait is needed; known_c / known_state pass on a slot the group wrote.
+__device__ __forceinline__ void plan_next_tick(const Dev& dv, int tick, const Group& g, TailScratch* sc,
+                                               bool started = false, int known_c = -1, int known_state = kDone) {
+  if (g.tid == 0 && !started) {
     if (!wait_count(dv.fin_started, gridDim.x) && atomicCAS(&dv.plan->err, kErrNone, kErrTimeout) == kErrNone)
       dv.plan->err_info[0] = -2;
   }
   g.sync();
-  plan_tick(dv, tick + 1, g, sc, false);
+  plan_tick(dv, tick + 1, g, sc, false, known_c, known_state);
 }
 
 // It does not wait for the whole LM-head grid: each CTA waits for the LM-head
@@ -82,14 +87,16 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   }
   const int row0 = blockIdx.x * kFinishRows;
   if (row0 >= n_rows) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = row0 + warp;
+  // the canvas of this warp's row, read before the wait so its latency is hidden
+  const int row_c = (lane == 0 && row < n_rows) ? __ldcg(dv.active + row / dv.L) : 0;
   if (threadIdx.x == 0) {
     const bool ok = wait_count(dv.slab_done + row0 / 128, (uint32_t)dv.n_chunks);
     if (!ok && atomicCAS(&dv.plan->err, kErrNone, kErrTimeout) == kErrNone) dv.plan->err_info[0] = -1 - (int)blockIdx.x;
   }
   __syncthreads();
   const int row1 = min(row0 + kFinishRows, n_rows);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = row0 + warp;
   if (row < row1) {
     Partial acc = empty_partial();
     const Partial* src = dv.part + (size_t)row * dv.n_sub;
@@ -108,7 +115,8 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
     }
     if (lane == 0) {
       const int a = row / dv.L, p = row - a * dv.L;
-      const int c = __ldcg(dv.active + a);
+      const int c = row_c;
+      sc.row_canvas[warp] = c;
       const float l2S = log2f(acc.S);
       const float H = 0.69314718055994531f * (l2S - acc.A / acc.S);
       const float lz = 0.69314718055994531f * (acc.m + l2S);
@@ -128,7 +136,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
     int nd = 0;
     for (int a = row0 / dv.L; a * dv.L < row1; ++a) {
       const int lo = max(a * dv.L, row0), hi = min((a + 1) * dv.L, row1);
-      const int c = __ldcg(dv.active + a);
+      const int c = sc.row_canvas[lo - row0];
       const unsigned old = atomicAdd(&dv.canvas_rows[c], (unsigned)(hi - lo));
       if (old + (unsigned)(hi - lo) == (unsigned)dv.L) {
         dv.canvas_rows[c] = 0u;  // every row of this canvas is combined: reset for the next tick
@@ -139,15 +147,18 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   }
   __syncthreads();
   const int nd = sc.flags[3];
+  const int na = n_rows / dv.L;  // canvases active this tick
   for (int i = 0; i < nd; ++i) {
     const int c = sc.done_list[i];
+    // whether every CTA of the grid has started (plain load; the fences below
+    // order it before the plan is rewritten)
+    const bool started = threadIdx.x == 0 && *(volatile const uint32_t*)dv.fin_started >= gridDim.x;
     __threadfence();
-    commit_canvas(dv, c, g, &sc);
+    const int state = commit_canvas(dv, c, g, &sc);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
       // the last commit of the tick plans the next; alone, this one is the last
-      const int na = __ldcg(&dv.plan->n_active);
       sc.flags[1] = (na == 1 || atomicAdd(&dv.plan->commits, 1u) == (unsigned)(na - 1)) ? 1 : 0;
     }
     __syncthreads();
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
     __syncthreads();
     if (plan_now) {
       __threadfence();
-      plan_next_tick(dv, tick, g, &sc);
+      plan_next_tick(dv, tick, g, &sc, started, c, state);
     }
   }
 }

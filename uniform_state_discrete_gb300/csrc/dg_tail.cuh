@@ -33,7 +33,8 @@ struct TailScratch {
   float redf[kTailThreads / 32][2];
   int redi[kTailThreads / 32][2];
   int flags[4];
-  int done_list[64];  // canvases completed by one CTA's rows (at most 8 / L + 2)
+  int done_list[64];   // canvases completed by one CTA's rows (at most 8 / L + 2)
+  int row_canvas[8];   // canvas of each of a finishing CTA's rows
 };
 
 // Sort 32 keys held one per lane, ascending (bitonic network over shuffles).
@@ -84,13 +85,15 @@ __device__ __forceinline__ void init_canvas(const Dev& dv, int c, int block, con
 // every active canvas, for a state loaded from the host.  Slots may have been
 // written by other CTAs of the grid, so they are read at L2 (ld.global.cg).
 // The group has kTailThreads threads; with at most that many canvases the
-// slots are read once.
-static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailScratch* sc, bool refresh_temps) {
+// slots are read once.  The state of canvas `known_c` (if >= 0), which the
+// calling group has just written itself, is taken as `known_state`.
+static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailScratch* sc, bool refresh_temps,
+                                 int known_c = -1, int known_state = kDone) {
   const int lane = g.tid & 31, w = g.tid >> 5;
   int st0 = kDone;  // state of canvas g.tid (first round)
   int run = 0, due = 0;
   for (int c = g.tid; c < dv.B; c += g.n) {
-    const int st = __ldcg(&dv.slots[c].state);
+    const int st = c == known_c ? known_state : __ldcg(&dv.slots[c].state);
     if (c == g.tid) st0 = st;
     run += st == kActive ? 1 : 0;
     due |= (st == kWaiting && __ldcg(&dv.slots[c].admit_tick) <= tick) ? 1 : 0;
@@ -180,8 +183,9 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
 // 31 entropies within the bound fall back to a bitonic sort of the canvas.
 // Every per-position input is read once, up front, into registers (this tick's
 // values were written by other CTAs: read at L2); the group has kTailThreads
-// threads, so each holds at most kTailPer positions.
-static __device__ void commit_canvas(const Dev& dv, int c, const Group& g, TailScratch* sc) {
+// threads, so each holds at most kTailPer positions.  Returns the canvas's
+// state after the commit (kActive, or kDone after its last block).
+static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailScratch* sc) {
   const int L = dv.L;
   dg_slot sl;
   sl.seed = __ldcg(&dv.slots[c].seed);
@@ -328,6 +332,8 @@ static __device__ void commit_canvas(const Dev& dv, int c, const Group& g, TailS
       so.n_committed = sl.n_committed + n_acc;
       so.mean_entropy = mean_H;
     }
+    g.sync();
+    return kActive;
   } else {
 #pragma unroll
     for (int i = 0; i < kTailPer; ++i) {
@@ -362,8 +368,9 @@ static __device__ void commit_canvas(const Dev& dv, int c, const Group& g, TailS
         so.state = kDone;
       }
     }
+    g.sync();
+    return more ? kActive : kDone;
   }
-  g.sync();
 }
 
 }  // namespace dg
