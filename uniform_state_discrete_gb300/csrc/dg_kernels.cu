@@ -150,12 +150,15 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   const int na = n_rows / dv.L;  // canvases active this tick
   for (int i = 0; i < nd; ++i) {
     const int c = sc.done_list[i];
-    // whether every CTA of the grid has started (plain load; the fences below
-    // order it before the plan is rewritten)
+    // whether every CTA of the grid has started (plain load; the fence below
+    // orders it before the plan is rewritten)
     const bool started = threadIdx.x == 0 && *(volatile const uint32_t*)dv.fin_started >= gridDim.x;
-    __threadfence();
+    __threadfence();  // the rows' results, seen complete through the canvas counter, are read after it
     const int state = commit_canvas(dv, c, g, &sc);
-    __threadfence();
+    // With several canvases, the commit's writes are released before the commit
+    // counter and the planner acquires the other commits' slots; alone, this CTA
+    // plans right away from what it wrote itself.
+    if (na > 1) __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
       // the last commit of the tick plans the next; alone, this one is the last
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
     const int plan_now = sc.flags[1];
     __syncthreads();
     if (plan_now) {
-      __threadfence();
+      if (na > 1) __threadfence();
       plan_next_tick(dv, tick, g, &sc, started, c, state);
     }
   }
