@@ -185,7 +185,7 @@ def oracle_positions_per_s(wl: dict, budget_s: float, seed_base: int, W16=None, 
     W16 = synth.wvocab(0, wl["vocab"], wl["hidden"]) if W16 is None else W16
     cfg = oracle.OracleConfig(vocab=wl["vocab"], hidden=wl["hidden"], canvas_len=wl["canvas_len"],
                               n_canvases=wl["n_canvases"], num_inference_steps=wl["steps"], gen_blocks=1 << 10,
-                              seeds=[seed_base + c for c in range(wl["n_canvases"])])
+                              seeds=[seed_base + c for c in range(wl["n_canvases"])], mode=wl.get("mode", "freeze"))
     o = oracle.OracleSampler(cfg, W16)
     fn = oracle.sampler.synth_resid_fn(cfg, W16, SIGMA_HIDDEN)
     positions, busy, ticks = 0, 0.0, 0
@@ -217,7 +217,7 @@ def run_reference(args, wl, world, rank):
     sample = max(1, min(n_pos, int(budget / max(1, args.steps + args.warmup) / per_pos)))
     cfg = oracle.OracleConfig(vocab=wl["vocab"], hidden=wl["hidden"], canvas_len=wl["canvas_len"],
                               n_canvases=wl["n_canvases"], num_inference_steps=wl["steps"], gen_blocks=1 << 10,
-                              seeds=list(range(wl["n_canvases"])))
+                              seeds=list(range(wl["n_canvases"])), mode=wl.get("mode", "freeze"))
     o = oracle.OracleSampler(cfg, W16)
     fn = oracle.sampler.synth_resid_fn(cfg, W16, SIGMA_HIDDEN)
     rows = np.arange(sample)
@@ -240,7 +240,7 @@ def run_reference(args, wl, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * busy / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "description": wl["text"]},
+            "config": {"workload": args.workload, "description": wl["text"], "commit_mode": wl["mode"]},
             "cpu_baseline": {"kind": "oracle", "cores": oracle.threads(), "value": value, "unit": UNIT,
                              "sample": f"each step: {sample} of {n_pos} positions of one tick (RMSNorm, fp64 LM head, "
                                        f"softmax statistics, Gumbel sample, acceptance), oracle as it stands"},
@@ -268,7 +268,8 @@ def run_ours(args, wl, world, rank, local):
     total_ticks = args.warmup + args.steps + args.kernel_steps + args.e2e_steps + 2
     blocks = total_ticks // N + 2
     seeds = [rank * B + c for c in range(B)]
-    cfg = dg.make_config(V, d, L, n_canvases=B, gen_blocks=blocks, num_inference_steps=N, seeds=seeds)
+    cfg = dg.make_config(V, d, L, n_canvases=B, gen_blocks=blocks, num_inference_steps=N, seeds=seeds,
+                         mode=dg.DG_REACCEPT if wl.get("mode") == "reaccept" else dg.DG_FREEZE)
     s = dg.Sampler(cfg, w_dev, stream=stream)
     resid = torch.empty(B, L, d, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -414,7 +415,7 @@ def run_ours(args, wl, world, rank, local):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": args.workload, "description": wl["text"],
+                "config": {"workload": args.workload, "description": wl["text"], "commit_mode": wl["mode"],
                            "positions_per_step": positions_per_tick,
                            "l2": "flushed before every timed tick: 256 MB device write, then read back (outside the "
                                  "events)" if args.flush == "writeread" else "flushed by a 256 MB write",
@@ -459,6 +460,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flush", choices=["write", "writeread"], default="writeread")
     ap.add_argument("--graph", type=int, default=1, help="replay each tick as a captured CUDA graph")
+    ap.add_argument("--mode", choices=["freeze", "reaccept"], default="freeze",
+                    help="commit mode: committed positions freeze (default), or every step re-accepts all positions")
     ap.add_argument("--kernel-steps", type=int, default=200, help="ticks of the per-kernel timing pass")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -466,7 +469,7 @@ def main():
     world, rank, local = dist_setup()
     if world != args.gpus and world > 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload], mode=args.mode)
     if args.impl == "reference":
         run_reference(args, wl, world, rank)
     else:

@@ -61,10 +61,20 @@ typedef enum dg_status {
   DG_ERR_TIMEOUT = 8      /* a kernel's bounded wait ran out (pipeline stalled)    */
 } dg_status;
 
-/* Commit semantics.  DG_FREEZE: a committed position keeps its token for the
- * rest of the block and only uncommitted positions enter each step's sort
- * (ComfyUI-DiffusionGemma, "What it is": confident positions freeze). */
-typedef enum dg_mode { DG_FREEZE = 0 } dg_mode;
+/* Commit semantics.
+ * DG_FREEZE: a committed position keeps its token for the rest of the block
+ *   and only uncommitted positions enter each step's sort
+ *   (ComfyUI-DiffusionGemma, "What it is": confident positions freeze).
+ * DG_REACCEPT: every step sorts all positions of the canvas afresh and accepts
+ *   the low-entropy prefix; accepted positions take this step's sample and all
+ *   others, including positions accepted at earlier steps, are re-noised (The
+ *   Annotated DiffusionGemma, "Keep a low-entropy prefix and renoise the rest"
+ *   and its "Denoise, stage, commit, and generate" code).  The committed mask
+ *   is then the set accepted at the latest step, commit_step the last step a
+ *   position was accepted, and the slot's n_remasked the positions accepted at
+ *   the previous step and re-noised at the latest one.  At the final step
+ *   every position takes its sample in both modes. */
+typedef enum dg_mode { DG_FREEZE = 0, DG_REACCEPT = 1 } dg_mode;
 
 /*
  * Sampler configuration.  Field names follow the pages' knobs (DiffusionGemma
@@ -85,7 +95,7 @@ typedef struct dg_config {
   float confidence;            /* early stop when mean H (nats) falls below this, >= 0           */
   int32_t stability;           /* steps the argmax canvas must stay unchanged; must be 1         */
   float rms_eps;               /* RMSNorm epsilon, added to ||x||_2, >= 0                        */
-  int32_t mode;                /* dg_mode; DG_FREEZE                                             */
+  int32_t mode;                /* dg_mode: DG_FREEZE or DG_REACCEPT                              */
   int32_t max_active;          /* most canvases active in one tick, 1..B (0 = B); sizes buffers  */
   const uint64_t* seeds;       /* host [B]: per-canvas Philox key; NULL = seed c for canvas c    */
   const int32_t* admit_tick;   /* host [B]: tick at which canvas c joins, >= 0; NULL = all at 0  */
@@ -99,12 +109,14 @@ typedef struct dg_slot {
   int32_t state;
   int32_t block;            /* current block (gen_blocks - 1 after the last one)      */
   int32_t step;             /* step of the current block the next tick runs           */
-  int32_t n_committed;      /* committed positions of the current block               */
+  int32_t n_committed;      /* committed positions of the current block (DG_REACCEPT:
+                               positions accepted at the latest step)                 */
   int32_t steps_used;       /* steps run over all finished blocks                     */
   int32_t converged_blocks; /* blocks ended by the early-stop test                    */
   float temperature;        /* T the next tick applies to this canvas                 */
   float mean_entropy;       /* mean H (nats) over the canvas at its last tick         */
-  int32_t reserved;
+  int32_t n_remasked;       /* DG_REACCEPT: positions accepted at the previous step and
+                               re-noised at the latest one; 0 under DG_FREEZE          */
 } dg_slot;
 
 typedef struct dg_sampler dg_sampler;

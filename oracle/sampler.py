@@ -11,18 +11,25 @@ every active canvas, at its own step s of its own block b:
                                             ("RMSNorm", "Compute entropy")
   3. early stop when s >= 1, mean_p H < confidence and the argmax canvas
      equals the previous step's                   ("Check for early stopping")
-  4. otherwise sort the uncommitted positions by (H, p) ascending and accept
+  4. otherwise sort the open positions by (H, p) ascending and accept
      position j of that order iff the sum of the entropies before it is
-     <= entropy_bound; accepted positions take y and freeze
+     <= entropy_bound; accepted positions take y
                             ("Keep a low-entropy prefix and renoise the rest")
-  5. on early stop or at s = N-1 every uncommitted position takes y and the
+  5. on early stop or at s = N-1 every open position takes y and the
      block is finished ("On convergence or after N steps, we commit")
-  6. every other uncommitted position is re-noised to a uniform token.
+  6. every other open position is re-noised to a uniform token.
+
+Two commit modes.  "freeze": accepted positions freeze and only uncommitted
+positions are open.  "reaccept": every position is open at every step, as the
+Annotated page's denoise code computes it (its `accepted` mask is recomputed
+from all entropies each step and `torch.where(accepted, sample, randint)`
+rebuilds the whole canvas); the committed mask is then the latest step's
+accepted set and commit_step the last step a position was accepted.
 
 Readings where the pages are silent or disagree (each listed in the design doc):
-committed positions stay frozen (ComfyUI-DiffusionGemma, "What it is": the
-lowest-entropy positions freeze into place) and only uncommitted positions
-enter the per-step sort; the prefix is exclusive and compared with <=; ties in
+by default committed positions stay frozen (ComfyUI-DiffusionGemma, "What it
+is": the lowest-entropy positions freeze into place) and only uncommitted
+positions enter the per-step sort; the prefix is exclusive and compared with <=; ties in
 H go to the lower position; the early-stop test is skipped at s = 0; the last
 step commits every remaining position to its sample; blocks of one canvas run
 one after another with a fresh uniform canvas each (DiffusionGemma Denoise
@@ -80,6 +87,7 @@ class OracleConfig:
     seeds: Optional[list] = None
     admit_tick: Optional[list] = None
     max_active: Optional[int] = None  # most canvases running in one tick (None: all)
+    mode: str = "freeze"  # "freeze" or "reaccept" (see the module docstring)
     # parity margins stated by the task for flagging near-ties
     margin_H: float = 1e-3
     margin_gap: float = 1e-4
@@ -109,6 +117,7 @@ class TickRecord:
     flag_amax: np.ndarray         # [n_active*L] argmax top-2 gap below margin
     flag_commit: np.ndarray       # [n_active, L] position sits on a commit-boundary near-tie
     flag_canvas: np.ndarray       # [n_active] canvas-level near-tie (prefix sum or early-stop test)
+    n_remasked: np.ndarray = None  # [n_active] reaccept: accepted at the previous step, re-noised now
 
 
 class OracleSampler:
@@ -194,7 +203,8 @@ class OracleSampler:
                              mean_H=np.zeros(n), converged=np.zeros(n, bool), final=np.zeros(n, bool),
                              accepted=np.zeros((n, L), bool), n_accepted=np.zeros(n, np.int32),
                              flag_y=st["ggap"] < cfg.margin_gap, flag_amax=st["zgap"] < cfg.margin_gap,
-                             flag_commit=np.zeros((n, L), bool), flag_canvas=np.zeros(n, bool))
+                             flag_commit=np.zeros((n, L), bool), flag_canvas=np.zeros(n, bool),
+                             n_remasked=np.zeros(n, np.int32))
             for i, c in enumerate(act):
                 self._commit(int(c), st[i * L:(i + 1) * L], rec, i, draw_u32, uniform_token, PURPOSE_RENOISE)
         self.tick_no += 1
@@ -215,7 +225,10 @@ class OracleSampler:
             rec.flag_canvas[i] = True
         final = converged or s == N - 1
         rec.converged[i], rec.final[i] = converged, final
-        unc = np.nonzero(~self.committed[c])[0]
+        reaccept = cfg.mode == "reaccept"
+        assert cfg.mode in ("freeze", "reaccept"), cfg.mode
+        # the open positions: under "reaccept" every position, else the uncommitted ones
+        unc = np.arange(L) if reaccept else np.nonzero(~self.committed[c])[0]
         if not final:
             order, excl, k = entropy_bounded_accept(H, unc, cfg.entropy_bound)
             acc = np.array(order[:k], dtype=np.int64)
@@ -231,12 +244,17 @@ class OracleSampler:
                 for p in order[k:]:
                     if H[p] < h_last_acc + cfg.margin_H:
                         rec.flag_commit[i, p] = True
+            if reaccept:
+                was = self.committed[c].copy()
+                self.committed[c] = False
             self.x[c, acc] = y[acc]
             self.committed[c, acc] = True
             self.commit_step[c, acc] = s
             rec.accepted[i, acc] = True
             rec.n_accepted[i] = k
-            # uniform re-noise of every position still uncommitted
+            if reaccept:
+                rec.n_remasked[i] = int(np.sum(was & ~self.committed[c]))
+            # uniform re-noise of every open position not accepted
             for p in unc:
                 if not self.committed[c, p]:
                     self.x[c, p] = uniform_token(draw_u32(cfg.seed(c), PURPOSE_RENOISE, b, s, int(p)), V)

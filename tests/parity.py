@@ -56,6 +56,7 @@ class Case:
     max_active: int = 0
     norm_seed: int = None  # RMSNorm weight from synth.norm_weight, or all ones
     rms_eps: float = 1e-6
+    mode: str = "freeze"  # commit mode: "freeze" (DG_FREEZE) or "reaccept" (DG_REACCEPT)
 
     def oracle_cfg(self) -> OracleConfig:
         return OracleConfig(vocab=self.vocab, hidden=self.hidden, canvas_len=self.canvas_len,
@@ -64,7 +65,7 @@ class Case:
                             confidence=f32(self.conf), rms_eps=f32(self.rms_eps),
                             seeds=list(self.seeds) if self.seeds else list(range(self.n_canvases)),
                             admit_tick=list(self.admit) if self.admit else None,
-                            max_active=self.max_active or None)
+                            max_active=self.max_active or None, mode=self.mode)
 
     def gpu_cfg(self):
         import uniform_state_discrete_gb300 as dg
@@ -72,6 +73,7 @@ class Case:
                               gen_blocks=self.gen_blocks, num_inference_steps=self.steps, t_min=self.t_min,
                               t_max=self.t_max, entropy_bound=self.bound, confidence=self.conf, rms_eps=self.rms_eps,
                               max_active=self.max_active,
+                              mode=dg.DG_REACCEPT if self.mode == "reaccept" else dg.DG_FREEZE,
                               seeds=list(self.seeds) if self.seeds else list(range(self.n_canvases)),
                               admit_tick=list(self.admit) if self.admit else None)
 
@@ -207,7 +209,8 @@ def compare_tick(s, o: OracleSampler, rec, case: Case, rep: Report):
         if not np.any(pos_flag):
             gs, os_ = gst["slots"][c], o
             for fld, ov in (("state", o.status[c]), ("block", o.block[c]), ("step", o.step_no[c]),
-                            ("steps_used", o.steps_used[c]), ("converged_blocks", o.converged_blocks[c])):
+                            ("steps_used", o.steps_used[c]), ("converged_blocks", o.converged_blocks[c]),
+                            ("n_committed", o.committed[c].sum()), ("n_remasked", rec.n_remasked[i])):
                 if int(gs[fld]) != int(ov):
                     rep.errors.append(f"tick {rec.tick} canvas {c}: slot {fld} {int(gs[fld])} != oracle {int(ov)}")
             if rec.final[i]:

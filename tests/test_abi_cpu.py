@@ -62,6 +62,13 @@ def test_unsupported_knobs_and_bad_pointers():
     h = ctypes.c_void_p()
     assert dg.lib.dg_sampler_create(ctypes.byref(cfg), ctypes.c_void_p(16), None, ctypes.c_void_p(256), 1 << 30,
                                     None, ctypes.byref(h)) == dg.DG_ERR_UNSUPPORTED
+    # the two commit modes size the same workspace; any other mode is an invalid config
+    cfg = dg.make_config(2048, 128, 16, mode=dg.DG_REACCEPT)
+    assert dg.dg_workspace_size(cfg) == dg.dg_workspace_size(dg.make_config(2048, 128, 16)) > 0
+    cfg = dg.make_config(2048, 128, 16, mode=2)
+    assert dg.dg_workspace_size(cfg) == 0
+    assert dg.lib.dg_sampler_create(ctypes.byref(cfg), ctypes.c_void_p(16), None, ctypes.c_void_p(256), 1 << 30,
+                                    None, ctypes.byref(h)) == dg.DG_ERR_ARG
     cfg = dg.make_config(2048, 128, 16)
     need = dg.dg_workspace_size(cfg)
     assert need > 0

@@ -107,6 +107,23 @@ def test_hot_schedule_noise_driven_regime():
     _assert_report(teacher_forced(case), "hot")
 
 
+def test_reaccept_tiny_config_teacher_forced():
+    """DG_REACCEPT at the tiny config: one position accepted per step (every entropy far above the
+    bound), every other position, earlier acceptances included, re-noised."""
+    rep = teacher_forced(Case(vocab=2048, hidden=128, canvas_len=16, steps=8, mode="reaccept"))
+    _assert_report(rep, "reaccept tiny")
+
+
+def test_reaccept_many_accepted_and_remasked():
+    """DG_REACCEPT with moderate hidden noise: several accepted positions per step, accepted sets
+    that change between steps (re-masking), two blocks; 256 positions take the SM-pair LM head and
+    more than 31 candidates take the commit's full sort."""
+    for L, bound in ((32, 1.0), (256, 3.0)):
+        case = Case(vocab=512, hidden=256, canvas_len=L, steps=12, bound=bound, sigma=0.3, sigma_w=0.1, w_seed=2,
+                    seeds=(9,), gen_blocks=2, mode="reaccept")
+        _assert_report(teacher_forced(case), f"reaccept L={L}")
+
+
 def _gpu_free_run(case, W):
     import torch
     import uniform_state_discrete_gb300 as dg

@@ -401,3 +401,101 @@ def test_committed_token_is_a_sample_not_the_argmax():
             hits += int(np.sum(committed_tok[acc] == amax[acc]))
             total += acc.size
     assert total == 4 * cfg.canvas_len and hits <= total // 8
+
+
+# ------------------------------------------------------------ re-accepting commit mode
+def _pages_next_canvas(H, y, seed, block, step, bound, V):
+    """The next canvas as the Annotated page's denoise code builds it ("Denoise, stage, commit, and
+    generate"): sort all entropies, accepted = scatter(cumsum(sH) - sH <= bound), then
+    where(accepted, sample, uniform token) over the whole canvas.  numpy's stable sort gives the
+    (H, p) tie order; the uniform tokens come from the pinned Philox re-noise draw."""
+    idx = np.argsort(H, kind="stable")
+    sH = H[idx]
+    accepted = np.zeros(H.size, bool)
+    accepted[idx] = (np.cumsum(sH) - sH) <= bound
+    noise = np.array([oracle.uniform_token(oracle.draw_u32(seed, oracle.PURPOSE_RENOISE, block, step, p), V)
+                      for p in range(H.size)])
+    return accepted, np.where(accepted, y, noise)
+
+
+def test_reaccept_rebuilds_the_canvas_as_the_pages_code_does():
+    """Moderate hidden noise: several positions fit the bound per step and the accepted set changes
+    from step to step, so positions accepted earlier are re-noised; every tick must equal the page's
+    expression evaluated on that tick's entropies and samples, and the last step takes every sample."""
+    V, d, L = 512, 256, 32
+    cfg = oracle.OracleConfig(vocab=V, hidden=d, canvas_len=L, num_inference_steps=12, entropy_bound=1.0,
+                              seeds=[9], mode="reaccept", confidence=0.0)
+    W = synth.wvocab(2, V, d, sigma_w=0.1)
+    s = oracle.OracleSampler(cfg, W)
+    fn = oracle.sampler.synth_resid_fn(cfg, W, 0.3)
+    remasked = 0
+    while not s.done():
+        rec = s.tick(fn)
+        st = rec.stats
+        H, y = st["H"], st["y"]
+        if rec.final[0]:
+            assert np.array_equal(s.tokens_out[0, 0], y)
+            continue
+        accepted, x_next = _pages_next_canvas(H, y, 9, int(rec.block[0]), int(rec.step[0]), cfg.entropy_bound, V)
+        assert np.array_equal(s.committed[0], accepted)
+        assert np.array_equal(s.x[0], x_next)
+        assert rec.n_accepted[0] == accepted.sum() == s.committed[0].sum()
+        remasked += int(rec.n_remasked[0])
+    assert remasked > 0  # the run did re-noise positions accepted at an earlier step
+
+
+def test_reaccept_remasks_a_position_whose_entropy_rank_rises():
+    """Hand-made entropies: position 0 is accepted at step 0; at step 1 two other positions have
+    lower entropy and use up the budget, so position 0 is re-noised (and counted), while under the
+    freezing mode it would keep its token."""
+    V, L = 64, 4
+    for mode in ("reaccept", "freeze"):
+        cfg = oracle.OracleConfig(vocab=V, hidden=8, canvas_len=L, num_inference_steps=4, entropy_bound=0.1,
+                                  confidence=0.0, seeds=[1], mode=mode)
+        s = oracle.OracleSampler(cfg, np.zeros((V, 8), np.uint16))
+        outs = []
+        for step, (H, y) in enumerate((([0.05, 2.0, 3.0, 4.0], [5, 6, 7, 8]),
+                                       ([3.0, 0.02, 0.07, 4.0], [9, 10, 11, 12]))):
+            st = np.zeros(L, oracle.POS_DTYPE)
+            st["H"], st["y"], st["amax"] = H, y, step
+            rec = oracle.sampler.TickRecord(
+                tick=step, canvases=np.array([0]), block=np.array([0]), step=np.array([step]), T=np.ones(1),
+                stats=st, mean_H=np.zeros(1), converged=np.zeros(1, bool), final=np.zeros(1, bool),
+                accepted=np.zeros((1, L), bool), n_accepted=np.zeros(1, np.int32),
+                flag_y=np.zeros(L, bool), flag_amax=np.zeros(L, bool), flag_commit=np.zeros((1, L), bool),
+                flag_canvas=np.zeros(1, bool), n_remasked=np.zeros(1, np.int32))
+            s._commit(0, st, rec, 0, oracle.draw_u32, oracle.uniform_token, oracle.PURPOSE_RENOISE)
+            s.step_no[0] = step + 1
+            outs.append((s.x[0].copy(), s.committed[0].copy(), int(rec.n_remasked[0]), int(rec.n_accepted[0])))
+        noise = lambda p, stp: oracle.uniform_token(oracle.draw_u32(1, oracle.PURPOSE_RENOISE, 0, stp, p), V)
+        # step 0 (both modes): sorted H 0.05, 2, ...; exclusive sums 0, 0.05, 2.05 -> positions 0 and 1
+        x0, c0, r0, k0 = outs[0]
+        assert k0 == 2 and list(c0) == [True, True, False, False] and r0 == 0
+        assert list(x0) == [5, 6, noise(2, 0), noise(3, 0)]
+        x1, c1, r1, k1 = outs[1]
+        if mode == "reaccept":
+            # all four open: sorted 0.02 (p1), 0.07 (p2), 3 (p0); sums 0, 0.02, 0.09 -> p1, p2, p0 accepted
+            assert k1 == 3 and list(c1) == [True, True, True, False] and r1 == 0
+            assert list(x1) == [9, 10, 11, noise(3, 1)]
+        else:
+            # p0, p1 frozen; open p2 (0.07), p3 (4): sums 0, 0.07 -> both accepted
+            assert k1 == 2 and list(c1) == [True, True, True, True]
+            assert list(x1) == [5, 6, 11, 12]
+
+
+def test_reaccept_remask_count_matches_mask_difference():
+    """n_remasked = |accepted(s-1) minus accepted(s)|, and at high entropy exactly one position is accepted
+    per step, so the canvas never keeps more than one accepted position before the last step."""
+    cfg = _cfg0(mode="reaccept")
+    W = synth.wvocab(0, cfg.vocab, cfg.hidden)
+    s = oracle.OracleSampler(cfg, W)
+    fn = oracle.sampler.synth_resid_fn(cfg, W, 0.5)
+    prev = np.zeros(cfg.canvas_len, bool)
+    while not s.done():
+        rec = s.tick(fn)
+        if rec.final[0]:
+            break
+        cur = s.committed[0].copy()
+        assert rec.n_accepted[0] == 1 and cur.sum() == 1
+        assert rec.n_remasked[0] == int(np.sum(prev & ~cur))
+        prev = cur

@@ -84,6 +84,7 @@ struct Dev {
   int32_t V, d, L, B, G, N;
   float t_min, t_max, bound, conf, eps;
   int32_t n_vtiles, tiles_per_chunk, n_chunks, n_sub, rows_cap, max_active;
+  bool reaccept;        // DG_REACCEPT: every step re-sorts all positions (see dg_mode)
 };
 
 // ------------------------------------------------------------ Philox4x32-10

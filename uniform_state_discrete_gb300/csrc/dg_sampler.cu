@@ -84,7 +84,8 @@ bool validate(const dg_config* c, char* why) {
 int make_layout(const dg_config* c, Layout* L, char* why) {
   if (!validate(c, why)) return 0;
   if (c->stability != 1) return set_err(why, "only stability = 1 is implemented (got %d)", c->stability), -1;
-  if (c->mode != DG_FREEZE) return set_err(why, "only mode DG_FREEZE is implemented (got %d)", c->mode), -1;
+  if (c->mode != DG_FREEZE && c->mode != DG_REACCEPT)
+    return set_err(why, "mode must be DG_FREEZE or DG_REACCEPT (got %d)", c->mode), 0;
   const size_t B = c->n_canvases, Lc = c->canvas_len, d = c->hidden, G = c->gen_blocks;
   L->max_active = c->max_active ? c->max_active : c->n_canvases;
   const size_t rows = (size_t)L->max_active * Lc;
@@ -306,6 +307,7 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.t_min = cfg->t_min;
   dv.t_max = cfg->t_max;
   dv.bound = cfg->entropy_bound;
+  dv.reaccept = cfg->mode == DG_REACCEPT;
   dv.conf = cfg->confidence;
   dv.eps = cfg->rms_eps;
   dv.n_vtiles = L.n_vtiles;

@@ -74,7 +74,7 @@ __global__ void k_static_prep(unsigned char* base, uint64_t seed, int block, int
   sl->converged_blocks = 0;
   sl->temperature = T;
   sl->mean_entropy = 0.f;
-  sl->reserved = 0;
+  sl->n_remasked = 0;
   pl->tick = 0;
   pl->n_active = 1;
   pl->commits = 0u;

@@ -33,6 +33,7 @@ struct TailScratch {
   float redf[kTailThreads / 32][2];
   int redi[kTailThreads / 32][2];
   int flags[4];
+  int remasked;        // DG_REACCEPT: positions accepted at the previous step and re-noised now
   int done_list[64];   // canvases completed by one CTA's rows (at most 8 / L + 2)
   int row_canvas[8];   // canvas of each of a finishing CTA's rows
 };
@@ -127,6 +128,7 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
           s.block = 0;
           s.step = 0;
           s.n_committed = 0;
+          s.n_remasked = 0;
           s.temperature = dv.temps[0];
         }
         ++running;
@@ -173,11 +175,13 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
 
 // The commit step of canvas c for this tick:
 //  (i)   early stop: s >= 1, mean_p H < confidence and argmax == previous argmax at every p;
-//  (ii)  otherwise order the uncommitted positions by (H, p) and accept the prefix whose
+//  (ii)  otherwise order the open positions by (H, p) and accept the prefix whose
 //        exclusive entropy sums stay <= entropy_bound; accepted positions take their sample;
-//  (iii) on early stop or at s = N-1 every uncommitted position takes its sample and the
+//  (iii) on early stop or at s = N-1 every open position takes its sample and the
 //        block ends (tokens copied out, next block or done);
-//  (iv)  every other uncommitted position is re-noised to a uniform token.
+//  (iv)  every other open position is re-noised to a uniform token.
+// The open positions are the uncommitted ones under DG_FREEZE and all of them
+// under DG_REACCEPT, where the committed mask becomes this step's accepted set.
 // Only entries whose entropy is <= bound, plus the smallest one above it, can be
 // accepted, so the common case sorts at most 32 candidates in one warp; more than
 // 31 entropies within the bound fall back to a bitonic sort of the canvas.
@@ -202,7 +206,7 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
   const float t_next = dv.temps[s + 1 < dv.N ? s + 1 : dv.N - 1], t_first = dv.temps[0];
   float Hv[kTailPer];
   int yv[kTailPer], av[kTailPer], pv[kTailPer], xv[kTailPer];
-  bool cm[kTailPer];
+  bool cm[kTailPer], was[kTailPer];
 #pragma unroll
   for (int i = 0; i < kTailPer; ++i) {
     const int p = g.tid + i * kTailThreads;
@@ -212,7 +216,8 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
       av[i] = __ldcg(dv.amax + base + p);
       pv[i] = __ldcg(dv.prev_amax + base + p);
       xv[i] = __ldcg(dv.x + base + p);
-      cm[i] = __ldcg(dv.committed + base + p) != 0;
+      was[i] = __ldcg(dv.committed + base + p) != 0;
+      cm[i] = was[i] && !dv.reaccept;  // frozen
     }
   }
   float hsum = 0.f, n_le = 0.f;
@@ -248,7 +253,10 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
     sc->redi[w][0] = stable;
     sc->redk[w] = kmin_above;
   }
-  if (g.tid == 0) sc->flags[1] = 0;
+  if (g.tid == 0) {
+    sc->flags[1] = 0;
+    sc->remasked = 0;
+  }
   g.sync();
   float tot_h = 0.f, tot_le = 0.f;
   for (int k = 0; k < kTailThreads / 32; ++k) {
@@ -309,6 +317,7 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
       for (int j = g.tid; j < n_acc; j += g.n) sc->acc[(unsigned)(sc->keys[j] & 0xFFFFFFFFu)] = 1;
       g.sync();
     }
+    int remasked = 0;
 #pragma unroll
     for (int i = 0; i < kTailPer; ++i) {
       const int p = g.tid + i * kTailThreads;
@@ -320,16 +329,23 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
             dv.commit_step[base + p] = (int16_t)s;
           } else {
             dv.x[base + p] = uniform_token(draw_u32(sl.seed, kPurposeRenoise, b, s, p), dv.V);
+            if (was[i]) {  // only under DG_REACCEPT: accepted before, re-noised now
+              dv.committed[base + p] = 0;
+              ++remasked;
+            }
           }
         }
         dv.prev_amax[base + p] = av[i];
       }
     }
+    if (dv.reaccept && remasked) atomicAdd(&sc->remasked, remasked);
+    g.sync();
     if (g.tid == 0) {
       dg_slot& so = dv.slots[c];
       so.step = s + 1;
       so.temperature = t_next;
-      so.n_committed = sl.n_committed + n_acc;
+      so.n_committed = dv.reaccept ? n_acc : sl.n_committed + n_acc;
+      so.n_remasked = sc->remasked;
       so.mean_entropy = mean_H;
     }
     g.sync();
@@ -358,6 +374,7 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
       so.steps_used = sl.steps_used + s + 1;
       so.converged_blocks = sl.converged_blocks + (converged ? 1 : 0);
       so.mean_entropy = mean_H;
+      so.n_remasked = 0;
       if (more) {
         so.block = b + 1;
         so.step = 0;
