@@ -185,7 +185,8 @@ def oracle_positions_per_s(wl: dict, budget_s: float, seed_base: int, W16=None, 
     W16 = synth.wvocab(0, wl["vocab"], wl["hidden"]) if W16 is None else W16
     cfg = oracle.OracleConfig(vocab=wl["vocab"], hidden=wl["hidden"], canvas_len=wl["canvas_len"],
                               n_canvases=wl["n_canvases"], num_inference_steps=wl["steps"], gen_blocks=1 << 10,
-                              seeds=[seed_base + c for c in range(wl["n_canvases"])], mode=wl.get("mode", "freeze"))
+                              seeds=[seed_base + c for c in range(wl["n_canvases"])], mode=wl.get("mode", "freeze"),
+                              softcap=float(wl.get("softcap", 0.0)))
     o = oracle.OracleSampler(cfg, W16)
     fn = oracle.sampler.synth_resid_fn(cfg, W16, SIGMA_HIDDEN)
     positions, busy, ticks = 0, 0.0, 0
@@ -217,7 +218,8 @@ def run_reference(args, wl, world, rank):
     sample = max(1, min(n_pos, int(budget / max(1, args.steps + args.warmup) / per_pos)))
     cfg = oracle.OracleConfig(vocab=wl["vocab"], hidden=wl["hidden"], canvas_len=wl["canvas_len"],
                               n_canvases=wl["n_canvases"], num_inference_steps=wl["steps"], gen_blocks=1 << 10,
-                              seeds=list(range(wl["n_canvases"])), mode=wl.get("mode", "freeze"))
+                              seeds=list(range(wl["n_canvases"])), mode=wl.get("mode", "freeze"),
+                              softcap=float(wl.get("softcap", 0.0)))
     o = oracle.OracleSampler(cfg, W16)
     fn = oracle.sampler.synth_resid_fn(cfg, W16, SIGMA_HIDDEN)
     rows = np.arange(sample)
@@ -228,7 +230,7 @@ def run_reference(args, wl, world, rank):
         s = int(o.step_no[act[0]])
         t0 = time.perf_counter()
         h = oracle.rmsnorm_bf16(r, cfg.rms_eps)
-        z = oracle.logits(h, W16)
+        z = oracle.softcap(oracle.logits(h, W16), cfg.softcap)
         T = oracle.temperature(s, cfg.num_inference_steps, cfg.t_min, cfg.t_max)
         st = oracle.stats(z, T, cfg.seed(int(act[0])), int(o.block[act[0]]), s, rows)
         oracle.sampler.entropy_bounded_accept(st["H"], range(sample), cfg.entropy_bound)
@@ -240,7 +242,8 @@ def run_reference(args, wl, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * busy / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "description": wl["text"], "commit_mode": wl["mode"]},
+            "config": {"workload": args.workload, "description": wl["text"], "commit_mode": wl["mode"],
+                       "softcap": wl["softcap"]},
             "cpu_baseline": {"kind": "oracle", "cores": oracle.threads(), "value": value, "unit": UNIT,
                              "sample": f"each step: {sample} of {n_pos} positions of one tick (RMSNorm, fp64 LM head, "
                                        f"softmax statistics, Gumbel sample, acceptance), oracle as it stands"},
@@ -269,7 +272,8 @@ def run_ours(args, wl, world, rank, local):
     blocks = total_ticks // N + 2
     seeds = [rank * B + c for c in range(B)]
     cfg = dg.make_config(V, d, L, n_canvases=B, gen_blocks=blocks, num_inference_steps=N, seeds=seeds,
-                         mode=dg.DG_REACCEPT if wl.get("mode") == "reaccept" else dg.DG_FREEZE)
+                         mode=dg.DG_REACCEPT if wl.get("mode") == "reaccept" else dg.DG_FREEZE,
+                         softcap=float(wl.get("softcap", 0.0)))
     s = dg.Sampler(cfg, w_dev, stream=stream)
     resid = torch.empty(B, L, d, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -416,6 +420,7 @@ def run_ours(args, wl, world, rank, local):
                 "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": args.workload, "description": wl["text"], "commit_mode": wl["mode"],
+                           "softcap": wl["softcap"],
                            "positions_per_step": positions_per_tick,
                            "l2": "flushed before every timed tick: 256 MB device write, then read back (outside the "
                                  "events)" if args.flush == "writeread" else "flushed by a 256 MB write",
@@ -462,6 +467,7 @@ def main():
     ap.add_argument("--graph", type=int, default=1, help="replay each tick as a captured CUDA graph")
     ap.add_argument("--mode", choices=["freeze", "reaccept"], default="freeze",
                     help="commit mode: committed positions freeze (default), or every step re-accepts all positions")
+    ap.add_argument("--softcap", type=float, default=0.0, help="final logit softcap c (0 = off, the workloads' setting)")
     ap.add_argument("--kernel-steps", type=int, default=200, help="ticks of the per-kernel timing pass")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -469,7 +475,7 @@ def main():
     world, rank, local = dist_setup()
     if world != args.gpus and world > 1:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
-    wl = dict(WORKLOADS[args.workload], mode=args.mode)
+    wl = dict(WORKLOADS[args.workload], mode=args.mode, softcap=args.softcap)
     if args.impl == "reference":
         run_reference(args, wl, world, rank)
     else:

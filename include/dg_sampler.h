@@ -99,6 +99,9 @@ typedef struct dg_config {
   int32_t max_active;          /* most canvases active in one tick, 1..B (0 = B); sizes buffers  */
   const uint64_t* seeds;       /* host [B]: per-canvas Philox key; NULL = seed c for canvas c    */
   const int32_t* admit_tick;   /* host [B]: tick at which canvas c joins, >= 0; NULL = all at 0  */
+  float softcap;               /* final logit softcap c >= 0: logits become c tanh(z / c) before
+                                  the temperature (The Annotated DiffusionGemma, "Logit
+                                  Softcapping"); 0 = off                                        */
 } dg_config;
 
 /* Per-canvas state, the layout of the device array returned by dg_slots().

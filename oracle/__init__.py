@@ -148,6 +148,14 @@ def logits_loop(h: np.ndarray, W: np.ndarray) -> np.ndarray:
     return z
 
 
+def softcap(z: np.ndarray, c: float) -> np.ndarray:
+    """Final logit softcap z -> c tanh(z / c) in fp64 ("The Annotated DiffusionGemma", "Logit
+    Softcapping": part of the model, applied to the final logits before the temperature).  c = 0
+    leaves the logits unchanged."""
+    z = np.asarray(z, dtype=np.float64)
+    return z if c == 0 else c * np.tanh(z / c)
+
+
 def stats(z: np.ndarray, T, seed, block, step, pos) -> np.ndarray:
     """Per-row temperature softmax statistics and Gumbel-max sample; returns POS_DTYPE [n]."""
     z = np.ascontiguousarray(z, dtype=np.float64)

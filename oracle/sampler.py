@@ -7,8 +7,9 @@ Sampling" states is the same procedure as its lazy order.  One tick runs, for
 every active canvas, at its own step s of its own block b:
 
   1. temperature T_s = t_max + (s/N)(t_min - t_max)        ("Apply temperature")
-  2. h = RMSNorm(r), z = h W^T, softmax(z/T): H, log Z, argmax, sample y
-                                            ("RMSNorm", "Compute entropy")
+  2. h = RMSNorm(r), z = h W^T (with the final softcap c tanh(z/c) when c > 0),
+     softmax(z/T): H, log Z, argmax, sample y
+                       ("RMSNorm", "Logit Softcapping", "Compute entropy")
   3. early stop when s >= 1, mean_p H < confidence and the argmax canvas
      equals the previous step's                   ("Check for early stopping")
   4. otherwise sort the open positions by (H, p) ascending and accept
@@ -88,6 +89,7 @@ class OracleConfig:
     admit_tick: Optional[list] = None
     max_active: Optional[int] = None  # most canvases running in one tick (None: all)
     mode: str = "freeze"  # "freeze" or "reaccept" (see the module docstring)
+    softcap: float = 0.0  # final logit softcap c (0 = off): z -> c tanh(z / c) before the temperature
     # parity margins stated by the task for flagging near-ties
     margin_H: float = 1e-3
     margin_gap: float = 1e-4
@@ -183,7 +185,7 @@ class OracleSampler:
 
     # ----------------------------------------------------------------- tick
     def tick(self, resid_fn: Callable) -> Optional[TickRecord]:
-        from . import PURPOSE_RENOISE, draw_u32, logits, rmsnorm_bf16, stats, uniform_token
+        from . import PURPOSE_RENOISE, draw_u32, logits, rmsnorm_bf16, softcap, stats, uniform_token
         cfg = self.cfg
         L, V, N = cfg.canvas_len, cfg.vocab, cfg.num_inference_steps
         act = self.active()
@@ -193,7 +195,7 @@ class OracleSampler:
             r = resid_fn(act, blocks, steps, self.x[act].copy())
             assert r.shape == (act.size * L, cfg.hidden)
             h = rmsnorm_bf16(r, cfg.rms_eps, self.norm_w)
-            z = logits(h, self.W)
+            z = softcap(logits(h, self.W), cfg.softcap)
             T = np.array([temperature(int(s), N, cfg.t_min, cfg.t_max) for s in steps])
             rows = lambda a: np.repeat(a, L)
             st = stats(z, rows(T), rows(np.array([cfg.seed(int(c)) for c in act], dtype=np.uint64)), rows(blocks),

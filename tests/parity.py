@@ -57,6 +57,7 @@ class Case:
     norm_seed: int = None  # RMSNorm weight from synth.norm_weight, or all ones
     rms_eps: float = 1e-6
     mode: str = "freeze"  # commit mode: "freeze" (DG_FREEZE) or "reaccept" (DG_REACCEPT)
+    softcap: float = 0.0  # final logit softcap c (0 = off)
 
     def oracle_cfg(self) -> OracleConfig:
         return OracleConfig(vocab=self.vocab, hidden=self.hidden, canvas_len=self.canvas_len,
@@ -65,7 +66,7 @@ class Case:
                             confidence=f32(self.conf), rms_eps=f32(self.rms_eps),
                             seeds=list(self.seeds) if self.seeds else list(range(self.n_canvases)),
                             admit_tick=list(self.admit) if self.admit else None,
-                            max_active=self.max_active or None, mode=self.mode)
+                            max_active=self.max_active or None, mode=self.mode, softcap=f32(self.softcap))
 
     def gpu_cfg(self):
         import uniform_state_discrete_gb300 as dg
@@ -73,7 +74,7 @@ class Case:
                               gen_blocks=self.gen_blocks, num_inference_steps=self.steps, t_min=self.t_min,
                               t_max=self.t_max, entropy_bound=self.bound, confidence=self.conf, rms_eps=self.rms_eps,
                               max_active=self.max_active,
-                              mode=dg.DG_REACCEPT if self.mode == "reaccept" else dg.DG_FREEZE,
+                              mode=dg.DG_REACCEPT if self.mode == "reaccept" else dg.DG_FREEZE, softcap=self.softcap,
                               seeds=list(self.seeds) if self.seeds else list(range(self.n_canvases)),
                               admit_tick=list(self.admit) if self.admit else None)
 

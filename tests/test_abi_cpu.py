@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_struct_layouts_match_header_sizes():
     import uniform_state_discrete_gb300 as dg
-    assert ctypes.sizeof(dg.dg_config) == 72
+    assert ctypes.sizeof(dg.dg_config) == 80
     assert ctypes.sizeof(dg.dg_slot) == 48
     assert ctypes.sizeof(dg.dg_state) == 56
 
@@ -42,7 +42,8 @@ def test_struct_layouts_match_header_sizes():
                                          ("canvas_len", 1025), ("num_inference_steps", 0),
                                          ("num_inference_steps", 1025), ("t_min", 0.0), ("t_max", -1.0),
                                          ("entropy_bound", -0.1), ("confidence", -1.0), ("n_canvases", 0),
-                                         ("gen_blocks", 0), ("rms_eps", -1.0), ("max_active", 5)])
+                                         ("gen_blocks", 0), ("rms_eps", -1.0), ("max_active", 5),
+                                         ("softcap", -1.0), ("softcap", float("inf"))])
 def test_invalid_configs_rejected_on_host(field, value):
     import uniform_state_discrete_gb300 as dg
     kw = dict(vocab=2048, hidden=128, canvas_len=16, n_canvases=2)

@@ -124,6 +124,19 @@ def test_reaccept_many_accepted_and_remasked():
         _assert_report(teacher_forced(case), f"reaccept L={L}")
 
 
+@pytest.mark.parametrize("case", [
+    pytest.param(Case(vocab=2048, hidden=128, canvas_len=16, steps=8, softcap=30.0), id="tiny-c30"),
+    pytest.param(Case(vocab=2048, hidden=128, canvas_len=32, steps=6, softcap=2.0, sigma_w=0.2, w_seed=4,
+                      t_max=1.5, t_min=0.1), id="tanh-saturating-c2"),
+    pytest.param(Case(vocab=4096, hidden=256, canvas_len=256, steps=4, softcap=3.0, sigma_w=0.1, w_seed=5,
+                      seeds=(7,)), id="pair-c3"),
+])
+def test_final_logit_softcap(case):
+    """Final logit softcap c tanh(z/c) before the temperature, from a barely active cap (c = 30 on
+    logits of order 0.2) to a saturating one (|z/c| around 1 and above), on both LM-head kernels."""
+    _assert_report(teacher_forced(case), f"softcap c={case.softcap}")
+
+
 def _gpu_free_run(case, W):
     import torch
     import uniform_state_discrete_gb300 as dg

@@ -499,3 +499,32 @@ def test_reaccept_remask_count_matches_mask_difference():
         assert rec.n_accepted[0] == 1 and cur.sum() == 1
         assert rec.n_remasked[0] == int(np.sum(prev & ~cur))
         prev = cur
+
+
+# ------------------------------------------------------------------ logit softcap
+def test_softcap_limits_and_shape():
+    """"Logit Softcapping": c tanh(z/c) leaves |z| << c essentially unchanged (z - z^3/(3c^2) to
+    third order), tends to +-c as z -> +-inf, is odd, monotone and bounded by c, and c -> inf
+    (here c = 0 meaning off, and a huge c) gives back the logits."""
+    z = np.linspace(-5.0, 5.0, 1001)
+    c = 30.0
+    zc = oracle.softcap(z, c)
+    small = np.abs(z) < 0.5
+    assert np.max(np.abs(zc[small] - (z[small] - z[small] ** 3 / (3 * c * c)))) < 1e-7
+    assert np.allclose(oracle.softcap(np.array([1e6, -1e6, 1e3]), c), [c, -c, c], rtol=0, atol=1e-12)
+    assert np.array_equal(oracle.softcap(-z, c), -zc)
+    assert np.all(np.diff(zc) > 0) and np.all(np.abs(zc) < c)
+    assert np.array_equal(oracle.softcap(z, 0.0), z)
+    assert np.max(np.abs(oracle.softcap(z, 1e9) - z)) < 1e-15 * 1e3
+
+
+def test_softcap_bounds_the_entropy_of_a_two_point_distribution():
+    """Two tokens with logits +-a: after the cap their gap is 2c tanh(a/c), so H is the binary
+    entropy of sigmoid(-gap/T), however large a grows (the stats routine on capped logits)."""
+    c, T = 2.0, 0.5
+    for a in (0.3, 3.0, 300.0):
+        z = oracle.softcap(np.array([[a, -a]]), c)
+        st = oracle.stats(z, T, 1, 0, 0, np.array([0]))
+        gap = 2 * c * math.tanh(a / c) / T
+        p = 1.0 / (1.0 + math.exp(gap))
+        assert abs(st["H"][0] - (-(p * math.log(p) + (1 - p) * math.log(1 - p)))) < 1e-12

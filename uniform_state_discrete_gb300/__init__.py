@@ -34,7 +34,8 @@ class dg_config(ctypes.Structure):
                 ("num_inference_steps", ctypes.c_int32), ("t_min", ctypes.c_float), ("t_max", ctypes.c_float),
                 ("entropy_bound", ctypes.c_float), ("confidence", ctypes.c_float), ("stability", ctypes.c_int32),
                 ("rms_eps", ctypes.c_float), ("mode", ctypes.c_int32), ("max_active", ctypes.c_int32),
-                ("seeds", ctypes.POINTER(ctypes.c_uint64)), ("admit_tick", ctypes.POINTER(ctypes.c_int32))]
+                ("seeds", ctypes.POINTER(ctypes.c_uint64)), ("admit_tick", ctypes.POINTER(ctypes.c_int32)),
+                ("softcap", ctypes.c_float)]
 
 
 class dg_slot(ctypes.Structure):
@@ -122,10 +123,11 @@ def _check(st: int, handle=None):
 
 def make_config(vocab, hidden, canvas_len, n_canvases=1, gen_blocks=1, num_inference_steps=48, t_min=0.4,
                 t_max=0.8, entropy_bound=0.1, confidence=0.005, stability=1, rms_eps=1e-6, mode=DG_FREEZE,
-                max_active=0, seeds=None, admit_tick=None):
+                max_active=0, seeds=None, admit_tick=None, softcap=0.0):
     """Build a ``dg_config``; the returned object keeps the seed/admit arrays alive."""
     cfg = dg_config(vocab, hidden, canvas_len, n_canvases, gen_blocks, num_inference_steps, t_min, t_max,
                     entropy_bound, confidence, stability, rms_eps, mode, max_active)
+    cfg.softcap = softcap
     keep = []
     if seeds is not None:
         a = (ctypes.c_uint64 * n_canvases)(*[int(s) for s in seeds])

@@ -85,6 +85,8 @@ struct Dev {
   float t_min, t_max, bound, conf, eps;
   int32_t n_vtiles, tiles_per_chunk, n_chunks, n_sub, rows_cap, max_active;
   bool reaccept;        // DG_REACCEPT: every step re-sorts all positions (see dg_mode)
+  float softcap;        // final logit softcap c (0 = off): z -> c tanh(z / c) before the temperature
+  float inv_softcap;    // 1 / c (0 when off)
 };
 
 // ------------------------------------------------------------ Philox4x32-10

@@ -284,6 +284,12 @@ __device__ __forceinline__ float key_ord(int k) { return __int_as_float(k >= 0 ?
 // Fold 16 columns [v0, v0+16) of one row (raw fp32 logits z) into its running
 // statistics.  kTail: some of the columns lie at or beyond V.
 //
+// With a final logit softcap c > 0 each logit first becomes c tanh(z / c)
+// ("The Annotated DiffusionGemma", "Logit Softcapping": part of the model,
+// applied before the temperature); tanhf is CUDA's, within 2 ulp.  kCap
+// selects the kernels compiled with the cap, so the uncapped ones carry none
+// of its code.
+//
 // Softmax statistics in base 2 with u = z log2(e)/T: running max m, S = sum
 // 2^(u-m), A = sum 2^(u-m)(u-m), formed from d = u - m = fma(z, log2(e)/T, -m).
 // The argmax index is looked up only when the fold raises the running max.
@@ -298,8 +304,13 @@ __device__ __forceinline__ float key_ord(int k) { return __int_as_float(k >= 0 ?
 // the result equals the unscreened maximum.  Candidates are scored one per lane
 // per round, all lanes of the warp together.  Equal scores keep the lower
 // index.
-template <bool kTail>
-__device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, int* best) {
+template <bool kTail, bool kCap>
+__device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, int* best,
+                                       float cap, float inv_cap) {
+  if (kCap) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) z[j] = cap * tanhf(z[j] * inv_cap);
+  }
   if (kTail) {
     if (v0 >= V) return;
 #pragma unroll
@@ -375,11 +386,13 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
 }
 
 // The fold of this warp's 16 columns of one accumulator tile.
-__device__ __forceinline__ void fold_cols(float (&acc)[16], int v0, int V, const RowMeta& rm, Partial& st, int* best) {
+template <bool kCap>
+__device__ __forceinline__ void fold_cols(float (&acc)[16], int v0, int V, const RowMeta& rm, Partial& st, int* best,
+                                          float cap, float inv_cap) {
   if (v0 + 16 <= V)
-    fold16<false>(acc, v0, V, rm, st, best);
+    fold16<false, kCap>(acc, v0, V, rm, st, best, cap, inv_cap);
   else
-    fold16<true>(acc, v0, V, rm, st, best);
+    fold16<true, kCap>(acc, v0, V, rm, st, best, cap, inv_cap);
 }
 
 // ---------------------------------------------------------------- CTA pairs
@@ -444,6 +457,7 @@ __device__ __forceinline__ bool rows_written(const Dev& dv, int n_rows, volatile
   return true;
 }
 
+template <bool kCap>
 __global__ void __launch_bounds__(kThreadsLM, 1)
     k_lmhead(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv) {
   extern __shared__ uint8_t smem_raw[];
@@ -632,7 +646,9 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
           }
-          if (rm.valid) fold_cols(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, gbest + rl);
+          if (rm.valid)
+            fold_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, gbest + rl, dv.softcap,
+                            dv.inv_softcap);
         }
       }
       // merge the four column groups of each row; one record per row and chunk.  Every
@@ -678,6 +694,7 @@ constexpr int kStagesPair = 6;
 constexpr int kStagePairA = kBM * kBK * 2;        // this CTA's 128 rows of h
 constexpr int kStagePairB = (kBN / 2) * kBK * 2;  // this CTA's 128 rows of the W tile
 
+template <bool kCap>
 __global__ void __launch_bounds__(kThreadsLM, 1)
     k_lmhead_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv,
                   const float* __restrict__ resid) {
@@ -954,7 +971,9 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader[ab]);
           }
-          if (rm.valid) fold_cols(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, gbest + rl);
+          if (rm.valid)
+            fold_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, gbest + rl, dv.softcap,
+                            dv.inv_softcap);
         }
       }
       mrg[cg * kBM + rl] = st;
@@ -995,9 +1014,13 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 }  // namespace
 
 cudaError_t lmhead_configure() {
-  cudaError_t e = cudaFuncSetAttribute(k_lmhead, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(k_lmhead<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_lmhead_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesPair);
+    e = cudaFuncSetAttribute(k_lmhead<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_lmhead_pair<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesPair);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_lmhead_pair<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesPair);
   return e;
 }
 
@@ -1022,7 +1045,8 @@ cudaError_t launch_lmhead_pair(const Dev& dv, const float* resid, const CUtensor
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_lmhead_pair, *tmA, *tmB, dv, resid);
+  return dv.softcap > 0.f ? cudaLaunchKernelEx(&cfg, k_lmhead_pair<true>, *tmA, *tmB, dv, resid)
+                          : cudaLaunchKernelEx(&cfg, k_lmhead_pair<false>, *tmA, *tmB, dv, resid);
 }
 
 cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorMap* tmB, int num_sms,
@@ -1043,7 +1067,8 @@ cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorM
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_lmhead, *tmA, *tmB, dv);
+  return dv.softcap > 0.f ? cudaLaunchKernelEx(&cfg, k_lmhead<true>, *tmA, *tmB, dv)
+                          : cudaLaunchKernelEx(&cfg, k_lmhead<false>, *tmA, *tmB, dv);
 }
 
 }  // namespace dg

@@ -70,6 +70,7 @@ bool validate(const dg_config* c, char* why) {
   if (!(c->confidence >= 0.f) || !std::isfinite(c->confidence))
     return set_err(why, "confidence must be finite and >= 0"), false;
   if (!(c->rms_eps >= 0.f) || !std::isfinite(c->rms_eps)) return set_err(why, "rms_eps must be finite and >= 0"), false;
+  if (!(c->softcap >= 0.f) || !std::isfinite(c->softcap)) return set_err(why, "softcap must be finite and >= 0"), false;
   if (c->max_active < 0 || c->max_active > c->n_canvases)
     return set_err(why, "max_active must be in [0, n_canvases]"), false;
   if ((int64_t)c->n_canvases * c->canvas_len > (int64_t)1 << 24)
@@ -310,6 +311,8 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.reaccept = cfg->mode == DG_REACCEPT;
   dv.conf = cfg->confidence;
   dv.eps = cfg->rms_eps;
+  dv.softcap = cfg->softcap;
+  dv.inv_softcap = cfg->softcap > 0.f ? 1.f / cfg->softcap : 0.f;
   dv.n_vtiles = L.n_vtiles;
   dv.tiles_per_chunk = L.tiles_per_chunk;
   dv.n_chunks = L.n_chunks;
