@@ -171,6 +171,16 @@ def reduce_max(value: float, world: int) -> float:
     return float(t.item())
 
 
+def replica_seeds(rank: int, n_canvases: int) -> list:
+    """Canvas seeds of one replica: ranks take disjoint seed ranges, so N GPUs denoise N*B distinct canvases."""
+    return [rank * n_canvases + c for c in range(n_canvases)]
+
+
+def whole_job_rate(units_per_rank_step: int, steps: int, world: int, max_s: float) -> float:
+    """Units all ranks processed, divided by the slowest rank's time (weak scaling: fixed work per rank)."""
+    return units_per_rank_step * steps * world / max_s
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -270,7 +280,7 @@ def run_ours(args, wl, world, rank, local):
     torch.cuda.synchronize(dev)
     total_ticks = args.warmup + args.steps + args.kernel_steps + args.e2e_steps + 2
     blocks = total_ticks // N + 2
-    seeds = [rank * B + c for c in range(B)]
+    seeds = replica_seeds(rank, B)
     cfg = dg.make_config(V, d, L, n_canvases=B, gen_blocks=blocks, num_inference_steps=N, seeds=seeds,
                          mode=dg.DG_REACCEPT if wl.get("mode") == "reaccept" else dg.DG_FREEZE,
                          softcap=float(wl.get("softcap", 0.0)))
@@ -361,7 +371,7 @@ def run_ours(args, wl, world, rank, local):
     device_s = float(tick_ms.sum()) / 1e3
     positions_per_tick = B * L
     max_s = reduce_max(device_s, world)
-    value = positions_per_tick * args.steps * world / max_s
+    value = whole_job_rate(positions_per_tick, args.steps, world, max_s)
 
     # roofline of the LM-head kernel (K2).  On SM pairs (256 positions or more, the
     # sampler's choice) it also forms the RMSNorm rows, and no RMSNorm kernel runs:
@@ -410,7 +420,7 @@ def run_ours(args, wl, world, rank, local):
         canvas_h, ent_h = s.step_host(hr)
         e2e_s += time.perf_counter() - t0
     e2e_max = reduce_max(e2e_s, world)
-    e2e = {"value": positions_per_tick * e2e_steps * world / e2e_max, "unit": UNIT,
+    e2e = {"value": whole_job_rate(positions_per_tick, e2e_steps, world, e2e_max), "unit": UNIT,
            "h2d_bytes_per_step": B * L * d * 4, "d2h_bytes_per_step": 2 * B * L * 4, "steps": e2e_steps,
            "api": "dg_denoise_step_host"}
 
