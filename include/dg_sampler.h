@@ -187,6 +187,9 @@ const float* dg_logz(const dg_sampler* s);          /* log Z of softmax(z/T) fro
 const int32_t* dg_sample(const dg_sampler* s);      /* sampled token from the last tick               */
 const int32_t* dg_argmax(const dg_sampler* s);      /* argmax token from the last tick                */
 const int32_t* dg_tokens_out(const dg_sampler* s);  /* [B, gen_blocks, L] tokens of finished blocks   */
+/* [B, gen_blocks, L] commit heatmap of finished blocks: the step at which each
+ * position took its final token (under DG_REACCEPT, the block's last step). */
+const int16_t* dg_commit_steps_out(const dg_sampler* s);
 const dg_slot* dg_slots(const dg_sampler* s);       /* [B] per-canvas state                           */
 /* bf16 [rows, d] normalised hidden rows of the last tick (the LM head's input), one row per
  * position of the active canvases in canvas order (active canvas a, position p -> row a*L + p). */
@@ -206,7 +209,7 @@ dg_status dg_set_timing_events(dg_sampler* s, void* const* events);
 dg_status dg_sync_info(dg_sampler* s, dg_slot* slots_host);
 
 /* Whole sampler state in host arrays ([B] and [B, L] row-major, [B, G, L] for
- * tokens_out), for checkpoint and resume.  prev_argmax is the argmax canvas of
+ * tokens_out and commit_steps_out), for checkpoint and resume.  prev_argmax is the argmax canvas of
  * each canvas's previous step (the early-stop test compares against it). */
 typedef struct dg_state {
   int32_t tick;
@@ -216,6 +219,7 @@ typedef struct dg_state {
   int16_t* commit_step; /* [B, L]     */
   int32_t* prev_argmax; /* [B, L]     */
   int32_t* tokens_out;  /* [B, G, L]  */
+  int16_t* commit_steps_out; /* [B, G, L]; NULL: not copied */
 } dg_state;
 
 /* Copy out the state (synchronizing). */

@@ -144,6 +144,8 @@ class OracleSampler:
         self.steps_used = np.zeros(B, dtype=np.int32)
         self.converged_blocks = np.zeros(B, dtype=np.int32)
         self.tokens_out = np.full((B, cfg.gen_blocks, L), -1, dtype=np.int32)
+        # commit heatmap of each finished block: the step at which each position took its final token
+        self.commit_steps_out = np.full((B, cfg.gen_blocks, L), -1, dtype=np.int16)
         self._admit(0)
 
     # ---------------------------------------------------------------- state
@@ -180,7 +182,8 @@ class OracleSampler:
     def snapshot(self) -> dict:
         """Copy of the whole state (used to teacher-force the CUDA path from the oracle)."""
         return {k: getattr(self, k).copy() for k in ("status", "block", "step_no", "x", "committed", "commit_step",
-                                                     "prev_amax", "steps_used", "converged_blocks", "tokens_out")} | {
+                                                     "prev_amax", "steps_used", "converged_blocks", "tokens_out",
+                                                     "commit_steps_out")} | {
             "tick": self.tick_no}
 
     # ----------------------------------------------------------------- tick
@@ -270,6 +273,7 @@ class OracleSampler:
             rec.accepted[i, unc] = True
             rec.n_accepted[i] = unc.size
             self.tokens_out[c, b] = self.x[c]
+            self.commit_steps_out[c, b] = self.commit_step[c]
             self.steps_used[c] += s + 1
             self.converged_blocks[c] += int(converged)
             if b + 1 < cfg.gen_blocks:

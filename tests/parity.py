@@ -108,7 +108,8 @@ def oracle_state_to_gpu(o: OracleSampler, case: Case) -> dict:
     slots["converged_blocks"] = o.converged_blocks
     return {"tick": o.tick_no, "slots": slots, "tokens": o.x.astype(np.int32),
             "committed": o.committed.astype(np.uint8), "commit_step": o.commit_step.astype(np.int16),
-            "prev_argmax": o.prev_amax.astype(np.int32), "tokens_out": o.tokens_out.astype(np.int32)}
+            "prev_argmax": o.prev_amax.astype(np.int32), "tokens_out": o.tokens_out.astype(np.int32),
+            "commit_steps_out": o.commit_steps_out.astype(np.int16)}
 
 
 @dataclasses.dataclass
@@ -218,3 +219,5 @@ def compare_tick(s, o: OracleSampler, rec, case: Case, rep: Report):
                 b = rec.block[i]
                 if not np.array_equal(gst["tokens_out"][c, b], o.tokens_out[c, b]):
                     rep.errors.append(f"tick {rec.tick} canvas {c}: finished block tokens differ")
+                if not np.array_equal(gst["commit_steps_out"][c, b], o.commit_steps_out[c, b]):
+                    rep.errors.append(f"tick {rec.tick} canvas {c}: finished block commit heatmap differs")

@@ -35,7 +35,7 @@ def test_struct_layouts_match_header_sizes():
     import uniform_state_discrete_gb300 as dg
     assert ctypes.sizeof(dg.dg_config) == 80
     assert ctypes.sizeof(dg.dg_slot) == 48
-    assert ctypes.sizeof(dg.dg_state) == 56
+    assert ctypes.sizeof(dg.dg_state) == 64
 
 
 @pytest.mark.parametrize("field,value", [("vocab", 1), ("hidden", 100), ("hidden", 0), ("canvas_len", 0),

@@ -160,8 +160,9 @@ def test_free_run_tiny_matches_oracle():
     W = weights(case)
     o = oracle.OracleSampler(case.oracle_cfg(), W)
     o.run(oracle.sampler.synth_resid_fn(case.oracle_cfg(), W, case.sigma))
-    _, tok, info = _gpu_free_run(case, W)
+    s, tok, info = _gpu_free_run(case, W)
     assert np.array_equal(tok, o.tokens_out)
+    assert np.array_equal(s.commit_steps_out().cpu().numpy(), o.commit_steps_out)
     assert np.array_equal(info["steps_used"], o.steps_used)
 
 
@@ -173,8 +174,9 @@ def test_idle_ticks_before_admission_pair_kernel():
     W = weights(case)
     o = oracle.OracleSampler(case.oracle_cfg(), W)
     o.run(oracle.sampler.synth_resid_fn(case.oracle_cfg(), W, case.sigma))
-    _, tok, info = _gpu_free_run(case, W)
+    s, tok, info = _gpu_free_run(case, W)
     assert np.array_equal(tok, o.tokens_out)
+    assert np.array_equal(s.commit_steps_out().cpu().numpy(), o.commit_steps_out)
     assert np.array_equal(info["steps_used"], o.steps_used)
 
 

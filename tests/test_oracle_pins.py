@@ -528,3 +528,20 @@ def test_softcap_bounds_the_entropy_of_a_two_point_distribution():
         gap = 2 * c * math.tanh(a / c) / T
         p = 1.0 / (1.0 + math.exp(gap))
         assert abs(st["H"][0] - (-(p * math.log(p) + (1 - p) * math.log(1 - p)))) < 1e-12
+
+
+def test_commit_heatmap_of_finished_blocks():
+    """The heatmap of a finished block records when each position took its final token.  At high
+    entropy (one commit per step, freezing mode) steps 0..N-2 appear exactly once and the last step
+    holds every remaining position; under re-acceptance the whole block takes the last step."""
+    for mode in ("freeze", "reaccept"):
+        cfg = _cfg0(gen_blocks=2, mode=mode)
+        W = synth.wvocab(0, cfg.vocab, cfg.hidden)
+        s = _run(cfg, W, 0.5)
+        N, L = cfg.num_inference_steps, cfg.canvas_len
+        for b in range(2):
+            hm = s.commit_steps_out[0, b].astype(np.int64)
+            if mode == "freeze":
+                assert np.array_equal(np.bincount(hm, minlength=N), [1] * (N - 1) + [L - N + 1])
+            else:
+                assert np.all(hm == N - 1)

@@ -54,7 +54,7 @@ assert SLOT_DTYPE.itemsize == ctypes.sizeof(dg_slot) == 48
 class dg_state(ctypes.Structure):
     _fields_ = [("tick", ctypes.c_int32), ("slots", ctypes.c_void_p), ("tokens", ctypes.c_void_p),
                 ("committed", ctypes.c_void_p), ("commit_step", ctypes.c_void_p),
-                ("prev_argmax", ctypes.c_void_p), ("tokens_out", ctypes.c_void_p)]
+                ("prev_argmax", ctypes.c_void_p), ("tokens_out", ctypes.c_void_p), ("commit_steps_out", ctypes.c_void_p)]
 
 
 DG_RESID_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
@@ -79,6 +79,7 @@ _SIGS = {
     "dg_sample": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_argmax": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_tokens_out": (ctypes.c_void_p, [ctypes.c_void_p]),
+    "dg_commit_steps_out": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_slots": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_normed": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_sync_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
@@ -245,19 +246,20 @@ class Sampler:
         B, L, G = self.B, self.L, self.G
         st = {"slots": np.empty(B, SLOT_DTYPE), "tokens": np.empty((B, L), np.int32),
               "committed": np.empty((B, L), np.uint8), "commit_step": np.empty((B, L), np.int16),
-              "prev_argmax": np.empty((B, L), np.int32), "tokens_out": np.empty((B, G, L), np.int32)}
+              "prev_argmax": np.empty((B, L), np.int32), "tokens_out": np.empty((B, G, L), np.int32),
+              "commit_steps_out": np.empty((B, G, L), np.int16)}
         s = dg_state(0, *[ctypes.c_void_p(st[k].ctypes.data) for k in ("slots", "tokens", "committed", "commit_step",
-                                                                       "prev_argmax", "tokens_out")])
+                                                                       "prev_argmax", "tokens_out",
+                                                                       "commit_steps_out")])
         _check(lib.dg_get_state(self.handle, ctypes.byref(s)), self.handle)
         st["tick"] = s.tick
         return st
 
     def set_state(self, st: dict):
-        arrs = {k: np.ascontiguousarray(st[k], dtype=dt) for k, dt in
-                (("slots", SLOT_DTYPE), ("tokens", np.int32), ("committed", np.uint8), ("commit_step", np.int16),
-                 ("prev_argmax", np.int32), ("tokens_out", np.int32))}
-        s = dg_state(int(st["tick"]), *[ctypes.c_void_p(arrs[k].ctypes.data) for k in
-                                        ("slots", "tokens", "committed", "commit_step", "prev_argmax", "tokens_out")])
+        names = ("slots", "tokens", "committed", "commit_step", "prev_argmax", "tokens_out", "commit_steps_out")
+        dts = (SLOT_DTYPE, np.int32, np.uint8, np.int16, np.int32, np.int32, np.int16)
+        arrs = {k: np.ascontiguousarray(st[k], dtype=dt) for k, dt in zip(names, dts) if st.get(k) is not None}
+        s = dg_state(int(st["tick"]), *[ctypes.c_void_p(arrs[k].ctypes.data) if k in arrs else None for k in names])
         _check(lib.dg_set_state(self.handle, ctypes.byref(s)), self.handle)
 
     # --------------------------------------------------------------- views
@@ -299,6 +301,11 @@ class Sampler:
     def tokens_out(self):
         import torch
         return self._view("dg_tokens_out", torch.int32, (self.B, self.G, self.L))
+
+    def commit_steps_out(self):
+        """[B, G, L] int16: the step at which each position of each finished block took its final token."""
+        import torch
+        return self._view("dg_commit_steps_out", torch.int16, (self.B, self.G, self.L))
 
     def normed(self, n_rows: int):
         """bf16 bit patterns (int16) of the first n_rows normalised hidden rows of the last tick."""

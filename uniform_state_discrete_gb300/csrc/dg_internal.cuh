@@ -68,6 +68,7 @@ struct Dev {
   int16_t* commit_step; // [B, L]
   int32_t* prev_amax;   // [B, L]
   int32_t* tokens_out;  // [B, G, L]
+  int16_t* commit_steps_out; // [B, G, L] commit step of each position of each finished block
   float* H;             // [B, L]
   float* logZ;          // [B, L]
   int32_t* y;           // [B, L]

@@ -44,7 +44,8 @@ void set_err(char* buf, const char* fmt, ...) {
 }
 
 struct Layout {
-  size_t slots, plan, active, x, committed, commit_step, prev_amax, tokens_out, H, logZ, y, amax, h, part, resid,
+  size_t slots, plan, active, x, committed, commit_step, prev_amax, tokens_out, commit_steps_out, H, logZ, y, amax, h,
+      part, resid,
       canvas_rows, temps, sync;
   size_t total;
   int rows_cap, n_vtiles, tiles_per_chunk, n_chunks, n_sub, max_active;
@@ -110,6 +111,7 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
   L->commit_step = take(2 * B * Lc);
   L->prev_amax = take(4 * B * Lc);
   L->tokens_out = take(4 * B * G * Lc);
+  L->commit_steps_out = take(2 * B * G * Lc);
   L->H = take(4 * B * Lc);
   L->logZ = take(4 * B * Lc);
   L->y = take(4 * B * Lc);
@@ -286,6 +288,7 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.commit_step = reinterpret_cast<int16_t*>(w + L.commit_step);
   dv.prev_amax = reinterpret_cast<int32_t*>(w + L.prev_amax);
   dv.tokens_out = reinterpret_cast<int32_t*>(w + L.tokens_out);
+  dv.commit_steps_out = reinterpret_cast<int16_t*>(w + L.commit_steps_out);
   dv.H = reinterpret_cast<float*>(w + L.H);
   dv.logZ = reinterpret_cast<float*>(w + L.logZ);
   dv.y = reinterpret_cast<int32_t*>(w + L.y);
@@ -445,6 +448,7 @@ dg_status dg_get_state(dg_sampler* s, dg_state* h) {
   } cp[] = {{h->slots, s->dv.slots, sizeof(dg_slot) * B},    {h->tokens, s->dv.x, 4 * BL},
             {h->committed, s->dv.committed, BL},             {h->commit_step, s->dv.commit_step, 2 * BL},
             {h->prev_argmax, s->dv.prev_amax, 4 * BL},       {h->tokens_out, s->dv.tokens_out, 4 * BL * s->dv.G},
+            {h->commit_steps_out, s->dv.commit_steps_out, 2 * BL * s->dv.G},
             {&pl, s->dv.plan, sizeof pl}};
   for (auto& c : cp)
     if (c.dst) DG_CUDA(s->err, cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, s->stream), "copy state");
@@ -477,7 +481,8 @@ dg_status dg_set_state(dg_sampler* s, const dg_state* h) {
     size_t n;
   } cp[] = {{s->dv.slots, sl.data(), sizeof(dg_slot) * B},  {s->dv.x, h->tokens, 4 * BL},
             {s->dv.committed, h->committed, BL},            {s->dv.commit_step, h->commit_step, 2 * BL},
-            {s->dv.prev_amax, h->prev_argmax, 4 * BL},      {s->dv.tokens_out, h->tokens_out, 4 * BL * s->dv.G}};
+            {s->dv.prev_amax, h->prev_argmax, 4 * BL},      {s->dv.tokens_out, h->tokens_out, 4 * BL * s->dv.G},
+            {s->dv.commit_steps_out, h->commit_steps_out, 2 * BL * s->dv.G}};
   for (auto& c : cp)
     if (c.src) DG_CUDA(s->err, cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s->stream), "copy state");
   DG_CUDA(s->err, dg::launch_plan(s->dv, h->tick, s->stream), "launch plan");
@@ -504,6 +509,7 @@ const float* dg_logz(const dg_sampler* s) { return s ? s->dv.logZ : nullptr; }
 const int32_t* dg_sample(const dg_sampler* s) { return s ? s->dv.y : nullptr; }
 const int32_t* dg_argmax(const dg_sampler* s) { return s ? s->dv.amax : nullptr; }
 const int32_t* dg_tokens_out(const dg_sampler* s) { return s ? s->dv.tokens_out : nullptr; }
+const int16_t* dg_commit_steps_out(const dg_sampler* s) { return s ? s->dv.commit_steps_out : nullptr; }
 const dg_slot* dg_slots(const dg_sampler* s) { return s ? s->dv.slots : nullptr; }
 const uint16_t* dg_normed(const dg_sampler* s) { return s ? s->dv.h : nullptr; }
 

@@ -356,13 +356,17 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
       const int p = g.tid + i * kTailThreads;
       if (p < L) {
         int xo = xv[i];
+        int16_t cs = (int16_t)s;
         if (!cm[i]) {
           xo = yv[i];
           dv.x[base + p] = xo;
           dv.committed[base + p] = 1;
-          dv.commit_step[base + p] = (int16_t)s;
+          dv.commit_step[base + p] = cs;
+        } else {
+          cs = __ldcg(dv.commit_step + base + p);
         }
         dv.tokens_out[((size_t)c * dv.G + b) * L + p] = xo;
+        dv.commit_steps_out[((size_t)c * dv.G + b) * L + p] = cs;
       }
     }
     g.sync();
