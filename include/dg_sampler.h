@@ -150,10 +150,13 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
 dg_status dg_denoise_step(dg_sampler* s, const float* resid);
 
 /*
- * The same tick from host memory.  Synchronizing.  Copies resid_host
- * (fp32 [B, L, d]; page-locked memory gives the fastest copy) into the
- * workspace, runs the tick, and copies back the canvas after the tick
- * (int32 [B, L], nullable) and this tick's entropies (fp32 [B, L], nullable).
+ * The same tick from host memory.  Synchronizing.  resid_host (fp32 [B, L, d])
+ * in page-locked memory mapped into the device's address space (cudaHostAlloc,
+ * cudaHostRegister, torch pin_memory) is read by the kernels directly; other
+ * host memory is first copied into the workspace.  The call runs the tick,
+ * copies back the canvas after the tick (int32 [B, L], nullable) and this
+ * tick's entropies (fp32 [B, L], nullable) in one copy, and waits once for the
+ * stream; resid_host must stay unchanged until it returns.
  */
 dg_status dg_denoise_step_host(dg_sampler* s, const float* resid_host, int32_t* canvas_host, float* entropy_host);
 

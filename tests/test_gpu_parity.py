@@ -218,17 +218,24 @@ def test_dg_run_callback_and_host_step():
     tokens, slots = s.run(cb, resid_dev)
     assert np.array_equal(tokens, o.tokens_out)
     assert np.all(slots["state"] == dg.DONE)
-    # the host-buffer tick gives what the device tick gives
-    s2 = dg.Sampler(case.gpu_cfg(), w_dev)
-    s3 = dg.Sampler(case.gpu_cfg(), w_dev)
-    for _ in range(3):
-        info = s2.sync_info()
-        act = np.nonzero(info["state"] == dg.ACTIVE)[0]
-        r = resid_slots(case, ocfg, W, act, info["block"][act], info["step"][act], s2.canvas().cpu().numpy()[act])
-        canvas_h, ent_h = s2.step_host(r)
-        s3.step(torch.from_numpy(r).to(dev))
-        assert np.array_equal(canvas_h, s3.canvas().cpu().numpy())
-        assert np.array_equal(ent_h, s3.entropy().cpu().numpy())
+    # the host-buffer tick gives what the device tick gives, from pageable memory (copied into the
+    # workspace) and from page-locked memory (read by the kernels in place), on both LM-head kernels
+    for c2 in (case, Case(vocab=4096, hidden=256, canvas_len=256, steps=4, seeds=(5,))):
+        W2 = weights(c2)
+        w2 = torch.from_numpy(W2.view(np.int16)).to(dev).view(torch.bfloat16)
+        o2 = c2.oracle_cfg()
+        s2 = dg.Sampler(c2.gpu_cfg(), w2)
+        s3 = dg.Sampler(c2.gpu_cfg(), w2)
+        for k in range(3):
+            info = s2.sync_info()
+            act = np.nonzero(info["state"] == dg.ACTIVE)[0]
+            r = resid_slots(c2, o2, W2, act, info["block"][act], info["step"][act], s2.canvas().cpu().numpy()[act])
+            if k % 2:
+                r = torch.from_numpy(r).pin_memory().numpy()
+            canvas_h, ent_h = s2.step_host(r)
+            s3.step(torch.from_numpy(r).to(dev))
+            assert np.array_equal(canvas_h, s3.canvas().cpu().numpy())
+            assert np.array_equal(ent_h, s3.entropy().cpu().numpy())
 
 
 def test_model_scale_two_ticks():

@@ -203,13 +203,18 @@ class Sampler:
         _check(self.dg_denoise_step(resid), self.handle)
 
     def step_host(self, resid_host: np.ndarray, want_canvas=True, want_entropy=True):
+        """dg_denoise_step_host; the results land in page-locked buffers kept by the sampler and are
+        returned as copies.  Pass a page-locked ``resid_host`` for an asynchronous input copy."""
+        import torch
         assert resid_host.dtype == np.float32 and resid_host.flags["C_CONTIGUOUS"]
-        canvas = np.empty((self.B, self.L), np.int32) if want_canvas else None
-        ent = np.empty((self.B, self.L), np.float32) if want_entropy else None
+        if getattr(self, "_host_out", None) is None:
+            self._host_out = (torch.empty((self.B, self.L), dtype=torch.int32).pin_memory(),
+                              torch.empty((self.B, self.L), dtype=torch.float32).pin_memory())
+        canvas, ent = self._host_out
         _check(lib.dg_denoise_step_host(self.handle, ctypes.c_void_p(resid_host.ctypes.data),
-                                        ctypes.c_void_p(canvas.ctypes.data) if canvas is not None else None,
-                                        ctypes.c_void_p(ent.ctypes.data) if ent is not None else None), self.handle)
-        return canvas, ent
+                                        ctypes.c_void_p(canvas.data_ptr()) if want_canvas else None,
+                                        ctypes.c_void_p(ent.data_ptr()) if want_entropy else None), self.handle)
+        return (canvas.numpy().copy() if want_canvas else None), (ent.numpy().copy() if want_entropy else None)
 
     def run(self, resid_fn, resid_dev=None):
         """dg_run with a Python callback ``resid_fn(tick, canvas_ptr, slots_ptr, resid_ptr, stream_ptr) -> int``."""

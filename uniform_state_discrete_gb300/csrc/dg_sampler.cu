@@ -30,6 +30,16 @@ struct dg_sampler {
   cudaEvent_t timing[4];
   bool timed;
   char err[512];
+  // pinned copy of the plan's error latch: reading it back does not go through
+  // a staged pageable copy, so a step that returns results synchronizes once
+  dg::Plan* pl_host = nullptr;
+  // pinned staging of the plan .. entropies span for dg_denoise_step_host, made on its first call
+  uint8_t* stage_host = nullptr;
+  size_t stage_bytes = 0, stage_x = 0, stage_H = 0;  // span size and offsets of x and H in it
+  ~dg_sampler() {
+    if (pl_host) cudaFreeHost(pl_host);
+    if (stage_host) cudaFreeHost(stage_host);
+  }
 };
 
 namespace {
@@ -104,15 +114,16 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
     return at;
   };
   L->slots = take(sizeof(dg_slot) * B);
+  // plan, canvas and entropies adjacent: a host step reads all three back in one copy
   L->plan = take(sizeof(dg::Plan));
-  L->active = take(sizeof(int32_t) * B);
   L->x = take(4 * B * Lc);
+  L->H = take(4 * B * Lc);
+  L->active = take(sizeof(int32_t) * B);
   L->committed = take(B * Lc);
   L->commit_step = take(2 * B * Lc);
   L->prev_amax = take(4 * B * Lc);
   L->tokens_out = take(4 * B * G * Lc);
   L->commit_steps_out = take(2 * B * G * Lc);
-  L->H = take(4 * B * Lc);
   L->logZ = take(4 * B * Lc);
   L->y = take(4 * B * Lc);
   L->amax = take(4 * B * Lc);
@@ -171,10 +182,17 @@ bool encode_2d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, 
   return true;
 }
 
+// The status a latched device error in the plan stands for.
+dg_status latched_status(dg_sampler* s, const dg::Plan& pl);
+
 dg_status check_device_error(dg_sampler* s) {
-  dg::Plan pl;
-  DG_CUDA(s->err, cudaMemcpyAsync(&pl, s->dv.plan, sizeof pl, cudaMemcpyDeviceToHost, s->stream), "read plan");
+  DG_CUDA(s->err, cudaMemcpyAsync(s->pl_host, s->dv.plan, sizeof(dg::Plan), cudaMemcpyDeviceToHost, s->stream),
+          "read plan");
   DG_CUDA(s->err, cudaStreamSynchronize(s->stream), "synchronize");
+  return latched_status(s, *s->pl_host);
+}
+
+dg_status latched_status(dg_sampler* s, const dg::Plan& pl) {
   if (pl.err == dg::kErrNonFinite) {
     set_err(s->err, "non-finite logit statistics at position index %d", pl.err_info[1]);
     return DG_ERR_NONFINITE;
@@ -353,6 +371,8 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
     const double prod = frac * span;
     temps[st] = (float)((double)cfg->t_max + prod);
   }
+  ce = cudaHostAlloc(reinterpret_cast<void**>(&s->pl_host), sizeof(dg::Plan), cudaHostAllocDefault);
+  if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "allocate the pinned error latch copy"));
   ce = cudaMemsetAsync(workspace, 0, L.total, s->stream);
   if (ce == cudaSuccess)
     ce = cudaMemcpyAsync(dv.slots, slots.data(), sizeof(dg_slot) * B, cudaMemcpyHostToDevice, s->stream);
@@ -376,18 +396,40 @@ dg_status dg_denoise_step_host(dg_sampler* s, const float* resid_host, int32_t* 
   if (!s) return DG_ERR_ARG;
   if (!resid_host) return set_err(s->err, "resid_host is NULL"), DG_ERR_ARG;
   const size_t BL = (size_t)s->dv.B * s->dv.L;
-  DG_CUDA(s->err,
-          cudaMemcpyAsync(s->dv.resid_stage, resid_host, BL * s->dv.d * sizeof(float), cudaMemcpyHostToDevice,
-                          s->stream),
-          "copy resid to device");
-  dg_status st = tick(s, s->dv.resid_stage);
+  // Page-locked input mapped into the device's address space is read by the
+  // RMSNorm straight from host memory (zero-copy: the rows cross the host link
+  // once, while the LM head sets up); anything else is copied into the workspace.
+  const float* resid = s->dv.resid_stage;
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, resid_host) == cudaSuccess && pa.type == cudaMemoryTypeHost && pa.devicePointer &&
+      reinterpret_cast<uintptr_t>(pa.devicePointer) % 16 == 0) {
+    resid = static_cast<const float*>(pa.devicePointer);
+  } else {
+    (void)cudaGetLastError();  // an unregistered pointer is not an error
+    DG_CUDA(s->err,
+            cudaMemcpyAsync(s->dv.resid_stage, resid_host, BL * s->dv.d * sizeof(float), cudaMemcpyHostToDevice,
+                            s->stream),
+            "copy resid to device");
+  }
+  dg_status st = tick(s, resid);
   if (st != DG_OK) return st;
-  if (canvas_host)
-    DG_CUDA(s->err, cudaMemcpyAsync(canvas_host, s->dv.x, BL * 4, cudaMemcpyDeviceToHost, s->stream), "copy canvas");
-  if (entropy_host)
-    DG_CUDA(s->err, cudaMemcpyAsync(entropy_host, s->dv.H, BL * 4, cudaMemcpyDeviceToHost, s->stream),
-            "copy entropy");
-  return check_device_error(s);
+  if (!canvas_host && !entropy_host) return check_device_error(s);
+  // plan, canvas and entropies lie next to each other in the workspace: one copy
+  // into a pinned staging buffer brings back all three
+  if (!s->stage_host) {
+    const uint8_t* p0 = reinterpret_cast<const uint8_t*>(s->dv.plan);
+    s->stage_x = (size_t)(reinterpret_cast<const uint8_t*>(s->dv.x) - p0);
+    s->stage_H = (size_t)(reinterpret_cast<const uint8_t*>(s->dv.H) - p0);
+    s->stage_bytes = s->stage_H + BL * 4;
+    DG_CUDA(s->err, cudaHostAlloc(reinterpret_cast<void**>(&s->stage_host), s->stage_bytes, cudaHostAllocDefault),
+            "allocate the pinned result staging");
+  }
+  DG_CUDA(s->err, cudaMemcpyAsync(s->stage_host, s->dv.plan, s->stage_bytes, cudaMemcpyDeviceToHost, s->stream),
+          "copy results");
+  DG_CUDA(s->err, cudaStreamSynchronize(s->stream), "synchronize");
+  if (canvas_host) memcpy(canvas_host, s->stage_host + s->stage_x, BL * 4);
+  if (entropy_host) memcpy(entropy_host, s->stage_host + s->stage_H, BL * 4);
+  return latched_status(s, *reinterpret_cast<const dg::Plan*>(s->stage_host));
 }
 
 dg_status dg_set_timing_events(dg_sampler* s, void* const* events) {
