@@ -233,6 +233,14 @@ dg_status dg_get_state(dg_sampler* s, dg_state* host);
  * and temperatures are taken from the config and the slots' steps. */
 dg_status dg_set_state(dg_sampler* s, const dg_state* host);
 
+/* Test hook for failure detection.  While on, the LM-head kernel does not
+ * count its finished units, so the finishing kernel's bounded wait for them
+ * runs out after about a second; the kernels then finish, the tick latches
+ * DG_ERR_TIMEOUT and the next synchronizing call reports it.  No wait hangs
+ * and nothing faults.  The sampler's state after such a tick is undefined;
+ * dg_set_state (which also clears the latch) makes it usable again. */
+dg_status dg_debug_hold_slabs(dg_sampler* s, int on);
+
 const char* dg_status_string(dg_status st);
 const char* dg_last_error(const dg_sampler* s); /* "" when none; s may be NULL (last create failure) */
 

@@ -244,3 +244,39 @@ def test_model_scale_two_ticks():
     rep = teacher_forced(Case(vocab=262144, hidden=2816, canvas_len=256, steps=48), ticks=2)
     _assert_report(rep, "model-scale")
     assert rep.ticks == 2
+
+
+@pytest.mark.parametrize("canvas_len,vocab", [(16, 2048), (256, 4096)], ids=["single-cta", "pair"])
+def test_bounded_wait_runs_out_and_sampler_recovers(canvas_len, vocab):
+    """Failure detection without a GPU fault: with the LM head holding back its unit counts, the
+    finishing kernel's bounded wait runs out after about a second, the tick reports DG_ERR_TIMEOUT
+    and the context stays usable; after dg_set_state the next tick matches a fresh sampler's."""
+    import time
+    import torch
+    import uniform_state_discrete_gb300 as dg
+    case = Case(vocab=vocab, hidden=128, canvas_len=canvas_len, steps=6, seeds=(4,))
+    W = weights(case)
+    dev = torch.device("cuda:0")
+    w_dev = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    ocfg = case.oracle_cfg()
+    s = dg.Sampler(case.gpu_cfg(), w_dev)
+    st0 = s.get_state()
+    r = torch.from_numpy(resid_slots(case, ocfg, W, np.array([0]), np.array([0]), np.array([0]),
+                                     st0["tokens"][:1])).to(dev)
+    s.debug_hold_slabs(True)
+    t0 = time.perf_counter()
+    s.step(r)
+    with pytest.raises(dg.DGError) as err:
+        s.sync_info()
+    waited = time.perf_counter() - t0
+    assert err.value.status == dg.DG_ERR_TIMEOUT
+    assert 0.9 < waited < 30.0
+    s.debug_hold_slabs(False)
+    s.set_state(st0)
+    s.step(r)
+    s.sync_info()
+    fresh = dg.Sampler(case.gpu_cfg(), w_dev)
+    fresh.step(r)
+    fresh.sync_info()
+    for view in ("canvas", "entropy", "sample"):
+        assert torch.equal(getattr(s, view)(), getattr(fresh, view)())

@@ -84,6 +84,7 @@ _SIGS = {
     "dg_normed": (ctypes.c_void_p, [ctypes.c_void_p]),
     "dg_sync_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "dg_set_timing_events": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "dg_debug_hold_slabs": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "dg_get_state": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(dg_state)]),
     "dg_set_state": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(dg_state)]),
     "dg_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -241,6 +242,10 @@ class Sampler:
         arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
         self._timing = (events, arr)
         _check(lib.dg_set_timing_events(self.handle, arr), self.handle)
+
+    def debug_hold_slabs(self, on: bool):
+        """Failure-detection test hook (dg_debug_hold_slabs): the next ticks' bounded waits run out."""
+        _check(lib.dg_debug_hold_slabs(self.handle, 1 if on else 0), self.handle)
 
     def sync_info(self) -> np.ndarray:
         slots = np.empty(self.B, SLOT_DTYPE)

@@ -88,6 +88,7 @@ struct Dev {
   bool reaccept;        // DG_REACCEPT: every step re-sorts all positions (see dg_mode)
   float softcap;        // final logit softcap c (0 = off): z -> c tanh(z / c) before the temperature
   float inv_softcap;    // 1 / c (0 when off)
+  int32_t hold_slabs;   // test hook (dg_debug_hold_slabs): the LM head does not count finished units
 };
 
 // ------------------------------------------------------------ Philox4x32-10

@@ -175,10 +175,15 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
 }
 
 // Planner kernel (sampler creation and dg_set_state): clears the tick's
-// counters, which an interrupted tick may have left behind, then plans `tick`.
+// counters and the error latch, which an interrupted tick may have left
+// behind, then plans `tick`.
 __global__ void __launch_bounds__(256) k_plan(const Dev dv, int tick) {
   __shared__ TailScratch sc;
   for (int i = threadIdx.x; i < dv.B; i += blockDim.x) dv.canvas_rows[i] = 0u;
+  if (threadIdx.x == 0) {
+    dv.plan->err = kErrNone;
+    for (int i = 0; i < 4; ++i) dv.plan->err_info[i] = 0;
+  }
   __syncthreads();
   plan_tick(dv, tick, Group{(int)threadIdx.x, (int)blockDim.x, 0}, &sc, true);
 }

@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       }
       if (cg == 0) gbest[rl] = ord_key(-INFINITY);  // the next unit may hold other rows
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-      if (warp == 2 && lane == 0 && mt * kBM < n_rows) {
+      if (warp == 2 && lane == 0 && mt * kBM < n_rows && !dv.hold_slabs) {
         __threadfence();  // this unit's partial records of the slab are written
         atomicAdd(dv.slab_done + mt, 1u);
       }
@@ -986,7 +986,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       }
       if (cg == 0) gbest[rl] = ord_key(-INFINITY);  // the next unit may hold other rows
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-      if (warp == 2 && lane == 0 && (mt * 2 + (int)rank) * kBM < n_rows) {
+      if (warp == 2 && lane == 0 && (mt * 2 + (int)rank) * kBM < n_rows && !dv.hold_slabs) {
         __threadfence();  // this unit's partial records of the slab are written
         atomicAdd(dv.slab_done + mt * 2 + (int)rank, 1u);
       }

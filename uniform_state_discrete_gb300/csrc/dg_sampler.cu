@@ -543,6 +543,12 @@ void dg_destroy(dg_sampler* s) {
   delete s;
 }
 
+dg_status dg_debug_hold_slabs(dg_sampler* s, int on) {
+  if (!s) return DG_ERR_ARG;
+  s->dv.hold_slabs = on ? 1 : 0;
+  return DG_OK;
+}
+
 const int32_t* dg_canvas(const dg_sampler* s) { return s ? s->dv.x : nullptr; }
 const uint8_t* dg_committed(const dg_sampler* s) { return s ? s->dv.committed : nullptr; }
 const int16_t* dg_commit_step(const dg_sampler* s) { return s ? s->dv.commit_step : nullptr; }
