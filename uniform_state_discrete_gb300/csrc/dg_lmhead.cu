@@ -134,25 +134,8 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane, waited in the same
+// 16 consecutive fp32 columns of this thread's TMEM lane, waited in the same
 // statement so no use of the registers can be scheduled before the wait.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-}
-
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
@@ -165,30 +148,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
       : "memory");
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-// -log2(E) for the Exp(1) variate E = -ln U of one Gumbel draw,
-// U = (r + 0.5) 2^-32.  For U < 3/4, E comes from lg2(U).  For U >= 3/4,
-// E = -ln(1 - q) with q = 1 - U taken exactly from the integer, through the
-// series -ln(1-q) = 2 atanh(s) = 2 (s + s^3/3 + s^5/5 + ...), s = q / (2 - q)
-// <= 1/7, truncated after s^9 (relative error < 4e-10), which keeps the large
-// Gumbel values (small E) accurate where lg2(U) would lose them.
-__device__ __forceinline__ float neg_log2_exp_variate(uint32_t r) {
-  float E;
-  if (r < 0xC0000000u) {
-    const float U = fmaf(__uint2float_rn(r), 0x1p-32f, 0x1p-33f);
-    E = -0.69314718055994531f * lg2_approx(U);
-  } else {
-    const float q = fmaf(__uint2float_rn(~r), 0x1p-32f, 0x1p-33f);
-    const float s = __fdividef(q, 2.0f - q);
-    const float s2 = s * s;
-    float t = fmaf(s2, 1.0f / 9.0f, 1.0f / 7.0f);
-    t = fmaf(s2, t, 1.0f / 5.0f);
-    t = fmaf(s2, t, 1.0f / 3.0f);
-    t = fmaf(s2, t, 1.0f);
-    E = 2.0f * s * t;
-  }
-  return -lg2_approx(E);
 }
 
 struct RowMeta {
@@ -232,8 +191,14 @@ __device__ __forceinline__ float screen_factor(float m, float g) {
 __device__ __forceinline__ float screen_word(uint32_t r) { return __uint_as_float(__funnelshift_r(r, 0x7Fu, 9)); }
 __device__ __forceinline__ float screen_threshold(float e, float K) { return fmaf(-e, K, 2.f - 0x1p-21f); }
 
-// The same transform without branches (both branches evaluated, one kept), so
-// a warp scores one candidate per lane in lockstep.  Same results.
+// -log2(E) for the Exp(1) variate E = -ln U of one Gumbel draw,
+// U = (r + 0.5) 2^-32.  For U < 3/4, E comes from lg2(U).  For U >= 3/4,
+// E = -ln(1 - q) with q = 1 - U taken exactly from the integer, through the
+// series -ln(1-q) = 2 atanh(s) = 2 (s + s^3/3 + s^5/5 + ...), s = q / (2 - q)
+// <= 1/7, truncated after s^9 (relative error < 4e-10), which keeps the large
+// Gumbel values (small E) accurate where lg2(U) would lose them.  Both
+// branches are evaluated and one kept, so a warp scores one candidate per lane
+// in lockstep.
 __device__ __forceinline__ float neg_log2_exp_variate_nb(uint32_t r) {
   const float U = fmaf(__uint2float_rn(r), 0x1p-32f, 0x1p-33f);
   const float Eu = -0.69314718055994531f * lg2_approx(U);
