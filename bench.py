@@ -400,6 +400,8 @@ def run_ours(args, wl, world, rank, local):
     roof["algorithmic_flops_per_launch"] = alg_flops
     roof["kernel_ms_mean"] = k2_s * 1e3
     roof["tensor_frac"] = alg_flops / k2_s / 1e12 / peaks["bf16_tflops"]
+    roof["tensor_frac_sustained"] = alg_flops / k2_s / 1e12 / peaks["bf16_tflops_sustained"]
+    roof["hbm_frac_of_nominal_7_9_tbs"] = alg_bytes / k2_s / 7.9e12
     roof["step_roofline_frac"] = max(t_hbm, t_tc) / (device_s / args.steps)
 
     # e2e through the host-buffer entry point
