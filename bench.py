@@ -53,6 +53,11 @@ WORKLOADS = {
                             text="1 canvas x 256 positions, V=262144, d=2816 (model-scale LM head), same knobs"),
     "tiny": dict(vocab=2048, hidden=128, canvas_len=16, n_canvases=1, steps=8,
                  text="1 canvas x 16 positions, V=2048, d=128, 8 steps"),
+    # the batched configuration at steady state (all 16 canvases active; the staggered admission is
+    # a parity-test case): 4096 positions per tick, tensor-bound.  Its oracle tick takes minutes, so
+    # run it with --no-cpu-baseline.
+    "batched16_v262k": dict(vocab=262144, hidden=2816, canvas_len=256, n_canvases=16, steps=48,
+                            text="16 canvases x 256 positions, V=262144, d=2816, per-canvas seeds, all active"),
 }
 SIGMA_HIDDEN = 0.5
 

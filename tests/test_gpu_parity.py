@@ -280,3 +280,37 @@ def test_bounded_wait_runs_out_and_sampler_recovers(canvas_len, vocab):
     fresh.sync_info()
     for view in ("canvas", "entropy", "sample"):
         assert torch.equal(getattr(s, view)(), getattr(fresh, view)())
+
+
+def test_batched_model_scale_sampled_rows():
+    """16 canvases x 256 positions at V=2^18, d=2816 (the batched configuration with every canvas
+    active: 16 row tiles of the SM-pair LM head per vocabulary chunk), one tick; sampled positions
+    across the canvases against the oracle computed for those rows alone."""
+    import torch
+    import uniform_state_discrete_gb300 as dg
+    B, L, V, d = 16, 256, 262144, 2816
+    case = Case(vocab=V, hidden=d, canvas_len=L, n_canvases=B, steps=48, seeds=tuple(range(B)))
+    W = weights(case)
+    dev = torch.device("cuda:0")
+    w_dev = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    ocfg = case.oracle_cfg()
+    s = dg.Sampler(case.gpu_cfg(), w_dev)
+    st = s.get_state()
+    canv = np.arange(B)
+    resid = resid_slots(case, ocfg, W, canv, np.zeros(B, np.int64), np.zeros(B, np.int64), st["tokens"])
+    s.step(torch.from_numpy(resid).to(dev))
+    H, lz = s.entropy().cpu().numpy(), s.logz().cpu().numpy()
+    y, am = s.sample().cpu().numpy(), s.argmax().cpu().numpy()
+    rng = np.random.default_rng(3)
+    pick = [(c, int(p)) for c in range(B) for p in rng.choice(L, 2, replace=False)]
+    r = np.stack([resid[c, p] for c, p in pick])
+    h = oracle.rmsnorm_bf16(r, ocfg.rms_eps)
+    z = oracle.logits(h, W)
+    T = oracle.temperature(0, ocfg.num_inference_steps, ocfg.t_min, ocfg.t_max)
+    ref = oracle.stats(z, T, np.array([ocfg.seed(c) for c, _ in pick], np.uint64), 0, 0,
+                       np.array([p for _, p in pick], np.int32))
+    for i, (c, p) in enumerate(pick):
+        assert abs(float(H[c, p]) - ref["H"][i]) <= 1e-3
+        assert abs(float(lz[c, p]) - ref["logZ"][i]) <= 1e-3 * abs(ref["logZ"][i])
+        assert y[c, p] == ref["y"][i] or ref["ggap"][i] < 1e-4
+        assert am[c, p] == ref["amax"][i] or ref["zgap"][i] < 1e-4
