@@ -314,3 +314,91 @@ def test_batched_model_scale_sampled_rows():
         assert abs(float(lz[c, p]) - ref["logZ"][i]) <= 1e-3 * abs(ref["logZ"][i])
         assert y[c, p] == ref["y"][i] or ref["ggap"][i] < 1e-4
         assert am[c, p] == ref["amax"][i] or ref["zgap"][i] < 1e-4
+
+
+_W_MODEL = {}
+
+
+def _model_weights():
+    """The model-scale W (V=2^18, d=2816, seed 0), generated once per session."""
+    if "w" not in _W_MODEL:
+        _W_MODEL["w"] = synth.wvocab(0, 262144, 2816)
+    return _W_MODEL["w"]
+
+
+@pytest.mark.parametrize("sigma", [0.1, 2.0])
+@pytest.mark.parametrize("t_max,t_min", [(0.8, 0.4), (1.5, 0.1)])
+@pytest.mark.parametrize("bound", [0.01, 0.1, 1.0])
+def test_stress_config_sweep_point(bound, t_max, t_min, sigma):
+    """The stress configuration at full size: 64 canvases x 4 blocks x 256 positions, V=2^18,
+    d=2816, one point of its sweep.  The first tick's sampled positions against the oracle; then
+    the whole run with the device residual generator, checking at every tick what holds at any
+    size: frozen positions keep their tokens, every step commits at least one position while any is
+    open, tokens stay in [0, V), and each finished block's heatmap holds steps of that block."""
+    import torch
+    import uniform_state_discrete_gb300 as dg
+    B, G, L, V, d, N = 64, 4, 256, 262144, 2816, 48
+    W = _model_weights()
+    case = Case(vocab=V, hidden=d, canvas_len=L, n_canvases=B, gen_blocks=G, steps=N, bound=bound, t_max=t_max,
+                t_min=t_min, sigma=sigma, seeds=tuple(range(B)))
+    dev = torch.device("cuda:0")
+    w_dev = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    ocfg = case.oracle_cfg()
+    stream = torch.cuda.Stream(dev)
+    s = dg.Sampler(case.gpu_cfg(), w_dev, stream=stream)
+    resid = torch.empty(B, L, d, dtype=torch.float32, device=dev)
+
+    def make_resid():
+        synth.resid_device(w_dev.data_ptr(), s.canvas().data_ptr(), s.slots_ptr(), B, L, d, sigma, resid.data_ptr(),
+                           stream.cuda_stream)
+
+    prev = s.get_state()
+    with torch.cuda.stream(stream):
+        make_resid()
+    stream.synchronize()
+    # first tick: sampled positions against the oracle on the same residual rows
+    r0 = resid.cpu().numpy()
+    with torch.cuda.stream(stream):
+        s.step(resid)
+    s.sync_info()
+    H, y = s.entropy().cpu().numpy(), s.sample().cpu().numpy()
+    pick = [(c, p) for c, p in zip(range(0, B, 8), (0, 37, 74, 111, 148, 185, 222, 255))]
+    h = oracle.rmsnorm_bf16(np.stack([r0[c, p] for c, p in pick]), ocfg.rms_eps)
+    ref = oracle.stats(oracle.logits(h, W), oracle.temperature(0, N, ocfg.t_min, ocfg.t_max),
+                       np.array([ocfg.seed(c) for c, _ in pick], np.uint64), 0, 0,
+                       np.array([p for _, p in pick], np.int32))
+    for i, (c, p) in enumerate(pick):
+        assert abs(float(H[c, p]) - ref["H"][i]) <= 1e-3
+        assert y[c, p] == ref["y"][i] or ref["ggap"][i] < 1e-4
+    # the whole run
+    for tick in range(1, G * N + 2):
+        cur = s.get_state()
+        for c in range(B):
+            a, b = prev["slots"][c], cur["slots"][c]
+            assert np.all((cur["tokens"][c] >= 0) & (cur["tokens"][c] < V))
+            if a["state"] != dg.ACTIVE:
+                continue
+            if b["block"] == a["block"] and b["state"] == dg.ACTIVE:
+                frozen = prev["committed"][c] != 0
+                assert np.array_equal(cur["tokens"][c][frozen], prev["tokens"][c][frozen])
+                assert np.all(cur["committed"][c][frozen] != 0)
+                # at least one commit per step while any position is open
+                assert b["n_committed"] > a["n_committed"] or a["n_committed"] == L
+                assert b["step"] == a["step"] + 1
+            else:  # the block ended at this tick
+                blk = a["block"]
+                assert np.all((cur["tokens_out"][c, blk] >= 0) & (cur["tokens_out"][c, blk] < V))
+                hm = cur["commit_steps_out"][c, blk]
+                assert np.all((hm >= 0) & (hm <= a["step"]))
+        prev = cur
+        if np.all(cur["slots"]["state"] == dg.DONE):
+            break
+        with torch.cuda.stream(stream):
+            make_resid()
+            s.step(resid)
+    info = s.sync_info()
+    assert np.all(info["state"] == dg.DONE)
+    assert np.all(info["steps_used"] <= G * N)
+    if sigma == 0.1 and bound == 1.0:
+        assert info["converged_blocks"].sum() > 0  # peaked distributions stop early
+    s.close()
