@@ -402,3 +402,42 @@ def test_stress_config_sweep_point(bound, t_max, t_min, sigma):
     if sigma == 0.1 and bound == 1.0:
         assert info["converged_blocks"].sum() > 0  # peaked distributions stop early
     s.close()
+
+
+def _device_free_run(case, W, sigma, max_ticks):
+    """Run a sampler to completion with the device residual generator; returns it."""
+    import torch
+    import uniform_state_discrete_gb300 as dg
+    dev = torch.device("cuda:0")
+    w_dev = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    stream = torch.cuda.Stream(dev)
+    s = dg.Sampler(case.gpu_cfg(), w_dev, stream=stream)
+    resid = torch.empty(case.n_canvases, case.canvas_len, case.hidden, dtype=torch.float32, device=dev)
+    for _ in range(max_ticks):
+        if np.all(s.sync_info()["state"] == dg.DONE):
+            break
+        with torch.cuda.stream(stream):
+            synth.resid_device(w_dev.data_ptr(), s.canvas().data_ptr(), s.slots_ptr(), case.n_canvases,
+                               case.canvas_len, case.hidden, sigma, resid.data_ptr(), stream.cuda_stream)
+            s.step(resid)
+    return s
+
+
+def test_batched_config_staggered_admission_invariance():
+    """The batched configuration as specified: 16 canvases x 256 positions at V=2^18, d=2816, seeds
+    0..15 admitted at ticks 12 * (c // 4).  Each canvas's tokens equal those of the same canvas
+    run alone (TensorSharp doc, "7. Test coverage": batched decode equals per-sequence decode)."""
+    import uniform_state_discrete_gb300 as dg
+    W = _model_weights()
+    B = 16
+    batch = Case(vocab=262144, hidden=2816, canvas_len=256, n_canvases=B, steps=48, seeds=tuple(range(B)),
+                 admit=tuple(12 * (c // 4) for c in range(B)))
+    s = _device_free_run(batch, W, 0.5, 48 + 36 + 2)
+    info = s.sync_info()
+    assert np.all(info["state"] == dg.DONE) and np.all(info["steps_used"] == 48)
+    tok = s.tokens_out().cpu().numpy()
+    s.close()
+    for c in (0, 5, 15):
+        alone = _device_free_run(Case(vocab=262144, hidden=2816, canvas_len=256, steps=48, seeds=(c,)), W, 0.5, 50)
+        assert np.array_equal(alone.tokens_out().cpu().numpy()[0], tok[c])
+        alone.close()
