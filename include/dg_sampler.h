@@ -5,14 +5,17 @@
  * One denoising step ("tick") runs, for every active canvas:
  *   1. the final RMSNorm of the residual stream, w * x * sqrt(D) / (||x||_2 + eps),
  *      cast to bf16                 ("The Annotated DiffusionGemma", "RMSNorm")
- *   2. the tied LM head z = h W_vocab^T, fp32 accumulate, never stored
- *                                   (same page, "Complete DiffusionGemma model")
+ *   2. the tied LM head z = h W_vocab^T, fp32 accumulate, never stored, with an
+ *      optional final logit softcap c tanh(z / c)
+ *                                   (same page, "Complete DiffusionGemma model",
+ *                                    "Logit Softcapping")
  *   3. softmax(z / T) with the per-position entropy H (nats), log Z, the argmax
  *      and one sampled token        (same page, "Apply temperature", "Compute
  *                                    entropy")
- *   4. the entropy-bounded commit: the uncommitted positions sorted by entropy,
- *      the prefix whose exclusive entropy sum stays <= entropy_bound freezes to
- *      its sampled tokens          (same page, "Keep a low-entropy prefix and
+ *   4. the entropy-bounded commit: the open positions sorted by entropy, the
+ *      prefix whose exclusive entropy sum stays <= entropy_bound takes its
+ *      sampled tokens and, under DG_FREEZE, freezes (dg_mode)
+ *                                   (same page, "Keep a low-entropy prefix and
  *                                    renoise the rest"; ComfyUI-DiffusionGemma,
  *                                    "What it is")
  *   5. the early-stop test (mean H < confidence and an unchanged argmax canvas)
@@ -25,7 +28,10 @@
  *   - "dev" pointers are CUDA device pointers, "host" pointers host memory.
  *   - The library never allocates device memory.  The caller allocates one
  *     workspace of dg_workspace_size() bytes and keeps it alive until
- *     dg_destroy().  Device buffers passed in are borrowed, not owned.
+ *     dg_destroy().  Device buffers passed in are borrowed, not owned.  A
+ *     sampler holds two small page-locked host buffers of its own (the error
+ *     latch read-back, made at creation, and the result staging of
+ *     dg_denoise_step_host, made on its first call), freed by dg_destroy().
  *   - Work is enqueued on the stream given to dg_sampler_create().  Calls
  *     marked "asynchronous" return before the GPU work ends; calls marked
  *     "synchronizing" wait for the stream.

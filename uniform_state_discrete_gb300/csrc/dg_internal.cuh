@@ -76,9 +76,9 @@ struct Dev {
   uint16_t* h;          // [rows_cap, d] bf16 bits, compact active rows
   Partial* part;        // [rows_cap, n_sub]
   uint32_t* canvas_rows;// [B] rows combined per canvas this tick
-  uint32_t* rows_ready; // normalised rows written this tick (K1 -> K2)
-  uint32_t* fin_started;// K3 CTAs that have read this tick's plan
-  uint32_t* slab_done;  // [rows_cap / 128] LM-head units finished per 128-row slab (K2 -> K3)
+  uint32_t* rows_ready; // normalised rows written this tick (RMSNorm -> LM-head producers)
+  uint32_t* fin_started;// finishing-kernel CTAs that have read this tick's plan
+  uint32_t* slab_done;  // [rows_cap / 128] LM-head units finished per 128-row slab (-> finishing kernel)
   float* resid_stage;   // [B, L, d]
   const float* norm_w;  // [d] or null
   const float* temps;   // [N] temperature of each step, T_s = t_max + (s/N)(t_min - t_max)

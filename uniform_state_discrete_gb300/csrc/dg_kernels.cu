@@ -1,5 +1,6 @@
-// K1 RMSNorm, the finishing kernel (split-vocabulary combine, entropy-bounded
-// commit, re-noise and next-tick plan) and the stand-alone tick planner.
+// The RMSNorm kernel (K1, for the single-CTA LM head), the finishing kernel
+// (K3: split-vocabulary combine, entropy-bounded commit, re-noise and
+// next-tick plan) and the stand-alone tick planner.
 #include <cuda_runtime.h>
 #include <math.h>
 

@@ -10,23 +10,31 @@
 // per position on the device; here the reduction moves into the GEMM's own
 // epilogue so the logits are never written.
 //
-// Structure (one persistent CTA per SM, 576 threads):
-//   warp 0      TMA producer: A = h tile [128 x 64] and B = W tile [256 x 64]
-//               per stage, 128-byte swizzle, 4-stage mbarrier ring.
-//   warp 1      allocates 512 TMEM columns; one lane issues
-//               tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32,
-//               M=128, N=256, K=16) into one of two TMEM accumulators and
-//               commits stage release / accumulator-ready barriers.
-//   warps 2..17 epilogue: four warps per TMEM lane quadrant (rows), each
-//               owning 64 of the 256 columns; per element
+// Two kernels share the epilogue.  k_lmhead_pair (256 positions and up) runs
+// persistent clusters of two CTAs, one per SM, 576 threads each:
+//   warp 0      TMA producer: this CTA's 128 rows of h and its 128-row half of
+//               the 256-row W tile per K stage of 64, 128-byte swizzle,
+//               6-stage mbarrier ring (completion on the leader's barriers);
+//               the first W stages are loaded before the kernel waits for
+//               anything, since W depends on no earlier kernel.
+//   warp 1      allocates 512 TMEM columns for the pair; the leader's lane 0
+//               issues tcgen05.mma.cta_group::2.kind::f16 (bf16 x bf16 -> fp32,
+//               M=256, N=256, K=16) into one of two TMEM accumulators and
+//               commits stage-release / accumulator-ready barriers to both CTAs.
+//   warps 2..17 first form this CTA's share of the RMSNorm rows (dg_norm.cuh)
+//               and count them; then the epilogue: four warps per TMEM lane
+//               quadrant (rows), each owning 64 of the 256 columns; per element
 //                 u = z * log2(e)/T, running (max, sum 2^(u-m), sum 2^(u-m)(u-m)),
 //                 argmax, and the perturbed score u - log2 E_v of the
 //                 Gumbel draw (E_v = -ln U_v, U_v from Philox).
-// Work unit = (128-row M tile of active positions, vocabulary chunk); the
-// epilogue keeps its running statistics in registers across the chunk's
-// tiles and writes one 32-byte partial record per row and column group.
-// Every mbarrier wait is bounded (1 s); on expiry the CTA latches an error,
-// drains what it issued and frees TMEM.
+// k_lmhead (fewer positions) is the same on one CTA: M=128, a 4-stage ring,
+// rows formed beforehand by the RMSNorm kernel.
+// Work unit = (row tile, vocabulary chunk); the epilogue keeps its running
+// statistics in registers across the chunk's tiles, merges the four column
+// groups in shared memory and writes one 32-byte partial record per row and
+// chunk, then counts the unit on its 128-row slab for the finishing kernel.
+// Every wait is bounded (1 s); on expiry the CTA latches an error, drains what
+// it issued and frees TMEM.
 #include <cuda_runtime.h>
 
 #include "dg_gumbel.cuh"
