@@ -296,7 +296,7 @@ def run_ours(args, wl, world, rank, local):
     canvas_ptr = s.canvas().data_ptr()
 
     def make_resid():
-        synth.resid_device(w_dev.data_ptr(), canvas_ptr, slots_ptr, B, L, d, SIGMA_HIDDEN, resid.data_ptr(),
+        synth.resid_device(w_dev.data_ptr(), canvas_ptr, slots_ptr, B, L, V, d, SIGMA_HIDDEN, resid.data_ptr(),
                            stream.cuda_stream)
 
     def flush_l2():

@@ -56,18 +56,18 @@ def build_gpu(force: bool = False) -> str:
     return _SO_GPU
 
 
-def resid_device(w_bf16_ptr: int, tokens_ptr: int, slots_ptr: int, B: int, L: int, d: int, sigma: float,
+def resid_device(w_bf16_ptr: int, tokens_ptr: int, slots_ptr: int, B: int, L: int, V: int, d: int, sigma: float,
                  out_ptr: int, stream_ptr: int) -> None:
     """Device residual rows for every active canvas (same definition as ``resid_rows``), enqueued on a stream."""
     global _lib_gpu
     if _lib_gpu is None:
         lib = ctypes.CDLL(build_gpu())
-        lib.synth_resid_device.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_double,
+        lib.synth_resid_device.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_double,
                                                                                           ctypes.c_void_p,
                                                                                           ctypes.c_void_p]
         lib.synth_resid_device.restype = ctypes.c_int
         _lib_gpu = lib
-    rc = _lib_gpu.synth_resid_device(w_bf16_ptr, tokens_ptr, slots_ptr, B, L, d, sigma, out_ptr, stream_ptr)
+    rc = _lib_gpu.synth_resid_device(w_bf16_ptr, tokens_ptr, slots_ptr, B, L, V, d, sigma, out_ptr, stream_ptr)
     if rc != 0:
         raise RuntimeError(f"synth_resid_device failed with CUDA error {rc}")
 

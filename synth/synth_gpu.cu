@@ -3,8 +3,9 @@
 // Box-Muller normal of Philox4x32-10 keyed by the canvas seed and counter
 // (k>>2, p, (block<<16)|step, 1) -- the same definition as the host code,
 // evaluated in fp64.  Reads the per-canvas state through the public dg_slot
-// layout; canvases that are not active are skipped.  Inputs only: none of the
-// sampler's arithmetic is here.
+// layout; canvases that are not active are skipped.  A token outside [0, V)
+// is never used as a W row: its residual row is written as zeros.  Inputs
+// only: none of the sampler's arithmetic is here.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,7 +25,7 @@ __device__ __forceinline__ uint4 syn_philox(uint4 c, uint32_t k0, uint32_t k1) {
 }
 
 __global__ void syn_resid_kernel(const uint16_t* __restrict__ w, const int32_t* __restrict__ tokens,
-                                 const dg_slot* __restrict__ slots, int B, int L, int d, double sigma,
+                                 const dg_slot* __restrict__ slots, int B, int L, int V, int d, double sigma,
                                  float* __restrict__ out) {
   const int groups = d >> 2;
   const long long n = (long long)B * L * groups;
@@ -34,6 +35,11 @@ __global__ void syn_resid_kernel(const uint16_t* __restrict__ w, const int32_t* 
     const int c = (int)(cp / L), p = (int)(cp % L);
     const dg_slot sl = slots[c];
     if (sl.state != 1) continue;
+    const int32_t tok = tokens[cp];
+    if (tok < 0 || tok >= V) {
+      reinterpret_cast<float4*>(out + (size_t)cp * d)[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+      continue;
+    }
     const uint32_t bs = ((uint32_t)sl.block << 16) | (uint32_t)sl.step;
     const uint4 x = syn_philox(make_uint4((uint32_t)g, (uint32_t)p, bs, 1u), (uint32_t)sl.seed,
                                (uint32_t)(sl.seed >> 32));
@@ -48,7 +54,7 @@ __global__ void syn_resid_kernel(const uint16_t* __restrict__ w, const int32_t* 
       nrm[2 * j] = rad * co;
       nrm[2 * j + 1] = rad * s;
     }
-    const uint16_t* wrow = w + (size_t)tokens[cp] * d + 4 * g;
+    const uint16_t* wrow = w + (size_t)tok * d + 4 * g;
     float4 o;
     float* of = &o.x;
     for (int j = 0; j < 4; ++j) {
@@ -62,12 +68,12 @@ __global__ void syn_resid_kernel(const uint16_t* __restrict__ w, const int32_t* 
 }  // namespace
 
 extern "C" int synth_resid_device(const void* w_bf16, const int32_t* tokens, const dg_slot* slots, int B, int L,
-                                  int d, double sigma, float* out, void* stream) {
-  if (d % 4) return -1;
+                                  int V, int d, double sigma, float* out, void* stream) {
+  if (d % 4 || V < 1) return -1;
   const long long n = (long long)B * L * (d / 4);
   long long blocks = (n + 255) / 256;
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
   syn_resid_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint16_t*>(w_bf16), tokens, slots, B, L, d, sigma, out);
+      static_cast<const uint16_t*>(w_bf16), tokens, slots, B, L, V, d, sigma, out);
   return (int)cudaGetLastError();
 }

@@ -349,7 +349,7 @@ def test_stress_config_sweep_point(bound, t_max, t_min, sigma):
     resid = torch.empty(B, L, d, dtype=torch.float32, device=dev)
 
     def make_resid():
-        synth.resid_device(w_dev.data_ptr(), s.canvas().data_ptr(), s.slots_ptr(), B, L, d, sigma, resid.data_ptr(),
+        synth.resid_device(w_dev.data_ptr(), s.canvas().data_ptr(), s.slots_ptr(), B, L, V, d, sigma, resid.data_ptr(),
                            stream.cuda_stream)
 
     prev = s.get_state()
@@ -418,7 +418,7 @@ def _device_free_run(case, W, sigma, max_ticks):
             break
         with torch.cuda.stream(stream):
             synth.resid_device(w_dev.data_ptr(), s.canvas().data_ptr(), s.slots_ptr(), case.n_canvases,
-                               case.canvas_len, case.hidden, sigma, resid.data_ptr(), stream.cuda_stream)
+                               case.canvas_len, case.vocab, case.hidden, sigma, resid.data_ptr(), stream.cuda_stream)
             s.step(resid)
     return s
 

@@ -124,9 +124,12 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
       const size_t o = (size_t)c * dv.L + p;
       dv.H[o] = H > 0.f ? H : 0.f;  // +0 for rounding below zero (and never -0: its bits would sort last)
       dv.logZ[o] = lz;
-      dv.y[o] = acc.gidx;
-      dv.amax[o] = acc.amax;
-      if (!isfinite(H) || !isfinite(lz) || !isfinite(acc.g) || acc.gidx < 0 || acc.gidx >= dv.V) {
+      // a row without valid statistics latches an error and never hands an
+      // out-of-range token to the canvas (callers index embeddings with it)
+      const bool y_ok = acc.gidx >= 0 && acc.gidx < dv.V, a_ok = acc.amax >= 0 && acc.amax < dv.V;
+      dv.y[o] = y_ok ? acc.gidx : 0;
+      dv.amax[o] = a_ok ? acc.amax : 0;
+      if (!isfinite(H) || !isfinite(lz) || !isfinite(acc.g) || !y_ok || !a_ok) {
         if (atomicCAS(&dv.plan->err, kErrNone, kErrNonFinite) == kErrNone) dv.plan->err_info[1] = (int)o;
       }
     }

@@ -114,9 +114,10 @@ __global__ void __launch_bounds__(256) k_static_combine(const dg::Dev dv, int ro
     const float lz = 0.69314718055994531f * (acc.m + l2S);
     H[row] = h > 0.f ? h : 0.f;
     logZ[row] = lz;
-    y[row] = acc.gidx;
-    amax[row] = acc.amax;
-    if (!isfinite(h) || !isfinite(lz) || !isfinite(acc.g) || acc.gidx < 0 || acc.gidx >= dv.V) {
+    const bool y_ok = acc.gidx >= 0 && acc.gidx < dv.V, a_ok = acc.amax >= 0 && acc.amax < dv.V;
+    y[row] = y_ok ? acc.gidx : 0;  // never an out-of-range token, even on the error path
+    amax[row] = a_ok ? acc.amax : 0;
+    if (!isfinite(h) || !isfinite(lz) || !isfinite(acc.g) || !y_ok || !a_ok) {
       if (atomicCAS(&dv.plan->err, dg::kErrNone, dg::kErrNonFinite) == dg::kErrNone) dv.plan->err_info[1] = row;
     }
   }
