@@ -99,7 +99,8 @@ typedef struct dg_config {
   float t_max;                 /* hot temperature endpoint (step 0), > 0                         */
   float entropy_bound;         /* per-step acceptance budget in nats, >= 0                       */
   float confidence;            /* early stop when mean H (nats) falls below this, >= 0           */
-  int32_t stability;           /* steps the argmax canvas must stay unchanged; must be 1         */
+  int32_t stability;           /* k, 1..1024: the early stop also needs the argmax canvas equal
+                                  to each of the k previous steps' (the pages use 1)             */
   float rms_eps;               /* RMSNorm epsilon, added to ||x||_2, >= 0                        */
   int32_t mode;                /* dg_mode: DG_FREEZE or DG_REACCEPT                              */
   int32_t max_active;          /* most canvases active in one tick, 1..B (0 = B); sizes buffers  */
@@ -126,6 +127,8 @@ typedef struct dg_slot {
   float mean_entropy;       /* mean H (nats) over the canvas at its last tick         */
   int32_t n_remasked;       /* DG_REACCEPT: positions accepted at the previous step and
                                re-noised at the latest one; 0 under DG_FREEZE          */
+  int32_t stable_steps;     /* consecutive latest steps whose argmax canvas equalled the
+                               one before (reset at each block start)                  */
 } dg_slot;
 
 typedef struct dg_sampler dg_sampler;

@@ -90,6 +90,7 @@ class OracleConfig:
     max_active: Optional[int] = None  # most canvases running in one tick (None: all)
     mode: str = "freeze"  # "freeze" or "reaccept" (see the module docstring)
     softcap: float = 0.0  # final logit softcap c (0 = off): z -> c tanh(z / c) before the temperature
+    stability: int = 1  # steps in a row the argmax canvas must equal the one before for an early stop
     # parity margins stated by the task for flagging near-ties
     margin_H: float = 1e-3
     margin_gap: float = 1e-4
@@ -141,6 +142,7 @@ class OracleSampler:
         self.committed = np.zeros((B, L), dtype=bool)
         self.commit_step = np.full((B, L), -1, dtype=np.int16)
         self.prev_amax = np.zeros((B, L), dtype=np.int32)
+        self.stable_run = np.zeros(B, dtype=np.int32)  # steps in a row with an unchanged argmax canvas
         self.steps_used = np.zeros(B, dtype=np.int32)
         self.converged_blocks = np.zeros(B, dtype=np.int32)
         self.tokens_out = np.full((B, cfg.gen_blocks, L), -1, dtype=np.int32)
@@ -158,6 +160,7 @@ class OracleSampler:
         self.committed[c] = False
         self.commit_step[c] = -1
         self.prev_amax[c] = 0
+        self.stable_run[c] = 0
         self.block[c] = b
         self.step_no[c] = 0
 
@@ -183,7 +186,7 @@ class OracleSampler:
         """Copy of the whole state (used to teacher-force the CUDA path from the oracle)."""
         return {k: getattr(self, k).copy() for k in ("status", "block", "step_no", "x", "committed", "commit_step",
                                                      "prev_amax", "steps_used", "converged_blocks", "tokens_out",
-                                                     "commit_steps_out")} | {
+                                                     "commit_steps_out", "stable_run")} | {
             "tick": self.tick_no}
 
     # ----------------------------------------------------------------- tick
@@ -223,8 +226,10 @@ class OracleSampler:
         H, y, amax = st["H"], st["y"], st["amax"]
         mean_H = float(np.mean(H))
         rec.mean_H[i] = mean_H
-        # early stop: confident (mean entropy below the threshold) and stable (argmax unchanged, stability 1)
-        converged = s >= 1 and mean_H < cfg.confidence and bool(np.all(amax == self.prev_amax[c]))
+        # early stop: confident (mean entropy below the threshold) and stable (the argmax canvas
+        # unchanged from the previous step's for `stability` steps in a row; none before step 1)
+        run = int(self.stable_run[c]) + 1 if (s >= 1 and bool(np.all(amax == self.prev_amax[c]))) else 0
+        converged = run >= cfg.stability and mean_H < cfg.confidence
         if s >= 1 and (abs(mean_H - cfg.confidence) < cfg.margin_H or
                        (mean_H < cfg.confidence + cfg.margin_H and bool(np.any(rec.flag_amax[i * L:(i + 1) * L])))):
             rec.flag_canvas[i] = True
@@ -264,6 +269,7 @@ class OracleSampler:
                 if not self.committed[c, p]:
                     self.x[c, p] = uniform_token(draw_u32(cfg.seed(c), PURPOSE_RENOISE, b, s, int(p)), V)
             self.prev_amax[c] = amax
+            self.stable_run[c] = run
             self.step_no[c] = s + 1
         else:
             # finish the block: every remaining position takes its sample
@@ -276,6 +282,7 @@ class OracleSampler:
             self.commit_steps_out[c, b] = self.commit_step[c]
             self.steps_used[c] += s + 1
             self.converged_blocks[c] += int(converged)
+            self.stable_run[c] = 0  # the count restarts with each block (and stays 0 once done)
             if b + 1 < cfg.gen_blocks:
                 self._init_canvas(c, b + 1)
             else:

@@ -58,6 +58,7 @@ class Case:
     rms_eps: float = 1e-6
     mode: str = "freeze"  # commit mode: "freeze" (DG_FREEZE) or "reaccept" (DG_REACCEPT)
     softcap: float = 0.0  # final logit softcap c (0 = off)
+    stability: int = 1  # steps in a row with an unchanged argmax canvas needed for an early stop
 
     def oracle_cfg(self) -> OracleConfig:
         return OracleConfig(vocab=self.vocab, hidden=self.hidden, canvas_len=self.canvas_len,
@@ -66,7 +67,8 @@ class Case:
                             confidence=f32(self.conf), rms_eps=f32(self.rms_eps),
                             seeds=list(self.seeds) if self.seeds else list(range(self.n_canvases)),
                             admit_tick=list(self.admit) if self.admit else None,
-                            max_active=self.max_active or None, mode=self.mode, softcap=f32(self.softcap))
+                            max_active=self.max_active or None, mode=self.mode, softcap=f32(self.softcap),
+                            stability=self.stability)
 
     def gpu_cfg(self):
         import uniform_state_discrete_gb300 as dg
@@ -75,6 +77,7 @@ class Case:
                               t_max=self.t_max, entropy_bound=self.bound, confidence=self.conf, rms_eps=self.rms_eps,
                               max_active=self.max_active,
                               mode=dg.DG_REACCEPT if self.mode == "reaccept" else dg.DG_FREEZE, softcap=self.softcap,
+                              stability=self.stability,
                               seeds=list(self.seeds) if self.seeds else list(range(self.n_canvases)),
                               admit_tick=list(self.admit) if self.admit else None)
 
@@ -106,6 +109,7 @@ def oracle_state_to_gpu(o: OracleSampler, case: Case) -> dict:
     slots["n_committed"] = o.committed.sum(axis=1)
     slots["steps_used"] = o.steps_used
     slots["converged_blocks"] = o.converged_blocks
+    slots["stable_steps"] = o.stable_run
     return {"tick": o.tick_no, "slots": slots, "tokens": o.x.astype(np.int32),
             "committed": o.committed.astype(np.uint8), "commit_step": o.commit_step.astype(np.int16),
             "prev_argmax": o.prev_amax.astype(np.int32), "tokens_out": o.tokens_out.astype(np.int32),
@@ -212,7 +216,8 @@ def compare_tick(s, o: OracleSampler, rec, case: Case, rep: Report):
             gs, os_ = gst["slots"][c], o
             for fld, ov in (("state", o.status[c]), ("block", o.block[c]), ("step", o.step_no[c]),
                             ("steps_used", o.steps_used[c]), ("converged_blocks", o.converged_blocks[c]),
-                            ("n_committed", o.committed[c].sum()), ("n_remasked", rec.n_remasked[i])):
+                            ("n_committed", o.committed[c].sum()), ("n_remasked", rec.n_remasked[i]),
+                            ("stable_steps", o.stable_run[c])):
                 if int(gs[fld]) != int(ov):
                     rep.errors.append(f"tick {rec.tick} canvas {c}: slot {fld} {int(gs[fld])} != oracle {int(ov)}")
             if rec.final[i]:

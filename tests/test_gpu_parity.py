@@ -100,6 +100,15 @@ def test_low_entropy_multi_commit_and_early_stop():
     _assert_report(rep, "low-entropy")
 
 
+@pytest.mark.parametrize("stability", [2, 3])
+def test_early_stop_with_longer_stability(stability):
+    """Early stop after `stability` steps in a row with an unchanged argmax canvas: the stable-step
+    counter, the convergence and the block hand-over against the oracle, teacher-forced."""
+    case = Case(vocab=512, hidden=256, canvas_len=32, steps=24, bound=1.0, sigma=0.1, sigma_w=0.1, w_seed=2,
+                seeds=(9,), gen_blocks=3, stability=stability)
+    _assert_report(teacher_forced(case), f"stability {stability}")
+
+
 def test_hot_schedule_noise_driven_regime():
     """t 1.5 -> 0.1 with large hidden noise: sampling ties get exercised."""
     case = Case(vocab=2048, hidden=256, canvas_len=64, steps=12, t_max=1.5, t_min=0.1, sigma=2.0, bound=0.01,

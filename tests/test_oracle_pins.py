@@ -545,3 +545,35 @@ def test_commit_heatmap_of_finished_blocks():
                 assert np.array_equal(np.bincount(hm, minlength=N), [1] * (N - 1) + [L - N + 1])
             else:
                 assert np.all(hm == N - 1)
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_early_stop_needs_k_unchanged_argmax_canvases(k):
+    """"the argmax canvas has remained unchanged for stability_threshold previous canvases"
+    ("Check for early stopping"): with a constant argmax and entropies ~0 the block stops at the
+    first step s with s >= k, i.e. after k + 1 equal argmax canvases."""
+    V, d, L = 64, 128, 16
+    cfg = oracle.OracleConfig(vocab=V, hidden=d, canvas_len=L, num_inference_steps=48, seeds=[3], stability=k)
+    W = synth.wvocab(5, V, d, sigma_w=1.0)
+    Wf = synth.bf16_to_f32(W)
+    fn = lambda canv, blocks, steps, tok: np.concatenate([Wf[:L] for _ in canv])  # r_p = W[p]
+    s = oracle.OracleSampler(cfg, W)
+    recs = []
+    s.run(fn, on_tick=recs.append)
+    assert len(recs) == k + 1 and recs[-1].converged[0] and not any(r.converged[0] for r in recs[:-1])
+    assert s.steps_used[0] == k + 1 and s.converged_blocks[0] == 1
+
+
+def test_early_stop_run_restarts_when_the_argmax_moves():
+    """Stability 2: the argmax canvas moves at step 2, so the run of unchanged canvases restarts and
+    the block stops at step 4 (canvases 2, 3, 4 equal) instead of step 2."""
+    V, d, L = 64, 128, 8
+    cfg = oracle.OracleConfig(vocab=V, hidden=d, canvas_len=L, num_inference_steps=48, seeds=[3], stability=2)
+    W = synth.wvocab(5, V, d, sigma_w=1.0)
+    Wf = synth.bf16_to_f32(W)
+    fn = lambda canv, blocks, steps, tok: np.concatenate([Wf[np.arange(L) + (8 if steps[0] >= 2 else 0)]
+                                                          for _ in canv])
+    s = oracle.OracleSampler(cfg, W)
+    recs = []
+    s.run(fn, on_tick=recs.append)
+    assert [int(r.converged[0]) for r in recs] == [0, 0, 0, 0, 1]

@@ -42,13 +42,15 @@ class dg_slot(ctypes.Structure):
     _fields_ = [("seed", ctypes.c_uint64), ("admit_tick", ctypes.c_int32), ("state", ctypes.c_int32),
                 ("block", ctypes.c_int32), ("step", ctypes.c_int32), ("n_committed", ctypes.c_int32),
                 ("steps_used", ctypes.c_int32), ("converged_blocks", ctypes.c_int32),
-                ("temperature", ctypes.c_float), ("mean_entropy", ctypes.c_float), ("n_remasked", ctypes.c_int32)]
+                ("temperature", ctypes.c_float), ("mean_entropy", ctypes.c_float), ("n_remasked", ctypes.c_int32),
+                ("stable_steps", ctypes.c_int32)]
 
 
 SLOT_DTYPE = np.dtype([("seed", "u8"), ("admit_tick", "i4"), ("state", "i4"), ("block", "i4"), ("step", "i4"),
                        ("n_committed", "i4"), ("steps_used", "i4"), ("converged_blocks", "i4"),
-                       ("temperature", "f4"), ("mean_entropy", "f4"), ("n_remasked", "i4")], align=True)
-assert SLOT_DTYPE.itemsize == ctypes.sizeof(dg_slot) == 48
+                       ("temperature", "f4"), ("mean_entropy", "f4"), ("n_remasked", "i4"),
+                       ("stable_steps", "i4")], align=True)
+assert SLOT_DTYPE.itemsize == ctypes.sizeof(dg_slot) == 56
 
 
 class dg_state(ctypes.Structure):

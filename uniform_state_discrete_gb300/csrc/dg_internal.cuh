@@ -86,6 +86,7 @@ struct Dev {
   float t_min, t_max, bound, conf, eps;
   int32_t n_vtiles, tiles_per_chunk, n_chunks, n_sub, rows_cap, max_active;
   bool reaccept;        // DG_REACCEPT: every step re-sorts all positions (see dg_mode)
+  int32_t stability;    // early stop needs this many consecutive steps with an unchanged argmax canvas
   float softcap;        // final logit softcap c (0 = off): z -> c tanh(z / c) before the temperature
   float inv_softcap;    // 1 / c (0 when off)
   int32_t hold_slabs;   // test hook (dg_debug_hold_slabs): the LM head does not count finished units

@@ -95,7 +95,8 @@ bool validate(const dg_config* c, char* why) {
 // Returns 1 ok, 0 invalid, -1 unsupported.
 int make_layout(const dg_config* c, Layout* L, char* why) {
   if (!validate(c, why)) return 0;
-  if (c->stability != 1) return set_err(why, "only stability = 1 is implemented (got %d)", c->stability), -1;
+  if (c->stability < 1 || c->stability > 1024)
+    return set_err(why, "stability must be in [1, 1024] (got %d)", c->stability), 0;
   if (c->mode != DG_FREEZE && c->mode != DG_REACCEPT)
     return set_err(why, "mode must be DG_FREEZE or DG_REACCEPT (got %d)", c->mode), 0;
   const size_t B = c->n_canvases, Lc = c->canvas_len, d = c->hidden, G = c->gen_blocks;
@@ -330,6 +331,7 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.t_max = cfg->t_max;
   dv.bound = cfg->entropy_bound;
   dv.reaccept = cfg->mode == DG_REACCEPT;
+  dv.stability = cfg->stability;
   dv.conf = cfg->confidence;
   dv.eps = cfg->rms_eps;
   dv.softcap = cfg->softcap;

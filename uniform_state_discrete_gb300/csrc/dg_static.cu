@@ -75,6 +75,7 @@ __global__ void k_static_prep(unsigned char* base, uint64_t seed, int block, int
   sl->temperature = T;
   sl->mean_entropy = 0.f;
   sl->n_remasked = 0;
+  sl->stable_steps = 0;
   pl->tick = 0;
   pl->n_active = 1;
   pl->commits = 0u;

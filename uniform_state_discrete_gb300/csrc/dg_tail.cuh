@@ -129,6 +129,7 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
           s.step = 0;
           s.n_committed = 0;
           s.n_remasked = 0;
+          s.stable_steps = 0;
           s.temperature = dv.temps[0];
         }
         ++running;
@@ -174,7 +175,8 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
 }
 
 // The commit step of canvas c for this tick:
-//  (i)   early stop: s >= 1, mean_p H < confidence and argmax == previous argmax at every p;
+//  (i)   early stop: mean_p H < confidence and the argmax canvas equal to the previous one
+//        at every p for the last `stability` steps in a row (s >= stability);
 //  (ii)  otherwise order the open positions by (H, p) and accept the prefix whose
 //        exclusive entropy sums stay <= entropy_bound; accepted positions take their sample;
 //  (iii) on early stop or at s = N-1 every open position takes its sample and the
@@ -198,6 +200,7 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
   sl.n_committed = __ldcg(&dv.slots[c].n_committed);
   sl.steps_used = __ldcg(&dv.slots[c].steps_used);
   sl.converged_blocks = __ldcg(&dv.slots[c].converged_blocks);
+  sl.stable_steps = __ldcg(&dv.slots[c].stable_steps);
   const int s = sl.step, b = sl.block;
   const size_t base = (size_t)c * L;
   const float bound = dv.bound;
@@ -267,7 +270,9 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
   }
   const float mean_H = tot_h / (float)L;
   const int count_le = (int)tot_le;
-  const bool converged = (s >= 1) && (mean_H < dv.conf) && stable;
+  // steps in a row whose argmax canvas equalled the one before (none before step 1)
+  const int run = (s >= 1 && stable) ? sl.stable_steps + 1 : 0;
+  const bool converged = run >= dv.stability && mean_H < dv.conf;
   const bool final_step = converged || (s == dv.N - 1);
 
   if (!final_step) {
@@ -346,6 +351,7 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
       so.temperature = t_next;
       so.n_committed = dv.reaccept ? n_acc : sl.n_committed + n_acc;
       so.n_remasked = sc->remasked;
+      so.stable_steps = run;
       so.mean_entropy = mean_H;
     }
     g.sync();
@@ -379,6 +385,7 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
       so.converged_blocks = sl.converged_blocks + (converged ? 1 : 0);
       so.mean_entropy = mean_H;
       so.n_remasked = 0;
+      so.stable_steps = 0;
       if (more) {
         so.block = b + 1;
         so.step = 0;
