@@ -327,8 +327,7 @@ def run_ours(args, wl, world, rank, local):
         torch.cuda.synchronize(dev)
         barrier(world)
         torch.cuda.synchronize(dev)
-        clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
-            os.path.join(ROOT, "gpurun_out")) else None)
+        clocks = ClockSampler(local, args.clocks_csv)
         clocks.start()
         time.sleep(0.3)
         # timed region: whole ticks only, so nothing separates the kernels of a tick.  The
@@ -491,6 +490,7 @@ def main():
                     help="commit mode: committed positions freeze (default), or every step re-accepts all positions")
     ap.add_argument("--softcap", type=float, default=0.0, help="final logit softcap c (0 = off, the workloads' setting)")
     ap.add_argument("--kernel-steps", type=int, default=200, help="ticks of the per-kernel timing pass")
+    ap.add_argument("--clocks-csv", default=None, help="also write the raw clock samples of the timed region here")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

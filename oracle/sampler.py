@@ -27,7 +27,7 @@ from all entropies each step and `torch.where(accepted, sample, randint)`
 rebuilds the whole canvas); the committed mask is then the latest step's
 accepted set and commit_step the last step a position was accepted.
 
-Readings where the pages are silent or disagree (each listed in the design doc):
+Readings where the pages are silent or disagree:
 by default committed positions stay frozen (ComfyUI-DiffusionGemma, "What it
 is": the lowest-entropy positions freeze into place) and only uncommitted
 positions enter the per-step sort; the prefix is exclusive and compared with <=; ties in
