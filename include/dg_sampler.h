@@ -30,8 +30,8 @@
  *     workspace of dg_workspace_size() bytes and keeps it alive until
  *     dg_destroy().  Device buffers passed in are borrowed, not owned.  A
  *     sampler holds two small page-locked host buffers of its own (the error
- *     latch read-back, made at creation, and the result staging of
- *     dg_denoise_step_host, made on its first call), freed by dg_destroy().
+ *     latch read-back and the result staging of dg_denoise_step_host), both
+ *     made by dg_sampler_create() and freed by dg_destroy().
  *   - Work is enqueued on the stream given to dg_sampler_create().  Calls
  *     marked "asynchronous" return before the GPU work ends; calls marked
  *     "synchronizing" wait for the stream.

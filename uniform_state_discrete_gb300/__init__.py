@@ -197,6 +197,9 @@ class Sampler:
                                    ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(h))
         _check(st)
         self.handle = h
+        # page-locked result buffers of step_host, allocated once here rather than in a step
+        self._host_out = (torch.empty((self.B, self.L), dtype=torch.int32).pin_memory(),
+                          torch.empty((self.B, self.L), dtype=torch.float32).pin_memory())
 
     # --------------------------------------------------------------- calls
     def dg_denoise_step(self, resid) -> int:
@@ -208,11 +211,7 @@ class Sampler:
     def step_host(self, resid_host: np.ndarray, want_canvas=True, want_entropy=True):
         """dg_denoise_step_host; the results land in page-locked buffers kept by the sampler and are
         returned as copies.  Pass a page-locked ``resid_host`` for an asynchronous input copy."""
-        import torch
         assert resid_host.dtype == np.float32 and resid_host.flags["C_CONTIGUOUS"]
-        if getattr(self, "_host_out", None) is None:
-            self._host_out = (torch.empty((self.B, self.L), dtype=torch.int32).pin_memory(),
-                              torch.empty((self.B, self.L), dtype=torch.float32).pin_memory())
         canvas, ent = self._host_out
         _check(lib.dg_denoise_step_host(self.handle, ctypes.c_void_p(resid_host.ctypes.data),
                                         ctypes.c_void_p(canvas.data_ptr()) if want_canvas else None,

@@ -375,6 +375,17 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   }
   ce = cudaHostAlloc(reinterpret_cast<void**>(&s->pl_host), sizeof(dg::Plan), cudaHostAllocDefault);
   if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "allocate the pinned error latch copy"));
+  // the host step's result staging: plan, canvas and entropies lie next to each
+  // other in the workspace, and one copy into this buffer brings back all three.
+  // Allocated here, so no host step pays for a page-locked allocation.
+  {
+    const uint8_t* p0 = reinterpret_cast<const uint8_t*>(dv.plan);
+    s->stage_x = (size_t)(reinterpret_cast<const uint8_t*>(dv.x) - p0);
+    s->stage_H = (size_t)(reinterpret_cast<const uint8_t*>(dv.H) - p0);
+    s->stage_bytes = s->stage_H + (size_t)B * cfg->canvas_len * 4;
+    ce = cudaHostAlloc(reinterpret_cast<void**>(&s->stage_host), s->stage_bytes, cudaHostAllocDefault);
+    if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "allocate the pinned result staging"));
+  }
   ce = cudaMemsetAsync(workspace, 0, L.total, s->stream);
   if (ce == cudaSuccess)
     ce = cudaMemcpyAsync(dv.slots, slots.data(), sizeof(dg_slot) * B, cudaMemcpyHostToDevice, s->stream);
@@ -416,16 +427,7 @@ dg_status dg_denoise_step_host(dg_sampler* s, const float* resid_host, int32_t* 
   dg_status st = tick(s, resid);
   if (st != DG_OK) return st;
   if (!canvas_host && !entropy_host) return check_device_error(s);
-  // plan, canvas and entropies lie next to each other in the workspace: one copy
-  // into a pinned staging buffer brings back all three
-  if (!s->stage_host) {
-    const uint8_t* p0 = reinterpret_cast<const uint8_t*>(s->dv.plan);
-    s->stage_x = (size_t)(reinterpret_cast<const uint8_t*>(s->dv.x) - p0);
-    s->stage_H = (size_t)(reinterpret_cast<const uint8_t*>(s->dv.H) - p0);
-    s->stage_bytes = s->stage_H + BL * 4;
-    DG_CUDA(s->err, cudaHostAlloc(reinterpret_cast<void**>(&s->stage_host), s->stage_bytes, cudaHostAllocDefault),
-            "allocate the pinned result staging");
-  }
+  // plan, canvas and entropies in one copy into the pinned staging buffer
   DG_CUDA(s->err, cudaMemcpyAsync(s->stage_host, s->dv.plan, s->stage_bytes, cudaMemcpyDeviceToHost, s->stream),
           "copy results");
   DG_CUDA(s->err, cudaStreamSynchronize(s->stream), "synchronize");
