@@ -92,6 +92,25 @@ def test_single_position_canvases_capacity_limited():
     _assert_report(teacher_forced(case), "L1")
 
 
+@pytest.mark.parametrize("mode", ["freeze", "reaccept"])
+def test_maximum_canvas_length_sorts_whole_canvas(mode):
+    """The largest canvas the ABI takes (1024 positions) with an entropy budget far above every
+    single entropy: all 1024 positions are candidates, so the commit sorts the whole canvas
+    (bitonic, 1024 keys) and walks ~33 acceptances a step; the last step commits the rest."""
+    case = Case(vocab=512, hidden=128, canvas_len=1024, steps=6, bound=200.0, sigma=0.02, mode=mode)
+    _assert_report(teacher_forced(case), f"L1024-{mode}")
+
+
+def test_maximum_step_count():
+    """The largest num_inference_steps the ABI takes (1024) on a 1024-position canvas: one commit per
+    step (every entropy is far above the budget), the temperature table's last entries, and the final
+    step committing the last position; every 64th tick and the last ones are checked."""
+    case = Case(vocab=64, hidden=64, canvas_len=1024, steps=1024, bound=0.1)
+    rep = teacher_forced(case, check_every=64)
+    _assert_report(rep, "N1024")
+    assert rep.ticks >= 16
+
+
 def test_low_entropy_multi_commit_and_early_stop():
     """Peaked distributions: several positions fit the bound per step and the early-stop test fires."""
     case = Case(vocab=512, hidden=256, canvas_len=32, steps=24, bound=1.0, sigma=0.1, sigma_w=0.1, w_seed=2,
