@@ -101,6 +101,15 @@ def test_maximum_canvas_length_sorts_whole_canvas(mode):
     _assert_report(teacher_forced(case), f"L1024-{mode}")
 
 
+@pytest.mark.parametrize("vocab,canvas_len", [(2, 16), (3, 16), (2, 256)], ids=["V2", "V3", "V2-pair"])
+def test_smallest_vocabularies(vocab, canvas_len):
+    """The smallest vocabularies (V = 2 is the ABI's minimum): one vocabulary chunk holding a single
+    ragged tile of 2 or 3 valid columns, on the single-CTA and the SM-pair LM head; entropies
+    bounded by ln V, and a budget of 1 nat, so two positions commit a step at V = 2, one at V = 3."""
+    case = Case(vocab=vocab, hidden=64, canvas_len=canvas_len, steps=4, bound=1.0)
+    _assert_report(teacher_forced(case), f"V{vocab}-L{canvas_len}")
+
+
 def test_maximum_step_count():
     """The largest num_inference_steps the ABI takes (1024) on a 1024-position canvas: one commit per
     step (every entropy is far above the budget), the temperature table's last entries, and the final
