@@ -79,8 +79,10 @@ def test_static_entry_matches_sampler_on_two_calls(rows, vocab, hidden, norm_see
         dg.dg_lmhead_stats_static(resid, W, nw, eps, T, seed, block, step, H, lz, y, am, stream=s.stream)
         torch.cuda.synchronize(dev)
         assert torch.cuda.memory_allocated(dev) <= torch_bytes
-        # nothing allocated outside torch either (the first call's static array is part of the module)
-        assert torch.cuda.mem_get_info(dev)[0] >= free_before - (4 << 20)
+        # nothing allocated outside torch either: the first call may bring in the module's static
+        # scratch (2.7 MB, in 2 MB pages), the second call nothing at all
+        slack = (4 << 20) if call == 0 else (1 << 20)
+        assert torch.cuda.mem_get_info(dev)[0] >= free_before - slack
         ref_H, ref_lz = s.entropy()[0].cpu().numpy(), s.logz()[0].cpu().numpy()
         ref_y, ref_am = s.sample()[0].cpu().numpy(), s.argmax()[0].cpu().numpy()
         got_H, got_lz, got_y, got_am = H.cpu().numpy(), lz.cpu().numpy(), y.cpu().numpy(), am.cpu().numpy()
