@@ -110,6 +110,32 @@ def test_smallest_vocabularies(vocab, canvas_len):
     _assert_report(teacher_forced(case), f"V{vocab}-L{canvas_len}")
 
 
+def test_step_after_every_canvas_finished_is_a_state_error():
+    """One canvas, one block, two steps: the third tick is refused with DG_ERR_STATE (the host can
+    tell that every canvas has finished), through both step entry points, and the finished block's
+    tokens stay readable."""
+    import torch
+    import uniform_state_discrete_gb300 as dg
+    case = Case(vocab=512, hidden=64, canvas_len=16, steps=2)
+    W = weights(case)
+    dev = torch.device("cuda:0")
+    s = dg.Sampler(case.gpu_cfg(), torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16))
+    resid = torch.zeros(1, case.canvas_len, case.hidden, device=dev)
+    s.step(resid)
+    s.step(resid)
+    with pytest.raises(dg.DGError) as e:
+        s.step(resid)
+    assert e.value.status == dg.DG_ERR_STATE
+    with pytest.raises(dg.DGError) as e:
+        s.step_host(np.zeros((1, case.canvas_len, case.hidden), np.float32))
+    assert e.value.status == dg.DG_ERR_STATE
+    info = s.sync_info()
+    assert int(info["state"][0]) == dg.DONE
+    toks = s.get_state()["tokens_out"][0, 0]
+    assert ((toks >= 0) & (toks < case.vocab)).all()
+    s.close()
+
+
 def test_maximum_step_count():
     """The largest num_inference_steps the ABI takes (1024) on a 1024-position canvas: one commit per
     step (every entropy is far above the budget), the temperature table's last entries, and the final
