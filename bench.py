@@ -90,6 +90,36 @@ def stored_traffic(workload: str):
         return None
 
 
+def vocab_chunks(V: int) -> int:
+    """Vocabulary chunks of the LM head: 256-column tiles, at most 76 chunks, the library's layout."""
+    tiles = math.ceil(V / 256)
+    per_chunk = math.ceil(tiles / min(tiles, 76))
+    return math.ceil(tiles / per_chunk)
+
+
+def lmhead_roofline(V: int, d: int, P: int, pair: bool, seconds: float, peaks: dict):
+    """Roofline of one LM-head launch over P positions taking `seconds`.
+
+    Algorithmic bytes: W once (V d bf16), the kernel's input rows (the fp32 residual and the norm
+    weights when the SM-pair kernel forms the RMSNorm rows itself, else the bf16 rows h) and the
+    32-byte partial records it writes (one per position and vocabulary chunk).  Algorithmic flops:
+    2 P V d.  The bound is whichever of the two takes longer at its peak.  Returns (roof, t_hbm, t_tc).
+    """
+    alg_bytes = V * d * 2 + (P * d * 4 + d * 4 if pair else P * d * 2) + P * vocab_chunks(V) * 32
+    alg_flops = 2.0 * P * V * d
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg_flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": alg_bytes / seconds / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": alg_flops / seconds / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["algorithmic_bytes_per_launch"] = alg_bytes
+    roof["algorithmic_flops_per_launch"] = alg_flops
+    return roof, t_hbm, t_tc
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -383,25 +413,11 @@ def run_ours(args, wl, world, rank, local):
     pair = B * L >= 256
     peaks = measured_peaks()
     k2_s = float((per_kernel[:, 0] + per_kernel[:, 1]).mean() if pair else per_kernel[:, 1].mean()) / 1e3
-    lay_chunks = math.ceil(math.ceil(V / 256) / math.ceil(math.ceil(V / 256) / min(math.ceil(V / 256), 76)))
-    n_sub = lay_chunks  # partial records per position: one per vocabulary chunk
-    P = positions_per_tick
-    # W once, the kernel's input rows (fp32 residual for the fused RMSNorm, else bf16 h), partial records
-    alg_bytes = V * d * 2 + (P * d * 4 + d * 4 if pair else P * d * 2) + P * n_sub * 32
-    alg_flops = 2.0 * P * V * d
-    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
-    t_tc = alg_flops / (peaks["bf16_tflops"] * 1e12)
-    if t_hbm >= t_tc:
-        roof = {"bound": "hbm", "achieved": alg_bytes / k2_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": alg_flops / k2_s / 1e12, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof, t_hbm, t_tc = lmhead_roofline(V, d, positions_per_tick, pair, k2_s, peaks)
+    alg_bytes, alg_flops = roof["algorithmic_bytes_per_launch"], roof["algorithmic_flops_per_launch"]
     roof["traffic"] = stored_traffic(args.workload)
     roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "fallback"
     roof["kernel"] = "k_lmhead_pair" if pair else "k_lmhead"  # the sampler's choice for these sizes
-    roof["algorithmic_bytes_per_launch"] = alg_bytes
-    roof["algorithmic_flops_per_launch"] = alg_flops
     roof["kernel_ms_mean"] = k2_s * 1e3
     roof["tensor_frac"] = alg_flops / k2_s / 1e12 / peaks["bf16_tflops"]
     roof["tensor_frac_sustained"] = alg_flops / k2_s / 1e12 / peaks["bf16_tflops_sustained"]
