@@ -36,6 +36,10 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
+# OpenMP worker threads of the host-side input generator and the CPU oracle sleep as soon as a
+# parallel region ends, instead of spinning on the cores the timed host steps run on (set before
+# any OpenMP runtime loads; an explicit setting in the environment wins)
+os.environ.setdefault("OMP_WAIT_POLICY", "PASSIVE")
 
 import numpy as np  # noqa: E402
 
