@@ -47,22 +47,34 @@ METRIC = "canvas positions denoised/sec (LM head+entropy+commit); % of bf16/HBM 
 UNIT = "positions/s"
 L2_FLUSH_BYTES = 256 << 20
 
-# The workloads of the pages' sampler at the sizes this benchmark knows.  The
-# default is the single-canvas V=32768 case; the others are selectable.
+# The workloads of the pages' sampler at the sizes this benchmark knows.  The default is the
+# largest single-GPU configuration (the stress workload); the others are selectable.  Knobs not
+# given take the pages' defaults: entropy_bound 0.1 nats, t 0.8 -> 0.4, hidden noise sigma 0.5.
 WORKLOADS = {
+    "stress64x4_v262k": dict(vocab=262144, hidden=2816, canvas_len=256, n_canvases=64, gen_blocks=4, steps=48,
+                             bound=0.1, t_max=0.8, t_min=0.4, sigma=2.0,
+                             text="stress: 64 canvases x gen_length 4 blocks x 256 positions (earlier blocks "
+                                  "committed and frozen), V=262144, d=2816, bf16 W_vocab N(0,0.02^2), 48 steps per "
+                                  "block; sweep point entropy_bound 0.1, t 0.8->0.4, hidden noise sigma 2.0"),
+    "batched16_stagger_v262k": dict(vocab=262144, hidden=2816, canvas_len=256, n_canvases=16, gen_blocks=1, steps=48,
+                                    admit=tuple(12 * (c // 4) for c in range(16)),
+                                    text="batched: 16 canvases x 256 positions, V=262144, d=2816, seeds 0..15 "
+                                         "admitted at ticks 0,12,24,36 (four per offset), 48 steps, t 0.8->0.4, "
+                                         "entropy_bound 0.1, confidence 0.005"),
+    "canvas256_v262k": dict(vocab=262144, hidden=2816, canvas_len=256, n_canvases=1, steps=48,
+                            text="1 canvas x 256 positions, V=262144, d=2816 (model-scale LM head), bf16 W_vocab "
+                                 "N(0,0.02^2), hidden W[x_p]+N(0,0.5^2), 48 steps, t 0.8->0.4, entropy_bound 0.1, "
+                                 "confidence 0.005"),
     "canvas256_v32k": dict(vocab=32768, hidden=1024, canvas_len=256, n_canvases=1, steps=48,
                            text="1 canvas x 256 positions, V=32768, d=1024, bf16 W_vocab N(0,0.02^2), hidden "
                                 "W[x_p]+N(0,0.5^2), 48 steps, T 0.8->0.4, entropy_bound 0.1, confidence 0.005"),
-    "canvas256_v262k": dict(vocab=262144, hidden=2816, canvas_len=256, n_canvases=1, steps=48,
-                            text="1 canvas x 256 positions, V=262144, d=2816 (model-scale LM head), same knobs"),
     "tiny": dict(vocab=2048, hidden=128, canvas_len=16, n_canvases=1, steps=8,
                  text="1 canvas x 16 positions, V=2048, d=128, 8 steps"),
-    # the batched configuration at steady state (all 16 canvases active; the staggered admission is
-    # a parity-test case): 4096 positions per tick, tensor-bound.  Its oracle tick takes minutes, so
-    # run it with --no-cpu-baseline.
+    # the batched configuration with every canvas active from the first tick (4096 positions a tick)
     "batched16_v262k": dict(vocab=262144, hidden=2816, canvas_len=256, n_canvases=16, steps=48,
                             text="16 canvases x 256 positions, V=262144, d=2816, per-canvas seeds, all active"),
 }
+DEFAULT_WORKLOAD = "stress64x4_v262k"
 SIGMA_HIDDEN = 0.5
 
 
@@ -150,7 +162,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                                          "--format=csv,noheader,nounits", "-lms", "25"], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
@@ -227,17 +239,53 @@ def barrier(world: int):
 
 
 # --------------------------------------------------------------------------- CPU oracle timing
+def wl_knob(wl: dict, name: str):
+    """A workload knob, or the pages' default (entropy_bound 0.1, t 0.8 -> 0.4, sigma 0.5, one block)."""
+    return wl.get(name, {"bound": 0.1, "t_max": 0.8, "t_min": 0.4, "sigma": SIGMA_HIDDEN, "gen_blocks": 1,
+                         "admit": None}[name])
+
+
+def oracle_cfg_for(wl: dict, n_canvases: int, seed_base: int):
+    import oracle
+    return oracle.OracleConfig(vocab=wl["vocab"], hidden=wl["hidden"], canvas_len=wl["canvas_len"],
+                               n_canvases=n_canvases, num_inference_steps=wl["steps"], gen_blocks=1 << 10,
+                               t_min=float(np.float32(wl_knob(wl, "t_min"))),
+                               t_max=float(np.float32(wl_knob(wl, "t_max"))),
+                               entropy_bound=float(np.float32(wl_knob(wl, "bound"))),
+                               seeds=[seed_base + c for c in range(n_canvases)], mode=wl.get("mode", "freeze"),
+                               softcap=float(wl.get("softcap", 0.0)))
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def oracle_positions_per_s(wl: dict, budget_s: float, seed_base: int, W16=None, max_ticks=None) -> dict:
-    """Time the CPU oracle, as it stands, on whole ticks of the workload until the budget is spent."""
+    """Time the CPU oracle, as it stands, on whole ticks of the workload until the budget is spent.
+
+    The oracle's work per position is the same whatever the batch, so a workload of more than one
+    canvas is timed on its first canvas alone and the rate is extrapolated to the whole batch."""
     import oracle
     import synth
     W16 = synth.wvocab(0, wl["vocab"], wl["hidden"]) if W16 is None else W16
-    cfg = oracle.OracleConfig(vocab=wl["vocab"], hidden=wl["hidden"], canvas_len=wl["canvas_len"],
-                              n_canvases=wl["n_canvases"], num_inference_steps=wl["steps"], gen_blocks=1 << 10,
-                              seeds=[seed_base + c for c in range(wl["n_canvases"])], mode=wl.get("mode", "freeze"),
-                              softcap=float(wl.get("softcap", 0.0)))
+    n_timed = 1 if wl["n_canvases"] > 1 else wl["n_canvases"]
+    cfg = oracle_cfg_for(wl, n_timed, seed_base)
     o = oracle.OracleSampler(cfg, W16)
-    fn = oracle.sampler.synth_resid_fn(cfg, W16, SIGMA_HIDDEN)
+    fn = oracle.sampler.synth_resid_fn(cfg, W16, wl_knob(wl, "sigma"))
     positions, busy, ticks = 0, 0.0, 0
     while (ticks == 0 or busy < budget_s) and (max_ticks is None or ticks < max_ticks):
         act = o.active()
@@ -247,9 +295,71 @@ def oracle_positions_per_s(wl: dict, budget_s: float, seed_base: int, W16=None, 
         busy += time.perf_counter() - t0
         positions += act.size * wl["canvas_len"]
         ticks += 1
+    what = (f"{ticks} whole oracle ticks ({positions} positions) of the workload from tick 0" if n_timed ==
+            wl["n_canvases"] else
+            f"{ticks} whole oracle ticks of canvas 0 alone ({positions} positions), extrapolated to the "
+            f"{wl['n_canvases']}-canvas batch (the oracle's work per position does not depend on the batch)")
     return {"value": positions / busy, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{ticks} whole oracle ticks ({positions} positions) of the workload from tick 0, "
-                      f"fp64, OpenMP + BLAS on all cores; input generation untimed", "seconds": busy}
+            "sample": f"{what}; fp64, OpenMP + BLAS on all cores; input generation untimed", "seconds": busy,
+            "extrapolated": n_timed != wl["n_canvases"]}
+
+
+def oracle_rows_per_s(wl: dict, n_rows: int, W16=None, seed: int = 0) -> float:
+    """Oracle positions/s on n_rows positions of the first tick of one canvas: RMSNorm, fp64 LM head,
+    softmax statistics, Gumbel sample and the entropy-bounded acceptance over those rows."""
+    import oracle
+    import synth
+    W16 = synth.wvocab(0, wl["vocab"], wl["hidden"]) if W16 is None else W16
+    cfg = oracle_cfg_for(wl, 1, seed)
+    o = oracle.OracleSampler(cfg, W16)
+    fn = oracle.sampler.synth_resid_fn(cfg, W16, wl_knob(wl, "sigma"))
+    act = o.active()
+    rows = np.arange(n_rows)
+    r = fn(act, o.block[act], o.step_no[act], o.x[act])[rows]
+    t0 = time.perf_counter()
+    h = oracle.rmsnorm_bf16(r, cfg.rms_eps)
+    z = oracle.softcap(oracle.logits(h, W16), cfg.softcap)
+    T = oracle.temperature(0, cfg.num_inference_steps, cfg.t_min, cfg.t_max)
+    st = oracle.stats(z, T, cfg.seed(0), 0, 0, rows)
+    oracle.sampler.entropy_bounded_accept(st["H"], range(n_rows), cfg.entropy_bound)
+    return n_rows / (time.perf_counter() - t0)
+
+
+def oracle_one_core(workload: str, n_rows: int) -> dict | None:
+    """The oracle on one host core (a child process pinned to one CPU, one OpenMP and BLAS thread)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-one-core", "--workload", workload,
+                              "--cpu-rows", str(n_rows)], capture_output=True, text=True, env=env, timeout=600)
+        return json.loads(out.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
+def cpu_one_core_main(args):
+    cpu = sorted(os.sched_getaffinity(0))[0]
+    os.sched_setaffinity(0, {cpu})
+    import synth
+    wl = WORKLOADS[args.workload]
+    W16 = synth.wvocab(0, wl["vocab"], wl["hidden"])
+    v = oracle_rows_per_s(wl, args.cpu_rows, W16=W16)
+    print(json.dumps({"value": v, "cores": 1, "rows": args.cpu_rows}), flush=True)
+
+
+def cpu_baseline(args, wl, W16) -> dict:
+    """cpu_baseline: the oracle on all host cores (whole ticks, extrapolated for a batch) and on one core
+    (a subset of one tick's positions), with the host CPU named."""
+    base = oracle_positions_per_s(wl, args.cpu_budget, 0, W16=W16)
+    # one core: about a tenth of the all-core budget, in positions of one tick
+    rows = int(max(1, min(wl["canvas_len"], base["value"] / max(1, base["cores"]) * args.cpu_budget / 10)))
+    one = oracle_one_core(args.workload, rows)
+    base["cpu_model"] = cpu_model()
+    if one is not None:
+        base["one_core"] = {"value": one["value"], "unit": UNIT, "cores": 1,
+                            "sample": f"{rows} positions of canvas 0's first tick (RMSNorm, fp64 LM head, softmax "
+                                      f"statistics, Gumbel sample, acceptance), one thread pinned to one CPU"}
+    return base
 
 
 def run_reference(args, wl, world, rank):
@@ -258,19 +368,14 @@ def run_reference(args, wl, world, rank):
     import oracle
     import synth
     W16 = synth.wvocab(0, wl["vocab"], wl["hidden"])
-    # each bench step is one oracle tick restricted to a bounded sample of the canvas positions,
+    # each bench step is one oracle tick of canvas 0 restricted to a bounded sample of its positions,
     # sized so the whole --steps/--warmup run stays within a few minutes
-    probe = oracle_positions_per_s(wl, 0.0, 0, W16=W16, max_ticks=1)
-    per_pos = 1.0 / probe["value"]
+    per_pos = 1.0 / oracle_rows_per_s(wl, 8, W16=W16)
     budget = 120.0
-    n_pos = wl["canvas_len"] * wl["n_canvases"]
-    sample = max(1, min(n_pos, int(budget / max(1, args.steps + args.warmup) / per_pos)))
-    cfg = oracle.OracleConfig(vocab=wl["vocab"], hidden=wl["hidden"], canvas_len=wl["canvas_len"],
-                              n_canvases=wl["n_canvases"], num_inference_steps=wl["steps"], gen_blocks=1 << 10,
-                              seeds=list(range(wl["n_canvases"])), mode=wl.get("mode", "freeze"),
-                              softcap=float(wl.get("softcap", 0.0)))
+    sample = max(1, min(wl["canvas_len"], int(budget / max(1, args.steps + args.warmup) / per_pos)))
+    cfg = oracle_cfg_for(wl, 1, 0)
     o = oracle.OracleSampler(cfg, W16)
-    fn = oracle.sampler.synth_resid_fn(cfg, W16, SIGMA_HIDDEN)
+    fn = oracle.sampler.synth_resid_fn(cfg, W16, wl_knob(wl, "sigma"))
     rows = np.arange(sample)
     busy = 0.0
     for k in range(args.warmup + args.steps):
@@ -294,13 +399,22 @@ def run_reference(args, wl, world, rank):
             "config": {"workload": args.workload, "description": wl["text"], "commit_mode": wl["mode"],
                        "softcap": wl["softcap"]},
             "cpu_baseline": {"kind": "oracle", "cores": oracle.threads(), "value": value, "unit": UNIT,
-                             "sample": f"each step: {sample} of {n_pos} positions of one tick (RMSNorm, fp64 LM head, "
-                                       f"softmax statistics, Gumbel sample, acceptance), oracle as it stands"},
+                             "cpu_model": cpu_model(),
+                             "sample": f"each step: {sample} of the {wl['canvas_len']} positions of one tick of "
+                                       f"canvas 0 (RMSNorm, fp64 LM head, softmax statistics, Gumbel sample, "
+                                       f"acceptance), oracle as it stands; the rate per position does not depend "
+                                       f"on the batch of {wl['n_canvases']} canvases"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # --------------------------------------------------------------------------- GPU arm
+def canvas_steps(info) -> int:
+    """Canvas-steps run so far: steps of finished blocks plus the steps of each running block."""
+    import uniform_state_discrete_gb300 as dg
+    return int(info["steps_used"].sum()) + int(info["step"][info["state"] == dg.ACTIVE].sum())
+
+
 def run_ours(args, wl, world, rank, local):
     import torch
     import synth
@@ -314,13 +428,19 @@ def run_ours(args, wl, world, rank, local):
     stream = torch.cuda.Stream(dev)  # a capturable (non-default) stream owns the sampler's work
 
     V, d, L, B, N = wl["vocab"], wl["hidden"], wl["canvas_len"], wl["n_canvases"], wl["steps"]
+    sigma = wl_knob(wl, "sigma")
     W16 = synth.wvocab(0, V, d)
     w_dev = torch.from_numpy(W16.view(np.int16)).to(dev).view(torch.bfloat16)
     torch.cuda.synchronize(dev)
+    # every canvas keeps running blocks until the bench ends (a block is 48 steps whatever its index;
+    # the workload's own gen_length is the lower bound)
     total_ticks = args.warmup + args.steps + args.kernel_steps + args.warmup + args.e2e_steps + 2
-    blocks = total_ticks // N + 2
+    admit = wl_knob(wl, "admit")
+    blocks = max(wl_knob(wl, "gen_blocks"), (total_ticks + (max(admit) if admit else 0)) // N + 2)
     seeds = replica_seeds(rank, B)
     cfg = dg.make_config(V, d, L, n_canvases=B, gen_blocks=blocks, num_inference_steps=N, seeds=seeds,
+                         t_min=wl_knob(wl, "t_min"), t_max=wl_knob(wl, "t_max"), entropy_bound=wl_knob(wl, "bound"),
+                         admit_tick=list(admit) if admit else None,
                          mode=dg.DG_REACCEPT if wl.get("mode") == "reaccept" else dg.DG_FREEZE,
                          softcap=float(wl.get("softcap", 0.0)))
     s = dg.Sampler(cfg, w_dev, stream=stream)
@@ -330,7 +450,7 @@ def run_ours(args, wl, world, rank, local):
     canvas_ptr = s.canvas().data_ptr()
 
     def make_resid():
-        synth.resid_device(w_dev.data_ptr(), canvas_ptr, slots_ptr, B, L, V, d, SIGMA_HIDDEN, resid.data_ptr(),
+        synth.resid_device(w_dev.data_ptr(), canvas_ptr, slots_ptr, B, L, V, d, sigma, resid.data_ptr(),
                            stream.cuda_stream)
 
     def flush_l2():
@@ -359,6 +479,7 @@ def run_ours(args, wl, world, rank, local):
             s.step(resid)
         graph = capture(False) if args.graph else None
         torch.cuda.synchronize(dev)
+        cs0 = canvas_steps(s.sync_info())
         barrier(world)
         torch.cuda.synchronize(dev)
         clocks = ClockSampler(local, args.clocks_csv)
@@ -389,6 +510,7 @@ def run_ours(args, wl, world, rank, local):
         barrier(world)
         torch.cuda.synchronize(dev)
         clk = clocks.stop()
+        cs1 = canvas_steps(s.sync_info())
         # per-kernel pass: the same ticks with events between the three kernels (which
         # serialise them); the LM-head kernel's mean is the roofline's launch duration
         kgraph = capture(True) if args.graph else None
@@ -406,53 +528,66 @@ def run_ours(args, wl, world, rank, local):
             per_kernel[k] = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
         s.set_timing_events(None)
     info = s.sync_info()  # also surfaces a latched device fault
+    cs2 = canvas_steps(info)
     device_s = float(tick_ms.sum()) / 1e3
-    positions_per_tick = B * L
+    # positions denoised in the timed ticks, counted from the sampler's own step counters
+    positions_timed = (cs1 - cs0) * L
     max_s = reduce_max(device_s, world)
-    value = whole_job_rate(positions_per_tick, args.steps, world, max_s)
+    value = world * positions_timed / max_s
+    positions_per_tick = positions_timed / args.steps
+    kernel_positions = (cs2 - cs1) * L / max(1, args.kernel_steps)
 
     # roofline of the LM-head kernel (K2).  On SM pairs (256 positions or more, the
     # sampler's choice) it also forms the RMSNorm rows, and no RMSNorm kernel runs:
     # the first event interval is then empty and is counted with K2.
-    pair = B * L >= 256
+    pair = B * L >= 256  # the sampler's rule: SM pairs once a tick can hold 256 rows
     peaks = measured_peaks()
     k2_s = float((per_kernel[:, 0] + per_kernel[:, 1]).mean() if pair else per_kernel[:, 1].mean()) / 1e3
-    roof, t_hbm, t_tc = lmhead_roofline(V, d, positions_per_tick, pair, k2_s, peaks)
+    roof, t_hbm, t_tc = lmhead_roofline(V, d, int(round(kernel_positions)), pair, k2_s, peaks)
     alg_bytes, alg_flops = roof["algorithmic_bytes_per_launch"], roof["algorithmic_flops_per_launch"]
+    roof["positions_per_launch"] = kernel_positions
     roof["traffic"] = stored_traffic(args.workload)
     roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "fallback"
     roof["kernel"] = "k_lmhead_pair" if pair else "k_lmhead"  # the sampler's choice for these sizes
     roof["kernel_ms_mean"] = k2_s * 1e3
     roof["tensor_frac"] = alg_flops / k2_s / 1e12 / peaks["bf16_tflops"]
     roof["tensor_frac_sustained"] = alg_flops / k2_s / 1e12 / peaks["bf16_tflops_sustained"]
+    roof["hbm_frac"] = alg_bytes / k2_s / 1e9 / peaks["hbm_gbs"]
     roof["hbm_frac_of_nominal_7_9_tbs"] = alg_bytes / k2_s / 7.9e12
-    roof["step_roofline_frac"] = max(t_hbm, t_tc) / (device_s / args.steps)
+    # the whole tick against the LM head's roofline at this tick's mean positions
+    t_roof_tick = max(2.0 * positions_per_tick * V * d / (peaks["bf16_tflops"] * 1e12),
+                      (V * d * 2 + positions_per_tick * d * 4) / (peaks["hbm_gbs"] * 1e9))
+    roof["step_roofline_frac"] = t_roof_tick / (device_s / args.steps)
 
     # e2e through the host-buffer entry point, after the same number of untimed warm-up steps
     e2e_steps = min(args.steps, args.e2e_steps)
     host_resid = torch.empty(B, L, d, dtype=torch.float32).pin_memory()
     hr = host_resid.numpy()
-    canvas_h = np.empty((B, L), np.int32)
-    e2e_s = 0.0
+    e2e_s, e2e_pos, h2d = 0.0, 0, 0
     for k in range(-args.warmup, e2e_steps):
         info = s.sync_info()
         act = np.nonzero(info["state"] == dg.ACTIVE)[0]
         tok = s.canvas().cpu().numpy()
         rows = synth.resid_rows(np.repeat(info["seed"][act], L), np.repeat(info["block"][act], L),
                                 np.repeat(info["step"][act], L), np.tile(np.arange(L), act.size),
-                                tok[act].reshape(-1), W16, SIGMA_HIDDEN)
+                                tok[act].reshape(-1), W16, sigma)
         hr[act] = rows.reshape(act.size, L, d)
         t0 = time.perf_counter()
         canvas_h, ent_h = s.step_host(hr)
         if k >= 0:
             e2e_s += time.perf_counter() - t0
+            e2e_pos += act.size * L
+            h2d += act.size * L * d * 4
     e2e_max = reduce_max(e2e_s, world)
-    e2e = {"value": whole_job_rate(positions_per_tick, e2e_steps, world, e2e_max), "unit": UNIT,
-           # the result copy spans the plan's error latch (256-byte slot), the canvas and the entropies
-           "h2d_bytes_per_step": B * L * d * 4, "d2h_bytes_per_step": 256 + -(-B * L * 4 // 256) * 256 + B * L * 4,
+    e2e = {"value": world * e2e_pos / e2e_max, "unit": UNIT,
+           # the active canvases' rows cross the host link; the result copy spans the plan's error latch
+           # (256-byte slot), the canvas and the entropies
+           "h2d_bytes_per_step": h2d // max(1, e2e_steps),
+           "d2h_bytes_per_step": 256 + -(-B * L * 4 // 256) * 256 + B * L * 4,
            "steps": e2e_steps,
            "api": "dg_denoise_step_host",
-           "h2d": "the page-locked residual rows are read by the kernels in place over the host link (zero-copy)"}
+           "h2d": "the page-locked residual rows of the active canvases are read by the kernels in place over the "
+                  "host link (zero-copy)"}
 
     line = None
     if rank == 0:
@@ -460,15 +595,20 @@ def run_ours(args, wl, world, rank, local):
                 "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": args.workload, "description": wl["text"], "commit_mode": wl["mode"],
-                           "softcap": wl["softcap"],
+                           "softcap": wl["softcap"], "canvases": B, "canvas_len": L, "vocab": V, "hidden": d,
+                           "steps_per_block": N, "entropy_bound": wl_knob(wl, "bound"),
+                           "t_max": wl_knob(wl, "t_max"), "t_min": wl_knob(wl, "t_min"), "hidden_sigma": sigma,
+                           "admit_ticks": list(admit) if admit else None,
+                           "blocks_per_canvas_run": blocks,
                            "positions_per_step": positions_per_tick,
                            "l2": "flushed before every timed tick: 256 MB device write, then read back (outside the "
                                  "events)" if args.flush == "writeread" else "flushed by a 256 MB write",
                            "graph": bool(args.graph),
                            "parallelism": f"replicas x{world} (independent canvases per GPU)" if world > 1 else "1 GPU",
                            "timing": "CUDA events around each whole tick on the sampler stream, ticks enqueued back "
-                                     "to back without host synchronisation (timed region); a second pass with events "
-                                     "between the kernels gives ms_per_kernel"},
+                                     "to back without host synchronisation (timed region); positions counted from "
+                                     "the sampler's step counters; a second pass with events between the kernels "
+                                     "gives ms_per_kernel"},
                 "ms_per_kernel": ({"k_lmhead_pair (RMSNorm fused)": k2_s * 1e3,
                                    "k_finish": float(per_kernel[:, 2].mean())} if pair else
                                   {n: float(per_kernel[:, i].mean()) for i, n in
@@ -484,7 +624,7 @@ def run_ours(args, wl, world, rank, local):
                                         "generator"),
                 "roofline": roof, "e2e": e2e, "clocks": clk}
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = oracle_positions_per_s(wl, args.cpu_budget, 0, W16=W16)
+            line["cpu_baseline"] = cpu_baseline(args, wl, W16)
         print(json.dumps(line), flush=True)
     s.close()
     if world > 1:
@@ -496,10 +636,11 @@ def run_ours(args, wl, world, rank, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed ticks (default: 200 on the model-scale workloads, 3000 on the small ones)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="canvas256_v32k")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -510,9 +651,19 @@ def main():
     ap.add_argument("--mode", choices=["freeze", "reaccept"], default="freeze",
                     help="commit mode: committed positions freeze (default), or every step re-accepts all positions")
     ap.add_argument("--softcap", type=float, default=0.0, help="final logit softcap c (0 = off, the workloads' setting)")
-    ap.add_argument("--kernel-steps", type=int, default=200, help="ticks of the per-kernel timing pass")
+    ap.add_argument("--kernel-steps", type=int, default=None,
+                    help="ticks of the per-kernel timing pass (default: 50 on the model-scale workloads, else 200)")
     ap.add_argument("--clocks-csv", default=None, help="also write the raw clock samples of the timed region here")
+    ap.add_argument("--cpu-one-core", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-rows", type=int, default=8, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_one_core:
+        return cpu_one_core_main(args)
+    big = WORKLOADS[args.workload]["vocab"] * WORKLOADS[args.workload]["hidden"] >= 1 << 28
+    if args.steps is None:
+        args.steps = 200 if big else 3000
+    if args.kernel_steps is None:
+        args.kernel_steps = 50 if big else 200
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()

@@ -259,16 +259,17 @@ const char* dg_last_error(const dg_sampler* s); /* "" when none; s may be NULL (
  *
  * Computes steps 1-3 above for the positions of ONE canvas -- RMSNorm, tied LM
  * head, and at temperature T the entropy H (nats), log Z, the sampled token
- * and the argmax of every position -- exactly as a sampler tick computes them
- * for an active canvas with this seed, block, step and temperature (position
- * p is row p of resid).  Nothing is committed or re-noised and no sampler is
- * needed.
+ * and the argmax of every position -- as a sampler tick computes them for an
+ * active canvas with this seed, block, step and temperature (position p is
+ * row p of resid), for a sampler whose final logit softcap is off (softcap 0;
+ * this call applies none).  Nothing is committed or re-noised and no sampler
+ * is needed.
  *
  * Who it is for: callers that cannot allocate device memory at the point of
  * the call, such as engines that reserve the whole device for their own pool
- * at start-up (a later cudaMalloc fails), or code that must not allocate
- * because cudaMalloc/cudaFree would synchronize the device.  The scratch this
- * call needs (the normalised rows and the split-vocabulary partial records)
+ * at start-up (a later cudaMalloc fails), or code where cudaMalloc/cudaFree
+ * would synchronize the device.  The scratch this call needs (the normalised
+ * rows, the split-vocabulary partial records and each row's best Gumbel score)
  * is one fixed array in device global memory inside the library, about
  * 2.7 MB on each device the library is loaded on, held until the process
  * exits.  Nothing is allocated per call, by this function or by anything it
@@ -287,9 +288,10 @@ const char* dg_last_error(const dg_sampler* s); /* "" when none; s may be NULL (
  *   stream    the work is enqueued on this stream, then the call waits for it.
  *   err       host buffer of err_len bytes for a message on failure, or NULL.
  *
- * Synchronizing: it returns after the stream has finished the work and
- * reports a non-finite statistic (DG_ERR_NONFINITE) or an expired bounded
- * wait (DG_ERR_TIMEOUT) found on the device.
+ * Synchronizing: it enqueues the work on `stream`, copies the device error
+ * latch back and waits for the stream before it returns, reporting a
+ * non-finite statistic (DG_ERR_NONFINITE) or an expired bounded wait
+ * (DG_ERR_TIMEOUT) found on the device.
  *
  * The first call on each device (with that device current) does a one-time
  * set-up: it looks up the scratch array's device address and sets the

@@ -12,8 +12,10 @@ Layout:
                  softmax, entropy, log Z, argmax, Gumbel-max sample, Philox).
   sampler.py  -- the denoising loop (schedule, early stop, entropy-bounded
                  commit, uniform re-noise, blocks, staggered admission).
-  gen_golden.py -- writes the stored expected values under tests/golden/ from
-                 this package only.
+
+Stored values under tests/golden/ are the pages' printed figures, published
+known-answer vectors, hand-worked values, or oracle states written by the
+script beside them that calls only this package and ``synth``.
 
 Every function is pinned by tests in tests/test_oracle_*.py against closed
 forms, brute force on tiny inputs, published known-answer vectors and
@@ -33,8 +35,8 @@ _SO = os.path.join(_BUILD, "liboracle.so")
 _lib = None
 
 PURPOSE_INIT = 2
-PURPOSE_GUMBEL = 3
 PURPOSE_RENOISE = 4
+PURPOSE_GUMBEL_ORDER = 5
 
 # numpy mirror of ``struct or_pos`` in oracle.c
 POS_DTYPE = np.dtype([("logZ", "f8"), ("H", "f8"), ("H_online", "f8"), ("zmax", "f8"), ("zgap", "f8"),
@@ -73,6 +75,8 @@ def _load():
         lib.or_stats.restype = None
         lib.or_logits.argtypes = [i64, i64, i64, vp, vp, vp, ctypes.c_int]
         lib.or_logits.restype = None
+        lib.or_exp_variates.argtypes = [u64, i32, i32, i32, i64, vp]
+        lib.or_exp_variates.restype = None
         _lib = lib
     return _lib
 
@@ -97,6 +101,16 @@ def philox(ctr, key) -> np.ndarray:
 
 def draw_u32(seed: int, purpose: int, block: int, step: int, p: int) -> int:
     return int(_load().or_draw_u32(seed, purpose, block, step, p))
+
+
+def exp_variates(seed: int, block: int, step: int, p: int, V: int) -> np.ndarray:
+    """The Exp(1) variates E_v (fp64 [V]) behind position p's Gumbel draws, G_v = -ln E_v: per group
+    of 16 entries the sixteen order statistics in increasing order, placed in a uniformly random
+    permutation of the slots (Renyi's representation of exponential order statistics; oracle.c
+    gives the counters)."""
+    E = np.empty(V, dtype=np.float64)
+    _load().or_exp_variates(seed, block, step, p, V, _p(E))
+    return E
 
 
 def uniform_token(u: int, V: int) -> int:

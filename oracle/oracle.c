@@ -20,11 +20,26 @@
  *       H = -sum_v p_v ln p_v in nats ("Compute entropy"), log Z, the argmax,
  *       and one categorical sample.  The sample is drawn by the Gumbel-max
  *       rule (Gumbel 1954; e.g. Maddison, Tarlow, Minka, "A* Sampling", 2014):
- *       y = argmax_v (z_v/T + G_v), G_v = -ln(-ln U_v), which has the law of
- *       Categorical(logits = z/T).sample() used in "Denoise, stage, commit,
- *       and generate".  U_v = (u + 0.5) 2^-32 with u a Philox4x32-10 word
- *       (Salmon et al., SC'11), key = canvas seed, counter =
- *       (v>>2, p, (block<<16)|step, 3), lane v&3.
+ *       y = argmax_v (z_v/T + G_v), G_v = -ln E_v with E_v i.i.d. Exp(1),
+ *       which has the law of Categorical(logits = z/T).sample() used in
+ *       "Denoise, stage, commit, and generate".
+ *
+ *   or_exp_variates -- the Exp(1) variates E_v of one position.  The
+ *       vocabulary is cut into groups of 16 entries, j = v >> 4, and each
+ *       group's sixteen i.i.d. Exp(1) variates are drawn in increasing order
+ *       by Renyi's representation of exponential order statistics (A. Renyi,
+ *       "On the theory of order statistics", 1953): the k-th smallest of n is
+ *       E_(k) = E_(k-1) + X_k / (n - k), k = 0 .. n-1, E_(-1) = 0, with
+ *       X_k i.i.d. Exp(1); and since the variates are exchangeable, the
+ *       slots that receive E_(0), E_(1), ... are a uniformly random
+ *       permutation, drawn here one slot at a time without replacement.  With
+ *       U(w) = (w + 0.5) 2^-32 for a Philox4x32-10 word w (Salmon et al.,
+ *       SC'11), key = canvas seed, step k of group j reads the words of
+ *         b = Philox((8 j + k / 2, p, (block<<16)|step, 5)):
+ *       X_k = -ln U(b[2 (k & 1)]) and, from w = b[2 (k & 1) + 1],
+ *       r = (w (16 - k)) >> 32 (Lemire's multiply-shift), so that E_(k) goes
+ *       to the r-th (from 0, in increasing order) slot not yet given a value.
+ *       Entries of the last group at or beyond V are simply not used.
  *
  *   or_draw_u32 -- one Philox word for the uniform re-noise ("Keep a
  *       low-entropy prefix and renoise the rest") and the uniform initial
@@ -40,7 +55,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { OR_PURPOSE_INIT = 2, OR_PURPOSE_GUMBEL = 3, OR_PURPOSE_RENOISE = 4 };
+enum { OR_PURPOSE_INIT = 2, OR_PURPOSE_RENOISE = 4, OR_PURPOSE_GUMBEL_ORDER = 5 };
 
 /* ---------------------------------------------------------------- Philox -- */
 
@@ -133,13 +148,35 @@ typedef struct or_pos {
   int32_t y;        /* argmax_v (z_v / T + G_v), lowest index on ties      */
 } or_pos;
 
-static double or_gumbel(uint64_t seed, int32_t block, int32_t step, int32_t p, int64_t v) {
-  uint32_t ctr[4] = {(uint32_t)(v >> 2), (uint32_t)p, ((uint32_t)block << 16) | (uint32_t)step, OR_PURPOSE_GUMBEL};
-  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
-  uint32_t out[4];
-  or_philox(ctr, key, out);
-  double U = ((double)out[v & 3] + 0.5) / 4294967296.0;
-  return -log(-log(U));
+static double or_unit(uint32_t w) { return ((double)w + 0.5) / 4294967296.0; }
+
+/* E[v] for v in [0, V): the Exp(1) variates of position p's Gumbel draws (see the header). */
+void or_exp_variates(uint64_t seed, int32_t block, int32_t step, int32_t p, int64_t V, double* E) {
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  const uint32_t bs = ((uint32_t)block << 16) | (uint32_t)step;
+  for (int64_t j = 0; 16 * j < V; ++j) {
+    double ek = 0.0;    /* E_(k-1) */
+    int taken[16] = {0};
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t c[4] = {(uint32_t)(8 * j + k / 2), (uint32_t)p, bs, OR_PURPOSE_GUMBEL_ORDER};
+      uint32_t b[4];
+      or_philox(c, key, b);
+      ek += -log(or_unit(b[2 * (k & 1)])) / (double)(16 - k);
+      const uint32_t r = (uint32_t)(((uint64_t)b[2 * (k & 1) + 1] * (uint64_t)(16 - k)) >> 32);
+      /* the r-th free slot */
+      int slot = -1;
+      for (int i = 0, seen = 0; i < 16; ++i) {
+        if (taken[i]) continue;
+        if (seen == (int)r) {
+          slot = i;
+          break;
+        }
+        ++seen;
+      }
+      taken[slot] = 1;
+      if (16 * j + slot < V) E[16 * j + slot] = ek;
+    }
+  }
 }
 
 static void or_stats_row(int64_t V, const double* z, double T, uint64_t seed, int32_t block, int32_t step, int32_t p,
@@ -189,11 +226,13 @@ static void or_stats_row(int64_t V, const double* z, double T, uint64_t seed, in
     oS = nS;
     oA = nA;
   }
-  /* Gumbel-max sample */
+  /* Gumbel-max sample, G_v = -ln E_v */
+  double* E = (double*)malloc(sizeof(double) * (size_t)V);
+  or_exp_variates(seed, block, step, p, V, E);
   double g1 = -INFINITY, g2 = -INFINITY;
   int32_t y = 0;
   for (int64_t v = 0; v < V; ++v) {
-    double s = z[v] / T + or_gumbel(seed, block, step, p, v);
+    double s = z[v] / T - log(E[v]);
     if (s > g1) {
       g2 = g1;
       g1 = s;
@@ -202,6 +241,7 @@ static void or_stats_row(int64_t V, const double* z, double T, uint64_t seed, in
       g2 = s;
     }
   }
+  free(E);
   o->logZ = logZ;
   o->H = H;
   o->H_online = log(oS) - oA / oS;

@@ -20,12 +20,13 @@ Nothing the CUDA path produces is fed to the oracle.
 from __future__ import annotations
 
 import dataclasses
+import os
 
 import numpy as np
 
 import oracle
 import synth
-from oracle.sampler import ACTIVE, OracleConfig, OracleSampler
+from oracle.sampler import ACTIVE, DONE, WAITING, OracleConfig, OracleSampler
 
 TOL_H = 1e-3
 TOL_LOGZ_REL = 1e-3
@@ -164,15 +165,21 @@ def teacher_forced(case: Case, ticks: int = 1 << 30, gpu=None, W=None, check_eve
     return rep
 
 
-def compare_tick(s, o: OracleSampler, rec, case: Case, rep: Report):
+def compare_tick(s, o: OracleSampler, rec, case: Case, rep: Report, cmap=None):
+    """Compare the CUDA sampler's outputs and state after a tick with the oracle's.  ``cmap`` maps an
+    oracle canvas to the CUDA sampler's canvas (default: the same index)."""
     L = case.canvas_len
-    H = s.entropy().cpu().numpy()
-    lz = s.logz().cpu().numpy()
-    y = s.sample().cpu().numpy()
-    am = s.argmax().cpu().numpy()
-    gst = s.get_state()
+    H_all = s.entropy().cpu().numpy()
+    lz_all = s.logz().cpu().numpy()
+    y_all = s.sample().cpu().numpy()
+    am_all = s.argmax().cpu().numpy()
+    gst_all = s.get_state()
     rep.ticks += 1
     for i, c in enumerate(rec.canvases):
+        g = c if cmap is None else cmap[int(c)]
+        H, lz, y, am = {c: H_all[g]}, {c: lz_all[g]}, {c: y_all[g]}, {c: am_all[g]}
+        gst = {k: ({c: v[g]} if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == case.n_canvases
+                   else v) for k, v in gst_all.items()}
         st = rec.stats[i * L:(i + 1) * L]
         rep.positions += L
         dH = np.abs(H[c].astype(np.float64) - st["H"])
@@ -213,7 +220,7 @@ def compare_tick(s, o: OracleSampler, rec, case: Case, rep: Report):
                 rep.state_mismatch_unflagged += int(bad.sum())
                 rep.errors.append(f"tick {rec.tick} canvas {c}: {name} differs at {np.nonzero(bad)[0][:8].tolist()}")
         if not np.any(pos_flag):
-            gs, os_ = gst["slots"][c], o
+            gs = gst["slots"][c]
             for fld, ov in (("state", o.status[c]), ("block", o.block[c]), ("step", o.step_no[c]),
                             ("steps_used", o.steps_used[c]), ("converged_blocks", o.converged_blocks[c]),
                             ("n_committed", o.committed[c].sum()), ("n_remasked", rec.n_remasked[i]),
@@ -222,7 +229,100 @@ def compare_tick(s, o: OracleSampler, rec, case: Case, rep: Report):
                     rep.errors.append(f"tick {rec.tick} canvas {c}: slot {fld} {int(gs[fld])} != oracle {int(ov)}")
             if rec.final[i]:
                 b = rec.block[i]
-                if not np.array_equal(gst["tokens_out"][c, b], o.tokens_out[c, b]):
+                if not np.array_equal(gst["tokens_out"][c][b], o.tokens_out[c, b]):
                     rep.errors.append(f"tick {rec.tick} canvas {c}: finished block tokens differ")
-                if not np.array_equal(gst["commit_steps_out"][c, b], o.commit_steps_out[c, b]):
+                if not np.array_equal(gst["commit_steps_out"][c][b], o.commit_steps_out[c, b]):
                     rep.errors.append(f"tick {rec.tick} canvas {c}: finished block commit heatmap differs")
+
+
+# --------------------------------------------------------------------------- stored oracle states
+STATES_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "model_scale_states.npz")
+STATE_FIELDS = ("x", "committed", "commit_step", "prev_amax", "stable_run", "step_no", "block", "status",
+                "steps_used", "converged_blocks")
+_STATES = {}
+
+
+def _load_states() -> dict:
+    if not _STATES:
+        with np.load(STATES_PATH) as z:
+            for k in z.files:
+                traj, step, field = k.split("/")
+                _STATES.setdefault(traj, {}).setdefault(step, {})[field] = z[k]
+    return _STATES
+
+
+def stored_state(name: str, key: str) -> dict:
+    """One canvas's oracle state before a tick, as written by tests/golden/make_model_scale_states.py
+    (``key`` is "s<step>" or "stop")."""
+    return {f: np.array(v) for f, v in _load_states()[name][key].items()}
+
+
+def stored_keys(name: str) -> list:
+    """The states stored for one trajectory ("s<step>" and, where its early stop fired, "stop")."""
+    return sorted(_load_states().get(name, {}))
+
+
+def init_state(case: Case, c: int, block: int = 0, step: int = 0) -> dict:
+    """Canvas c at the start of a block (its uniform initial canvas), as the oracle draws it; the slot
+    step may be set past 0 for a stand-in canvas whose outputs are not compared."""
+    cfg = case.oracle_cfg()
+    L = case.canvas_len
+    x = np.array([oracle.uniform_token(oracle.draw_u32(cfg.seed(c), oracle.PURPOSE_INIT, block, 0, p), case.vocab)
+                  for p in range(L)], dtype=np.int32)
+    return {"x": x, "committed": np.zeros(L, bool), "commit_step": np.full(L, -1, np.int16),
+            "prev_amax": np.zeros(L, np.int32), "stable_run": np.array(0), "step_no": np.array(step),
+            "block": np.array(block), "status": np.array(ACTIVE), "steps_used": np.array(0),
+            "converged_blocks": np.array(0)}
+
+
+def oracle_from_state(case: Case, W: np.ndarray, c: int, st: dict, tick: int) -> OracleSampler:
+    """A one-canvas oracle for canvas c of the case (its seed and knobs), holding the state ``st``."""
+    cfg = dataclasses.replace(case.oracle_cfg(), n_canvases=1, seeds=[case.oracle_cfg().seed(c)], admit_tick=None,
+                              max_active=None)
+    o = OracleSampler(cfg, W)
+    for f in STATE_FIELDS:
+        getattr(o, f)[0] = st[f]
+    o.tick_no = tick
+    return o
+
+
+def batch_state(case: Case, states: dict, tick: int) -> dict:
+    """The CUDA sampler's state for a whole batch: ``states[c]`` is canvas c's state (fields of
+    STATE_FIELDS); canvases not listed wait for admission."""
+    import uniform_state_discrete_gb300 as dg
+    B, L, G = case.n_canvases, case.canvas_len, case.gen_blocks
+    slots = np.zeros(B, dg.SLOT_DTYPE)
+    out = {"tick": tick, "slots": slots, "tokens": np.zeros((B, L), np.int32),
+           "committed": np.zeros((B, L), np.uint8), "commit_step": np.full((B, L), -1, np.int16),
+           "prev_argmax": np.zeros((B, L), np.int32), "tokens_out": np.zeros((B, G, L), np.int32),
+           "commit_steps_out": np.zeros((B, G, L), np.int16)}
+    slots["state"] = WAITING
+    for c, st in states.items():
+        slots["state"][c] = int(st["status"])
+        slots["block"][c] = int(st["block"])
+        slots["step"][c] = int(st["step_no"])
+        slots["n_committed"][c] = int(np.sum(st["committed"]))
+        slots["steps_used"][c] = int(st["steps_used"])
+        slots["converged_blocks"][c] = int(st["converged_blocks"])
+        slots["stable_steps"][c] = int(st["stable_run"])
+        out["tokens"][c] = st["x"]
+        out["committed"][c] = np.asarray(st["committed"], bool).astype(np.uint8)
+        out["commit_step"][c] = st["commit_step"]
+        out["prev_argmax"][c] = st["prev_amax"]
+    return out
+
+
+def tick_from_states(s, case: Case, W: np.ndarray, states: dict, tick: int, check, rep: Report):
+    """Load a batch state into the CUDA sampler, run one tick of it on synth's residual rows, and
+    compare the canvases in ``check`` with one-canvas oracles started from the same states."""
+    import torch
+    ocfg = case.oracle_cfg()
+    act = np.array(sorted(c for c, st in states.items() if int(st["status"]) == ACTIVE))
+    resid = resid_slots(case, ocfg, W, act, [int(states[c]["block"]) for c in act],
+                        [int(states[c]["step_no"]) for c in act], np.stack([states[c]["x"] for c in act]))
+    s.set_state(batch_state(case, states, tick))
+    s.step(torch.from_numpy(resid).to(getattr(s, "device", "cuda:0")))
+    for c in check:
+        o = oracle_from_state(case, W, c, states[c], tick)
+        rec = o.tick(lambda canv, blocks, steps, tok: resid[c].reshape(-1, case.hidden))
+        compare_tick(s, o, rec, case, rep, cmap={0: c})

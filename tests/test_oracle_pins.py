@@ -198,6 +198,74 @@ def test_gumbel_sample_follows_softmax():
     assert (st2["y"] != st["y"]).mean() > 0.5
 
 
+def test_gumbel_sample_follows_softmax_across_groups():
+    """40 entries span two whole groups of 16 and a partial one: the sample still follows softmax."""
+    V, n, T = 40, 24000, 0.9
+    z = np.random.default_rng(8).uniform(-1.5, 1.5, V)
+    st = oracle.stats(np.tile(z, (n, 1)), T, 77, 1, 5, np.arange(n))
+    counts = np.bincount(st["y"], minlength=V)
+    assert scipy.stats.chisquare(counts, scipy.special.softmax(z / T) * n).pvalue > 1e-3
+
+
+def _exp_variates(n, V, seed=11, block=0, step=2):
+    return np.stack([oracle.exp_variates(seed, block, step, p, V) for p in range(n)])
+
+
+def test_exp_variates_marginals_are_exponential():
+    """Every entry's E_v is Exp(1) (Kolmogorov-Smirnov over 3000 positions), including the entries
+    of a partial last group (V = 40)."""
+    E = _exp_variates(3000, 40)
+    pvals = [scipy.stats.kstest(E[:, v], "expon").pvalue for v in range(40)]
+    assert min(pvals) > 1e-4, min(pvals)
+    assert abs(E.mean() - 1.0) < 0.02
+
+
+def test_exp_variates_group_minimum_slot_and_independence():
+    """Renyi's representation: the minimum of a group of 16 is Exp(16), the slot holding it is
+    uniform over the 16, and the entries of a group are uncorrelated."""
+    n = 4000
+    E = _exp_variates(n, 32, seed=3, block=1, step=7)
+    for g in range(2):
+        grp = E[:, 16 * g:16 * g + 16]
+        assert scipy.stats.kstest(16.0 * grp.min(axis=1), "expon").pvalue > 1e-3
+        assert scipy.stats.chisquare(np.bincount(grp.argmin(axis=1), minlength=16)).pvalue > 1e-3
+        c = np.corrcoef(grp.T)
+        assert np.max(np.abs(c - np.eye(16))) < 5.0 / math.sqrt(n)
+    # the two groups draw independently
+    assert abs(np.corrcoef(E[:, :16].min(axis=1), E[:, 16:].min(axis=1))[0, 1]) < 5.0 / math.sqrt(n)
+
+
+def test_exp_variates_sorted_spacings_are_exponential():
+    """For i.i.d. Exp(1) variates, the k-th spacing of the sorted sixteen, scaled by 16 - k, is Exp(1)
+    and independent of the others (Renyi, 1953): checked for the first, a middle and the last
+    spacing of each group over 4000 positions."""
+    n = 4000
+    E = np.sort(_exp_variates(n, 32, seed=21, block=3, step=9).reshape(n, 2, 16), axis=2)
+    gaps = np.diff(np.concatenate([np.zeros((n, 2, 1)), E], axis=2), axis=2) * (16 - np.arange(16))
+    for k in (0, 1, 7, 15):
+        for g in range(2):
+            assert scipy.stats.kstest(gaps[:, g, k], "expon").pvalue > 1e-3, (k, g)
+    assert abs(np.corrcoef(gaps[:, 0, 1], gaps[:, 0, 2])[0, 1]) < 5.0 / math.sqrt(n)
+
+
+def test_exp_variates_rekey_with_position_step_block_and_seed():
+    base = oracle.exp_variates(5, 0, 0, 0, 64)
+    for args in ((6, 0, 0, 0), (5, 1, 0, 0), (5, 0, 1, 0), (5, 0, 0, 1)):
+        assert np.mean(oracle.exp_variates(*args, 64) != base) > 0.9
+
+
+def test_gumbel_sample_is_argmax_of_perturbed_logits():
+    """The sample stats() reports is argmax_v (z_v/T - ln E_v) of the oracle's own variates."""
+    V, T = 50, 0.6
+    rng = np.random.default_rng(4)
+    z = rng.standard_normal((20, V))
+    st = oracle.stats(z, T, 9, 2, 3, np.arange(20))
+    for p in range(20):
+        s = z[p] / T - np.log(oracle.exp_variates(9, 2, 3, p, V))
+        assert st["y"][p] == int(np.argmax(s))
+        assert abs(st["gbest"][p] - s.max()) < 1e-12
+
+
 def test_gumbel_sample_of_dominant_token_is_argmax():
     V = 4096
     z = np.random.default_rng(5).standard_normal(V)

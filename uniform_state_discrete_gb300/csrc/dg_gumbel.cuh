@@ -1,14 +1,15 @@
 // Philox4x32-10 draws of one position's Gumbel stream with the per-position
 // work hoisted out of the per-element loop.
 //
-// A position's Gumbel words come from the counter (x, p, (block<<16)|step,
-// GUMBEL) under the canvas seed, with x = v / 4 the only word that changes
-// along the vocabulary.  In the first two rounds of the Philox bijection
-// (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
-// SC'11) half of the products and XORs involve only the fixed words, so they
-// are computed once per position; the round keys of the remaining eight
-// rounds are kept as well.  draw(x) returns exactly the block
-// philox((x, p, bs, GUMBEL), seed), at 37 integer operations instead of 60.
+// A position's Gumbel draws come from the counters (x, p, (block<<16)|step,
+// GUMBEL_ORDER) under the canvas seed, with x = 8 j + k / 2 for step k of the
+// order statistics of vocabulary group j the only word that changes.  In the
+// first two rounds of the Philox bijection (Salmon, Moraes, Dror, Shaw,
+// "Parallel random numbers: as easy as 1, 2, 3", SC'11) half of the products
+// and XORs involve only the fixed words, so they are computed once per
+// position; the round keys of the remaining eight rounds are kept as well.
+// draw(x) returns exactly the block philox((x, p, bs, GUMBEL_ORDER), seed), at
+// 37 integer operations instead of 60.
 #pragma once
 
 #include <stdint.h>

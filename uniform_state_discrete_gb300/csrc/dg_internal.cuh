@@ -35,7 +35,7 @@ constexpr int kSubPerChunk = 1;                 // column groups are merged in t
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after 1 s
 
 // Philox counter "purpose" word (word 3); see the oracle's definition.
-enum : uint32_t { kPurposeInit = 2u, kPurposeGumbel = 3u, kPurposeRenoise = 4u };
+enum : uint32_t { kPurposeInit = 2u, kPurposeRenoise = 4u, kPurposeGumbelOrder = 5u };
 enum : int32_t { kWaiting = 0, kActive = 1, kDone = 2 };
 // Device error codes latched in Plan::err.
 enum : int32_t { kErrNone = 0, kErrNonFinite = 1, kErrTimeout = 2 };
@@ -56,6 +56,7 @@ struct Plan {
   uint32_t commits;  // canvases committed so far this tick
   int32_t err;
   int32_t err_info[4];
+  uint32_t epoch;    // advanced by every planning; tags this tick's per-row best Gumbel scores
 };
 
 // Everything a kernel needs, by value.
@@ -75,6 +76,8 @@ struct Dev {
   int32_t* amax;        // [B, L]
   uint16_t* h;          // [rows_cap, d] bf16 bits, compact active rows
   Partial* part;        // [rows_cap, n_sub]
+  unsigned long long* row_best; // [rows_cap] best perturbed score found so far for each row this tick,
+                                //   (epoch << 32) | ordered score bits; other epochs read as none
   uint32_t* canvas_rows;// [B] rows combined per canvas this tick
   uint32_t* rows_ready; // normalised rows written this tick (RMSNorm -> LM-head producers)
   uint32_t* fin_started;// finishing-kernel CTAs that have read this tick's plan
@@ -202,6 +205,23 @@ __device__ __forceinline__ Partial load_partial(const Partial* p) {
   r.pad0 = b.z;
   r.pad1 = b.w;
   return r;
+}
+
+// Order-preserving unsigned image of a float (for atomicMax on scores) and back.
+__device__ __forceinline__ uint32_t score_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// The best score recorded for a row in this epoch, or -inf.
+__device__ __forceinline__ float row_best_score(const unsigned long long* e, uint32_t epoch) {
+  const unsigned long long v = __ldcg(e);
+  return (uint32_t)(v >> 32) == epoch ? key_score((uint32_t)v) : -INFINITY;
+}
+__device__ __forceinline__ void row_best_raise(unsigned long long* e, uint32_t epoch, float score) {
+  atomicMax(e, ((unsigned long long)epoch << 32) | score_key(score));
 }
 
 __device__ __forceinline__ Partial empty_partial() {

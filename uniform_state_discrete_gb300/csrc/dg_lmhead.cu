@@ -107,6 +107,24 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// The same with an L2 cache policy for the copied lines.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+// L2 policy for the normalised rows h: keep them in L2 ahead of the W stream.
+// Each unit re-reads its 128- or 256-row slab of h once per vocabulary tile of
+// its chunk, while W passes through L2 once per tick; with thousands of rows
+// (tens of MB of h) the W stream would otherwise evict h between those reads.
+__device__ __forceinline__ uint64_t policy_keep() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -174,40 +192,38 @@ __device__ __forceinline__ RowMeta row_meta(const Dev& dv, int row, int n_rows) 
     const int a = row / dv.L;
     const dg_slot* sl = dv.slots + __ldcg(dv.active + a);
     rm.gs.init(__ldcg(&sl->seed), (uint32_t)(row - a * dv.L),
-               ((uint32_t)__ldcg(&sl->block) << 16) | (uint32_t)__ldcg(&sl->step), kPurposeGumbel);
+               ((uint32_t)__ldcg(&sl->block) << 16) | (uint32_t)__ldcg(&sl->step), kPurposeGumbelOrder);
     rm.scale = 1.4426950408889634f / __ldcg(&sl->temperature);
   } else {
-    rm.gs.init(0ull, 0u, 0u, kPurposeGumbel);
+    rm.gs.init(0ull, 0u, 0u, kPurposeGumbelOrder);
   }
   return rm;
 }
 
-// Screen factor K ~ 2^(m - g).  A Gumbel draw can raise the best perturbed
-// score g only if q < 2^(u - g) = e 2^(m - g), where q = 1 - U <= -ln U = E and
-// e = 2^(u - m) is the element's softmax weight.  The factor carries 0.2 %
-// slack for the approximate exponentials and logarithms, plus the rounding of
-// scores of magnitude up to |m| + 64, so the screen never drops an element
-// that could win.
+// Screen factor K ~ 2^(m - g).  An entry can raise the best perturbed score g
+// only if its Exp(1) variate E < 2^(u - g) = e 2^(m - g), where e = 2^(u - m) is
+// its softmax weight.  The factor carries 0.2 % slack for the approximate
+// exponentials and logarithms, plus the rounding of scores of magnitude up to
+// |m| + 64, so the screen never drops an entry that could win.
 __device__ __forceinline__ float screen_factor(float m, float g) {
   return ex2_approx(m - g) * fmaf(fabsf(m) + 64.f, 0x1p-20f, 1.002f);
 }
 
 // Pass test of the screen without an integer-to-float conversion: with
-// Ut = (r >> 9) 2^-23 <= U, f = 1 + Ut is built by one funnel shift, and
-// q < e K implies f > 2 - e K - 2^-22; the threshold below leaves a further
-// 2^-22 for its own rounding.
+// Ut = (r >> 9) 2^-23 <= U and q = 1 - U, f = 1 + Ut is built by one funnel
+// shift, and q < t implies f > 2 - t - 2^-22; the threshold below leaves a
+// further 2^-22 for its own rounding.
 __device__ __forceinline__ float screen_word(uint32_t r) { return __uint_as_float(__funnelshift_r(r, 0x7Fu, 9)); }
-__device__ __forceinline__ float screen_threshold(float e, float K) { return fmaf(-e, K, 2.f - 0x1p-21f); }
+__device__ __forceinline__ float screen_threshold(float t) { return 2.f - 0x1p-21f - t; }
 
-// -log2(E) for the Exp(1) variate E = -ln U of one Gumbel draw,
-// U = (r + 0.5) 2^-32.  For U < 3/4, E comes from lg2(U).  For U >= 3/4,
-// E = -ln(1 - q) with q = 1 - U taken exactly from the integer, through the
-// series -ln(1-q) = 2 atanh(s) = 2 (s + s^3/3 + s^5/5 + ...), s = q / (2 - q)
-// <= 1/7, truncated after s^9 (relative error < 4e-10), which keeps the large
-// Gumbel values (small E) accurate where lg2(U) would lose them.  Both
-// branches are evaluated and one kept, so a warp scores one candidate per lane
-// in lockstep.
-__device__ __forceinline__ float neg_log2_exp_variate_nb(uint32_t r) {
+// The Exp(1) variate E = -ln U of a word r, U = (r + 0.5) 2^-32.  For U < 3/4,
+// E comes from lg2(U).  For U >= 3/4, E = -ln(1 - q) with q = 1 - U taken
+// exactly from the integer, through the series -ln(1-q) = 2 atanh(s) =
+// 2 (s + s^3/3 + s^5/5 + ...), s = q / (2 - q) <= 1/7, truncated after s^9
+// (relative error < 4e-10), which keeps small variates (large Gumbel values)
+// accurate where lg2(U) would lose them.  Both branches are evaluated and one
+// kept, so a warp scores in lockstep.
+__device__ __forceinline__ float exp_variate(uint32_t r) {
   const float U = fmaf(__uint2float_rn(r), 0x1p-32f, 0x1p-33f);
   const float Eu = -0.69314718055994531f * lg2_approx(U);
   const float q = fmaf(__uint2float_rn(~r), 0x1p-32f, 0x1p-33f);
@@ -218,33 +234,7 @@ __device__ __forceinline__ float neg_log2_exp_variate_nb(uint32_t r) {
   t = fmaf(s2, t, 1.0f / 3.0f);
   t = fmaf(s2, t, 1.0f);
   const float Eq = 2.0f * sq * t;
-  return -lg2_approx(r < 0xC0000000u ? Eu : Eq);
-}
-
-// z[j] and w[j] for a lane-varying j, by a four-level select tree (registers
-// cannot be indexed).
-__device__ __forceinline__ void select16(const float (&z)[16], const uint32_t (&w)[16], uint32_t j, float& zj,
-                                         uint32_t& wj) {
-  float a[8];
-  uint32_t b[8];
-  const bool b0 = j & 1u, b1 = j & 2u, b2 = j & 4u, b3 = j & 8u;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    a[i] = b0 ? z[2 * i + 1] : z[2 * i];
-    b[i] = b0 ? w[2 * i + 1] : w[2 * i];
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    a[i] = b1 ? a[2 * i + 1] : a[2 * i];
-    b[i] = b1 ? b[2 * i + 1] : b[2 * i];
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    a[i] = b2 ? a[2 * i + 1] : a[2 * i];
-    b[i] = b2 ? b[2 * i + 1] : b[2 * i];
-  }
-  zj = b3 ? a[1] : a[0];
-  wj = b3 ? b[1] : b[0];
+  return r < 0xC0000000u ? Eu : Eq;
 }
 
 // Order-preserving int image of a float (for atomicMax on shared scores).
@@ -254,8 +244,55 @@ __device__ __forceinline__ int ord_key(float f) {
 }
 __device__ __forceinline__ float key_ord(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF)); }
 
+// z[j] for a lane-varying j, by a four-level select tree (registers cannot be indexed).
+__device__ __forceinline__ float select16(const float (&z)[16], uint32_t j) {
+  float a[8];
+  const bool b0 = j & 1u, b1 = j & 2u, b2 = j & 4u, b3 = j & 8u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = b0 ? z[2 * i + 1] : z[2 * i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a[i] = b1 ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) a[i] = b2 ? a[2 * i + 1] : a[2 * i];
+  return b3 ? a[1] : a[0];
+}
+
+// Index of the r-th set bit (from 0, lowest first) of a 16-bit mask holding more than r set bits.
+__device__ __forceinline__ uint32_t nth_set_bit16(uint32_t mask, uint32_t r) {
+  uint32_t pos = 0u, c = __popc(mask & 0xFFu);
+  if (r >= c) {
+    r -= c;
+    pos = 8u;
+  }
+  c = __popc((mask >> pos) & 0xFu);
+  if (r >= c) {
+    r -= c;
+    pos += 4u;
+  }
+  c = __popc((mask >> pos) & 0x3u);
+  if (r >= c) {
+    r -= c;
+    pos += 2u;
+  }
+  return pos + (r >= ((mask >> pos) & 1u) ? 1u : 0u);
+}
+
+// Where a row's best perturbed score is kept: this CTA's column groups share
+// `cta` (shared memory), every unit of the row in the tick shares `glob`
+// (global memory, tagged with the tick's epoch).  `known` is the global value
+// read at the start of the current tile; a stream publishes its own best to
+// the global value once per tile, at the tile's end, if it rose.
+struct BestScore {
+  int* cta;
+  unsigned long long* glob;
+  uint32_t epoch;
+  float known;
+  bool raised;  // this stream's own best rose during the current tile (published at its end)
+};
+
 // Fold 16 columns [v0, v0+16) of one row (raw fp32 logits z) into its running
-// statistics.  kTail: some of the columns lie at or beyond V.
+// statistics.  v0 is a multiple of 16, so the columns are one group of the
+// Gumbel draws.  kTail: some of the columns lie at or beyond V.
 //
 // With a final logit softcap c > 0 each logit first becomes c tanh(z / c)
 // ("The Annotated DiffusionGemma", "Logit Softcapping": part of the model,
@@ -267,18 +304,23 @@ __device__ __forceinline__ float key_ord(int k) { return __int_as_float(k >= 0 ?
 // 2^(u-m), A = sum 2^(u-m)(u-m), formed from d = u - m = fma(z, log2(e)/T, -m).
 // The argmax index is looked up only when the fold raises the running max.
 //
-// Gumbel-max sample: the perturbed score of an element is (m + d) - log2 E
-// with E = -ln U the Exp(1) variate of its Philox word.  The screen compares
-// each element against the best score known for the row: this stream's own,
-// seeded with the maximum element's draw by the first fold that sets the
-// maximum, or a better one another column group of the CTA found for the same
-// row (`best`, shared memory).  Either is the score of a real element, so the
-// row's winner always passes the screen, and candidates are scored exactly:
-// the result equals the unscreened maximum.  Candidates are scored one per lane
-// per round, all lanes of the warp together.  Equal scores keep the lower
-// index.
+// Gumbel-max sample: the perturbed score of entry v is (m + d) - log2 E_v with
+// E_v its Exp(1) variate.  A group's sixteen variates are drawn in increasing
+// order, E_(k) = E_(k-1) + X_k / (16 - k), each placed in a slot drawn
+// uniformly from those still free (Renyi's representation of exponential
+// order statistics; the counters are in dg_gumbel.cuh), so the group is walked
+// from its smallest variate up and the walk stops as soon as
+// E_(k) >= 2^(u_max - g): every entry not yet scored then scores below g, the
+// best score known for the row -- this stream's own, one another column group
+// of the CTA found (shared memory), or one any unit of the row found this tick
+// (global memory).  Each is the score of a real entry, so the row's winner is
+// always scored and the result equals the unscreened maximum.  The walk is
+// started only if E_(0) can pass: since -ln U >= 1 - U = q, the group is skipped
+// when q(a0) >= 16 2^(u_max - g), on the first Philox block alone -- one block
+// for sixteen entries.  Walks run one step per lane per round, all lanes of
+// the warp together.  Equal scores keep the lower index.
 template <bool kTail, bool kCap>
-__device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, int* best,
+__device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, BestScore& bs,
                                        float cap, float inv_cap) {
   if (kCap) {
 #pragma unroll
@@ -290,14 +332,10 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
     for (int j = 0; j < 16; ++j)
       if (v0 + j >= V) z[j] = -INFINITY;
   }
-  uint32_t w[16];
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    uint32_t t4[4];
-    rm.gs.draw(((uint32_t)v0 >> 2) + (uint32_t)g, t4);
-#pragma unroll
-    for (int l = 0; l < 4; ++l) w[4 * g + l] = t4[l];
-  }
+  // the first block of the group's order statistics: its latency overlaps the statistics below
+  const uint32_t x0 = 8u * ((uint32_t)v0 >> 4);
+  uint32_t w4[4];
+  rm.gs.draw(x0, w4);
   float t8[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) t8[i] = fmaxf(z[i], z[i + 8]);
@@ -315,57 +353,69 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
     for (int j = 15; j >= 0; --j)
       if (z[j] == cmz) ci = j;  // first index holding the maximum
     st.amax = v0 + ci;
-    if (st.g == -INFINITY) {
-      float zc;
-      uint32_t wc;
-      select16(z, w, (uint32_t)ci, zc, wc);
-      st.g = (cm + fmaf(cmz, rm.scale, -cm)) + neg_log2_exp_variate_nb(wc);
-      st.gidx = v0 + ci;
-      atomicMax(best, ord_key(st.g));
-    }
   }
   const float m = st.m, nm = -st.m;
-  const float K = screen_factor(m, fmaxf(st.g, key_ord(*(volatile int*)best)));
   float S[4] = {0.f, 0.f, 0.f, 0.f}, A[4] = {0.f, 0.f, 0.f, 0.f};
-  uint32_t mask = 0u;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float d = fmaf(z[j], rm.scale, nm);
     const float e = ex2_approx(d);  // +0 for a masked column (d = -inf)
     S[j & 3] += e;
     if (!kTail || v0 + j < V) A[j & 3] = fmaf(e, d, A[j & 3]);
-    if (screen_word(w[j]) > screen_threshold(e, K) && (!kTail || v0 + j < V)) mask |= 1u << j;
   }
-  const unsigned act = __activemask();
-  bool improved = false;
-  while (__any_sync(act, mask != 0u)) {
-    const bool has = mask != 0u;
-    const uint32_t j = has ? (uint32_t)(__ffs(mask) - 1) : 0u;
-    mask &= mask - 1u;
-    float zj;
-    uint32_t wj;
-    select16(z, w, j, zj, wj);
-    const float sc = (m + fmaf(zj, rm.scale, nm)) + neg_log2_exp_variate_nb(wj);
-    const int idx = v0 + (int)j;
-    if (has && (sc > st.g || (sc == st.g && idx < st.gidx))) {
-      st.g = sc;
-      st.gidx = idx;
-      improved = true;
-    }
-  }
-  if (improved) atomicMax(best, ord_key(st.g));
   st.S += (S[0] + S[1]) + (S[2] + S[3]);
   st.A += (A[0] + A[1]) + (A[2] + A[3]);
+  // can the group's smallest variate E_(0) = X_0 / 16 >= q(a0) / 16 beat g?
+  const float emax = ex2_approx(fmaf(cmz, rm.scale, nm));  // 2^(u_max - m)
+  const float g0 = fmaxf(fmaxf(st.g, bs.known), key_ord(*(volatile int*)bs.cta));
+  bool live = g0 == -INFINITY || screen_word(w4[0]) > screen_threshold(16.f * emax * screen_factor(m, g0));
+  const unsigned act = __activemask();
+  if (!__any_sync(act, live)) return;
+  bool improved = false;
+  float E = 0.f;
+  uint32_t rem = 0xFFFFu;  // slots not yet given a variate
+  uint32_t k = 0u;
+  while (__any_sync(act, live)) {
+    if (live) {
+      const uint32_t xw = (k & 1u) ? w4[2] : w4[0], rw = (k & 1u) ? w4[3] : w4[1];
+      E = fmaf(exp_variate(xw), __frcp_rn((float)(16u - k)), E);  // E_(k)
+      const float g = fmaxf(g0, st.g);
+      if (g != -INFINITY && !(E < emax * screen_factor(m, g))) {
+        live = false;  // no entry left in the group can score above g
+      } else {
+        const uint32_t slot = nth_set_bit16(rem, __umulhi(rw, 16u - k));
+        rem &= ~(1u << slot);
+        const int idx = v0 + (int)slot;
+        if (!kTail || idx < V) {
+          const float sc = (m + fmaf(select16(z, slot), rm.scale, nm)) - lg2_approx(E);
+          if (sc > st.g || (sc == st.g && idx < st.gidx)) {
+            st.g = sc;
+            st.gidx = idx;
+            improved = true;
+          }
+        }
+        if (++k == 16u) {
+          live = false;
+        } else if (!(k & 1u)) {
+          rm.gs.draw(x0 + (k >> 1), w4);
+        }
+      }
+    }
+  }
+  if (improved) {
+    atomicMax(bs.cta, ord_key(st.g));
+    bs.raised = true;
+  }
 }
 
 // The fold of this warp's 16 columns of one accumulator tile.
 template <bool kCap>
-__device__ __forceinline__ void fold_cols(float (&acc)[16], int v0, int V, const RowMeta& rm, Partial& st, int* best,
-                                          float cap, float inv_cap) {
+__device__ __forceinline__ void fold_cols(float (&acc)[16], int v0, int V, const RowMeta& rm, Partial& st,
+                                          BestScore& bs, float cap, float inv_cap) {
   if (v0 + 16 <= V)
-    fold16<false, kCap>(acc, v0, V, rm, st, best, cap, inv_cap);
+    fold16<false, kCap>(acc, v0, V, rm, st, bs, cap, inv_cap);
   else
-    fold16<true, kCap>(acc, v0, V, rm, st, best, cap, inv_cap);
+    fold16<true, kCap>(acc, v0, V, rm, st, bs, cap, inv_cap);
 }
 
 // ---------------------------------------------------------------- CTA pairs
@@ -394,6 +444,14 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* t
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster_addr)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorMap* tm, int x, int y,
+                                                      uint32_t bar_cluster_addr, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster_addr), "l"(policy)
       : "memory");
 }
 // Instruction descriptor for the pair MMA: D fp32, A and B bf16, K-major, M = 256, N = 256.
@@ -485,6 +543,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   // the plan is read before the next kernel may launch, so its planner cannot have
   // rewritten it for the next tick yet
   const int n_rows = __ldcg(&dv.plan->n_active) * dv.L;
+  const uint32_t epoch = __ldcg(&dv.plan->epoch);
   pdl_allow_next();
   const int n_mt = (n_rows + kBM - 1) / kBM;
   const int n_units = n_mt * dv.n_chunks;
@@ -496,6 +555,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       int issued_parity[kStages];
       for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
       bool ok = rows_written(dv, n_rows, abort_flag);
+      const uint64_t keep = policy_keep();
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int chunk = u / n_mt, mt = u - chunk * n_mt;
         const int vt0 = chunk * dv.tiles_per_chunk;
@@ -507,7 +567,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
               break;
             }
             mbar_expect_tx(&full[stage], (uint32_t)(kStageA + kStageB));
-            tma_load_2d(sA + stage * kStageA, &tmA, kb * kBK, mt * kBM, &full[stage]);
+            tma_load_2d_hint(sA + stage * kStageA, &tmA, kb * kBK, mt * kBM, &full[stage], keep);
             tma_load_2d(sB + stage * kStageB, &tmB, kb * kBK, vt * kBN, &full[stage]);
             issued_parity[stage] = (int)phase;
             if (++stage == (uint32_t)kStages) {
@@ -594,10 +654,13 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       const int rl = q * 32 + lane;         // row within the tile
       const int row = mt * kBM + rl;
       const RowMeta rm = row_meta(dv, row, n_rows);
+      BestScore bs{gbest + rl, dv.row_best + row, epoch, -INFINITY, false};
       Partial st = empty_partial();
       for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
         if (aborted) continue;
         const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
+        // the best score other units of this row have found so far (read while the tile completes)
+        if (rm.valid) bs.known = row_best_score(bs.glob, epoch);
         int got = 0;
         if (lane == 0) got = mbar_wait(&tfull[ab], aph, abort_flag, dv.plan) ? 1 : 0;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
@@ -620,8 +683,12 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             if (lane == 0) mbar_arrive(&tempty[ab]);
           }
           if (rm.valid)
-            fold_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, gbest + rl, dv.softcap,
+            fold_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, bs, dv.softcap,
                             dv.inv_softcap);
+        }
+        if (bs.raised) {
+          row_best_raise(bs.glob, epoch, st.g);
+          bs.raised = false;
         }
       }
       // merge the four column groups of each row; one record per row and chunk.  Every
@@ -698,10 +765,12 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   // prefetch of that row as it lies when canvas k is the k-th active one.
   const int et = (int)threadIdx.x - 64, grp = et >> 8, r_first = (int)blockIdx.x + grp * (int)gridDim.x;
   int n_active = 0, c_first = 0;
+  uint32_t epoch = 0;
   if (warp >= 2) {
     if (dv.norm_w) prefetch_row<256>(dv.norm_w, dv.d >> 2, et & 255);
     pdl_wait();
     n_active = __ldcg(&dv.plan->n_active);
+    epoch = __ldcg(&dv.plan->epoch);
     if (r_first < dv.max_active * dv.L) {
       const int a = r_first / dv.L;
       c_first = __ldcg(dv.active + a);
@@ -802,6 +871,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = rows_written(dv, n_rows, abort_flag);
+      const uint64_t keep = policy_keep();
       int issued = 0;
       for (int u = cid; u < n_units && ok; u += n_clusters) {
         const int chunk = u / n_mt, mt = u - chunk * n_mt;
@@ -813,16 +883,16 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             if (issued < pre) {
               // first lap, W half already in flight: the h half and the leader's arrival
               if (leader) mbar_expect_tx(&full[stage], (uint32_t)(2 * kStagePairA));
-              tma_load_2d_pair(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
-                               full_leader);
+              tma_load_2d_pair_hint(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
+                                    full_leader, keep);
             } else {
               if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
                 ok = false;
                 break;
               }
               if (leader) mbar_expect_tx(&full[stage], (uint32_t)(2 * (kStagePairA + kStagePairB)));
-              tma_load_2d_pair(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
-                               full_leader);
+              tma_load_2d_pair_hint(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
+                                    full_leader, keep);
               tma_load_2d_pair(sB + stage * kStagePairB, &tmB, kb * kBK, vt * kBN + (int)rank * (kBN / 2),
                                full_leader);
             }
@@ -920,10 +990,13 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       const int rl = q * 32 + lane;
       const int row = mt * 2 * kBM + (int)rank * kBM + rl;
       const RowMeta rm = row_meta(dv, row, n_rows);
+      BestScore bs{gbest + rl, dv.row_best + row, epoch, -INFINITY, false};
       Partial st = empty_partial();
       for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
         if (aborted) continue;
         const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
+        // the best score other units of this row have found so far (read while the tile completes)
+        if (rm.valid) bs.known = row_best_score(bs.glob, epoch);
         int got = 0;
         if (lane == 0) got = mbar_wait(&tfull[ab], aph, abort_flag, dv.plan) ? 1 : 0;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
@@ -945,8 +1018,12 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             if (lane == 0) mbar_arrive_cluster(tempty_leader[ab]);
           }
           if (rm.valid)
-            fold_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, gbest + rl, dv.softcap,
+            fold_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, bs, dv.softcap,
                             dv.inv_softcap);
+        }
+        if (bs.raised) {
+          row_best_raise(bs.glob, epoch, st.g);
+          bs.raised = false;
         }
       }
       mrg[cg * kBM + rl] = st;

@@ -55,7 +55,7 @@ void set_err(char* buf, const char* fmt, ...) {
 
 struct Layout {
   size_t slots, plan, active, x, committed, commit_step, prev_amax, tokens_out, commit_steps_out, H, logZ, y, amax, h,
-      part, resid,
+      part, row_best, resid,
       canvas_rows, temps, sync;
   size_t total;
   int rows_cap, n_vtiles, tiles_per_chunk, n_chunks, n_sub, max_active;
@@ -130,6 +130,7 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
   L->amax = take(4 * B * Lc);
   L->h = take(2 * (size_t)L->rows_cap * d);
   L->part = take(sizeof(dg::Partial) * (size_t)L->rows_cap * L->n_sub);
+  L->row_best = take(sizeof(unsigned long long) * (size_t)L->rows_cap);
   L->resid = take(4 * B * Lc * d);
   L->canvas_rows = take(4 * B);
   L->temps = take(4 * (size_t)c->num_inference_steps);
@@ -314,6 +315,7 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.amax = reinterpret_cast<int32_t*>(w + L.amax);
   dv.h = reinterpret_cast<uint16_t*>(w + L.h);
   dv.part = reinterpret_cast<dg::Partial*>(w + L.part);
+  dv.row_best = reinterpret_cast<unsigned long long*>(w + L.row_best);
   dv.resid_stage = reinterpret_cast<float*>(w + L.resid);
   dv.canvas_rows = reinterpret_cast<uint32_t*>(w + L.canvas_rows);
   dv.rows_ready = reinterpret_cast<uint32_t*>(w + L.sync);

@@ -5,12 +5,12 @@
 // The sampler's entry points take a caller-allocated workspace.  This one is
 // for callers that cannot hand one over: programs that reserve the whole
 // device for their own memory pool at start-up (so a later cudaMalloc fails),
-// and code running where cudaMalloc is not allowed or would stall the device
-// (inside allocator callbacks, or latency-critical loops that must not
-// synchronize).  Its scratch -- the normalised rows and the split-vocabulary
-// partial records -- lives in one fixed-size array in device global memory,
-// declared below, which every GPU that loads this library holds until the
-// process exits.
+// and code running where cudaMalloc is not allowed or would stall the device,
+// such as allocator callbacks.  Its scratch -- the normalised rows, the
+// split-vocabulary partial records and the rows' best Gumbel scores -- lives in
+// one fixed-size array in device global memory, declared below, which every
+// GPU that loads this library holds until the process exits.  The call waits
+// for its stream before it returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -35,7 +35,9 @@ constexpr size_t kOffH = 1024;
 constexpr size_t kBytesH = (size_t)2 * DG_STATIC_MAX_ROWS * DG_STATIC_MAX_HIDDEN;
 constexpr size_t kOffPart = kOffH + kBytesH;
 constexpr size_t kBytesPart = sizeof(dg::Partial) * DG_STATIC_MAX_ROWS * dg::kChunkTarget;
-constexpr size_t kStaticBytes = (kOffPart + kBytesPart + 255) & ~size_t(255);
+constexpr size_t kOffRowBest = kOffPart + kBytesPart;
+constexpr size_t kBytesRowBest = sizeof(unsigned long long) * DG_STATIC_MAX_ROWS;
+constexpr size_t kStaticBytes = (kOffRowBest + kBytesRowBest + 255) & ~size_t(255);
 static_assert(sizeof(dg_slot) <= 256 && sizeof(dg::Plan) <= 256, "scratch header fits");
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
@@ -45,9 +47,10 @@ struct DeviceSetup {
   bool ready;
   unsigned char* base;  // device address of g_static_scratch on this device
   int num_sms;
+  PFN_cuTensorMapEncodeTiled_v12000 encode;  // the driver's tensor-map encoder
 };
 DeviceSetup g_setup[kMaxDevices];
-std::mutex g_setup_mutex;
+std::mutex g_setup_mutex;  // guards g_setup: every call reads its device's entry under it
 
 void put_err(char* buf, size_t len, const char* fmt, ...) {
   if (!buf || len == 0) return;
@@ -78,6 +81,7 @@ __global__ void k_static_prep(unsigned char* base, uint64_t seed, int block, int
   sl->stable_steps = 0;
   pl->tick = 0;
   pl->n_active = 1;
+  pl->epoch += 1u;  // the per-row best scores of earlier calls no longer count
   pl->commits = 0u;
   pl->err = dg::kErrNone;
   for (int i = 0; i < 4; ++i) pl->err_info[i] = 0;
@@ -124,20 +128,8 @@ __global__ void __launch_bounds__(256) k_static_combine(const dg::Dev dv, int ro
   }
 }
 
-bool encode(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, char* err,
-            size_t err_len) {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !p) {
-      put_err(err, err_len, "cuTensorMapEncodeTiled not available from the driver");
-      return false;
-    }
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+bool encode(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
+            uint32_t box_rows, char* err, size_t err_len) {
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {(cuuint32_t)dg::kBK, box_rows};
@@ -210,6 +202,15 @@ extern "C" dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, co
       if (e != cudaSuccess || !ptr) return cuda_err(e, "cudaGetSymbolAddress of the static scratch", err, err_len);
       e = dg::lmhead_configure();
       if (e != cudaSuccess) return cuda_err(e, "configure kernels", err, err_len);
+      void* enc = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &enc, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !enc) {
+        put_err(err, err_len, "cuTensorMapEncodeTiled not available from the driver");
+        return DG_ERR_CUDA;
+      }
+      g_setup[dev].encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(enc);
       g_setup[dev].base = static_cast<unsigned char*>(ptr);
       g_setup[dev].num_sms = sms;
       g_setup[dev].ready = true;
@@ -235,6 +236,7 @@ extern "C" dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, co
   dv.slab_done = dv.rows_ready + 2;
   dv.h = reinterpret_cast<uint16_t*>(su.base + kOffH);
   dv.part = reinterpret_cast<dg::Partial*>(su.base + kOffPart);
+  dv.row_best = reinterpret_cast<unsigned long long*>(su.base + kOffRowBest);
   dv.norm_w = norm_w;
   dv.V = vocab;
   dv.d = hidden;
@@ -255,8 +257,10 @@ extern "C" dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, co
   // the pair kernel when the rows fill a 256-row pair tile, as the sampler chooses
   const bool pair = rows >= 2 * dg::kBM && su.num_sms >= 2;
   CUtensorMap tmA, tmB;
-  if (!encode(&tmA, dv.h, (uint64_t)DG_STATIC_MAX_ROWS, (uint64_t)hidden, dg::kBM, err, err_len)) return DG_ERR_ARG;
-  if (!encode(&tmB, w_vocab, (uint64_t)vocab, (uint64_t)hidden, pair ? dg::kBN / 2 : dg::kBN, err, err_len))
+  if (!encode(su.encode, &tmA, dv.h, (uint64_t)DG_STATIC_MAX_ROWS, (uint64_t)hidden, dg::kBM, err, err_len))
+    return DG_ERR_ARG;
+  if (!encode(su.encode, &tmB, w_vocab, (uint64_t)vocab, (uint64_t)hidden, pair ? dg::kBN / 2 : dg::kBN, err,
+              err_len))
     return DG_ERR_ARG;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

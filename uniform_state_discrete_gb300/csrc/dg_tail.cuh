@@ -170,6 +170,7 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
     dv.plan->n_active = base < dv.max_active ? base : dv.max_active;  // above it only after an inconsistent dg_set_state
     dv.plan->tick = tick;
     dv.plan->commits = 0u;
+    dv.plan->epoch += 1u;  // the per-row best scores of earlier ticks no longer count
   }
   g.sync();
 }
