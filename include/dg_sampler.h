@@ -109,6 +109,10 @@ typedef struct dg_config {
   float softcap;               /* final logit softcap c >= 0: logits become c tanh(z / c) before
                                   the temperature (The Annotated DiffusionGemma, "Logit
                                   Softcapping"); 0 = off                                        */
+  int32_t vocab_ranks;         /* G: ranks the vocabulary is split across, 0 or 1 = not split;
+                                  at most the number of vocabulary chunks (see
+                                  dg_denoise_step_partial)                                       */
+  int32_t vocab_rank;          /* this sampler's rank r in [0, G)                                */
 } dg_config;
 
 /* Per-canvas state, the layout of the device array returned by dg_slots().
@@ -168,6 +172,48 @@ dg_status dg_denoise_step(dg_sampler* s, const float* resid);
  * stream; resid_host must stay unchanged until it returns.
  */
 dg_status dg_denoise_step_host(dg_sampler* s, const float* resid_host, int32_t* canvas_host, float* entropy_host);
+
+/*
+ * Vocabulary-parallel ticks.  The LM head cuts the vocabulary into chunks of
+ * whole 256-entry tiles (the chunking depends on V only) and writes one 32-byte
+ * partial record of softmax statistics and Gumbel-max candidate per position
+ * and chunk; the finishing step merges a position's records in chunk order
+ * (log Z = m + ln S, H = ln S - A/S with "The Annotated DiffusionGemma",
+ * "Compute entropy"), then commits and re-noises.  With vocab_ranks = G > 1 the
+ * chunks are split into G contiguous ranges, rank r taking chunks
+ * [floor(r n / G), floor((r + 1) n / G)) of the n, and each rank holds only the
+ * W rows of its range: w_vocab given to dg_sampler_create is then that slice,
+ * rows [chunk_begin * tiles_per_chunk * 256, min(chunk_end * tiles_per_chunk *
+ * 256, V)) of the whole matrix (dg_vocab_slice gives both ends).  Vocabulary
+ * indices stay global (Philox counters, tie-breaks, tokens), so a tick split
+ * this way gives bit for bit what one unsplit sampler gives.  A tick is then:
+ *   1. dg_denoise_step_partial on every rank (RMSNorm and the LM head over its
+ *      chunks; asynchronous);
+ *   2. the caller copies each rank's records -- rows [0, rows_cap), chunk
+ *      columns [chunk_begin, chunk_end) of the [rows_cap, n_chunks] array
+ *      that dg_partial_records describes -- into every other rank's array
+ *      (a collective across GPUs, or device copies on one GPU), ordered on
+ *      the samplers' streams after step 1;
+ *   3. dg_denoise_step_finish on every rank (asynchronous): each merges all n
+ *      records and commits, so every rank holds the same canvas state.
+ * dg_denoise_step, dg_denoise_step_host and dg_run refuse a split sampler
+ * (DG_ERR_STATE).  Without the exchange of step 2 the finishing step merges
+ * stale records.
+ */
+dg_status dg_denoise_step_partial(dg_sampler* s, const float* resid);
+dg_status dg_denoise_step_finish(dg_sampler* s);
+
+/* Layout of the partial records for the exchange: records_dev (dev, 32-byte
+ * records, [rows_cap, n_chunks] row-major, inside the workspace), the row
+ * capacity, the number of vocabulary chunks and this rank's chunk range.  Any
+ * output pointer may be NULL. */
+dg_status dg_partial_records(const dg_sampler* s, void** records_dev, int32_t* rows_cap, int32_t* n_chunks,
+                             int32_t* chunk_begin, int32_t* chunk_end);
+
+/* The rows [v_begin, v_end) of W_vocab that rank `rank` of `ranks` holds for a
+ * vocabulary of `vocab` entries (any hidden size), so a caller can cut W
+ * before creating the rank's sampler.  DG_ERR_ARG for an invalid split. */
+dg_status dg_vocab_slice(int32_t vocab, int32_t ranks, int32_t rank, int32_t* v_begin, int32_t* v_end);
 
 /* Residual supplier for dg_run: the backbone's place in the loop.  Must fill
  * resid_dev [B, L, d] for the active canvases of this tick from their current

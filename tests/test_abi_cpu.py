@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_struct_layouts_match_header_sizes():
     import uniform_state_discrete_gb300 as dg
-    assert ctypes.sizeof(dg.dg_config) == 80
+    assert ctypes.sizeof(dg.dg_config) == 88
     assert ctypes.sizeof(dg.dg_slot) == 56
     assert ctypes.sizeof(dg.dg_state) == 64
 
@@ -108,3 +108,22 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_vocab_split_rules():
+    """Vocabulary-parallel configs: the rank must lie in [0, vocab_ranks) and there can be no more
+    ranks than vocabulary chunks; dg_vocab_slice cuts V into contiguous, tile-aligned slices."""
+    import uniform_state_discrete_gb300 as dg
+    for ranks, rank, ok in ((2, 0, True), (2, 1, True), (2, 2, False), (3, -1, False), (9, 0, False), (8, 7, True)):
+        cfg = dg.make_config(2048, 128, 16, vocab_ranks=ranks, vocab_rank=rank)  # 8 tiles -> 8 chunks
+        assert (dg.dg_workspace_size(cfg) > 0) == ok, (ranks, rank)
+    for V in (2048, 1000, 262144, 300000):
+        for G in (1, 2, 3, 4, 7):
+            if G > -(-V // 256):
+                continue  # more ranks than chunks
+            cuts = [dg.vocab_slice(V, G, r) for r in range(G)]
+            assert cuts[0][0] == 0 and cuts[-1][1] == V
+            assert all(a[1] == b[0] for a, b in zip(cuts, cuts[1:]))
+            assert all(c[0] % 256 == 0 and c[1] > c[0] for c in cuts)
+    with pytest.raises(dg.DGError):
+        dg.vocab_slice(1000, 5, 0)  # 4 tiles, 4 chunks

@@ -35,7 +35,7 @@ class dg_config(ctypes.Structure):
                 ("entropy_bound", ctypes.c_float), ("confidence", ctypes.c_float), ("stability", ctypes.c_int32),
                 ("rms_eps", ctypes.c_float), ("mode", ctypes.c_int32), ("max_active", ctypes.c_int32),
                 ("seeds", ctypes.POINTER(ctypes.c_uint64)), ("admit_tick", ctypes.POINTER(ctypes.c_int32)),
-                ("softcap", ctypes.c_float)]
+                ("softcap", ctypes.c_float), ("vocab_ranks", ctypes.c_int32), ("vocab_rank", ctypes.c_int32)]
 
 
 class dg_slot(ctypes.Structure):
@@ -69,6 +69,13 @@ _SIGS = {
                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                          ctypes.POINTER(ctypes.c_void_p)]),
     "dg_denoise_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "dg_denoise_step_partial": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "dg_denoise_step_finish": (ctypes.c_int, [ctypes.c_void_p]),
+    "dg_partial_records": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
+                                          ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
+    "dg_vocab_slice": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
     "dg_denoise_step_host": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "dg_run": (ctypes.c_int, [ctypes.c_void_p, DG_RESID_FN, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                               ctypes.c_void_p]),
@@ -127,11 +134,13 @@ def _check(st: int, handle=None):
 
 def make_config(vocab, hidden, canvas_len, n_canvases=1, gen_blocks=1, num_inference_steps=48, t_min=0.4,
                 t_max=0.8, entropy_bound=0.1, confidence=0.005, stability=1, rms_eps=1e-6, mode=DG_FREEZE,
-                max_active=0, seeds=None, admit_tick=None, softcap=0.0):
+                max_active=0, seeds=None, admit_tick=None, softcap=0.0, vocab_ranks=0, vocab_rank=0):
     """Build a ``dg_config``; the returned object keeps the seed/admit arrays alive."""
     cfg = dg_config(vocab, hidden, canvas_len, n_canvases, gen_blocks, num_inference_steps, t_min, t_max,
                     entropy_bound, confidence, stability, rms_eps, mode, max_active)
     cfg.softcap = softcap
+    cfg.vocab_ranks = vocab_ranks
+    cfg.vocab_rank = vocab_rank
     keep = []
     if seeds is not None:
         a = (ctypes.c_uint64 * n_canvases)(*[int(s) for s in seeds])
@@ -147,6 +156,46 @@ def make_config(vocab, hidden, canvas_len, n_canvases=1, gen_blocks=1, num_infer
 
 def dg_workspace_size(cfg: dg_config) -> int:
     return int(lib.dg_workspace_size(ctypes.byref(cfg)))
+
+
+def vocab_slice(vocab: int, ranks: int, rank: int):
+    """dg_vocab_slice: the W rows [v_begin, v_end) rank ``rank`` of ``ranks`` holds."""
+    b, e = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.dg_vocab_slice(vocab, ranks, rank, ctypes.byref(b), ctypes.byref(e)))
+    return b.value, e.value
+
+
+def exchange_partials(samplers) -> None:
+    """The exchange of a vocabulary-parallel tick for ranks that share one GPU: every rank's chunk
+    columns of the partial records are copied into every other rank's array, each copy ordered after
+    both samplers' partial ticks (device copies only)."""
+    import torch
+    for dst in samplers:
+        rec_d, (b_d, e_d) = dst.partial_records(), dst.chunk_range()
+        for src in samplers:
+            if src is dst:
+                continue
+            rec_s, (b, e) = src.partial_records(), src.chunk_range()
+            dst.stream.wait_stream(src.stream)
+            with torch.cuda.stream(dst.stream):
+                rec_d[:, b:e].copy_(rec_s[:, b:e])
+            src.stream.wait_stream(dst.stream)
+
+
+def all_gather_partials(records, chunk_ranges, rank: int, group=None) -> None:
+    """The exchange of a vocabulary-parallel tick across processes (torch.distributed): ``records`` is
+    this rank's [rows_cap, n_chunks, 8] record array (a view of the workspace, or any tensor of that
+    layout), ``chunk_ranges`` every rank's (chunk_begin, chunk_end).  Each rank's columns are packed,
+    all-gathered and written into every rank's array in place."""
+    import torch
+    import torch.distributed as dist
+    b, e = chunk_ranges[rank]
+    mine = records[:, b:e].contiguous()
+    parts = [torch.empty((records.shape[0], e1 - b1, records.shape[2]), dtype=records.dtype, device=records.device)
+             for b1, e1 in chunk_ranges]
+    dist.all_gather(parts, mine, group=group)
+    for (b1, e1), part in zip(chunk_ranges, parts):
+        records[:, b1:e1].copy_(part)
 
 
 def dg_lmhead_stats_static(resid, w_vocab, norm_w, rms_eps, temperature, seed, block, step, entropy, logz, sample,
@@ -207,6 +256,32 @@ class Sampler:
 
     def step(self, resid):
         _check(self.dg_denoise_step(resid), self.handle)
+
+    def step_partial(self, resid):
+        """dg_denoise_step_partial: RMSNorm and the LM head over this rank's vocabulary chunks."""
+        _check(lib.dg_denoise_step_partial(self.handle, ctypes.c_void_p(resid.data_ptr())), self.handle)
+
+    def step_finish(self):
+        """dg_denoise_step_finish: merge every chunk's records, commit and re-noise."""
+        _check(lib.dg_denoise_step_finish(self.handle), self.handle)
+
+    def _records_layout(self):
+        ptr, rows, n, b, e = ctypes.c_void_p(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib.dg_partial_records(self.handle, ctypes.byref(ptr), ctypes.byref(rows), ctypes.byref(n),
+                                      ctypes.byref(b), ctypes.byref(e)), self.handle)
+        return ptr.value, rows.value, n.value, b.value, e.value
+
+    def partial_records(self):
+        """The [rows_cap, n_chunks, 8] int32 view of the 32-byte partial records (dg_partial_records)."""
+        import torch
+        ptr, rows, n, _, _ = self._records_layout()
+        off = ptr - self.workspace.data_ptr()
+        return self.workspace[off:off + rows * n * 32].view(torch.int32).view(rows, n, 8)
+
+    def chunk_range(self):
+        """This rank's vocabulary chunks [chunk_begin, chunk_end)."""
+        _, _, _, b, e = self._records_layout()
+        return b, e
 
     def step_host(self, resid_host: np.ndarray, want_canvas=True, want_entropy=True):
         """dg_denoise_step_host; the results land in page-locked buffers kept by the sampler and are

@@ -88,6 +88,10 @@ struct Dev {
   int32_t V, d, L, B, G, N;
   float t_min, t_max, bound, conf, eps;
   int32_t n_vtiles, tiles_per_chunk, n_chunks, n_sub, rows_cap, max_active;
+  // vocabulary chunks this LM head computes, [chunk_begin, chunk_end) of the n_chunks (all of them
+  // unless the vocabulary is split across ranks), and the first vocabulary tile of the W rows the
+  // tensor map covers (its row 0 is vocabulary entry vt_base * kBN)
+  int32_t chunk_begin, chunk_end, vt_base;
   bool reaccept;        // DG_REACCEPT: every step re-sorts all positions (see dg_mode)
   int32_t stability;    // early stop needs this many consecutive steps with an unchanged argmax canvas
   float softcap;        // final logit softcap c (0 = off): z -> c tanh(z / c) before the temperature

@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   // the canvas of this warp's row, read before the wait so its latency is hidden
   const int row_c = (lane == 0 && row < n_rows) ? __ldcg(dv.active + row / dv.L) : 0;
   if (threadIdx.x == 0) {
-    const bool ok = wait_count(dv.slab_done + row0 / 128, (uint32_t)dv.n_chunks);
+    const bool ok = wait_count(dv.slab_done + row0 / 128, (uint32_t)(dv.chunk_end - dv.chunk_begin));
     if (!ok && atomicCAS(&dv.plan->err, kErrNone, kErrTimeout) == kErrNone) dv.plan->err_info[0] = -1 - (int)blockIdx.x;
   }
   __syncthreads();

@@ -107,25 +107,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
-// The same with an L2 cache policy for the copied lines.
-__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar,
-                                                 uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-// L2 policy for the normalised rows h: keep them in L2 ahead of the W stream.
-// Each unit re-reads its 128- or 256-row slab of h once per vocabulary tile of
-// its chunk, while W passes through L2 once per tick; with thousands of rows
-// (tens of MB of h) the W stream would otherwise evict h between those reads.
-__device__ __forceinline__ uint64_t policy_keep() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -446,14 +427,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* t
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster_addr)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorMap* tm, int x, int y,
-                                                      uint32_t bar_cluster_addr, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster_addr), "l"(policy)
-      : "memory");
-}
 // Instruction descriptor for the pair MMA: D fp32, A and B bf16, K-major, M = 256, N = 256.
 constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                                 ((uint32_t)(256 >> 4) << 24);
@@ -487,6 +460,34 @@ __device__ __forceinline__ bool rows_written(const Dev& dv, int n_rows, volatile
   asm volatile("fence.proxy.async.global;" ::: "memory");
   return true;
 }
+
+// Work units (row tile, vocabulary chunk) in the order the persistent grid takes
+// them.  Row tiles are taken in groups whose rows of h fit in about 48 MB of L2,
+// and each group runs through all of this rank's chunks before the next
+// starts: every unit re-reads its rows of h once per vocabulary tile, so the
+// rows the grid works on at any time have to stay in L2 beside the W tiles
+// streaming through, and W is then read from DRAM once per group.  The order
+// decides nothing about the results: a unit's partial record depends only on
+// its rows and chunk.
+struct UnitMap {
+  int n_mt, n_local, group;  // row tiles, chunks of this rank, row tiles per group
+  __device__ __forceinline__ UnitMap(const Dev& dv, int n_mt_, int rows_per_tile) {
+    n_mt = n_mt_;
+    n_local = dv.chunk_end - dv.chunk_begin;
+    const long long bytes_per_tile = (long long)rows_per_tile * dv.d * 2;
+    const long long g = (48ll << 20) / (bytes_per_tile > 0 ? bytes_per_tile : 1);
+    group = (int)(g < 1 ? 1 : (g > n_mt ? n_mt : g));
+  }
+  __device__ __forceinline__ int units() const { return n_mt * n_local; }
+  __device__ __forceinline__ void at(const Dev& dv, int u, int& chunk, int& mt) const {
+    const int g = u / (group * n_local);
+    const int g0 = g * group;
+    const int rows_g = min(group, n_mt - g0);  // the last group may hold fewer row tiles
+    const int r = u - g0 * n_local;
+    chunk = dv.chunk_begin + r / rows_g;
+    mt = g0 + r % rows_g;
+  }
+};
 
 template <bool kCap>
 __global__ void __launch_bounds__(kThreadsLM, 1)
@@ -546,7 +547,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   const uint32_t epoch = __ldcg(&dv.plan->epoch);
   pdl_allow_next();
   const int n_mt = (n_rows + kBM - 1) / kBM;
-  const int n_units = n_mt * dv.n_chunks;
+  const UnitMap um(dv, n_mt, kBM);
+  const int n_units = um.units();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -555,9 +557,9 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       int issued_parity[kStages];
       for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
       bool ok = rows_written(dv, n_rows, abort_flag);
-      const uint64_t keep = policy_keep();
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const int chunk = u / n_mt, mt = u - chunk * n_mt;
+        int chunk, mt;
+        um.at(dv, u, chunk, mt);
         const int vt0 = chunk * dv.tiles_per_chunk;
         const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
         for (int vt = vt0; vt < vt1 && ok; ++vt) {
@@ -567,8 +569,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
               break;
             }
             mbar_expect_tx(&full[stage], (uint32_t)(kStageA + kStageB));
-            tma_load_2d_hint(sA + stage * kStageA, &tmA, kb * kBK, mt * kBM, &full[stage], keep);
-            tma_load_2d(sB + stage * kStageB, &tmB, kb * kBK, vt * kBN, &full[stage]);
+            tma_load_2d(sA + stage * kStageA, &tmA, kb * kBK, mt * kBM, &full[stage]);
+            tma_load_2d(sB + stage * kStageB, &tmB, kb * kBK, (vt - dv.vt_base) * kBN, &full[stage]);
             issued_parity[stage] = (int)phase;
             if (++stage == (uint32_t)kStages) {
               stage = 0;
@@ -597,7 +599,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true, any = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const int chunk = u / n_mt;
+        int chunk, mt;
+        um.at(dv, u, chunk, mt);
         const int vt0 = chunk * dv.tiles_per_chunk;
         const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
         for (int vt = vt0; vt < vt1 && ok; ++vt, ++tcount) {
@@ -648,7 +651,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     uint32_t tcount = 0;
     bool aborted = false;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const int chunk = u / n_mt, mt = u - chunk * n_mt;
+      int chunk, mt;
+        um.at(dv, u, chunk, mt);
       const int vt0 = chunk * dv.tiles_per_chunk;
       const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
       const int rl = q * 32 + lane;         // row within the tile
@@ -817,14 +821,14 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   // canvas is active.  The leader raises the stage's expected bytes by the W
   // halves now and arrives, with the h halves, after the wait.
   int pre = 0;
-  if ((dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM) == 1 && cid < dv.n_chunks) {
-    const int vt0 = cid * dv.tiles_per_chunk;
+  if ((dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM) == 1 && cid < dv.chunk_end - dv.chunk_begin) {
+    const int vt0 = (dv.chunk_begin + cid) * dv.tiles_per_chunk;
     pre = min(kStagesPair, KB * (min(vt0 + dv.tiles_per_chunk, dv.n_vtiles) - vt0));
     if (warp == 0 && lane == 0) {
       for (int it = 0; it < pre; ++it) {
         const int vt = vt0 + it / KB, kb = it % KB;
         if (leader) mbar_expect_tx_only(&full[it], (uint32_t)(2 * kStagePairB));
-        tma_load_2d_pair(sB + it * kStagePairB, &tmB, kb * kBK, vt * kBN + (int)rank * (kBN / 2),
+        tma_load_2d_pair(sB + it * kStagePairB, &tmB, kb * kBK, (vt - dv.vt_base) * kBN + (int)rank * (kBN / 2),
                          peer_addr(smem_u32(&full[it]), 0));
       }
     }
@@ -839,7 +843,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   const int n_rows = n_active * dv.L;
   pdl_allow_next_after(n_rows);
   const int n_mt = (n_rows + 2 * kBM - 1) / (2 * kBM);  // 256-row pair tiles
-  const int n_units = n_mt * dv.n_chunks;
+  const UnitMap um(dv, n_mt, 2 * kBM);
+  const int n_units = um.units();
 
   if (warp >= 2) {
     // RMSNorm: the epilogue warps form rows blockIdx.x + j * gridDim.x of h, two
@@ -871,10 +876,10 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = rows_written(dv, n_rows, abort_flag);
-      const uint64_t keep = policy_keep();
       int issued = 0;
       for (int u = cid; u < n_units && ok; u += n_clusters) {
-        const int chunk = u / n_mt, mt = u - chunk * n_mt;
+        int chunk, mt;
+        um.at(dv, u, chunk, mt);
         const int vt0 = chunk * dv.tiles_per_chunk;
         const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
         for (int vt = vt0; vt < vt1 && ok; ++vt) {
@@ -883,17 +888,17 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             if (issued < pre) {
               // first lap, W half already in flight: the h half and the leader's arrival
               if (leader) mbar_expect_tx(&full[stage], (uint32_t)(2 * kStagePairA));
-              tma_load_2d_pair_hint(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
-                                    full_leader, keep);
+              tma_load_2d_pair(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
+                                    full_leader);
             } else {
               if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
                 ok = false;
                 break;
               }
               if (leader) mbar_expect_tx(&full[stage], (uint32_t)(2 * (kStagePairA + kStagePairB)));
-              tma_load_2d_pair_hint(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
-                                    full_leader, keep);
-              tma_load_2d_pair(sB + stage * kStagePairB, &tmB, kb * kBK, vt * kBN + (int)rank * (kBN / 2),
+              tma_load_2d_pair(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
+                                    full_leader);
+              tma_load_2d_pair(sB + stage * kStagePairB, &tmB, kb * kBK, (vt - dv.vt_base) * kBN + (int)rank * (kBN / 2),
                                full_leader);
             }
             ++issued;
@@ -935,7 +940,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true, any = false;
       for (int u = cid; u < n_units && ok; u += n_clusters) {
-        const int chunk = u / n_mt;
+        int chunk, mt;
+        um.at(dv, u, chunk, mt);
         const int vt0 = chunk * dv.tiles_per_chunk;
         const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
         for (int vt = vt0; vt < vt1 && ok; ++vt, ++tcount) {
@@ -984,7 +990,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     uint32_t tcount = 0;
     bool aborted = false;
     for (int u = cid; u < n_units; u += n_clusters) {
-      const int chunk = u / n_mt, mt = u - chunk * n_mt;
+      int chunk, mt;
+        um.at(dv, u, chunk, mt);
       const int vt0 = chunk * dv.tiles_per_chunk;
       const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
       const int rl = q * 32 + lane;
@@ -1078,7 +1085,7 @@ cudaError_t launch_lmhead_pair(const Dev& dv, const float* resid, const CUtensor
                                int num_sms, cudaStream_t st) {
   // persistent grid of CTA pairs, never more pairs than the largest number of work units
   const int max_mt = (dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM);
-  int pairs = max_mt * dv.n_chunks;
+  int pairs = max_mt * (dv.chunk_end - dv.chunk_begin);
   if (pairs > num_sms / 2) pairs = num_sms / 2;
   if (pairs < 1) pairs = 1;
   cudaLaunchAttribute attr[2];
@@ -1104,7 +1111,7 @@ cudaError_t launch_lmhead(const Dev& dv, const CUtensorMap* tmA, const CUtensorM
   // Persistent grid: one CTA per SM (the shared-memory ring keeps it at one),
   // never more CTAs than the largest number of work units.
   const int max_mt = (dv.max_active * dv.L + kBM - 1) / kBM;
-  int grid = max_mt * dv.n_chunks;
+  int grid = max_mt * (dv.chunk_end - dv.chunk_begin);
   if (grid > num_sms) grid = num_sms;
   if (grid < 1) grid = 1;
   cudaLaunchAttribute attr[1];

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -21,6 +22,8 @@ struct dg_sampler {
   dg::Dev dv;
   CUtensorMap tmA, tmB;
   bool pair;  // LM head on CTA pairs (tcgen05 cta_group::2), chosen when a tick can hold >= 256 rows
+  bool split = false;            // the vocabulary is split across ranks (dg_denoise_step_partial / _finish)
+  bool partial_pending = false;  // a partial tick waits for its finishing step
   cudaStream_t stream;
   int num_sms;
   int64_t host_tick;
@@ -59,7 +62,28 @@ struct Layout {
       canvas_rows, temps, sync;
   size_t total;
   int rows_cap, n_vtiles, tiles_per_chunk, n_chunks, n_sub, max_active;
+  int chunk_begin, chunk_end;  // this rank's vocabulary chunks
 };
+
+// The LM head's vocabulary chunking, which depends on V only: 256-entry tiles,
+// at most kChunkTarget chunks of equally many tiles (the last may be shorter).
+void vocab_chunking(int32_t V, int* n_vtiles, int* tiles_per_chunk, int* n_chunks) {
+  *n_vtiles = (V + dg::kBN - 1) / dg::kBN;
+  const int target = *n_vtiles < dg::kChunkTarget ? *n_vtiles : dg::kChunkTarget;
+  *tiles_per_chunk = (*n_vtiles + target - 1) / target;
+  *n_chunks = (*n_vtiles + *tiles_per_chunk - 1) / *tiles_per_chunk;
+}
+
+// Chunks [c0, c1) of rank r of G (G <= 1: all of them).
+void rank_chunks(int n_chunks, int G, int r, int* c0, int* c1) {
+  if (G <= 1) {
+    *c0 = 0;
+    *c1 = n_chunks;
+    return;
+  }
+  *c0 = (int)((int64_t)r * n_chunks / G);
+  *c1 = (int)((int64_t)(r + 1) * n_chunks / G);
+}
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -89,6 +113,9 @@ bool validate(const dg_config* c, char* why) {
   if (c->admit_tick)
     for (int i = 0; i < c->n_canvases; ++i)
       if (c->admit_tick[i] < 0) return set_err(why, "admit_tick[%d] is negative", i), false;
+  if (c->vocab_ranks < 0 || c->vocab_rank < 0 || c->vocab_rank >= (c->vocab_ranks > 1 ? c->vocab_ranks : 1))
+    return set_err(why, "vocab_rank must be in [0, vocab_ranks) (got %d of %d)", c->vocab_rank, c->vocab_ranks),
+           false;
   return true;
 }
 
@@ -103,11 +130,12 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
   L->max_active = c->max_active ? c->max_active : c->n_canvases;
   const size_t rows = (size_t)L->max_active * Lc;
   L->rows_cap = (int)((rows + 255) / 256 * 256);
-  L->n_vtiles = (c->vocab + dg::kBN - 1) / dg::kBN;
-  const int target = L->n_vtiles < dg::kChunkTarget ? L->n_vtiles : dg::kChunkTarget;
-  L->tiles_per_chunk = (L->n_vtiles + target - 1) / target;
-  L->n_chunks = (L->n_vtiles + L->tiles_per_chunk - 1) / L->tiles_per_chunk;
+  vocab_chunking(c->vocab, &L->n_vtiles, &L->tiles_per_chunk, &L->n_chunks);
   L->n_sub = L->n_chunks * dg::kSubPerChunk;
+  if (c->vocab_ranks > L->n_chunks)
+    return set_err(why, "vocab_ranks must be at most the %d vocabulary chunks (got %d)", L->n_chunks, c->vocab_ranks),
+           0;
+  rank_chunks(L->n_chunks, c->vocab_ranks, c->vocab_rank, &L->chunk_begin, &L->chunk_end);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -206,31 +234,49 @@ dg_status latched_status(dg_sampler* s, const dg::Plan& pl) {
   return DG_OK;
 }
 
+// The first part of a tick: RMSNorm and the LM head (with the timing marks 0..2).
+dg_status tick_front(dg_sampler* s, const float* resid);
+// The finishing kernel of a tick (timing mark 3).
+dg_status tick_back(dg_sampler* s);
+
 dg_status tick(dg_sampler* s, const float* resid) {
+  dg_status st = tick_front(s, resid);
+  return st == DG_OK ? tick_back(s) : st;
+}
+
+dg_status mark_event(dg_sampler* s, int i) {
+  // external event nodes when the tick is captured in a CUDA graph, plain records otherwise
+  if (!s->timed) return DG_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  DG_CUDA(s->err, cudaStreamIsCapturing(s->stream, &cap), "query stream capture");
+  const unsigned rec_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+  DG_CUDA(s->err, cudaEventRecordWithFlags(s->timing[i], s->stream, rec_flags), "record timing event");
+  return DG_OK;
+}
+
+dg_status tick_back(dg_sampler* s) {
+  DG_CUDA(s->err, dg::launch_finish(s->dv, s->stream), "launch finish");
+  dg_status st = mark_event(s, 3);
+  if (st != DG_OK) return st;
+  ++s->host_tick;
+  return DG_OK;
+}
+
+dg_status tick_front(dg_sampler* s, const float* resid) {
   if (s->host_tick >= s->tick_bound) {
     set_err(s->err, "every canvas has finished (tick %lld)", (long long)s->host_tick);
     return DG_ERR_STATE;
   }
-  // external event nodes when the tick is captured in a CUDA graph, plain records otherwise
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (s->timed) DG_CUDA(s->err, cudaStreamIsCapturing(s->stream, &cap), "query stream capture");
-  const unsigned rec_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
-  auto mark = [&](int i) {
-    return s->timed ? cudaEventRecordWithFlags(s->timing[i], s->stream, rec_flags) : cudaSuccess;
-  };
-  DG_CUDA(s->err, mark(0), "record timing event");
+  dg_status st = mark_event(s, 0);
+  if (st != DG_OK) return st;
   // the LM head on SM pairs forms the RMSNorm rows itself
   if (!s->pair) DG_CUDA(s->err, dg::launch_rmsnorm(s->dv, resid, s->stream), "launch rmsnorm");
-  DG_CUDA(s->err, mark(1), "record timing event");
+  if ((st = mark_event(s, 1)) != DG_OK) return st;
   DG_CUDA(s->err,
           s->pair ? dg::launch_lmhead_pair(s->dv, resid, &s->tmA, &s->tmB, s->num_sms, s->stream)
                   : dg::launch_lmhead(s->dv, &s->tmA, &s->tmB, s->num_sms, s->stream),
           "launch lm head");
-  DG_CUDA(s->err, mark(2), "record timing event");
-  DG_CUDA(s->err, dg::launch_finish(s->dv, s->stream), "launch finish");
-  DG_CUDA(s->err, mark(3), "record timing event");
-  ++s->host_tick;
-  return DG_OK;
+  return mark_event(s, 2);
 }
 
 }  // namespace
@@ -344,6 +390,10 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.n_sub = L.n_sub;
   dv.rows_cap = L.rows_cap;
   dv.max_active = L.max_active;
+  dv.chunk_begin = L.chunk_begin;
+  dv.chunk_end = L.chunk_end;
+  dv.vt_base = L.chunk_begin * L.tiles_per_chunk;
+  s->split = cfg->vocab_ranks > 1;
 
   auto fail = [&](dg_status st) {
     memcpy(g_create_err, s->err, sizeof g_create_err);
@@ -352,7 +402,11 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   };
   if (!encode_2d(&s->tmA, dv.h, (uint64_t)L.rows_cap, (uint64_t)dv.d, dg::kBM, s->err)) return fail(DG_ERR_ARG);
   s->pair = (int64_t)L.max_active * cfg->canvas_len >= 2 * dg::kBM && sms >= 2;
-  if (!encode_2d(&s->tmB, w_vocab, (uint64_t)dv.V, (uint64_t)dv.d, s->pair ? dg::kBN / 2 : dg::kBN, s->err))
+  // W: the whole matrix, or this rank's slice of whole chunks
+  const int64_t v_begin = (int64_t)dv.vt_base * dg::kBN;
+  const int64_t v_end = std::min<int64_t>((int64_t)L.chunk_end * L.tiles_per_chunk * dg::kBN, dv.V);
+  if (!encode_2d(&s->tmB, w_vocab, (uint64_t)(v_end - v_begin), (uint64_t)dv.d, s->pair ? dg::kBN / 2 : dg::kBN,
+                 s->err))
     return fail(DG_ERR_ARG);
   cudaError_t ce = dg::lmhead_configure();
   if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "configure kernels"));
@@ -400,8 +454,55 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   return DG_OK;
 }
 
+static dg_status refuse_split(dg_sampler* s) {
+  set_err(s->err, "the vocabulary of this sampler is split across ranks: tick with dg_denoise_step_partial, "
+                  "exchange the partial records, then dg_denoise_step_finish");
+  return DG_ERR_STATE;
+}
+
+dg_status dg_denoise_step_partial(dg_sampler* s, const float* resid) {
+  if (!s) return DG_ERR_ARG;
+  if (!resid) return set_err(s->err, "resid is NULL"), DG_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(resid) % 16) return set_err(s->err, "resid must be 16-byte aligned"), DG_ERR_ALIGN;
+  if (s->partial_pending)
+    return set_err(s->err, "the previous partial tick has not been finished (dg_denoise_step_finish)"), DG_ERR_STATE;
+  dg_status st = tick_front(s, resid);
+  if (st == DG_OK) s->partial_pending = true;
+  return st;
+}
+
+dg_status dg_denoise_step_finish(dg_sampler* s) {
+  if (!s) return DG_ERR_ARG;
+  if (!s->partial_pending) return set_err(s->err, "no partial tick to finish"), DG_ERR_STATE;
+  s->partial_pending = false;
+  return tick_back(s);
+}
+
+dg_status dg_partial_records(const dg_sampler* s, void** records_dev, int32_t* rows_cap, int32_t* n_chunks,
+                             int32_t* chunk_begin, int32_t* chunk_end) {
+  if (!s) return DG_ERR_ARG;
+  if (records_dev) *records_dev = s->dv.part;
+  if (rows_cap) *rows_cap = s->dv.rows_cap;
+  if (n_chunks) *n_chunks = s->dv.n_sub;
+  if (chunk_begin) *chunk_begin = s->dv.chunk_begin;
+  if (chunk_end) *chunk_end = s->dv.chunk_end;
+  return DG_OK;
+}
+
+dg_status dg_vocab_slice(int32_t vocab, int32_t ranks, int32_t rank, int32_t* v_begin, int32_t* v_end) {
+  if (vocab < 2 || ranks < 0 || rank < 0 || rank >= (ranks > 1 ? ranks : 1) || !v_begin || !v_end) return DG_ERR_ARG;
+  int n_vtiles, tpc, n_chunks, c0, c1;
+  vocab_chunking(vocab, &n_vtiles, &tpc, &n_chunks);
+  if (ranks > n_chunks) return DG_ERR_ARG;
+  rank_chunks(n_chunks, ranks, rank, &c0, &c1);
+  *v_begin = c0 * tpc * dg::kBN;
+  *v_end = std::min(c1 * tpc * dg::kBN, vocab);
+  return DG_OK;
+}
+
 dg_status dg_denoise_step(dg_sampler* s, const float* resid) {
   if (!s) return DG_ERR_ARG;
+  if (s->split) return refuse_split(s);
   if (!resid) return set_err(s->err, "resid is NULL"), DG_ERR_ARG;
   if (reinterpret_cast<uintptr_t>(resid) % 16) return set_err(s->err, "resid must be 16-byte aligned"), DG_ERR_ALIGN;
   return tick(s, resid);
@@ -409,6 +510,7 @@ dg_status dg_denoise_step(dg_sampler* s, const float* resid) {
 
 dg_status dg_denoise_step_host(dg_sampler* s, const float* resid_host, int32_t* canvas_host, float* entropy_host) {
   if (!s) return DG_ERR_ARG;
+  if (s->split) return refuse_split(s);
   if (!resid_host) return set_err(s->err, "resid_host is NULL"), DG_ERR_ARG;
   const size_t BL = (size_t)s->dv.B * s->dv.L;
   // Page-locked input mapped into the device's address space is read by the
@@ -460,6 +562,7 @@ dg_status dg_sync_info(dg_sampler* s, dg_slot* slots_host) {
 dg_status dg_run(dg_sampler* s, dg_resid_fn fn, void* user, float* resid_dev, int32_t* tokens_host,
                  dg_slot* slots_host) {
   if (!s || !fn) return DG_ERR_ARG;
+  if (s->split) return refuse_split(s);
   float* resid = resid_dev ? resid_dev : s->dv.resid_stage;
   if (reinterpret_cast<uintptr_t>(resid) % 16) return set_err(s->err, "resid_dev must be 16-byte aligned"), DG_ERR_ALIGN;
   std::vector<dg_slot> sl(s->dv.B);
@@ -536,6 +639,7 @@ dg_status dg_set_state(dg_sampler* s, const dg_state* h) {
   DG_CUDA(s->err, dg::launch_plan(s->dv, h->tick, s->stream), "launch plan");
   DG_CUDA(s->err, cudaStreamSynchronize(s->stream), "synchronize");
   s->host_tick = h->tick;
+  s->partial_pending = false;  // a partial tick of the replaced state is dropped
   int32_t max_admit = 0;
   for (int32_t a : s->admit) max_admit = a > max_admit ? a : max_admit;
   s->tick_bound = (int64_t)(h->tick > max_admit ? h->tick : max_admit) +

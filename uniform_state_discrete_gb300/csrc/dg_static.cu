@@ -251,6 +251,9 @@ extern "C" dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, co
   dv.tiles_per_chunk = tpc;
   dv.n_chunks = n_chunks;
   dv.n_sub = n_chunks * dg::kSubPerChunk;
+  dv.chunk_begin = 0;
+  dv.chunk_end = n_chunks;
+  dv.vt_base = 0;
   dv.rows_cap = DG_STATIC_MAX_ROWS;
   dv.max_active = 1;
 
