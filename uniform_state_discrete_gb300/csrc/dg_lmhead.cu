@@ -296,10 +296,10 @@ struct BestScore {
 // of the CTA found (shared memory), or one any unit of the row found this tick
 // (global memory).  Each is the score of a real entry, so the row's winner is
 // always scored and the result equals the unscreened maximum.  The walk is
-// started only if E_(0) can pass: since -ln U >= 1 - U = q, the group is skipped
-// when q(a0) >= 16 2^(u_max - g), on the first Philox block alone -- one block
-// for sixteen entries.  Walks run one step per lane per round, all lanes of
-// the warp together.  Equal scores keep the lower index.
+// started only if its first entry or the second order statistic can pass,
+// tested on the first Philox block alone -- one block for sixteen entries (see
+// below).  Walks run one step per lane per round, all lanes of the warp
+// together.  Equal scores keep the lower index.
 template <bool kTail, bool kCap>
 __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, BestScore& bs,
                                        float cap, float inv_cap) {
@@ -346,10 +346,19 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
   }
   st.S += (S[0] + S[1]) + (S[2] + S[3]);
   st.A += (A[0] + A[1]) + (A[2] + A[3]);
-  // can the group's smallest variate E_(0) = X_0 / 16 >= q(a0) / 16 beat g?
+  // Can any entry of the group beat g?  The entry holding E_(0) = X_0 / 16 (slot r_0, known from
+  // the first slot word alone) only if X_0 / 16 < 2^(u_slot - g); every other entry only if
+  // E_(1) = X_0 / 16 + X_1 / 15 < 2^(u_max - g).  With X >= q = 1 - U and, from the funnel-shift
+  // word f = 1 + Ut, q >= 2 - f - 2^-23, both tests take the first Philox block alone.
   const float emax = ex2_approx(fmaf(cmz, rm.scale, nm));  // 2^(u_max - m)
   const float g0 = fmaxf(fmaxf(st.g, bs.known), key_ord(*(volatile int*)bs.cta));
-  bool live = g0 == -INFINITY || screen_word(w4[0]) > screen_threshold(16.f * emax * screen_factor(m, g0));
+  bool live = true;
+  if (g0 != -INFINITY) {
+    const float K = screen_factor(m, g0);
+    const float q0 = (2.f - 0x1p-23f) - screen_word(w4[0]), q1 = (2.f - 0x1p-23f) - screen_word(w4[2]);
+    const float e0 = ex2_approx(fmaf(select16(z, __umulhi(w4[1], 16u)), rm.scale, nm));  // 2^(u_slot - m)
+    live = q0 * 0.0625f < e0 * K || fmaf(q1, 1.f / 15.f, q0 * 0.0625f) < emax * K;
+  }
   const unsigned act = __activemask();
   if (!__any_sync(act, live)) return;
   bool improved = false;
@@ -368,7 +377,7 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
         rem &= ~(1u << slot);
         const int idx = v0 + (int)slot;
         if (!kTail || idx < V) {
-          const float sc = (m + fmaf(select16(z, slot), rm.scale, nm)) - lg2_approx(E);
+          const float sc = fmaf(select16(z, slot), rm.scale, -lg2_approx(E));
           if (sc > st.g || (sc == st.g && idx < st.gidx)) {
             st.g = sc;
             st.gidx = idx;
@@ -386,6 +395,29 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
   if (improved) {
     atomicMax(bs.cta, ord_key(st.g));
     bs.raised = true;
+  }
+}
+
+// A first score for a row whose unit has none yet: the entry holding its
+// group's smallest variate, E_(0) = X_0 / 16 at slot r_0 (the first Philox block
+// of the group alone), scored exactly as the walk in fold16 scores it.  Run
+// over a tile's groups before they are folded, it gives the folds the best of
+// those entries to screen against instead of starting from nothing.
+template <bool kCap>
+__device__ __forceinline__ void seed16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, float cap,
+                                       float inv_cap) {
+  if (v0 >= V) return;
+  uint32_t w4[4];
+  rm.gs.draw(8u * ((uint32_t)v0 >> 4), w4);
+  const uint32_t slot = __umulhi(w4[1], 16u);
+  const int idx = v0 + (int)slot;
+  if (idx >= V) return;
+  float zs = select16(z, slot);
+  if (kCap) zs = cap * tanhf(zs * inv_cap);
+  const float sc = fmaf(zs, rm.scale, -lg2_approx(exp_variate(w4[0]) * 0.0625f));
+  if (sc > st.g || (sc == st.g && idx < st.gidx)) {
+    st.g = sc;
+    st.gidx = idx;
   }
 }
 
@@ -675,6 +707,19 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         tc_fence_after();
         const uint32_t tbase =
             tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(cg * kColsPerWarp);
+        // no score known for the row yet (its unit's first tile, no other unit ahead of it): seed one
+        if (__any_sync(0xFFFFFFFFu, rm.valid && st.g == -INFINITY && bs.known == -INFINITY)) {
+          const bool seed = rm.valid && st.g == -INFINITY && bs.known == -INFINITY;
+#pragma unroll 1
+          for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
+            float acc[16];
+            __syncwarp();
+            tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
+            if (seed)
+              seed16<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, dv.softcap, dv.inv_softcap);
+          }
+          if (seed && st.g != -INFINITY) atomicMax(bs.cta, ord_key(st.g));
+        }
 #pragma unroll 1
         for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
           float acc[16];
@@ -1014,6 +1059,19 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         tc_fence_after();
         const uint32_t tbase =
             tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(cg * kColsPerWarp);
+        // no score known for the row yet (its unit's first tile, no other unit ahead of it): seed one
+        if (__any_sync(0xFFFFFFFFu, rm.valid && st.g == -INFINITY && bs.known == -INFINITY)) {
+          const bool seed = rm.valid && st.g == -INFINITY && bs.known == -INFINITY;
+#pragma unroll 1
+          for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
+            float acc[16];
+            __syncwarp();
+            tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
+            if (seed)
+              seed16<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, dv.softcap, dv.inv_softcap);
+          }
+          if (seed && st.g != -INFINITY) atomicMax(bs.cta, ord_key(st.g));
+        }
 #pragma unroll 1
         for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
           float acc[16];
