@@ -113,6 +113,9 @@ typedef struct dg_config {
                                   at most the number of vocabulary chunks (see
                                   dg_denoise_step_partial)                                       */
   int32_t vocab_rank;          /* this sampler's rank r in [0, G)                                */
+  int32_t self_cond;           /* 1: also hold what dg_self_condition needs (a transposed copy of
+                                  W and a bf16 [rows, V] buffer for the probabilities); 0: off.
+                                  Not with vocab_ranks > 1                                        */
 } dg_config;
 
 /* Per-canvas state, the layout of the device array returned by dg_slots().
@@ -214,6 +217,24 @@ dg_status dg_partial_records(const dg_sampler* s, void** records_dev, int32_t* r
  * vocabulary of `vocab` entries (any hidden size), so a caller can cut W
  * before creating the rank's sampler.  DG_ERR_ARG for an invalid split. */
 dg_status dg_vocab_slice(int32_t vocab, int32_t ranks, int32_t rank, int32_t* v_begin, int32_t* v_end);
+
+/*
+ * Self-conditioning input of the next step ("The Annotated DiffusionGemma",
+ * decode mode: "P @ E computes the expected token embeddings from the previous
+ * iteration"; `_forward`'s condition_x before the embedding scale): for every
+ * position of the canvases active at the last tick,
+ *   out[c, p, :] = sum_v P[v] W[v, :],  P = softmax(z / T) of that tick
+ * (after the softcap, at the tick's temperature: the distribution whose
+ * entropy the commit used), with P rounded to bf16 before the contraction, as
+ * the page casts it to the activation dtype, and fp32 accumulation.
+ *   out  dev, fp32 [B, L, d]; rows of canvases not active at the last tick are
+ *        left as they are.
+ * Asynchronous.  Call it after a tick and before the next one (it reads what
+ * the tick left in the workspace); needs a sampler created with self_cond = 1,
+ * else DG_ERR_STATE.  It runs the LM head once more (its epilogue writes P) and
+ * a tensor-core contraction of P with W, so it costs about two LM heads.
+ */
+dg_status dg_self_condition(dg_sampler* s, float* out);
 
 /* Residual supplier for dg_run: the backbone's place in the loop.  Must fill
  * resid_dev [B, L, d] for the active canvases of this tick from their current

@@ -170,6 +170,28 @@ def softcap(z: np.ndarray, c: float) -> np.ndarray:
     return z if c == 0 else c * np.tanh(z / c)
 
 
+def expected_embedding(z: np.ndarray, T, W: np.ndarray, block_rows: int = 8192):
+    """Self-conditioning input: e[p, :] = sum_v P[p, v] W[v, :] with P = softmax(z / T) row by row, in
+    fp64 from the bf16 values of W ("The Annotated DiffusionGemma", decode mode: "P @ E computes the
+    expected token embeddings from the previous iteration", P the previous step's post-softmax
+    distribution, which its denoise loop forms as Categorical(logits = model output / t); `_forward`'s
+    condition_x before the embedding scale).  ``z`` are the logits after the final softcap.  Returns
+    (e, a): e fp64 [n, d], and a[p, k] = sum_v P[p, v] |W[v, k]|, the scale of each coordinate."""
+    z = np.asarray(z, dtype=np.float64)
+    T = np.broadcast_to(np.asarray(T, dtype=np.float64), (z.shape[0],))[:, None]
+    zz = z / T
+    P = np.exp(zz - zz.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    V, d = W.shape
+    e = np.zeros((z.shape[0], d))
+    a = np.zeros((z.shape[0], d))
+    for v0 in range(0, V, block_rows):
+        Wv = bf16_value(W[v0:v0 + block_rows])
+        e += P[:, v0:v0 + block_rows] @ Wv
+        a += P[:, v0:v0 + block_rows] @ np.abs(Wv)
+    return e, a
+
+
 def stats(z: np.ndarray, T, seed, block, step, pos) -> np.ndarray:
     """Per-row temperature softmax statistics and Gumbel-max sample; returns POS_DTYPE [n]."""
     z = np.ascontiguousarray(z, dtype=np.float64)

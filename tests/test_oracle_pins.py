@@ -280,6 +280,50 @@ def test_gumbel_sample_uniform_when_logits_equal():
     assert scipy.stats.chisquare(np.bincount(st["y"], minlength=V)).pvalue > 1e-3
 
 
+# ------------------------------------------------------- self-conditioning input
+def test_expected_embedding_uniform_logits_is_mean_embedding():
+    """Equal logits: P is uniform, so P W is the mean of the W rows."""
+    W = synth.wvocab(1, 300, 24, sigma_w=0.3)
+    e, a = oracle.expected_embedding(np.full((3, 300), 0.7), 0.5, W)
+    mean = np.array([[np.mean([float(oracle.bf16_value(W[v, k])) for v in range(300)]) for k in range(24)]])
+    np.testing.assert_allclose(e, np.repeat(mean, 3, axis=0), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(a, np.repeat(np.abs(oracle.bf16_value(W)).mean(axis=0, keepdims=True), 3, 0),
+                               atol=1e-14)
+
+
+def test_expected_embedding_of_a_dominant_token_is_its_row():
+    W = synth.wvocab(2, 512, 16, sigma_w=0.3)
+    z = np.random.default_rng(3).standard_normal((2, 512))
+    z[0, 77] = 60.0  # a 40-nat margin at T = 1: every other weight is below e^-40
+    z[1, 500] = 60.0
+    e, _ = oracle.expected_embedding(z, 1.0, W)
+    np.testing.assert_allclose(e[0], oracle.bf16_value(W[77]), atol=1e-12)
+    np.testing.assert_allclose(e[1], oracle.bf16_value(W[500]), atol=1e-12)
+
+
+def test_expected_embedding_two_point_closed_form():
+    """Two finite logits: e = s W_a + (1 - s) W_b with s = sigmoid((z_a - z_b) / T)."""
+    W = synth.wvocab(4, 64, 8, sigma_w=0.3)
+    z = np.full((1, 64), -np.inf)
+    z[0, 5], z[0, 40] = 0.9, -0.3
+    e, _ = oracle.expected_embedding(z, 0.6, W)
+    s_ = 1.0 / (1.0 + math.exp(-(0.9 + 0.3) / 0.6))
+    np.testing.assert_allclose(e[0], s_ * oracle.bf16_value(W[5]) + (1 - s_) * oracle.bf16_value(W[40]), atol=1e-15)
+
+
+def test_expected_embedding_is_a_convex_combination_and_temperature_sharpens_it():
+    W = synth.wvocab(5, 1000, 32, sigma_w=0.3)
+    Wv = oracle.bf16_value(W)
+    z = np.random.default_rng(6).standard_normal((4, 1000))
+    for T in (0.3, 1.0, 3.0):
+        e, a = oracle.expected_embedding(z, T, W)
+        assert np.all(e >= Wv.min(axis=0) - 1e-15) and np.all(e <= Wv.max(axis=0) + 1e-15)
+        assert np.all(np.abs(e) <= a + 1e-15)
+    # as T -> 0 the distribution collapses onto the argmax token
+    e0, _ = oracle.expected_embedding(z, 1e-3, W)
+    np.testing.assert_allclose(e0, Wv[np.argmax(z, axis=1)], atol=1e-12)
+
+
 # ----------------------------------------------------------------- commit rule
 def test_acceptance_matches_pages_prefix_expression():
     """The pages' acceptance: sort H, accept where cumsum(sH) - sH <= bound ("Denoise, stage,

@@ -35,7 +35,8 @@ class dg_config(ctypes.Structure):
                 ("entropy_bound", ctypes.c_float), ("confidence", ctypes.c_float), ("stability", ctypes.c_int32),
                 ("rms_eps", ctypes.c_float), ("mode", ctypes.c_int32), ("max_active", ctypes.c_int32),
                 ("seeds", ctypes.POINTER(ctypes.c_uint64)), ("admit_tick", ctypes.POINTER(ctypes.c_int32)),
-                ("softcap", ctypes.c_float), ("vocab_ranks", ctypes.c_int32), ("vocab_rank", ctypes.c_int32)]
+                ("softcap", ctypes.c_float), ("vocab_ranks", ctypes.c_int32), ("vocab_rank", ctypes.c_int32),
+                ("self_cond", ctypes.c_int32)]
 
 
 class dg_slot(ctypes.Structure):
@@ -71,6 +72,7 @@ _SIGS = {
     "dg_denoise_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "dg_denoise_step_partial": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "dg_denoise_step_finish": (ctypes.c_int, [ctypes.c_void_p]),
+    "dg_self_condition": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "dg_partial_records": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
                                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
@@ -134,13 +136,14 @@ def _check(st: int, handle=None):
 
 def make_config(vocab, hidden, canvas_len, n_canvases=1, gen_blocks=1, num_inference_steps=48, t_min=0.4,
                 t_max=0.8, entropy_bound=0.1, confidence=0.005, stability=1, rms_eps=1e-6, mode=DG_FREEZE,
-                max_active=0, seeds=None, admit_tick=None, softcap=0.0, vocab_ranks=0, vocab_rank=0):
+                max_active=0, seeds=None, admit_tick=None, softcap=0.0, vocab_ranks=0, vocab_rank=0, self_cond=0):
     """Build a ``dg_config``; the returned object keeps the seed/admit arrays alive."""
     cfg = dg_config(vocab, hidden, canvas_len, n_canvases, gen_blocks, num_inference_steps, t_min, t_max,
                     entropy_bound, confidence, stability, rms_eps, mode, max_active)
     cfg.softcap = softcap
     cfg.vocab_ranks = vocab_ranks
     cfg.vocab_rank = vocab_rank
+    cfg.self_cond = self_cond
     keep = []
     if seeds is not None:
         a = (ctypes.c_uint64 * n_canvases)(*[int(s) for s in seeds])
@@ -256,6 +259,12 @@ class Sampler:
 
     def step(self, resid):
         _check(self.dg_denoise_step(resid), self.handle)
+
+    def self_condition(self, out):
+        """dg_self_condition: the expected embedding softmax(z/T) W of every position of the canvases
+        active at the last tick, into ``out`` (fp32 [B, L, d] on the device)."""
+        assert out.dtype.itemsize == 4 and out.is_contiguous() and out.numel() == self.B * self.L * self.d
+        _check(lib.dg_self_condition(self.handle, ctypes.c_void_p(out.data_ptr())), self.handle)
 
     def step_partial(self, resid):
         """dg_denoise_step_partial: RMSNorm and the LM head over this rank's vocabulary chunks."""

@@ -17,8 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 SO = os.path.join(BUILD, "libdgsampler.so")
-SOURCES = ["dg_sampler.cu", "dg_kernels.cu", "dg_lmhead.cu", "dg_static.cu"]
-HEADERS = ["dg_internal.cuh", "dg_tail.cuh", "dg_gumbel.cuh", "dg_norm.cuh"]
+SOURCES = ["dg_sampler.cu", "dg_kernels.cu", "dg_lmhead.cu", "dg_static.cu", "dg_selfcond.cu"]
+HEADERS = ["dg_internal.cuh", "dg_tail.cuh", "dg_gumbel.cuh", "dg_norm.cuh", "dg_tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -92,6 +92,16 @@ struct Dev {
   // unless the vocabulary is split across ranks), and the first vocabulary tile of the W rows the
   // tensor map covers (its row 0 is vocabulary entry vt_base * kBN)
   int32_t chunk_begin, chunk_end, vt_base;
+  // self-conditioning (dg_self_condition; all null / 0 when the sampler was created without it):
+  // what a tick leaves for it -- each row's temperature factor log2(e)/T (LM head), its log2 Z
+  // and canvas (finishing kernel) and the tick's row count -- and its buffers
+  float* row_scale;        // [rows_cap]
+  float* row_log2z;        // [rows_cap]
+  int32_t* row_canvas;     // [B] canvas of each active slot a (rows a L .. a L + L - 1)
+  uint32_t* sc_rows;       // rows of the last tick
+  uint16_t* sc_probs;      // [rows_cap, sc_vpad] bf16 P
+  float* sc_part;          // [sc_kc, rows_cap, d] per-chunk shares of P W
+  int32_t sc_vpad, sc_kc, sc_kbpc;  // V rounded up to 256; vocabulary chunks of the contraction, 64-wide K blocks each
   bool reaccept;        // DG_REACCEPT: every step re-sorts all positions (see dg_mode)
   int32_t stability;    // early stop needs this many consecutive steps with an unchanged argmax canvas
   float softcap;        // final logit softcap c (0 = off): z -> c tanh(z / c) before the temperature
@@ -250,5 +260,9 @@ cudaError_t launch_lmhead_pair(const Dev& dv, const float* resid, const CUtensor
 cudaError_t launch_finish(const Dev& dv, cudaStream_t st);
 cudaError_t launch_plan(const Dev& dv, int tick, cudaStream_t st);
 cudaError_t lmhead_configure();
+cudaError_t selfcond_configure();
+cudaError_t launch_transpose_w(const void* w, uint16_t* wt, int V, int d, int v_pad, cudaStream_t st);
+cudaError_t launch_selfcond(const Dev& dv, const CUtensorMap* tm_h, const CUtensorMap* tm_w, const CUtensorMap* tm_p,
+                            const CUtensorMap* tm_wt, float* out, int num_sms, cudaStream_t st);
 
 }  // namespace dg

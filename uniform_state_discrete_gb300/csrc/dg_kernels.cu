@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   // so a CTA that starts late cannot mistake the next tick's plan for this one's.
   const int n_rows = __ldcg(&dv.plan->n_active) * dv.L;
   const int tick = __ldcg(&dv.plan->tick);
+  if (dv.sc_rows && blockIdx.x == 0 && threadIdx.x == 0) *dv.sc_rows = (uint32_t)n_rows;  // for self-conditioning
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -124,6 +125,10 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
       const size_t o = (size_t)c * dv.L + p;
       dv.H[o] = H > 0.f ? H : 0.f;  // +0 for rounding below zero (and never -0: its bits would sort last)
       dv.logZ[o] = lz;
+      if (dv.row_log2z) {  // what the self-conditioning pass reads after the tick
+        dv.row_log2z[row] = acc.m + l2S;
+        if (p == 0) dv.row_canvas[a] = c;
+      }
       // a row without valid statistics latches an error and never hands an
       // out-of-range token to the canvas (callers index embeddings with it)
       const bool y_ok = acc.gidx >= 0 && acc.gidx < dv.V, a_ok = acc.amax >= 0 && acc.amax < dv.V;

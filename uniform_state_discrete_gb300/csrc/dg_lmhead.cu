@@ -38,124 +38,12 @@
 #include <cuda_runtime.h>
 
 #include "dg_gumbel.cuh"
-#include "dg_norm.cuh"
 #include "dg_internal.cuh"
+#include "dg_norm.cuh"
+#include "dg_tc.cuh"
 
 namespace dg {
 namespace {
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-// Raise the barrier's expected transaction bytes without arriving on it.
-__device__ __forceinline__ void mbar_expect_tx_only(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cluster.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Wait for the phase of `parity` to complete, giving up after kWaitLimitNs or
-// as soon as another role of this CTA gave up.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, Plan* plan) {
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0u) {
-      if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicExch(&plan->err, kErrTimeout);
-        atomicExch(&plan->err_info[0], (int)blockIdx.x);
-        return false;
-      }
-    }
-  }
-}
-
-// The common case -- the phase has already completed -- without a call.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, Plan* plan) {
-  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, plan);
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor for a K-major tile stored with the
-// 128-byte swizzle (rows of 128 bytes, 8-row groups 1024 bytes apart).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address >> 4
-  d |= (uint64_t)1 << 16;                            // leading byte offset (unused with this swizzle)
-  d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset: 8 rows x 128 B
-  d |= (uint64_t)1 << 46;                            // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;                            // layout: 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
-constexpr uint32_t kIdesc = (1u << 4)                         // D format fp32
-                            | (1u << 7)                       // A format bf16
-                            | (1u << 10)                      // B format bf16
-                            | ((uint32_t)(kBN >> 3) << 17)    // N / 8
-                            | ((uint32_t)(kBM >> 4) << 24);   // M / 16
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-// 16 consecutive fp32 columns of this thread's TMEM lane, waited in the same
-// statement so no use of the registers can be scheduled before the wait.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-}
 
 struct RowMeta {
   GumbelStream gs;  // this position's Philox stream of Gumbel words
@@ -190,12 +78,10 @@ __device__ __forceinline__ float screen_factor(float m, float g) {
   return ex2_approx(m - g) * fmaf(fabsf(m) + 64.f, 0x1p-20f, 1.002f);
 }
 
-// Pass test of the screen without an integer-to-float conversion: with
-// Ut = (r >> 9) 2^-23 <= U and q = 1 - U, f = 1 + Ut is built by one funnel
-// shift, and q < t implies f > 2 - t - 2^-22; the threshold below leaves a
-// further 2^-22 for its own rounding.
+// A lower bound of q = 1 - U without an integer-to-float conversion: with
+// Ut = (r >> 9) 2^-23, U - Ut < 2^-23, so q >= 2 - f - 2^-23 for f = 1 + Ut, which
+// one funnel shift builds exactly (and the subtraction from 2 - 2^-23 is exact).
 __device__ __forceinline__ float screen_word(uint32_t r) { return __uint_as_float(__funnelshift_r(r, 0x7Fu, 9)); }
-__device__ __forceinline__ float screen_threshold(float t) { return 2.f - 0x1p-21f - t; }
 
 // The Exp(1) variate E = -ln U of a word r, U = (r + 0.5) 2^-32.  For U < 3/4,
 // E comes from lg2(U).  For U >= 3/4, E = -ln(1 - q) with q = 1 - U taken
@@ -690,6 +576,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       const int rl = q * 32 + lane;         // row within the tile
       const int row = mt * kBM + rl;
       const RowMeta rm = row_meta(dv, row, n_rows);
+      if (dv.row_scale && rm.valid && cg == 0) dv.row_scale[row] = rm.scale;  // for the self-conditioning pass
       BestScore bs{gbest + rl, dv.row_best + row, epoch, -INFINITY, false};
       Partial st = empty_partial();
       for (int vt = vt0; vt < vt1; ++vt, ++tcount) {
@@ -1042,6 +929,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       const int rl = q * 32 + lane;
       const int row = mt * 2 * kBM + (int)rank * kBM + rl;
       const RowMeta rm = row_meta(dv, row, n_rows);
+      if (dv.row_scale && rm.valid && cg == 0) dv.row_scale[row] = rm.scale;  // for the self-conditioning pass
       BestScore bs{gbest + rl, dv.row_best + row, epoch, -INFINITY, false};
       Partial st = empty_partial();
       for (int vt = vt0; vt < vt1; ++vt, ++tcount) {

@@ -21,6 +21,7 @@ struct dg_sampler {
   std::vector<int32_t> admit;
   dg::Dev dv;
   CUtensorMap tmA, tmB;
+  CUtensorMap tmW256, tmP, tmWT;  // self-conditioning: W in 256-row boxes, P, W^T
   bool pair;  // LM head on CTA pairs (tcgen05 cta_group::2), chosen when a tick can hold >= 256 rows
   bool split = false;            // the vocabulary is split across ranks (dg_denoise_step_partial / _finish)
   bool partial_pending = false;  // a partial tick waits for its finishing step
@@ -63,6 +64,9 @@ struct Layout {
   size_t total;
   int rows_cap, n_vtiles, tiles_per_chunk, n_chunks, n_sub, max_active;
   int chunk_begin, chunk_end;  // this rank's vocabulary chunks
+  // self-conditioning buffers (0 when off)
+  size_t wt, probs, sc_part, row_scale, row_log2z, row_canvas, sc_rows;
+  int sc_vpad, sc_kc, sc_kbpc;
 };
 
 // The LM head's vocabulary chunking, which depends on V only: 256-entry tiles,
@@ -113,6 +117,9 @@ bool validate(const dg_config* c, char* why) {
   if (c->admit_tick)
     for (int i = 0; i < c->n_canvases; ++i)
       if (c->admit_tick[i] < 0) return set_err(why, "admit_tick[%d] is negative", i), false;
+  if (c->self_cond != 0 && c->self_cond != 1) return set_err(why, "self_cond must be 0 or 1"), false;
+  if (c->self_cond && c->vocab_ranks > 1)
+    return set_err(why, "self_cond needs the whole vocabulary (vocab_ranks <= 1)"), false;
   if (c->vocab_ranks < 0 || c->vocab_rank < 0 || c->vocab_rank >= (c->vocab_ranks > 1 ? c->vocab_ranks : 1))
     return set_err(why, "vocab_rank must be in [0, vocab_ranks) (got %d of %d)", c->vocab_rank, c->vocab_ranks),
            false;
@@ -163,6 +170,24 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
   L->canvas_rows = take(4 * B);
   L->temps = take(4 * (size_t)c->num_inference_steps);
   L->sync = take(4 * (2 + (size_t)L->rows_cap / 128));  // rows_ready, fin_started, slab_done[rows_cap / 128]
+  L->wt = L->probs = L->sc_part = L->row_scale = L->row_log2z = L->row_canvas = L->sc_rows = 0;
+  L->sc_vpad = L->sc_kc = L->sc_kbpc = 0;
+  if (c->self_cond) {
+    // the contraction's grid: row tiles x 256-wide d tiles x vocabulary chunks, about two units per SM
+    L->sc_vpad = L->n_vtiles * dg::kBN;
+    const int kbv = L->sc_vpad / dg::kBK, n_mt = (int)((rows + dg::kBM - 1) / dg::kBM), n_dt = (int)((d + 255) / 256);
+    int kc = (304 + n_mt * n_dt - 1) / (n_mt * n_dt);
+    kc = kc < 1 ? 1 : (kc > kbv ? kbv : kc);
+    L->sc_kbpc = (kbv + kc - 1) / kc;
+    L->sc_kc = (kbv + L->sc_kbpc - 1) / L->sc_kbpc;  // every chunk holds at least one K block
+    L->wt = take(2 * d * (size_t)L->sc_vpad);
+    L->probs = take(2 * (size_t)L->rows_cap * L->sc_vpad);
+    L->sc_part = take(4 * (size_t)L->sc_kc * L->rows_cap * d);
+    L->row_scale = take(4 * (size_t)L->rows_cap);
+    L->row_log2z = take(4 * (size_t)L->rows_cap);
+    L->row_canvas = take(4 * B);
+    L->sc_rows = take(4);
+  }
   L->total = o;
   return 1;
 }
@@ -394,6 +419,17 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.chunk_end = L.chunk_end;
   dv.vt_base = L.chunk_begin * L.tiles_per_chunk;
   s->split = cfg->vocab_ranks > 1;
+  if (cfg->self_cond) {
+    dv.row_scale = reinterpret_cast<float*>(w + L.row_scale);
+    dv.row_log2z = reinterpret_cast<float*>(w + L.row_log2z);
+    dv.row_canvas = reinterpret_cast<int32_t*>(w + L.row_canvas);
+    dv.sc_rows = reinterpret_cast<uint32_t*>(w + L.sc_rows);
+    dv.sc_probs = reinterpret_cast<uint16_t*>(w + L.probs);
+    dv.sc_part = reinterpret_cast<float*>(w + L.sc_part);
+    dv.sc_vpad = L.sc_vpad;
+    dv.sc_kc = L.sc_kc;
+    dv.sc_kbpc = L.sc_kbpc;
+  }
 
   auto fail = [&](dg_status st) {
     memcpy(g_create_err, s->err, sizeof g_create_err);
@@ -410,6 +446,15 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
     return fail(DG_ERR_ARG);
   cudaError_t ce = dg::lmhead_configure();
   if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "configure kernels"));
+  if (cfg->self_cond) {
+    uint16_t* wt = reinterpret_cast<uint16_t*>(w + L.wt);
+    if (!encode_2d(&s->tmW256, w_vocab, (uint64_t)dv.V, (uint64_t)dv.d, dg::kBN, s->err) ||
+        !encode_2d(&s->tmP, dv.sc_probs, (uint64_t)L.rows_cap, (uint64_t)L.sc_vpad, dg::kBM, s->err) ||
+        !encode_2d(&s->tmWT, wt, (uint64_t)dv.d, (uint64_t)L.sc_vpad, dg::kBN, s->err))
+      return fail(DG_ERR_ARG);
+    ce = dg::selfcond_configure();
+    if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "configure self-conditioning kernels"));
+  }
 
   std::vector<dg_slot> slots(B);
   for (int c = 0; c < B; ++c) {
@@ -443,6 +488,8 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
     if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "allocate the pinned result staging"));
   }
   ce = cudaMemsetAsync(workspace, 0, L.total, s->stream);
+  if (ce == cudaSuccess && cfg->self_cond)
+    ce = dg::launch_transpose_w(w_vocab, reinterpret_cast<uint16_t*>(w + L.wt), dv.V, dv.d, L.sc_vpad, s->stream);
   if (ce == cudaSuccess)
     ce = cudaMemcpyAsync(dv.slots, slots.data(), sizeof(dg_slot) * B, cudaMemcpyHostToDevice, s->stream);
   if (ce == cudaSuccess)
@@ -497,6 +544,19 @@ dg_status dg_vocab_slice(int32_t vocab, int32_t ranks, int32_t rank, int32_t* v_
   rank_chunks(n_chunks, ranks, rank, &c0, &c1);
   *v_begin = c0 * tpc * dg::kBN;
   *v_end = std::min(c1 * tpc * dg::kBN, vocab);
+  return DG_OK;
+}
+
+dg_status dg_self_condition(dg_sampler* s, float* out) {
+  if (!s) return DG_ERR_ARG;
+  if (!out) return set_err(s->err, "out is NULL"), DG_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(out) % 16) return set_err(s->err, "out must be 16-byte aligned"), DG_ERR_ALIGN;
+  if (!s->dv.sc_probs) return set_err(s->err, "the sampler was created without self_cond"), DG_ERR_STATE;
+  if (s->partial_pending) return set_err(s->err, "a partial tick is not finished"), DG_ERR_STATE;
+  DG_CUDA(s->err,
+          dg::launch_selfcond(s->dv, &s->tmA, s->pair ? &s->tmW256 : &s->tmB, &s->tmP, &s->tmWT, out, s->num_sms,
+                              s->stream),
+          "launch self-conditioning");
   return DG_OK;
 }
 

@@ -1,0 +1,356 @@
+// Self-conditioning input for the next denoising step: the expected token
+// embedding under this step's distribution,
+//   e[p, :] = sum_v P[p, v] W[v, :],  P[p, :] = softmax(z[p, :] / T),
+// "The Annotated DiffusionGemma", decode mode ("P @ E computes the expected
+// token embeddings from the previous iteration, L independent convex sums")
+// and `_forward`'s condition_x, before the embedding scale; P is the same
+// distribution whose entropy the commit uses (the page's denoise loop forms
+// Categorical(logits = model output / t) and passes its probs to the next
+// decode), cast to bf16 before the contraction as the page casts it to the
+// activation dtype.
+//
+// It runs after a tick, from what the tick left: the normalised rows h, each
+// row's temperature factor (LM head) and log2 Z (finishing kernel).  Three
+// kernels on the sampler's stream:
+//   k_selfcond<kProbs>  the tied LM head again (tcgen05, M = 128, N = 256),
+//                       whose epilogue writes P = 2^(z log2(e)/T - log2 Z) in
+//                       bf16 to a [rows, V_pad] buffer (zeros past V);
+//   k_selfcond<kGemm>   E_part[kc] = P[:, chunk kc] W^T[:, chunk kc]^T on the
+//                       same tensor-core mainloop, A = P and B = W^T (a
+//                       transposed copy of W made at sampler creation), both
+//                       K-major along the vocabulary, split into vocabulary
+//                       chunks kc so the grid fills the GPU;
+//   k_selfcond_reduce   e = sum over kc in order (deterministic), written to
+//                       the caller's [B, L, d] array at each row's canvas.
+// Producer (warp 0), MMA issuer (warp 1) and 16 epilogue warps as in the LM
+// head; every wait is bounded (1 s) and latches DG_ERR_TIMEOUT.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "dg_internal.cuh"
+#include "dg_tc.cuh"
+
+namespace dg {
+namespace {
+
+enum : int { kProbs = 0, kGemm = 1 };
+
+// The units of one launch: kProbs (row tile, vocabulary chunk) with the chunk's
+// vocabulary tiles as N tiles and the hidden dimension as K; kGemm (row tile,
+// d tile, vocabulary chunk kc) with one N tile and the chunk's vocabulary
+// columns as K.
+struct ScUnits {
+  int n_mt, n_dt, KB;
+  __device__ __forceinline__ int units(const Dev& dv, int mode) const {
+    return mode == kProbs ? n_mt * dv.n_chunks : n_mt * n_dt * dv.sc_kc;
+  }
+  // first/last N tile and first/last K block of unit u, and its row tile
+  __device__ __forceinline__ void at(const Dev& dv, int mode, int u, int& mt, int& t0, int& t1, int& kb0,
+                                     int& kb1) const {
+    if (mode == kProbs) {
+      const int chunk = u / n_mt;
+      mt = u - chunk * n_mt;
+      t0 = chunk * dv.tiles_per_chunk;
+      t1 = min(t0 + dv.tiles_per_chunk, dv.n_vtiles);
+      kb0 = 0;
+      kb1 = KB;
+    } else {
+      const int kc = u / (n_mt * n_dt), r = u - kc * n_mt * n_dt;
+      const int dt = r / n_mt;
+      mt = r - dt * n_mt;
+      t0 = dt;
+      t1 = dt + 1;
+      kb0 = kc * dv.sc_kbpc;
+      kb1 = min(kb0 + dv.sc_kbpc, dv.sc_vpad / kBK);
+    }
+  }
+};
+
+template <int kMode, bool kCap>
+__global__ void __launch_bounds__(kThreadsLM, 1)
+    k_selfcond(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kStageA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kStageB);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"((uint32_t)kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // rows of the tick that left h, the temperature factors and log2 Z behind
+  const int n_rows = (int)__ldcg(dv.sc_rows);
+  const ScUnits su{(n_rows + kBM - 1) / kBM, (dv.d + kBN - 1) / kBN, (dv.d + kBK - 1) / kBK};
+  const int n_units = su.units(dv, kMode);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int issued_parity[kStages];
+      for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        int mt, t0, t1, kb0, kb1;
+        su.at(dv, kMode, u, mt, t0, t1, kb0, kb1);
+        for (int t = t0; t < t1 && ok; ++t) {
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&full[stage], (uint32_t)(kStageA + kStageB));
+            tma_load_2d(sA + stage * kStageA, &tmA, kb * kBK, mt * kBM, &full[stage]);
+            tma_load_2d(sB + stage * kStageB, &tmB, kb * kBK, t * kBN, &full[stage]);
+            issued_parity[stage] = (int)phase;
+            if (++stage == (uint32_t)kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kStages; ++s) {
+          if (issued_parity[s] < 0) continue;
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(&full[s], (uint32_t)issued_parity[s]) && global_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint64_t adesc0 = sw128_desc(smem_u32(sA)), bdesc0 = sw128_desc(smem_u32(sB));
+      uint32_t stage = 0, phase = 0, tcount = 0;
+      bool ok = true, any = false;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        int mt, t0, t1, kb0, kb1;
+        su.at(dv, kMode, u, mt, t0, t1, kb0, kb1);
+        for (int t = t0; t < t1 && ok; ++t, ++tcount) {
+          const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
+          if (!mbar_wait(&tempty[ab], aph ^ 1u, abort_flag, dv.plan)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + ab * (uint32_t)kBN;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, dv.plan)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad = adesc0 + (uint64_t)((stage * kStageA) >> 4);
+            const uint64_t bd = bdesc0 + (uint64_t)((stage * kStageB) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), (kb != kb0 || kk != 0) ? 1u : 0u);
+            mma_commit(&empty[stage]);
+            any = true;
+            if (++stage == (uint32_t)kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&tfull[ab]);
+        }
+      }
+      if (!ok && any) {
+        mma_commit(drain);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(drain, 0u) && global_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int cg = (warp - 2) >> 2;
+    uint32_t tcount = 0;
+    bool aborted = false;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      int mt, t0, t1, kb0, kb1;
+      su.at(dv, kMode, u, mt, t0, t1, kb0, kb1);
+      const int row = mt * kBM + q * 32 + lane;
+      const bool valid = row < n_rows;
+      const float scale = valid && kMode == kProbs ? __ldcg(dv.row_scale + row) : 0.f;
+      const float l2z = valid && kMode == kProbs ? __ldcg(dv.row_log2z + row) : 0.f;
+      for (int t = t0; t < t1; ++t, ++tcount) {
+        if (aborted) continue;
+        const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
+        int got = 0;
+        if (lane == 0) got = mbar_wait(&tfull[ab], aph, abort_flag, dv.plan) ? 1 : 0;
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!got) {
+          aborted = true;
+          continue;
+        }
+        tc_fence_after();
+        const uint32_t tbase =
+            tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(cg * kColsPerWarp);
+#pragma unroll 1
+        for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
+          float acc[16];
+          __syncwarp();
+          tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
+          if (cc == kColsPerWarp / 16 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ab]);
+          }
+          if (!valid) continue;
+          const int c0 = t * kBN + cg * kColsPerWarp + cc * 16;  // vocabulary entry (kProbs) or hidden column (kGemm)
+          if (kMode == kProbs) {
+            // P = 2^(u - log2 Z), u = z log2(e)/T, rounded to bf16 (zero past V)
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              float z0 = acc[j], z1 = acc[j + 1];
+              if (kCap) {
+                z0 = dv.softcap * tanhf(z0 * dv.inv_softcap);
+                z1 = dv.softcap * tanhf(z1 * dv.inv_softcap);
+              }
+              const float p0 = c0 + j < dv.V ? ex2_approx(fmaf(z0, scale, -l2z)) : 0.f;
+              const float p1 = c0 + j + 1 < dv.V ? ex2_approx(fmaf(z1, scale, -l2z)) : 0.f;
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(dv.sc_probs + (size_t)row * dv.sc_vpad + c0);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else {
+            // this vocabulary chunk's share of e for hidden columns [c0, c0 + 16)
+            const int kc = kb0 / dv.sc_kbpc;
+            float* dst = dv.sc_part + ((size_t)kc * dv.rows_cap + row) * dv.d + c0;
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+              if (c0 + j < dv.d) *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)kTmemCols)
+                 : "memory");
+  }
+}
+
+// e[c, p, :] = sum over the vocabulary chunks, in chunk order, of their shares
+// of row a L + p, written where canvas c = row_canvas[a] keeps its positions.
+__global__ void __launch_bounds__(256) k_selfcond_reduce(const Dev dv, float* __restrict__ out) {
+  const int n_rows = (int)__ldcg(dv.sc_rows);
+  const int d4 = dv.d >> 2;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)n_rows * d4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int row = (int)(i / d4), k = (int)(i - (long long)row * d4) * 4;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int kc = 0; kc < dv.sc_kc; ++kc) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(dv.sc_part + ((size_t)kc * dv.rows_cap + row) * dv.d + k));
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+    const int a = row / dv.L, p = row - a * dv.L;
+    const int c = __ldcg(dv.row_canvas + a);
+    *reinterpret_cast<float4*>(out + ((size_t)c * dv.L + p) * dv.d + k) = s;
+  }
+}
+
+// W [V, d] -> W^T [d, V_pad], zero past V, through 32 x 32 tiles in shared memory.
+__global__ void __launch_bounds__(256) k_transpose_w(const uint16_t* __restrict__ W, uint16_t* __restrict__ WT, int V,
+                                                     int d, int v_pad) {
+  __shared__ uint16_t t[32][33];
+  const int v0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int v = v0 + i, k = k0 + (int)threadIdx.x;
+    t[i][threadIdx.x] = (v < V && k < d) ? W[(size_t)v * d + k] : (uint16_t)0;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int k = k0 + i, v = v0 + (int)threadIdx.x;
+    if (k < d && v < v_pad) WT[(size_t)k * v_pad + v] = t[threadIdx.x][i];
+  }
+}
+
+constexpr size_t kSmemBytesSc = 1024 + (size_t)kStages * (kStageA + kStageB) + 256;
+static_assert(kSmemBytesSc <= 232448, "shared memory per CTA");
+
+}  // namespace
+
+cudaError_t selfcond_configure() {
+  cudaError_t e = cudaSuccess;
+  for (auto k : {k_selfcond<kProbs, false>, k_selfcond<kProbs, true>, k_selfcond<kGemm, false>,
+                 k_selfcond<kGemm, true>})
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesSc);
+  return e;
+}
+
+cudaError_t launch_transpose_w(const void* w, uint16_t* wt, int V, int d, int v_pad, cudaStream_t st) {
+  k_transpose_w<<<dim3(v_pad / 32, (d + 31) / 32), dim3(32, 8), 0, st>>>(static_cast<const uint16_t*>(w), wt, V, d,
+                                                                        v_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selfcond(const Dev& dv, const CUtensorMap* tm_h, const CUtensorMap* tm_w, const CUtensorMap* tm_p,
+                            const CUtensorMap* tm_wt, float* out, int num_sms, cudaStream_t st) {
+  const int max_mt = (dv.max_active * dv.L + kBM - 1) / kBM;
+  const int n_dt = (dv.d + kBN - 1) / kBN;
+  int g1 = max_mt * dv.n_chunks, g2 = max_mt * n_dt * dv.sc_kc;
+  g1 = g1 < num_sms ? g1 : num_sms;
+  g2 = g2 < num_sms ? g2 : num_sms;
+  const bool cap = dv.softcap > 0.f;
+  if (cap)
+    k_selfcond<kProbs, true><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
+  else
+    k_selfcond<kProbs, false><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_selfcond<kGemm, false><<<g2, kThreadsLM, kSmemBytesSc, st>>>(*tm_p, *tm_wt, dv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long work = (long long)dv.max_active * dv.L * (dv.d >> 2);
+  long long blocks = (work + 255) / 256;
+  if (blocks > 8 * num_sms) blocks = 8 * num_sms;
+  k_selfcond_reduce<<<(int)(blocks > 0 ? blocks : 1), 256, 0, st>>>(dv, out);
+  return cudaGetLastError();
+}
+
+}  // namespace dg
