@@ -64,7 +64,9 @@ typedef enum dg_status {
   DG_ERR_STATE = 5,       /* call not valid in the sampler's state (e.g. all done) */
   DG_ERR_NONFINITE = 6,   /* a kernel met a non-finite logit statistic             */
   DG_ERR_UNSUPPORTED = 7, /* a valid request this build does not implement         */
-  DG_ERR_TIMEOUT = 8      /* a kernel's bounded wait ran out (pipeline stalled)    */
+  DG_ERR_TIMEOUT = 8,     /* a kernel's bounded wait ran out (pipeline stalled)    */
+  DG_ERR_BOUNDS = 9       /* debug build: an index check failed, the access was
+                             skipped (dg_debug_check)                             */
 } dg_status;
 
 /* Commit semantics.
@@ -316,6 +318,21 @@ dg_status dg_set_state(dg_sampler* s, const dg_state* host);
  * and nothing faults.  The sampler's state after such a tick is undefined;
  * dg_set_state (which also clears the latch) makes it usable again. */
 dg_status dg_debug_hold_slabs(dg_sampler* s, int on);
+
+/*
+ * Race and bounds checks of the debug build (the library compiled with
+ * DG_DEBUG_CHECKS; the release build returns DG_ERR_UNSUPPORTED).  In that
+ * build every sub-buffer of the workspace is followed by a 256-byte guard
+ * filled with 0xA5 at creation, and the kernels check their indices (canvas,
+ * position, block and token ranges, row tiles, vocabulary tiles and partial
+ * records) before they touch memory: a failed check skips the access and
+ * latches DG_ERR_BOUNDS with the check's site and value instead of faulting.
+ * dg_debug_check (synchronizing) reads every guard back: DG_OK when all are
+ * intact, else DG_ERR_BOUNDS with the workspace offset of the first damaged
+ * guard in *first_bad (NULL allowed); a latched index failure is reported the
+ * same way, with its site and value in the message.
+ */
+dg_status dg_debug_check(dg_sampler* s, uint64_t* first_bad);
 
 const char* dg_status_string(dg_status st);
 const char* dg_last_error(const dg_sampler* s); /* "" when none; s may be NULL (last create failure) */

@@ -127,3 +127,11 @@ def test_vocab_split_rules():
             assert all(c[0] % 256 == 0 and c[1] > c[0] for c in cuts)
     with pytest.raises(dg.DGError):
         dg.vocab_slice(1000, 5, 0)  # 4 tiles, 4 chunks
+
+
+def test_release_build_has_no_debug_checks():
+    """dg_debug_check answers DG_ERR_UNSUPPORTED in the release build (no guards, no index checks) and
+    DG_ERR_ARG for a NULL sampler."""
+    import uniform_state_discrete_gb300 as dg
+    assert dg.lib.dg_debug_check(None, None) == dg.DG_ERR_ARG
+    assert dg.lib.dg_status_string(dg.DG_ERR_BOUNDS) == b"DG_ERR_BOUNDS"

@@ -18,11 +18,13 @@ from typing import Optional
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_build", "libdgsampler.so")
+# DG_LIBRARY=debug selects the index-checking build (libdgsampler_debug.so, build.py --debug)
+LIB_PATH = os.path.join(_PKG, "_build", "libdgsampler_debug.so" if os.environ.get("DG_LIBRARY") == "debug"
+                        else "libdgsampler.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "dg_sampler.h")
 
 DG_OK, DG_ERR_ARG, DG_ERR_ALIGN, DG_ERR_WORKSPACE, DG_ERR_CUDA, DG_ERR_STATE, DG_ERR_NONFINITE, \
-    DG_ERR_UNSUPPORTED, DG_ERR_TIMEOUT = range(9)
+    DG_ERR_UNSUPPORTED, DG_ERR_TIMEOUT, DG_ERR_BOUNDS = range(10)
 DG_FREEZE = 0
 DG_REACCEPT = 1
 WAITING, ACTIVE, DONE = 0, 1, 2
@@ -98,6 +100,7 @@ _SIGS = {
     "dg_debug_hold_slabs": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "dg_get_state": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(dg_state)]),
     "dg_set_state": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(dg_state)]),
+    "dg_debug_check": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64)]),
     "dg_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dg_last_error": (ctypes.c_char_p, [ctypes.c_void_p]),
     "dg_lmhead_stats_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
@@ -331,6 +334,12 @@ class Sampler:
     def debug_hold_slabs(self, on: bool):
         """Failure-detection test hook (dg_debug_hold_slabs): the next ticks' bounded waits run out."""
         _check(lib.dg_debug_hold_slabs(self.handle, 1 if on else 0), self.handle)
+
+    def debug_check(self):
+        """dg_debug_check (debug build): raises DGError(DG_ERR_BOUNDS) on a damaged workspace guard or a
+        failed index check; returns None when all is intact."""
+        off = ctypes.c_uint64()
+        _check(lib.dg_debug_check(self.handle, ctypes.byref(off)), self.handle)
 
     def sync_info(self) -> np.ndarray:
         slots = np.empty(self.B, SLOT_DTYPE)

@@ -38,7 +38,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after
 enum : uint32_t { kPurposeInit = 2u, kPurposeRenoise = 4u, kPurposeGumbelOrder = 5u };
 enum : int32_t { kWaiting = 0, kActive = 1, kDone = 2 };
 // Device error codes latched in Plan::err.
-enum : int32_t { kErrNone = 0, kErrNonFinite = 1, kErrTimeout = 2 };
+enum : int32_t { kErrNone = 0, kErrNonFinite = 1, kErrTimeout = 2, kErrBounds = 3 };
 
 // Split-vocabulary partial statistics of one position over one column range,
 // in base-2 units: u = z * log2(e) / T.
@@ -108,6 +108,24 @@ struct Dev {
   float inv_softcap;    // 1 / c (0 when off)
   int32_t hold_slabs;   // test hook (dg_debug_hold_slabs): the LM head does not count finished units
 };
+
+// ------------------------------------------------------------ debug index checks
+// In the debug build (DG_DEBUG_CHECKS) an index check that fails latches
+// DG_ERR_BOUNDS with the check's site number and the offending value in the
+// plan and makes the caller skip the access; nothing traps.  In the release
+// build the checks compile to nothing.
+__device__ __noinline__ inline bool bounds_fail(Plan* plan, int site, long long value) {
+  if (atomicCAS(&plan->err, kErrNone, kErrBounds) == kErrNone) {
+    plan->err_info[2] = site;
+    plan->err_info[3] = (int)value;
+  }
+  return false;
+}
+#ifdef DG_DEBUG_CHECKS
+#define DG_IN_BOUNDS(plan, cond, site, value) ((cond) || ::dg::bounds_fail((plan), (site), (long long)(value)))
+#else
+#define DG_IN_BOUNDS(plan, cond, site, value) true
+#endif
 
 // ------------------------------------------------------------ Philox4x32-10
 // Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3"

@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float* __restric
   if ((int)blockIdx.x >= n_rows) return;  // uniform per CTA
   const int row = blockIdx.x;
   const int a = row / dv.L, p = row - a * dv.L;
+  if (!DG_IN_BOUNDS(dv.plan, row < dv.rows_cap && dv.active[a] >= 0 && dv.active[a] < dv.B, 9, row)) return;
   norm_row<kNormThreads, kNormVec>(resid + ((size_t)dv.active[a] * dv.L + p) * dv.d, dv.norm_w,
                                    dv.h + (size_t)row * dv.d, dv.d, dv.eps, (int)threadIdx.x, red,
                                    [] { __syncthreads(); });
@@ -92,7 +93,8 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = row0 + warp;
   // the canvas of this warp's row, read before the wait so its latency is hidden
-  const int row_c = (lane == 0 && row < n_rows) ? __ldcg(dv.active + row / dv.L) : 0;
+  int row_c = (lane == 0 && row < n_rows) ? __ldcg(dv.active + row / dv.L) : 0;
+  if (lane == 0 && !DG_IN_BOUNDS(dv.plan, row_c >= 0 && row_c < dv.B, 5, row_c)) row_c = 0;
   if (threadIdx.x == 0) {
     const bool ok = wait_count(dv.slab_done + row0 / 128, (uint32_t)(dv.chunk_end - dv.chunk_begin));
     if (!ok && atomicCAS(&dv.plan->err, kErrNone, kErrTimeout) == kErrNone) dv.plan->err_info[0] = -1 - (int)blockIdx.x;

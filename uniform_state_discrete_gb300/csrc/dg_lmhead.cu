@@ -59,7 +59,9 @@ __device__ __forceinline__ RowMeta row_meta(const Dev& dv, int row, int n_rows) 
   rm.scale = 0.f;
   if (rm.valid) {
     const int a = row / dv.L;
-    const dg_slot* sl = dv.slots + __ldcg(dv.active + a);
+    int c = __ldcg(dv.active + a);
+    if (!DG_IN_BOUNDS(dv.plan, c >= 0 && c < dv.B, 7, c)) c = 0;
+    const dg_slot* sl = dv.slots + c;
     rm.gs.init(__ldcg(&sl->seed), (uint32_t)(row - a * dv.L),
                ((uint32_t)__ldcg(&sl->block) << 16) | (uint32_t)__ldcg(&sl->step), kPurposeGumbelOrder);
     rm.scale = 1.4426950408889634f / __ldcg(&sl->temperature);
@@ -480,6 +482,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         um.at(dv, u, chunk, mt);
         const int vt0 = chunk * dv.tiles_per_chunk;
         const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
+        DG_IN_BOUNDS(dv.plan, mt * kBM < dv.rows_cap && vt0 >= dv.vt_base && vt1 <= dv.n_vtiles, 8, mt);
         for (int vt = vt0; vt < vt1 && ok; ++vt) {
           for (int kb = 0; kb < KB; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
@@ -636,7 +639,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         Partial m = st;
 #pragma unroll
         for (int k = 1; k < kColGroups; ++k) m = merge_partial(m, mrg[k * kBM + rl]);
-        dv.part[(size_t)row * dv.n_sub + chunk] = m;
+        if (DG_IN_BOUNDS(dv.plan, row < dv.rows_cap && chunk >= 0 && chunk < dv.n_sub, 6, row))
+          dv.part[(size_t)row * dv.n_sub + chunk] = m;
       }
       if (cg == 0) gbest[rl] = ord_key(-INFINITY);  // the next unit may hold other rows
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
@@ -786,7 +790,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     // than the bounded wait fails the tick with a timeout instead of hanging it.
     for (int r = r_first; r < n_rows; r += 2 * (int)gridDim.x) {
       const int a = r / dv.L, p = r - a * dv.L;
-      const int c = r == r_first ? c_first : __ldcg(dv.active + a);
+      int c = r == r_first ? c_first : __ldcg(dv.active + a);
+      if (!DG_IN_BOUNDS(dv.plan, c >= 0 && c < dv.B && r < dv.rows_cap, 9, c)) c = 0;
       norm_row<256, 4>(resid + ((size_t)c * dv.L + p) * dv.d, dv.norm_w, dv.h + (size_t)r * dv.d,
                        dv.d, dv.eps, et & 255, red_norm[grp],
                        [grp] {
@@ -814,6 +819,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         um.at(dv, u, chunk, mt);
         const int vt0 = chunk * dv.tiles_per_chunk;
         const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
+        DG_IN_BOUNDS(dv.plan, (mt * 2 + 1) * kBM < dv.rows_cap && vt0 >= dv.vt_base && vt1 <= dv.n_vtiles, 8, mt);
         for (int vt = vt0; vt < vt1 && ok; ++vt) {
           for (int kb = 0; kb < KB; ++kb) {
             const uint32_t full_leader = peer_addr(smem_u32(&full[stage]), 0);
@@ -985,7 +991,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         Partial m = st;
 #pragma unroll
         for (int k = 1; k < kColGroups; ++k) m = merge_partial(m, mrg[k * kBM + rl]);
-        dv.part[(size_t)row * dv.n_sub + chunk] = m;
+        if (DG_IN_BOUNDS(dv.plan, row < dv.rows_cap && chunk >= 0 && chunk < dv.n_sub, 6, row))
+          dv.part[(size_t)row * dv.n_sub + chunk] = m;
       }
       if (cg == 0) gbest[rl] = ord_key(-INFINITY);  // the next unit may hold other rows
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");

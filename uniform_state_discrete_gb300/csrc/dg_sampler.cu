@@ -31,6 +31,7 @@ struct dg_sampler {
   int64_t tick_bound;
   void* ws;
   size_t ws_bytes;
+  std::vector<size_t> guards;  // debug build: workspace offsets of the canary guards
   cudaEvent_t timing[4];
   bool timed;
   char err[512];
@@ -62,6 +63,7 @@ struct Layout {
       part, row_best, resid,
       canvas_rows, temps, sync;
   size_t total;
+  std::vector<size_t> guards;  // debug build: offsets of the 256-byte canary guards
   int rows_cap, n_vtiles, tiles_per_chunk, n_chunks, n_sub, max_active;
   int chunk_begin, chunk_end;  // this rank's vocabulary chunks
   // self-conditioning buffers (0 when off)
@@ -90,6 +92,8 @@ void rank_chunks(int n_chunks, int G, int r, int* c0, int* c1) {
 }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+constexpr size_t kGuardBytes = 256;
+constexpr unsigned char kGuardByte = 0xA5;
 
 bool validate(const dg_config* c, char* why) {
   if (!c) return set_err(why, "config is NULL"), false;
@@ -144,9 +148,14 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
            0;
   rank_chunks(L->n_chunks, c->vocab_ranks, c->vocab_rank, &L->chunk_begin, &L->chunk_end);
   size_t o = 0;
+  L->guards.clear();
   auto take = [&](size_t bytes) {
     const size_t at = o;
     o = align256(o + bytes);
+#ifdef DG_DEBUG_CHECKS
+    L->guards.push_back(o);  // a guard after every sub-buffer
+    o += kGuardBytes;
+#endif
     return at;
   };
   L->slots = take(sizeof(dg_slot) * B);
@@ -255,6 +264,11 @@ dg_status latched_status(dg_sampler* s, const dg::Plan& pl) {
   if (pl.err == dg::kErrTimeout) {
     set_err(s->err, "a bounded wait in the LM-head kernel expired (CTA %d)", pl.err_info[0]);
     return DG_ERR_TIMEOUT;
+  }
+  if (pl.err == dg::kErrBounds) {
+    set_err(s->err, "a debug index check failed at site %d (value %d); the access was skipped", pl.err_info[2],
+            pl.err_info[3]);
+    return DG_ERR_BOUNDS;
   }
   return DG_OK;
 }
@@ -488,6 +502,9 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
     if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "allocate the pinned result staging"));
   }
   ce = cudaMemsetAsync(workspace, 0, L.total, s->stream);
+  s->guards = L.guards;
+  for (size_t g : L.guards)
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(w + g, kGuardByte, kGuardBytes, s->stream);
   if (ce == cudaSuccess && cfg->self_cond)
     ce = dg::launch_transpose_w(w_vocab, reinterpret_cast<uint16_t*>(w + L.wt), dv.V, dv.d, L.sc_vpad, s->stream);
   if (ce == cudaSuccess)
@@ -731,6 +748,32 @@ const int16_t* dg_commit_steps_out(const dg_sampler* s) { return s ? s->dv.commi
 const dg_slot* dg_slots(const dg_sampler* s) { return s ? s->dv.slots : nullptr; }
 const uint16_t* dg_normed(const dg_sampler* s) { return s ? s->dv.h : nullptr; }
 
+dg_status dg_debug_check(dg_sampler* s, uint64_t* first_bad) {
+  if (!s) return DG_ERR_ARG;
+  if (first_bad) *first_bad = 0;
+#ifndef DG_DEBUG_CHECKS
+  set_err(s->err, "this library was built without DG_DEBUG_CHECKS");
+  return DG_ERR_UNSUPPORTED;
+#else
+  std::vector<unsigned char> host(s->guards.size() * kGuardBytes);
+  for (size_t i = 0; i < s->guards.size(); ++i)
+    DG_CUDA(s->err,
+            cudaMemcpyAsync(host.data() + i * kGuardBytes, static_cast<uint8_t*>(s->ws) + s->guards[i], kGuardBytes,
+                            cudaMemcpyDeviceToHost, s->stream),
+            "copy guards");
+  dg_status st = check_device_error(s);  // synchronizes the copies too
+  if (st != DG_OK) return st;
+  for (size_t i = 0; i < host.size(); ++i)
+    if (host[i] != kGuardByte) {
+      const uint64_t off = s->guards[i / kGuardBytes] + i % kGuardBytes;
+      if (first_bad) *first_bad = off;
+      set_err(s->err, "workspace guard damaged at offset %llu", (unsigned long long)off);
+      return DG_ERR_BOUNDS;
+    }
+  return DG_OK;
+#endif
+}
+
 const char* dg_status_string(dg_status st) {
   switch (st) {
     case DG_OK: return "DG_OK";
@@ -742,6 +785,7 @@ const char* dg_status_string(dg_status st) {
     case DG_ERR_NONFINITE: return "DG_ERR_NONFINITE";
     case DG_ERR_UNSUPPORTED: return "DG_ERR_UNSUPPORTED";
     case DG_ERR_TIMEOUT: return "DG_ERR_TIMEOUT";
+    case DG_ERR_BOUNDS: return "DG_ERR_BOUNDS";
   }
   return "unknown dg_status";
 }

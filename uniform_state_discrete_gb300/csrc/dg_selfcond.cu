@@ -290,7 +290,8 @@ __global__ void __launch_bounds__(256) k_selfcond_reduce(const Dev dv, float* __
     }
     const int a = row / dv.L, p = row - a * dv.L;
     const int c = __ldcg(dv.row_canvas + a);
-    *reinterpret_cast<float4*>(out + ((size_t)c * dv.L + p) * dv.d + k) = s;
+    if (DG_IN_BOUNDS(dv.plan, c >= 0 && c < dv.B && row < dv.rows_cap, 10, c))
+      *reinterpret_cast<float4*>(out + ((size_t)c * dv.L + p) * dv.d + k) = s;
   }
 }
 

@@ -292,5 +292,9 @@ extern "C" dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, co
     put_err(err, err_len, "a bounded wait in the LM-head kernel expired");
     return DG_ERR_TIMEOUT;
   }
+  if (pl.err == dg::kErrBounds) {
+    put_err(err, err_len, "a debug index check failed at site %d (value %d)", pl.err_info[2], pl.err_info[3]);
+    return DG_ERR_BOUNDS;
+  }
   return DG_OK;
 }

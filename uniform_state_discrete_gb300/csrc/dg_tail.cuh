@@ -69,6 +69,7 @@ __device__ __forceinline__ int accept_walk(const unsigned long long* keys, int n
 }
 
 __device__ __forceinline__ void init_canvas(const Dev& dv, int c, int block, const Group& g) {
+  if (!DG_IN_BOUNDS(dv.plan, c >= 0 && c < dv.B && block >= 0 && block < dv.G, 1, c)) return;
   const uint64_t seed = __ldcg(&dv.slots[c].seed);
   for (int p = g.tid; p < dv.L; p += g.n) {
     const size_t o = (size_t)c * dv.L + p;
@@ -155,7 +156,7 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
     }
     if (act) {
       const int idx = off + __popc(bal & ((1u << lane) - 1u));
-      if (idx < dv.max_active) dv.active[idx] = c;
+      if (idx < dv.max_active && DG_IN_BOUNDS(dv.plan, c < dv.B, 2, c)) dv.active[idx] = c;
       if (refresh_temps) {
         int st = __ldcg(&dv.slots[c].step);
         st = st < 0 ? 0 : (st >= dv.N ? dv.N - 1 : st);
@@ -203,6 +204,9 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
   sl.converged_blocks = __ldcg(&dv.slots[c].converged_blocks);
   sl.stable_steps = __ldcg(&dv.slots[c].stable_steps);
   const int s = sl.step, b = sl.block;
+  if (!DG_IN_BOUNDS(dv.plan, c >= 0 && c < dv.B && b >= 0 && b < dv.G && s >= 0 && s < dv.N, 3,
+                    c < 0 || c >= dv.B ? c : (b < 0 || b >= dv.G ? b : s)))
+    return kActive;  // the group skips the commit (every thread takes the same branch)
   const size_t base = (size_t)c * L;
   const float bound = dv.bound;
   const int lane = g.tid & 31, w = g.tid >> 5;
@@ -330,7 +334,7 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
       if (p < L) {
         if (!cm[i]) {
           if (sc->acc[p]) {
-            dv.x[base + p] = yv[i];
+            if (DG_IN_BOUNDS(dv.plan, yv[i] >= 0 && yv[i] < dv.V, 4, yv[i])) dv.x[base + p] = yv[i];
             dv.committed[base + p] = 1;
             dv.commit_step[base + p] = (int16_t)s;
           } else {
@@ -365,7 +369,7 @@ static __device__ int commit_canvas(const Dev& dv, int c, const Group& g, TailSc
         int xo = xv[i];
         int16_t cs = (int16_t)s;
         if (!cm[i]) {
-          xo = yv[i];
+          xo = DG_IN_BOUNDS(dv.plan, yv[i] >= 0 && yv[i] < dv.V, 4, yv[i]) ? yv[i] : xv[i];
           dv.x[base + p] = xo;
           dv.committed[base + p] = 1;
           dv.commit_step[base + p] = cs;
