@@ -68,3 +68,36 @@ def test_split_vocabulary_matches_one_sampler(case, G, ticks):
             assert np.array_equal(s.sync_info(), ref.sync_info()), f"tick {t} rank {r}: slots differ"
     for s in ranks + [ref]:
         s.close()
+
+
+def test_two_replicas_equal_one_sampler_on_the_union_of_canvases():
+    """The replicas path of the multi-GPU benchmark on one GPU: two samplers seeded as bench.py seeds
+    ranks 0 and 1 (disjoint seed ranges) finish with exactly the tokens, heatmaps and step counts of
+    one sampler holding all their canvases (canvases are independent; no collective is needed)."""
+    import torch
+    import bench
+    import uniform_state_discrete_gb300 as dg
+    B, V, d, L = 3, 4096, 256, 64
+    W = synth.wvocab(0, V, d)
+    dev = torch.device("cuda:0")
+    w = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def run(seeds):
+        case = Case(vocab=V, hidden=d, canvas_len=L, n_canvases=len(seeds), steps=6, gen_blocks=2, seeds=tuple(seeds))
+        s = dg.Sampler(case.gpu_cfg(), w, stream=torch.cuda.Stream(dev))
+        resid = torch.empty(len(seeds), L, d, device=dev)
+        for _ in range(64):
+            if np.all(s.sync_info()["state"] == dg.DONE):
+                break
+            with torch.cuda.stream(s.stream):
+                synth.resid_device(w.data_ptr(), s.canvas().data_ptr(), s.slots_ptr(), len(seeds), L, V, d, 0.5,
+                                   resid.data_ptr(), s.stream.cuda_stream)
+                s.step(resid)
+        out = (s.tokens_out().cpu().numpy(), s.commit_steps_out().cpu().numpy(), s.sync_info()["steps_used"])
+        s.close()
+        return out
+
+    reps = [run(bench.replica_seeds(r, B)) for r in range(2)]
+    union = run(bench.replica_seeds(0, B) + bench.replica_seeds(1, B))
+    for k in range(3):
+        assert np.array_equal(np.concatenate([reps[0][k], reps[1][k]]), union[k])
