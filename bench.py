@@ -82,7 +82,8 @@ def kernel_source_digest() -> str:
     """Digest of the LM-head kernel sources; a stored ncu traffic figure is valid only for this digest."""
     h = hashlib.sha256()
     for rel in ("uniform_state_discrete_gb300/csrc/dg_lmhead.cu", "uniform_state_discrete_gb300/csrc/dg_internal.cuh",
-                "uniform_state_discrete_gb300/csrc/dg_gumbel.cuh", "uniform_state_discrete_gb300/csrc/dg_norm.cuh"):
+                "uniform_state_discrete_gb300/csrc/dg_gumbel.cuh", "uniform_state_discrete_gb300/csrc/dg_norm.cuh",
+                "uniform_state_discrete_gb300/csrc/dg_tc.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
