@@ -370,9 +370,10 @@ def run_reference(args, wl, world, rank):
     import synth
     W16 = synth.wvocab(0, wl["vocab"], wl["hidden"])
     # each bench step is one oracle tick of canvas 0 restricted to a bounded sample of its positions,
-    # sized so the whole --steps/--warmup run stays within a few minutes
-    per_pos = 1.0 / oracle_rows_per_s(wl, 8, W16=W16)
-    budget = 120.0
+    # sized so the whole --steps/--warmup run stays within a few minutes (the probe times a whole
+    # canvas: the oracle's fixed cost per call, converting W to fp64, is then spread as in a tick)
+    per_pos = 1.0 / oracle_rows_per_s(wl, wl["canvas_len"], W16=W16)
+    budget = 150.0
     sample = max(1, min(wl["canvas_len"], int(budget / max(1, args.steps + args.warmup) / per_pos)))
     cfg = oracle_cfg_for(wl, 1, 0)
     o = oracle.OracleSampler(cfg, W16)
