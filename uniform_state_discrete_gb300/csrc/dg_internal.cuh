@@ -82,6 +82,7 @@ struct Dev {
   uint32_t* rows_ready; // normalised rows written this tick (RMSNorm -> LM-head producers)
   uint32_t* fin_started;// finishing-kernel CTAs that have read this tick's plan
   uint32_t* slab_done;  // [rows_cap / 128] LM-head units finished per 128-row slab (-> finishing kernel)
+  uint32_t* units_done; // LM-head units finished this tick, counted by both CTAs of a pair (paces the producers)
   float* resid_stage;   // [B, L, d]
   const float* norm_w;  // [d] or null
   const float* temps;   // [N] temperature of each step, T_s = t_max + (s/N)(t_min - t_max)

@@ -813,8 +813,22 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = rows_written(dv, n_rows, abort_flag);
-      int issued = 0;
-      for (int u = cid; u < n_units && ok; u += n_clusters) {
+      int issued = 0, round = 0;
+      for (int u = cid; u < n_units && ok; u += n_clusters, ++round) {
+        // Pacing, when the row tiles span more than one L2-sized group: a pair starts its unit of
+        // round r only once every unit of round r - 1 is finished (counted by both CTAs of each
+        // pair).  Left alone, the pairs drift apart over the rounds and the W and h tiles they
+        // share leave L2 between their reads: at 64 x 256 rows, 32-55 GB of DRAM reads a launch
+        // instead of 4.9 GB.  With one group (16 x 256 rows and fewer) the drift costs little
+        // and the pacing's pause at each round boundary costs more.  The slowest pair never waits.
+        if (round > 0 && um.group < n_mt &&
+            !wait_count(dv.units_done, 2u * (uint32_t)min(round * n_clusters, n_units))) {
+          *abort_flag = 1;
+          atomicExch(&dv.plan->err, kErrTimeout);
+          atomicExch(&dv.plan->err_info[0], (int)blockIdx.x);
+          ok = false;
+          break;
+        }
         int chunk, mt;
         um.at(dv, u, chunk, mt);
         const int vt0 = chunk * dv.tiles_per_chunk;
@@ -1000,6 +1014,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         __threadfence();  // this unit's partial records of the slab are written
         atomicAdd(dv.slab_done + mt * 2 + (int)rank, 1u);
       }
+      if (warp == 2 && lane == 0) atomicAdd(dv.units_done, 1u);  // paces the producers (below)
     }
   }
 

@@ -178,7 +178,8 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
   L->resid = take(4 * B * Lc * d);
   L->canvas_rows = take(4 * B);
   L->temps = take(4 * (size_t)c->num_inference_steps);
-  L->sync = take(4 * (2 + (size_t)L->rows_cap / 128));  // rows_ready, fin_started, slab_done[rows_cap / 128]
+  // rows_ready, fin_started, slab_done[rows_cap / 128], units_done
+  L->sync = take(4 * (3 + (size_t)L->rows_cap / 128));
   L->wt = L->probs = L->sc_part = L->row_scale = L->row_log2z = L->row_canvas = L->sc_rows = 0;
   L->sc_vpad = L->sc_kc = L->sc_kbpc = 0;
   if (c->self_cond) {
@@ -406,6 +407,7 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dv.rows_ready = reinterpret_cast<uint32_t*>(w + L.sync);
   dv.fin_started = dv.rows_ready + 1;
   dv.slab_done = dv.rows_ready + 2;
+  dv.units_done = dv.slab_done + L.rows_cap / 128;
   dv.norm_w = norm_w;
   dv.temps = reinterpret_cast<const float*>(w + L.temps);
   dv.V = cfg->vocab;

@@ -30,7 +30,7 @@ namespace {
 constexpr size_t kOffSlot = 0;
 constexpr size_t kOffPlan = 256;
 constexpr size_t kOffActive = 512;
-constexpr size_t kOffSync = 768;  // rows written by RMSNorm, (unused here), LM-head units per 128-row slab (2)
+constexpr size_t kOffSync = 768;  // rows written by RMSNorm, (unused here), LM-head units per 128-row slab (2), units done
 constexpr size_t kOffH = 1024;
 constexpr size_t kBytesH = (size_t)2 * DG_STATIC_MAX_ROWS * DG_STATIC_MAX_HIDDEN;
 constexpr size_t kOffPart = kOffH + kBytesH;
@@ -87,7 +87,7 @@ __global__ void k_static_prep(unsigned char* base, uint64_t seed, int block, int
   for (int i = 0; i < 4; ++i) pl->err_info[i] = 0;
   active[0] = 0;
   uint32_t* sync = reinterpret_cast<uint32_t*>(base + kOffSync);
-  for (int i = 0; i < 4; ++i) sync[i] = 0u;
+  for (int i = 0; i < 5; ++i) sync[i] = 0u;  // rows_ready, fin_started, slab_done[2], units_done
 }
 
 // One warp per position: merge its split-vocabulary partial records into the
@@ -234,6 +234,7 @@ extern "C" dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, co
   dv.rows_ready = reinterpret_cast<uint32_t*>(su.base + kOffSync);
   dv.fin_started = dv.rows_ready + 1;
   dv.slab_done = dv.rows_ready + 2;
+  dv.units_done = dv.slab_done + 2;
   dv.h = reinterpret_cast<uint16_t*>(su.base + kOffH);
   dv.part = reinterpret_cast<dg::Partial*>(su.base + kOffPart);
   dv.row_best = reinterpret_cast<unsigned long long*>(su.base + kOffRowBest);

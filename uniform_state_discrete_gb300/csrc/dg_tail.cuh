@@ -166,7 +166,8 @@ static __device__ void plan_tick(const Dev& dv, int tick, const Group& g, TailSc
     base += tot;
   }
   // the tick's hand-off counters: every kernel that waited on them is past its wait
-  for (int i = g.tid; i < 2 + dv.rows_cap / 128; i += g.n) dv.rows_ready[i] = 0u;  // and fin_started, slab_done
+  // and fin_started, slab_done, units_done
+  for (int i = g.tid; i < 3 + dv.rows_cap / 128; i += g.n) dv.rows_ready[i] = 0u;
   if (g.tid == 0) {
     dv.plan->n_active = base < dv.max_active ? base : dv.max_active;  // above it only after an inconsistent dg_set_state
     dv.plan->tick = tick;
