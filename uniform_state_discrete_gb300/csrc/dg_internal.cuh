@@ -82,7 +82,7 @@ struct Dev {
   uint32_t* rows_ready; // normalised rows written this tick (RMSNorm -> LM-head producers)
   uint32_t* fin_started;// finishing-kernel CTAs that have read this tick's plan
   uint32_t* slab_done;  // [rows_cap / 128] LM-head units finished per 128-row slab (-> finishing kernel)
-  uint32_t* units_done; // LM-head units finished this tick, counted by both CTAs of a pair (paces the producers)
+  uint32_t* units_done; // LM-head units finished this tick, counted by the rank-0 CTA of a pair (paces the producers)
   float* resid_stage;   // [B, L, d]
   const float* norm_w;  // [d] or null
   const float* temps;   // [N] temperature of each step, T_s = t_max + (s/N)(t_min - t_max)
@@ -109,6 +109,36 @@ struct Dev {
   float inv_softcap;    // 1 / c (0 when off)
   int32_t hold_slabs;   // test hook (dg_debug_hold_slabs): the LM head does not count finished units
 };
+
+// ------------------------------------------------------------ expired waits
+// Where a bounded wait gave up.  The first wait to give up latches DG_ERR_TIMEOUT with
+// its CTA (err_info[0]), its site (err_info[2]) and a detail (err_info[3]: a barrier's
+// shared-memory offset times 2 plus the parity waited for, or the counter's value);
+// later ones, which usually wait on the first, leave the latch as it is.
+enum : int32_t {
+  kWaitRowsReady = 1,   // LM-head producer: normalised rows of the tick
+  kWaitPacing = 2,      // LM-head producer: units of the previous round
+  kWaitBarrier = 3,     // LM-head: an mbarrier phase (stage ring, TMEM buffers)
+  kWaitFinStarted = 4,  // finishing kernel: every CTA has read the plan
+  kWaitSlab = 5,        // finishing kernel: LM-head units of a 128-row slab
+};
+inline const char* wait_site_name(int site) {
+  switch (site) {
+    case kWaitRowsReady: return "LM head, normalised rows";
+    case kWaitPacing: return "LM head, pacing of the unit rounds";
+    case kWaitBarrier: return "LM head, stage or TMEM barrier";
+    case kWaitFinStarted: return "finishing kernel, plan read by every CTA";
+    case kWaitSlab: return "finishing kernel, LM-head units of a slab";
+    default: return "unknown site";
+  }
+}
+__device__ __noinline__ inline void timeout_latch(Plan* plan, int cta, int site, long long detail) {
+  if (atomicCAS(&plan->err, kErrNone, kErrTimeout) == kErrNone) {
+    plan->err_info[0] = cta;
+    plan->err_info[2] = site;
+    plan->err_info[3] = (int)detail;
+  }
+}
 
 // ------------------------------------------------------------ debug index checks
 // In the debug build (DG_DEBUG_CHECKS) an index check that fails latches

@@ -58,8 +58,8 @@ static_assert(kFinishRows <= (int)(sizeof(TailScratch::row_canvas) / sizeof(int)
 __device__ __forceinline__ void plan_next_tick(const Dev& dv, int tick, const Group& g, TailScratch* sc,
                                                bool started = false, int known_c = -1, int known_state = kDone) {
   if (g.tid == 0 && !started) {
-    if (!wait_count(dv.fin_started, gridDim.x) && atomicCAS(&dv.plan->err, kErrNone, kErrTimeout) == kErrNone)
-      dv.plan->err_info[0] = -2;
+    if (!wait_count(dv.fin_started, gridDim.x))
+      timeout_latch(dv.plan, (int)blockIdx.x, kWaitFinStarted, *(volatile uint32_t*)dv.fin_started);
   }
   g.sync();
   plan_tick(dv, tick + 1, g, sc, false, known_c, known_state);
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   if (lane == 0 && !DG_IN_BOUNDS(dv.plan, row_c >= 0 && row_c < dv.B, 5, row_c)) row_c = 0;
   if (threadIdx.x == 0) {
     const bool ok = wait_count(dv.slab_done + row0 / 128, (uint32_t)(dv.chunk_end - dv.chunk_begin));
-    if (!ok && atomicCAS(&dv.plan->err, kErrNone, kErrTimeout) == kErrNone) dv.plan->err_info[0] = -1 - (int)blockIdx.x;
+    if (!ok) timeout_latch(dv.plan, (int)blockIdx.x, kWaitSlab, row0 / 128);
   }
   __syncthreads();
   const int row1 = min(row0 + kFinishRows, n_rows);

@@ -373,8 +373,7 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask) {
 __device__ __forceinline__ bool rows_written(const Dev& dv, int n_rows, volatile int* abort_flag) {
   if (!wait_count(dv.rows_ready, (uint32_t)n_rows)) {
     *abort_flag = 1;
-    atomicExch(&dv.plan->err, kErrTimeout);
-    atomicExch(&dv.plan->err_info[0], (int)blockIdx.x);
+    timeout_latch(dv.plan, (int)blockIdx.x, kWaitRowsReady, *(volatile uint32_t*)dv.rows_ready);
     return false;
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -816,16 +815,14 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       int issued = 0, round = 0;
       for (int u = cid; u < n_units && ok; u += n_clusters, ++round) {
         // Pacing, when the row tiles span more than one L2-sized group: a pair starts its unit of
-        // round r only once every unit of round r - 1 is finished (counted by both CTAs of each
-        // pair).  Left alone, the pairs drift apart over the rounds and the W and h tiles they
+        // round r only once every unit of round r - 1 is finished.  Left alone, the pairs drift apart over the rounds and the W and h tiles they
         // share leave L2 between their reads: at 64 x 256 rows, 32-55 GB of DRAM reads a launch
         // instead of 4.9 GB.  With one group (16 x 256 rows and fewer) the drift costs little
         // and the pacing's pause at each round boundary costs more.  The slowest pair never waits.
         if (round > 0 && um.group < n_mt &&
-            !wait_count(dv.units_done, 2u * (uint32_t)min(round * n_clusters, n_units))) {
+            !wait_count(dv.units_done, (uint32_t)min(round * n_clusters, n_units))) {
           *abort_flag = 1;
-          atomicExch(&dv.plan->err, kErrTimeout);
-          atomicExch(&dv.plan->err_info[0], (int)blockIdx.x);
+          timeout_latch(dv.plan, (int)blockIdx.x, kWaitPacing, *(volatile uint32_t*)dv.units_done);
           ok = false;
           break;
         }
@@ -843,6 +840,9 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
               tma_load_2d_pair(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM,
                                     full_leader);
             } else {
+              // Both CTAs' loads complete the leader's full barrier, so the leader's MMAs never
+              // run a lap ahead of either producer: the commits arriving on this CTA's empty
+              // barrier stay within one phase of this wait, and its parity cannot alias.
               if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
                 ok = false;
                 break;
@@ -1010,11 +1010,16 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       }
       if (cg == 0) gbest[rl] = ord_key(-INFINITY);  // the next unit may hold other rows
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-      if (warp == 2 && lane == 0 && (mt * 2 + (int)rank) * kBM < n_rows && !dv.hold_slabs) {
-        __threadfence();  // this unit's partial records of the slab are written
-        atomicAdd(dv.slab_done + mt * 2 + (int)rank, 1u);
+      if (warp == 2 && lane == 0) {
+        // The pacing count, one per unit from the CTA whose rows always lie below n_rows, comes
+        // before that CTA's slab count: once the finishing kernel has seen every slab done it
+        // may reset the tick's counters, and a later increment would carry into the next tick.
+        if (rank == 0) atomicAdd(dv.units_done, 1u);
+        if ((mt * 2 + (int)rank) * kBM < n_rows && !dv.hold_slabs) {
+          __threadfence();  // this unit's partial records of the slab are written
+          atomicAdd(dv.slab_done + mt * 2 + (int)rank, 1u);
+        }
       }
-      if (warp == 2 && lane == 0) atomicAdd(dv.units_done, 1u);  // paces the producers (below)
     }
   }
 

@@ -263,7 +263,8 @@ dg_status latched_status(dg_sampler* s, const dg::Plan& pl) {
     return DG_ERR_NONFINITE;
   }
   if (pl.err == dg::kErrTimeout) {
-    set_err(s->err, "a bounded wait in the LM-head kernel expired (CTA %d)", pl.err_info[0]);
+    set_err(s->err, "a bounded wait expired: %s (CTA %d, detail %d)", dg::wait_site_name(pl.err_info[2]),
+            pl.err_info[0], pl.err_info[3]);
     return DG_ERR_TIMEOUT;
   }
   if (pl.err == dg::kErrBounds) {

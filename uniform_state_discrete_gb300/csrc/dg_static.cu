@@ -290,7 +290,8 @@ extern "C" dg_status dg_lmhead_stats_static(const float* resid, int32_t rows, co
     return DG_ERR_NONFINITE;
   }
   if (pl.err == dg::kErrTimeout) {
-    put_err(err, err_len, "a bounded wait in the LM-head kernel expired");
+    put_err(err, err_len, "a bounded wait expired: %s (CTA %d, detail %d)", dg::wait_site_name(pl.err_info[2]),
+            pl.err_info[0], pl.err_info[3]);
     return DG_ERR_TIMEOUT;
   }
   if (pl.err == dg::kErrBounds) {

@@ -55,8 +55,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, vola
       if (*abort_flag) return false;
       if (global_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1;
-        atomicExch(&plan->err, kErrTimeout);
-        atomicExch(&plan->err_info[0], (int)blockIdx.x);
+        timeout_latch(plan, (int)blockIdx.x, kWaitBarrier, 2ll * smem_u32(bar) + parity);
         return false;
       }
     }
