@@ -325,6 +325,8 @@ def test_bounded_wait_runs_out_and_sampler_recovers(canvas_len, vocab):
         s.sync_info()
     waited = time.perf_counter() - t0
     assert err.value.status == dg.DG_ERR_TIMEOUT
+    # the first wait to give up is latched: the finishing kernel's, not the LM head's
+    assert "finishing kernel, LM-head units of a slab" in str(err.value)
     assert 0.9 < waited < 30.0
     s.debug_hold_slabs(False)
     s.set_state(st0)

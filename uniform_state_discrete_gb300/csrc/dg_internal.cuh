@@ -278,10 +278,12 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
-// The best score recorded for a row in this epoch, or -inf.
-__device__ __forceinline__ float row_best_score(const unsigned long long* e, uint32_t epoch) {
-  const unsigned long long v = __ldcg(e);
+// The best score a row's word records for this epoch, or -inf.
+__device__ __forceinline__ float row_best_decode(unsigned long long v, uint32_t epoch) {
   return (uint32_t)(v >> 32) == epoch ? key_score((uint32_t)v) : -INFINITY;
+}
+__device__ __forceinline__ float row_best_score(const unsigned long long* e, uint32_t epoch) {
+  return row_best_decode(__ldcg(e), epoch);
 }
 __device__ __forceinline__ void row_best_raise(unsigned long long* e, uint32_t epoch, float score) {
   atomicMax(e, ((unsigned long long)epoch << 32) | score_key(score));

@@ -148,19 +148,22 @@ __device__ __forceinline__ uint32_t nth_set_bit16(uint32_t mask, uint32_t r) {
 
 // Where a row's best perturbed score is kept: this CTA's column groups share
 // `cta` (shared memory), every unit of the row in the tick shares `glob`
-// (global memory, tagged with the tick's epoch).  `known` is the global value
-// read at the start of the current tile; a stream publishes its own best to
-// the global value once per tile, at the tile's end, if it rose.
+// (global memory, tagged with the tick's epoch).  `known` is the largest global
+// value read so far, refreshed before every group; a stream publishes its own
+// best to the global value as soon as it rises (its seed, then each fold that
+// raised it), so the units of a row that run at the same time -- at small V,
+// all of them -- screen against each other's finds within the same tile.
 struct BestScore {
   int* cta;
   unsigned long long* glob;
   uint32_t epoch;
   float known;
-  bool raised;  // this stream's own best rose during the current tile (published at its end)
+  bool raised;  // this stream's best rose in the last fold and raised the CTA's (published right after)
 };
 
 // Fold 16 columns [v0, v0+16) of one row (raw fp32 logits z) into its running
-// statistics.  v0 is a multiple of 16, so the columns are one group of the
+// statistics and Gumbel sample (fold16 below: group_prep, then stats16, then
+// screen16).  v0 is a multiple of 16, so the columns are one group of the
 // Gumbel draws.  kTail: some of the columns lie at or beyond V.
 //
 // With a final logit softcap c > 0 each logit first becomes c tanh(z / c)
@@ -188,29 +191,34 @@ struct BestScore {
 // tested on the first Philox block alone -- one block for sixteen entries (see
 // below).  Walks run one step per lane per round, all lanes of the warp
 // together.  Equal scores keep the lower index.
+// The logits of a group as the statistics and the screen take them: capped (kCap), with
+// columns at or beyond V set to -inf (kTail); returns the group's maximum logit in `cmz`, or
+// false when the whole group lies beyond V.
 template <bool kTail, bool kCap>
-__device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, BestScore& bs,
-                                       float cap, float inv_cap) {
+__device__ __forceinline__ bool group_prep(float (&z)[16], int v0, int V, float cap, float inv_cap, float& cmz) {
   if (kCap) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) z[j] = cap * tanhf(z[j] * inv_cap);
   }
   if (kTail) {
-    if (v0 >= V) return;
+    if (v0 >= V) return false;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       if (v0 + j >= V) z[j] = -INFINITY;
   }
-  // the first block of the group's order statistics: its latency overlaps the statistics below
-  const uint32_t x0 = 8u * ((uint32_t)v0 >> 4);
-  uint32_t w4[4];
-  rm.gs.draw(x0, w4);
   float t8[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) t8[i] = fmaxf(z[i], z[i + 8]);
 #pragma unroll
   for (int i = 0; i < 4; ++i) t8[i] = fmaxf(t8[i], t8[i + 4]);
-  const float cmz = fmaxf(fmaxf(t8[0], t8[2]), fmaxf(t8[1], t8[3]));
+  cmz = fmaxf(fmaxf(t8[0], t8[2]), fmaxf(t8[1], t8[3]));
+  return true;
+}
+
+// The softmax statistics of a prepared group (the running max, S, A and the argmax).
+template <bool kTail>
+__device__ __forceinline__ void stats16(const float (&z)[16], float cmz, int v0, int V, const RowMeta& rm,
+                                        Partial& st) {
   const float cm = cmz * rm.scale;
   if (cm > st.m) {
     const float f = ex2_approx(st.m - cm);
@@ -223,7 +231,7 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
       if (z[j] == cmz) ci = j;  // first index holding the maximum
     st.amax = v0 + ci;
   }
-  const float m = st.m, nm = -st.m;
+  const float nm = -st.m;
   float S[4] = {0.f, 0.f, 0.f, 0.f}, A[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -234,6 +242,15 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
   }
   st.S += (S[0] + S[1]) + (S[2] + S[3]);
   st.A += (A[0] + A[1]) + (A[2] + A[3]);
+}
+
+// The Gumbel screen and walk of a prepared group against the best score known for the row
+// (the running max m only scales the test: any m gives the same decisions up to the slack).
+template <bool kTail>
+__device__ __forceinline__ void screen16(const float (&z)[16], float cmz, int v0, int V, const RowMeta& rm,
+                                         Partial& st, BestScore& bs, const uint32_t (&pw)[2]) {
+  const uint32_t x0 = 8u * ((uint32_t)v0 >> 4);
+  const float m = st.m, nm = -st.m;
   // Can any entry of the group beat g?  The entry holding E_(0) = X_0 / 16 (slot r_0, known from
   // the first slot word alone) only if X_0 / 16 < 2^(u_slot - g); every other entry only if
   // E_(1) = X_0 / 16 + X_1 / 15 < 2^(u_max - g).  With X >= q = 1 - U and, from the funnel-shift
@@ -243,12 +260,14 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
   bool live = true;
   if (g0 != -INFINITY) {
     const float K = screen_factor(m, g0);
-    const float q0 = (2.f - 0x1p-23f) - screen_word(w4[0]), q1 = (2.f - 0x1p-23f) - screen_word(w4[2]);
-    const float e0 = ex2_approx(fmaf(select16(z, __umulhi(w4[1], 16u)), rm.scale, nm));  // 2^(u_slot - m)
+    const float q0 = (2.f - 0x1p-23f) - screen_word(pw[0]), q1 = (2.f - 0x1p-23f) - screen_word(pw[1]);
+    const float e0 = ex2_approx(fmaf(select16(z, pw[1] & 15u), rm.scale, nm));  // 2^(u_slot - m)
     live = q0 * 0.0625f < e0 * K || fmaf(q1, 1.f / 15.f, q0 * 0.0625f) < emax * K;
   }
   const unsigned act = __activemask();
   if (!__any_sync(act, live)) return;
+  uint32_t w4[4];
+  rm.gs.draw(x0, w4);  // a walk takes the whole first block: its fourth word is the second slot word
   bool improved = false;
   float E = 0.f;
   uint32_t rem = 0xFFFFu;  // slots not yet given a variate
@@ -280,10 +299,18 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
       }
     }
   }
-  if (improved) {
-    atomicMax(bs.cta, ord_key(st.g));
-    bs.raised = true;
-  }
+  // the column group that raises the CTA's best publishes it (the word's other writers already hold
+  // no more than the CTA's best, which its raiser published)
+  if (improved && atomicMax(bs.cta, ord_key(st.g)) < ord_key(st.g)) bs.raised = true;
+}
+
+template <bool kTail, bool kCap>
+__device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, BestScore& bs,
+                                       const uint32_t (&pw)[2], float cap, float inv_cap) {
+  float cmz;
+  if (!group_prep<kTail, kCap>(z, v0, V, cap, inv_cap, cmz)) return;
+  stats16<kTail>(z, cmz, v0, V, rm, st);
+  screen16<kTail>(z, cmz, v0, V, rm, st, bs, pw);
 }
 
 // A first score for a row whose unit has none yet: the entry holding its
@@ -292,17 +319,15 @@ __device__ __forceinline__ void fold16(float (&z)[16], int v0, int V, const RowM
 // over a tile's groups before they are folded, it gives the folds the best of
 // those entries to screen against instead of starting from nothing.
 template <bool kCap>
-__device__ __forceinline__ void seed16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st, float cap,
-                                       float inv_cap) {
+__device__ __forceinline__ void seed16(float (&z)[16], int v0, int V, const RowMeta& rm, Partial& st,
+                                       const uint32_t (&pw)[2], float cap, float inv_cap) {
   if (v0 >= V) return;
-  uint32_t w4[4];
-  rm.gs.draw(8u * ((uint32_t)v0 >> 4), w4);
-  const uint32_t slot = __umulhi(w4[1], 16u);
+  const uint32_t slot = pw[1] & 15u;
   const int idx = v0 + (int)slot;
   if (idx >= V) return;
   float zs = select16(z, slot);
   if (kCap) zs = cap * tanhf(zs * inv_cap);
-  const float sc = fmaf(zs, rm.scale, -lg2_approx(exp_variate(w4[0]) * 0.0625f));
+  const float sc = fmaf(zs, rm.scale, -lg2_approx(exp_variate(pw[0]) * 0.0625f));
   if (sc > st.g || (sc == st.g && idx < st.gidx)) {
     st.g = sc;
     st.gidx = idx;
@@ -312,11 +337,61 @@ __device__ __forceinline__ void seed16(float (&z)[16], int v0, int V, const RowM
 // The fold of this warp's 16 columns of one accumulator tile.
 template <bool kCap>
 __device__ __forceinline__ void fold_cols(float (&acc)[16], int v0, int V, const RowMeta& rm, Partial& st,
-                                          BestScore& bs, float cap, float inv_cap) {
+                                          BestScore& bs, const uint32_t (&pw)[2], float cap, float inv_cap) {
   if (v0 + 16 <= V)
-    fold16<false, kCap>(acc, v0, V, rm, st, bs, cap, inv_cap);
+    fold16<false, kCap>(acc, v0, V, rm, st, bs, pw, cap, inv_cap);
   else
-    fold16<true, kCap>(acc, v0, V, rm, st, bs, cap, inv_cap);
+    fold16<true, kCap>(acc, v0, V, rm, st, bs, pw, cap, inv_cap);
+}
+
+// A unit's first tile in two passes: the statistics of every group first (while the seeds just
+// published by the row's other units reach L2), then the screens and walks against the best of
+// them.  Neither pass changes what the other computes, so the results equal fold_cols's.
+template <bool kCap>
+__device__ __forceinline__ void stats_cols(float (&acc)[16], int v0, int V, const RowMeta& rm, Partial& st, float cap,
+                                           float inv_cap) {
+  float cmz;
+  if (v0 + 16 <= V) {
+    if (group_prep<false, kCap>(acc, v0, V, cap, inv_cap, cmz)) stats16<false>(acc, cmz, v0, V, rm, st);
+  } else {
+    if (group_prep<true, kCap>(acc, v0, V, cap, inv_cap, cmz)) stats16<true>(acc, cmz, v0, V, rm, st);
+  }
+}
+template <bool kCap>
+__device__ __forceinline__ void screen_cols(float (&acc)[16], int v0, int V, const RowMeta& rm, Partial& st,
+                                            BestScore& bs, const uint32_t (&pw)[2], float cap, float inv_cap) {
+  float cmz;
+  if (v0 + 16 <= V) {
+    if (group_prep<false, kCap>(acc, v0, V, cap, inv_cap, cmz)) screen16<false>(acc, cmz, v0, V, rm, st, bs, pw);
+  } else {
+    if (group_prep<true, kCap>(acc, v0, V, cap, inv_cap, cmz)) screen16<true>(acc, cmz, v0, V, rm, st, bs, pw);
+  }
+}
+
+// What the screens take from the first Philox block of each of a warp's four 16-column groups
+// of a tile, drawn before the tile's accumulator is ready: four independent chains interleave
+// and overlap the tile's MMAs, and no fold draws for its screen.  pw[0] is word 0 (the smallest
+// variate's); pw[1] is word 2 (the second's: only its bits 9-31 are read) with the first slot,
+// the top four bits of word 1, in its low four bits.
+constexpr int kGroupsPerWarp = kColsPerWarp / 16;
+__device__ __forceinline__ void first_blocks(const RowMeta& rm, int v0, uint32_t (&pw)[kGroupsPerWarp][2]) {
+#pragma unroll
+  for (int c = 0; c < kGroupsPerWarp; ++c) {
+    uint32_t w[4];
+    rm.gs.draw(8u * ((uint32_t)(v0 + 16 * c) >> 4), w);
+    pw[c][0] = w[0];
+    pw[c][1] = (w[2] & ~15u) | (w[1] >> 28);
+  }
+}
+// Brings the next group's words to the front (registers cannot be indexed by a loop counter).
+__device__ __forceinline__ void rotate_blocks(uint32_t (&pw)[kGroupsPerWarp][2]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t t = pw[0][i];
+#pragma unroll
+    for (int c = 0; c + 1 < kGroupsPerWarp; ++c) pw[c][i] = pw[c + 1][i];
+    pw[kGroupsPerWarp - 1][i] = t;
+  }
 }
 
 // ---------------------------------------------------------------- CTA pairs
@@ -481,7 +556,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         um.at(dv, u, chunk, mt);
         const int vt0 = chunk * dv.tiles_per_chunk;
         const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
-        DG_IN_BOUNDS(dv.plan, mt * kBM < dv.rows_cap && vt0 >= dv.vt_base && vt1 <= dv.n_vtiles, 8, mt);
+        (void)DG_IN_BOUNDS(dv.plan, mt * kBM < dv.rows_cap && vt0 >= dv.vt_base && vt1 <= dv.n_vtiles, 8, mt);
         for (int vt = vt0; vt < vt1 && ok; ++vt) {
           for (int kb = 0; kb < KB; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
@@ -586,6 +661,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
         // the best score other units of this row have found so far (read while the tile completes)
         if (rm.valid) bs.known = row_best_score(bs.glob, epoch);
+        uint32_t pw[kGroupsPerWarp][2];
+        first_blocks(rm, vt * kBN + cg * kColsPerWarp, pw);
         int got = 0;
         if (lane == 0) got = mbar_wait(&tfull[ab], aph, abort_flag, dv.plan) ? 1 : 0;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
@@ -596,8 +673,11 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         tc_fence_after();
         const uint32_t tbase =
             tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(cg * kColsPerWarp);
-        // no score known for the row yet (its unit's first tile, no other unit ahead of it): seed one
-        if (__any_sync(0xFFFFFFFFu, rm.valid && st.g == -INFINITY && bs.known == -INFINITY)) {
+        // No score known for the row yet (its unit's first tile, no other unit ahead of it): seed
+        // one and publish it, then form the tile's statistics, and only then screen (below) --
+        // against the seeds the row's other units have published meanwhile.
+        const bool seeding = __any_sync(0xFFFFFFFFu, rm.valid && st.g == -INFINITY && bs.known == -INFINITY);
+        if (seeding) {
           const bool seed = rm.valid && st.g == -INFINITY && bs.known == -INFINITY;
 #pragma unroll 1
           for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
@@ -605,13 +685,36 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             __syncwarp();
             tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
             if (seed)
-              seed16<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, dv.softcap, dv.inv_softcap);
+              seed16<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, pw[0], dv.softcap,
+                           dv.inv_softcap);
+            rotate_blocks(pw);  // four turns: back in order for the screens
           }
-          if (seed && st.g != -INFINITY) atomicMax(bs.cta, ord_key(st.g));
+          if (seed && st.g != -INFINITY) {
+            // published at once, by the column group whose seed raised the CTA's best only (a few
+            // atomics per row, not one per column group): the other units of the row, folding
+            // their own tiles now, screen against it
+            if (atomicMax(bs.cta, ord_key(st.g)) < ord_key(st.g)) row_best_raise(bs.glob, epoch, st.g);
+          }
+#pragma unroll 1
+          for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
+            float acc[16];
+            __syncwarp();
+            tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
+            if (rm.valid)
+              stats_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, dv.softcap, dv.inv_softcap);
+          }
         }
+        // the best score any unit of the row has published, refreshed for every group: the value
+        // a group screens against is loaded one group ahead, so its latency overlaps a fold (and a
+        // load never follows this lane's own atomic on the same word, which it would wait for)
+        // (the raw word is carried and decoded where it is used, so nothing waits on the load early)
+        unsigned long long known_next = (unsigned long long)(epoch ^ 1u) << 32;  // another epoch: no score
+        if (seeding && rm.valid) known_next = __ldcg(bs.glob);  // the seeds published meanwhile
 #pragma unroll 1
         for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
           float acc[16];
+          const unsigned long long known = known_next;
+          if (rm.valid && cc + 1 < kColsPerWarp / 16) known_next = __ldcg(bs.glob);
           __syncwarp();  // tcgen05.ld is .sync.aligned: the fold below may leave lanes diverged
           tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
           if (cc == kColsPerWarp / 16 - 1) {
@@ -620,13 +723,20 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
           }
-          if (rm.valid)
-            fold_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, bs, dv.softcap,
-                            dv.inv_softcap);
-        }
-        if (bs.raised) {
-          row_best_raise(bs.glob, epoch, st.g);
-          bs.raised = false;
+          bs.known = fmaxf(bs.known, row_best_decode(known, epoch));
+          if (rm.valid) {
+            if (seeding)
+              screen_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, bs, pw[0], dv.softcap,
+                                dv.inv_softcap);
+            else
+              fold_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, bs, pw[0], dv.softcap,
+                              dv.inv_softcap);
+          }
+          if (bs.raised) {  // published as soon as it rises, for the same reason
+            row_best_raise(bs.glob, epoch, st.g);
+            bs.raised = false;
+          }
+          rotate_blocks(pw);
         }
       }
       // merge the four column groups of each row; one record per row and chunk.  Every
@@ -830,7 +940,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         um.at(dv, u, chunk, mt);
         const int vt0 = chunk * dv.tiles_per_chunk;
         const int vt1 = min(vt0 + dv.tiles_per_chunk, dv.n_vtiles);
-        DG_IN_BOUNDS(dv.plan, (mt * 2 + 1) * kBM < dv.rows_cap && vt0 >= dv.vt_base && vt1 <= dv.n_vtiles, 8, mt);
+        (void)DG_IN_BOUNDS(dv.plan, (mt * 2 + 1) * kBM < dv.rows_cap && vt0 >= dv.vt_base && vt1 <= dv.n_vtiles, 8, mt);
         for (int vt = vt0; vt < vt1 && ok; ++vt) {
           for (int kb = 0; kb < KB; ++kb) {
             const uint32_t full_leader = peer_addr(smem_u32(&full[stage]), 0);
@@ -957,6 +1067,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
         // the best score other units of this row have found so far (read while the tile completes)
         if (rm.valid) bs.known = row_best_score(bs.glob, epoch);
+        uint32_t pw[kGroupsPerWarp][2];
+        first_blocks(rm, vt * kBN + cg * kColsPerWarp, pw);
         int got = 0;
         if (lane == 0) got = mbar_wait(&tfull[ab], aph, abort_flag, dv.plan) ? 1 : 0;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
@@ -967,8 +1079,11 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         tc_fence_after();
         const uint32_t tbase =
             tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(cg * kColsPerWarp);
-        // no score known for the row yet (its unit's first tile, no other unit ahead of it): seed one
-        if (__any_sync(0xFFFFFFFFu, rm.valid && st.g == -INFINITY && bs.known == -INFINITY)) {
+        // No score known for the row yet (its unit's first tile, no other unit ahead of it): seed
+        // one and publish it, then form the tile's statistics, and only then screen (below) --
+        // against the seeds the row's other units have published meanwhile.
+        const bool seeding = __any_sync(0xFFFFFFFFu, rm.valid && st.g == -INFINITY && bs.known == -INFINITY);
+        if (seeding) {
           const bool seed = rm.valid && st.g == -INFINITY && bs.known == -INFINITY;
 #pragma unroll 1
           for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
@@ -976,13 +1091,36 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             __syncwarp();
             tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
             if (seed)
-              seed16<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, dv.softcap, dv.inv_softcap);
+              seed16<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, pw[0], dv.softcap,
+                           dv.inv_softcap);
+            rotate_blocks(pw);  // four turns: back in order for the screens
           }
-          if (seed && st.g != -INFINITY) atomicMax(bs.cta, ord_key(st.g));
+          if (seed && st.g != -INFINITY) {
+            // published at once, by the column group whose seed raised the CTA's best only (a few
+            // atomics per row, not one per column group): the other units of the row, folding
+            // their own tiles now, screen against it
+            if (atomicMax(bs.cta, ord_key(st.g)) < ord_key(st.g)) row_best_raise(bs.glob, epoch, st.g);
+          }
+#pragma unroll 1
+          for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
+            float acc[16];
+            __syncwarp();
+            tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
+            if (rm.valid)
+              stats_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, dv.softcap, dv.inv_softcap);
+          }
         }
+        // the best score any unit of the row has published, refreshed for every group: the value
+        // a group screens against is loaded one group ahead, so its latency overlaps a fold (and a
+        // load never follows this lane's own atomic on the same word, which it would wait for)
+        // (the raw word is carried and decoded where it is used, so nothing waits on the load early)
+        unsigned long long known_next = (unsigned long long)(epoch ^ 1u) << 32;  // another epoch: no score
+        if (seeding && rm.valid) known_next = __ldcg(bs.glob);  // the seeds published meanwhile
 #pragma unroll 1
         for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
           float acc[16];
+          const unsigned long long known = known_next;
+          if (rm.valid && cc + 1 < kColsPerWarp / 16) known_next = __ldcg(bs.glob);
           __syncwarp();  // tcgen05.ld is .sync.aligned: the fold below may leave lanes diverged
           tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
           if (cc == kColsPerWarp / 16 - 1) {
@@ -990,13 +1128,20 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader[ab]);
           }
-          if (rm.valid)
-            fold_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, bs, dv.softcap,
-                            dv.inv_softcap);
-        }
-        if (bs.raised) {
-          row_best_raise(bs.glob, epoch, st.g);
-          bs.raised = false;
+          bs.known = fmaxf(bs.known, row_best_decode(known, epoch));
+          if (rm.valid) {
+            if (seeding)
+              screen_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, bs, pw[0], dv.softcap,
+                                dv.inv_softcap);
+            else
+              fold_cols<kCap>(acc, vt * kBN + cg * kColsPerWarp + cc * 16, dv.V, rm, st, bs, pw[0], dv.softcap,
+                              dv.inv_softcap);
+          }
+          if (bs.raised) {  // published as soon as it rises, for the same reason
+            row_best_raise(bs.glob, epoch, st.g);
+            bs.raised = false;
+          }
+          rotate_blocks(pw);
         }
       }
       mrg[cg * kBM + rl] = st;
