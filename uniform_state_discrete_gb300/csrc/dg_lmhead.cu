@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         uint32_t pw[kGroupsPerWarp][2];
         first_blocks(rm, vt * kBN + cg * kColsPerWarp, pw);
         int got = 0;
-        if (lane == 0) got = mbar_wait(&tfull[ab], aph, abort_flag, dv.plan) ? 1 : 0;
+        if (lane == 0) got = mbar_wait_poll(&tfull[ab], aph, 256u, abort_flag, dv.plan) ? 1 : 0;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
         if (!got) {
           aborted = true;
@@ -1070,7 +1070,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         uint32_t pw[kGroupsPerWarp][2];
         first_blocks(rm, vt * kBN + cg * kColsPerWarp, pw);
         int got = 0;
-        if (lane == 0) got = mbar_wait(&tfull[ab], aph, abort_flag, dv.plan) ? 1 : 0;
+        if (lane == 0) got = mbar_wait_poll(&tfull[ab], aph, 256u, abort_flag, dv.plan) ? 1 : 0;
         got = __shfl_sync(0xFFFFFFFFu, got, 0);
         if (!got) {
           aborted = true;

@@ -81,6 +81,43 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, plan);
 }
 
+// A non-blocking test of the phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// For long waits with slack to spare (the epilogue's wait for its next tile, most of a tile's
+// time): tests the phase every `sleep_ns` and sleeps in between.  Even with a suspend hint,
+// try_wait comes back well before such a phase completes, and its retries take issue slots
+// from the MMA and producer warps of the same sub-partitions.
+__device__ __noinline__ bool mbar_wait_poll_slow(uint64_t* bar, uint32_t parity, uint32_t sleep_ns,
+                                                 volatile int* abort_flag, Plan* plan) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(sleep_ns);
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 15u) == 0u) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        timeout_latch(plan, (int)blockIdx.x, kWaitBarrier, 2ll * smem_u32(bar) + parity);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, uint32_t sleep_ns,
+                                               volatile int* abort_flag, Plan* plan) {
+  return mbar_test_wait(bar, parity) || mbar_wait_poll_slow(bar, parity, sleep_ns, abort_flag, plan);
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
