@@ -487,6 +487,7 @@ template <bool kCap>
 __global__ void __launch_bounds__(kThreadsLM, 1)
     k_lmhead(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int tile_ok[2];  // the epilogue's poller found the tile's accumulator ready (per TMEM buffer)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kStageA;
@@ -663,9 +664,16 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         if (rm.valid) bs.known = row_best_score(bs.glob, epoch);
         uint32_t pw[kGroupsPerWarp][2];
         first_blocks(rm, vt * kBN + cg * kColsPerWarp, pw);
-        int got = 0;
-        if (lane == 0) got = mbar_wait_poll(&tfull[ab], aph, 256u, abort_flag, dv.plan) ? 1 : 0;
-        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        // One warp polls for the tile; the other fifteen wait on a hardware barrier, which issues
+        // nothing (sixteen pollers took issue slots from the MMA and producer warps).  The result
+        // goes through shared memory, double-buffered: the poller cannot write this slot again
+        // before every warp has passed the next tile's barrier, so after reading it.
+        if (warp == 2) {
+          if (lane == 0) tile_ok[ab] = mbar_wait_poll(&tfull[ab], aph, 256u, abort_flag, dv.plan) ? 1 : 0;
+          __syncwarp();
+        }
+        asm volatile("bar.sync 4, %0;" ::"r"(32 * kEpiWarps) : "memory");
+        const int got = *(volatile int*)&tile_ok[ab];
         if (!got) {
           aborted = true;
           continue;
@@ -789,6 +797,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
                   const float* __restrict__ resid) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ float red_norm[2][8][2];  // RMSNorm reductions of the two row groups
+  __shared__ int tile_ok[2];           // the epilogue's poller found the tile's accumulator ready (per TMEM buffer)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStagesPair * kStagePairA;
@@ -1069,9 +1078,16 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         if (rm.valid) bs.known = row_best_score(bs.glob, epoch);
         uint32_t pw[kGroupsPerWarp][2];
         first_blocks(rm, vt * kBN + cg * kColsPerWarp, pw);
-        int got = 0;
-        if (lane == 0) got = mbar_wait_poll(&tfull[ab], aph, 256u, abort_flag, dv.plan) ? 1 : 0;
-        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        // One warp polls for the tile; the other fifteen wait on a hardware barrier, which issues
+        // nothing (sixteen pollers took issue slots from the MMA and producer warps).  The result
+        // goes through shared memory, double-buffered: the poller cannot write this slot again
+        // before every warp has passed the next tile's barrier, so after reading it.
+        if (warp == 2) {
+          if (lane == 0) tile_ok[ab] = mbar_wait_poll(&tfull[ab], aph, 256u, abort_flag, dv.plan) ? 1 : 0;
+          __syncwarp();
+        }
+        asm volatile("bar.sync 4, %0;" ::"r"(32 * kEpiWarps) : "memory");
+        const int got = *(volatile int*)&tile_ok[ab];
         if (!got) {
           aborted = true;
           continue;
