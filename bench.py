@@ -137,6 +137,28 @@ def lmhead_roofline(V: int, d: int, P: int, pair: bool, seconds: float, peaks: d
     return roof, t_hbm, t_tc
 
 
+def self_cond_roofline(V: int, d: int, P: float, seconds: float, peaks: dict) -> dict:
+    """Roofline of one dg_self_condition call over P positions taking `seconds`: the expected
+    embedding softmax(z/T) W, with z = h W^T formed again.  Algorithmic bytes: W once, the bf16
+    rows h and the fp32 output; flops: the two contractions, 4 P V d."""
+    alg_bytes = V * d * 2 + P * d * (2 + 4)
+    alg_flops = 4.0 * P * V * d
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg_flops / (peaks["bf16_tflops"] * 1e12)
+    r = {"ms_mean": seconds * 1e3, "positions_per_call": P, "algorithmic_bytes_per_call": alg_bytes,
+         "algorithmic_flops_per_call": alg_flops,
+         "kernels": "k_selfcond (the LM head again, writing P = softmax(z/T) in bf16), k_selfcond (P W over "
+                    "vocabulary chunks, tcgen05), k_selfcond_reduce (fixed-order sum of the chunks)",
+         "timing": "CUDA events around the call on the sampler stream, after a tick, L2 flushed before it"}
+    if t_hbm >= t_tc:
+        r.update(bound="hbm", achieved=alg_bytes / seconds / 1e9, peak=peaks["hbm_gbs"], unit="GB/s")
+    else:
+        r.update(bound="tensor", achieved=alg_flops / seconds / 1e12, peak=peaks["bf16_tflops"], unit="TFLOP/s")
+    r["frac"] = r["achieved"] / r["peak"]
+    r["roofline_time_ms"] = max(t_hbm, t_tc) * 1e3
+    return r
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -444,7 +466,7 @@ def run_ours(args, wl, world, rank, local):
                          t_min=wl_knob(wl, "t_min"), t_max=wl_knob(wl, "t_max"), entropy_bound=wl_knob(wl, "bound"),
                          admit_tick=list(admit) if admit else None,
                          mode=dg.DG_REACCEPT if wl.get("mode") == "reaccept" else dg.DG_FREEZE,
-                         softcap=float(wl.get("softcap", 0.0)))
+                         softcap=float(wl.get("softcap", 0.0)), self_cond=1 if args.self_cond else 0)
     s = dg.Sampler(cfg, w_dev, stream=stream)
     resid = torch.empty(B, L, d, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -529,8 +551,25 @@ def run_ours(args, wl, world, rank, local):
             ev[3].synchronize()
             per_kernel[k] = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
         s.set_timing_events(None)
-    info = s.sync_info()  # also surfaces a latched device fault
-    cs2 = canvas_steps(info)
+        cs2 = canvas_steps(s.sync_info())  # also surfaces a latched device fault
+        sc_ms, sc_rows = [], []
+        if args.self_cond:
+            # the self-conditioning input after a tick (dg_self_condition), timed alone, L2 flushed
+            sc_out = torch.empty(B, L, d, dtype=torch.float32, device=dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for k in range(args.kernel_steps):
+                make_resid()
+                flush_l2()
+                before = canvas_steps(s.sync_info())
+                s.step(resid)
+                flush_l2()
+                e0.record(stream)
+                s.self_condition(sc_out)
+                e1.record(stream)
+                e1.synchronize()
+                sc_ms.append(e0.elapsed_time(e1))
+                sc_rows.append((canvas_steps(s.sync_info()) - before) * L)
+    s.sync_info()  # a fault latched by the self-conditioning calls
     device_s = float(tick_ms.sum()) / 1e3
     # positions denoised in the timed ticks, counted from the sampler's own step counters
     positions_timed = (cs1 - cs0) * L
@@ -625,6 +664,8 @@ def run_ours(args, wl, world, rank, local):
                                         "statistics and sample; combine + commit + re-noise + plan) + 1 residual "
                                         "generator"),
                 "roofline": roof, "e2e": e2e, "clocks": clk}
+        if sc_ms:
+            line["self_cond"] = self_cond_roofline(V, d, float(np.mean(sc_rows)), float(np.mean(sc_ms)) / 1e3, peaks)
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args, wl, W16)
         print(json.dumps(line), flush=True)
@@ -656,6 +697,8 @@ def main():
     ap.add_argument("--kernel-steps", type=int, default=None,
                     help="ticks of the per-kernel timing pass (default: 50 on the model-scale workloads, else 200)")
     ap.add_argument("--clocks-csv", default=None, help="also write the raw clock samples of the timed region here")
+    ap.add_argument("--self-cond", action="store_true",
+                    help="also time dg_self_condition after the per-kernel pass and report its roofline")
     ap.add_argument("--cpu-one-core", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-rows", type=int, default=8, help=argparse.SUPPRESS)
     args = ap.parse_args()
