@@ -21,6 +21,10 @@ constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kStageA = kBM * kBK * 2;  // 16 KB
 constexpr int kStageB = kBN * kBK * 2;  // 32 KB
+// on SM pairs (cta_group::2) each CTA stages its own 128 rows of A and its own 128-row half of B
+constexpr int kStagesPair = 6;
+constexpr int kStagePairA = kBM * kBK * 2;        // 16 KB
+constexpr int kStagePairB = (kBN / 2) * kBK * 2;  // 16 KB
 constexpr int kEpiWarps = 16;           // four per TMEM lane quadrant, each owning 64 of the 256 columns
 constexpr int kThreadsLM = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 2 * kBN;      // double-buffered accumulator
@@ -313,7 +317,9 @@ cudaError_t launch_plan(const Dev& dv, int tick, cudaStream_t st);
 cudaError_t lmhead_configure();
 cudaError_t selfcond_configure();
 cudaError_t launch_transpose_w(const void* w, uint16_t* wt, int V, int d, int v_pad, cudaStream_t st);
-cudaError_t launch_selfcond(const Dev& dv, const CUtensorMap* tm_h, const CUtensorMap* tm_w, const CUtensorMap* tm_p,
-                            const CUtensorMap* tm_wt, float* out, int num_sms, cudaStream_t st);
+// pair: the sampler runs its LM head on SM pairs (256 positions and up); tm_w and tm_wt then have
+// 128-row boxes, else 256-row ones
+cudaError_t launch_selfcond(const Dev& dv, bool pair, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
+                            const CUtensorMap* tm_p, const CUtensorMap* tm_wt, float* out, int num_sms, cudaStream_t st);
 
 }  // namespace dg

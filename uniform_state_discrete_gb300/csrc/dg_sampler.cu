@@ -21,7 +21,7 @@ struct dg_sampler {
   std::vector<int32_t> admit;
   dg::Dev dv;
   CUtensorMap tmA, tmB;
-  CUtensorMap tmW256, tmP, tmWT;  // self-conditioning: W in 256-row boxes, P, W^T
+  CUtensorMap tmP, tmWT;  // self-conditioning: P, and W^T in boxes of the LM head's B rows
   bool pair;  // LM head on CTA pairs (tcgen05 cta_group::2), chosen when a tick can hold >= 256 rows
   bool split = false;            // the vocabulary is split across ranks (dg_denoise_step_partial / _finish)
   bool partial_pending = false;  // a partial tick waits for its finishing step
@@ -183,10 +183,14 @@ int make_layout(const dg_config* c, Layout* L, char* why) {
   L->wt = L->probs = L->sc_part = L->row_scale = L->row_log2z = L->row_canvas = L->sc_rows = 0;
   L->sc_vpad = L->sc_kc = L->sc_kbpc = 0;
   if (c->self_cond) {
-    // the contraction's grid: row tiles x 256-wide d tiles x vocabulary chunks, about two units per SM
+    // the contraction's grid: row tiles x 256-wide d tiles x vocabulary chunks, about two units per
+    // SM (single CTAs) or per SM pair (256 positions and up, the sampler's rule), rounded so that no
+    // pair takes a third
     L->sc_vpad = L->n_vtiles * dg::kBN;
-    const int kbv = L->sc_vpad / dg::kBK, n_mt = (int)((rows + dg::kBM - 1) / dg::kBM), n_dt = (int)((d + 255) / 256);
-    int kc = (304 + n_mt * n_dt - 1) / (n_mt * n_dt);
+    const bool pair = rows >= 2 * dg::kBM;
+    const int kbv = L->sc_vpad / dg::kBK, n_dt = (int)((d + 255) / 256);
+    const int n_mt = (int)((rows + (pair ? 2 : 1) * dg::kBM - 1) / ((pair ? 2 : 1) * dg::kBM));
+    int kc = pair ? 152 / (n_mt * n_dt) : (304 + n_mt * n_dt - 1) / (n_mt * n_dt);
     kc = kc < 1 ? 1 : (kc > kbv ? kbv : kc);
     L->sc_kbpc = (kbv + kc - 1) / kc;
     L->sc_kc = (kbv + L->sc_kbpc - 1) / L->sc_kbpc;  // every chunk holds at least one K block
@@ -465,9 +469,8 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "configure kernels"));
   if (cfg->self_cond) {
     uint16_t* wt = reinterpret_cast<uint16_t*>(w + L.wt);
-    if (!encode_2d(&s->tmW256, w_vocab, (uint64_t)dv.V, (uint64_t)dv.d, dg::kBN, s->err) ||
-        !encode_2d(&s->tmP, dv.sc_probs, (uint64_t)L.rows_cap, (uint64_t)L.sc_vpad, dg::kBM, s->err) ||
-        !encode_2d(&s->tmWT, wt, (uint64_t)dv.d, (uint64_t)L.sc_vpad, dg::kBN, s->err))
+    if (!encode_2d(&s->tmP, dv.sc_probs, (uint64_t)L.rows_cap, (uint64_t)L.sc_vpad, dg::kBM, s->err) ||
+        !encode_2d(&s->tmWT, wt, (uint64_t)dv.d, (uint64_t)L.sc_vpad, s->pair ? dg::kBN / 2 : dg::kBN, s->err))
       return fail(DG_ERR_ARG);
     ce = dg::selfcond_configure();
     if (ce != cudaSuccess) return fail(cuda_fail(s->err, ce, "configure self-conditioning kernels"));
@@ -574,8 +577,7 @@ dg_status dg_self_condition(dg_sampler* s, float* out) {
   if (!s->dv.sc_probs) return set_err(s->err, "the sampler was created without self_cond"), DG_ERR_STATE;
   if (s->partial_pending) return set_err(s->err, "a partial tick is not finished"), DG_ERR_STATE;
   DG_CUDA(s->err,
-          dg::launch_selfcond(s->dv, &s->tmA, s->pair ? &s->tmW256 : &s->tmB, &s->tmP, &s->tmWT, out, s->num_sms,
-                              s->stream),
+          dg::launch_selfcond(s->dv, s->pair, &s->tmA, &s->tmB, &s->tmP, &s->tmWT, out, s->num_sms, s->stream),
           "launch self-conditioning");
   return DG_OK;
 }

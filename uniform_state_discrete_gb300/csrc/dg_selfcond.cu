@@ -66,6 +66,38 @@ struct ScUnits {
   }
 };
 
+// An epilogue's 16 accumulator columns [c0, c0 + 16) of `row`: kProbs writes P = 2^(u - log2 Z),
+// u = z log2(e)/T, rounded to bf16 (zero past V); kGemm writes the vocabulary chunk's share of e
+// for hidden columns [c0, c0 + 16).
+template <int kMode, bool kCap>
+__device__ __forceinline__ void store_cols(const Dev& dv, const float (&acc)[16], int row, int c0, int kb0,
+                                           float scale, float l2z) {
+  if (kMode == kProbs) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      float z0 = acc[j], z1 = acc[j + 1];
+      if (kCap) {
+        z0 = dv.softcap * tanhf(z0 * dv.inv_softcap);
+        z1 = dv.softcap * tanhf(z1 * dv.inv_softcap);
+      }
+      const float p0 = c0 + j < dv.V ? ex2_approx(fmaf(z0, scale, -l2z)) : 0.f;
+      const float p1 = c0 + j + 1 < dv.V ? ex2_approx(fmaf(z1, scale, -l2z)) : 0.f;
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+      pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(dv.sc_probs + (size_t)row * dv.sc_vpad + c0);
+    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  } else {
+    const int kc = kb0 / dv.sc_kbpc;
+    float* dst = dv.sc_part + ((size_t)kc * dv.rows_cap + row) * dv.d + c0;
+#pragma unroll
+    for (int j = 0; j < 16; j += 4)
+      if (c0 + j < dv.d) *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+  }
+}
+
 template <int kMode, bool kCap>
 __global__ void __launch_bounds__(kThreadsLM, 1)
     k_selfcond(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv) {
@@ -231,33 +263,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             if (lane == 0) mbar_arrive(&tempty[ab]);
           }
           if (!valid) continue;
-          const int c0 = t * kBN + cg * kColsPerWarp + cc * 16;  // vocabulary entry (kProbs) or hidden column (kGemm)
-          if (kMode == kProbs) {
-            // P = 2^(u - log2 Z), u = z log2(e)/T, rounded to bf16 (zero past V)
-            uint32_t pk[8];
-#pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-              float z0 = acc[j], z1 = acc[j + 1];
-              if (kCap) {
-                z0 = dv.softcap * tanhf(z0 * dv.inv_softcap);
-                z1 = dv.softcap * tanhf(z1 * dv.inv_softcap);
-              }
-              const float p0 = c0 + j < dv.V ? ex2_approx(fmaf(z0, scale, -l2z)) : 0.f;
-              const float p1 = c0 + j + 1 < dv.V ? ex2_approx(fmaf(z1, scale, -l2z)) : 0.f;
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-              pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(dv.sc_probs + (size_t)row * dv.sc_vpad + c0);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          } else {
-            // this vocabulary chunk's share of e for hidden columns [c0, c0 + 16)
-            const int kc = kb0 / dv.sc_kbpc;
-            float* dst = dv.sc_part + ((size_t)kc * dv.rows_cap + row) * dv.d + c0;
-#pragma unroll
-            for (int j = 0; j < 16; j += 4)
-              if (c0 + j < dv.d) *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-          }
+          store_cols<kMode, kCap>(dv, acc, row, t * kBN + cg * kColsPerWarp + cc * 16, kb0, scale, l2z);
         }
       }
     }
@@ -268,6 +274,215 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)kTmemCols)
+                 : "memory");
+  }
+}
+
+// The same two contractions on SM pairs, as the LM head runs above 256 positions: M = 256 rows
+// per tcgen05.mma.cta_group::2 instruction, each CTA staging its own 128 rows of A (h, or P) and
+// its own 128-row half of the 256-row B tile (W, or W^T), so B is streamed once for 256 rows and
+// each SM takes in 32 KB from L2 per K block instead of 48 (the single-CTA form, whose 256-row
+// B stage beside a 128-row A stage asks more of an SM's L2 ingress than the MMA rate allows).
+// Units as ScUnits with 256-row tiles; barriers as in the LM head on pairs:
+//   full[s]   (leader)  both CTAs' TMA bytes; the leader arms it with the total
+//   empty[s]  (both)    released by the leader's commit, multicast to the pair
+//   tfull[b]  (both)    accumulator ready, multicast from the leader's commit
+//   tempty[b] (leader)  both CTAs' 16 epilogue warps release the accumulator
+template <int kMode, bool kCap>
+__global__ void __launch_bounds__(kThreadsLM, 1)
+    k_selfcond_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Dev dv) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int tile_ok[2];  // the epilogue's poller found the tile's accumulator ready (per TMEM buffer)
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStagesPair * kStagePairA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStagesPair * kStagePairB);
+  uint64_t* empty = full + kStagesPair;
+  uint64_t* tfull = empty + kStagesPair;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesPair; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 1) {
+    // one warp of each CTA of the pair allocates together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"((uint32_t)kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before anything arrives on them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  // rows of the tick that left h, the temperature factors and log2 Z behind
+  const int n_rows = (int)__ldcg(dv.sc_rows);
+  const ScUnits su{(n_rows + 2 * kBM - 1) / (2 * kBM), (dv.d + kBN - 1) / kBN, (dv.d + kBK - 1) / kBK};
+  const int n_units = su.units(dv, kMode);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int u = cid; u < n_units && ok; u += n_clusters) {
+        int mt, t0, t1, kb0, kb1;
+        su.at(dv, kMode, u, mt, t0, t1, kb0, kb1);
+        for (int t = t0; t < t1 && ok; ++t) {
+          for (int kb = kb0; kb < kb1; ++kb) {
+            // both CTAs' loads complete the leader's full barrier, so the leader's MMAs never run a
+            // lap ahead of either producer and this parity wait cannot alias
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full_leader = peer_addr(smem_u32(&full[stage]), 0);
+            if (leader) mbar_expect_tx(&full[stage], (uint32_t)(2 * (kStagePairA + kStagePairB)));
+            tma_load_2d_pair(sA + stage * kStagePairA, &tmA, kb * kBK, mt * 2 * kBM + (int)rank * kBM, full_leader);
+            tma_load_2d_pair(sB + stage * kStagePairB, &tmB, kb * kBK, t * kBN + (int)rank * (kBN / 2), full_leader);
+            if (++stage == (uint32_t)kStagesPair) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // drain: one more lap of the ring's waits covers the releases of the last kStagesPair loads
+      // (laps before the first load pass at once), so no copy or release is still in flight toward
+      // this CTA when the pair exits
+      for (int i = 0; i < kStagesPair; ++i) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, dv.plan)) break;
+        if (++stage == (uint32_t)kStagesPair) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer (leader)
+    if (lane == 0 && leader) {
+      const uint64_t adesc0 = sw128_desc(smem_u32(sA)), bdesc0 = sw128_desc(smem_u32(sB));
+      uint32_t stage = 0, phase = 0, tcount = 0;
+      bool ok = true, any = false;
+      for (int u = cid; u < n_units && ok; u += n_clusters) {
+        int mt, t0, t1, kb0, kb1;
+        su.at(dv, kMode, u, mt, t0, t1, kb0, kb1);
+        for (int t = t0; t < t1 && ok; ++t, ++tcount) {
+          const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
+          if (!mbar_wait(&tempty[ab], aph ^ 1u, abort_flag, dv.plan)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + ab * (uint32_t)kBN;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, dv.plan)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad = adesc0 + (uint64_t)((stage * kStagePairA) >> 4);
+            const uint64_t bd = bdesc0 + (uint64_t)((stage * kStagePairB) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+                            (kb != kb0 || kk != 0) ? 1u : 0u);
+            mma_commit_pair(&empty[stage], (uint16_t)0x3);
+            any = true;
+            if (++stage == (uint32_t)kStagesPair) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit_pair(&tfull[ab], (uint16_t)0x3);
+        }
+      }
+      if (!ok && any) {
+        // wait (bounded) for the MMAs already issued before TMEM is freed
+        mma_commit_pair(drain, (uint16_t)0x1);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(drain, 0u) && global_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int cg = (warp - 2) >> 2;
+    const uint32_t tempty_leader[2] = {peer_addr(smem_u32(&tempty[0]), 0), peer_addr(smem_u32(&tempty[1]), 0)};
+    uint32_t tcount = 0;
+    bool aborted = false;
+    for (int u = cid; u < n_units; u += n_clusters) {
+      int mt, t0, t1, kb0, kb1;
+      su.at(dv, kMode, u, mt, t0, t1, kb0, kb1);
+      const int row = mt * 2 * kBM + (int)rank * kBM + q * 32 + lane;
+      const bool valid = row < n_rows;
+      const float scale = valid && kMode == kProbs ? __ldcg(dv.row_scale + row) : 0.f;
+      const float l2z = valid && kMode == kProbs ? __ldcg(dv.row_log2z + row) : 0.f;
+      for (int t = t0; t < t1; ++t, ++tcount) {
+        if (aborted) continue;
+        const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
+        // one warp polls for the tile, the other fifteen wait on a named barrier (as in the LM head)
+        if (warp == 2) {
+          if (lane == 0) tile_ok[ab] = mbar_wait_poll(&tfull[ab], aph, 256u, abort_flag, dv.plan) ? 1 : 0;
+          __syncwarp();
+        }
+        asm volatile("bar.sync 4, %0;" ::"r"(32 * kEpiWarps) : "memory");
+        if (!*(volatile int*)&tile_ok[ab]) {
+          aborted = true;
+          continue;
+        }
+        tc_fence_after();
+        const uint32_t tbase =
+            tmem_base + ((uint32_t)(q * 32) << 16) + ab * (uint32_t)kBN + (uint32_t)(cg * kColsPerWarp);
+#pragma unroll 1
+        for (int cc = 0; cc < kColsPerWarp / 16; ++cc) {
+          float acc[16];
+          __syncwarp();
+          tmem_ld16(tbase + (uint32_t)(cc * 16), acc);
+          if (cc == kColsPerWarp / 16 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader[ab]);
+          }
+          if (!valid) continue;
+          store_cols<kMode, kCap>(dv, acc, row, t * kBN + cg * kColsPerWarp + cc * 16, kb0, scale, l2z);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs are done with the pair's TMEM and barriers
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)kTmemCols)
                  : "memory");
   }
 }
@@ -312,7 +527,28 @@ __global__ void __launch_bounds__(256) k_transpose_w(const uint16_t* __restrict_
 }
 
 constexpr size_t kSmemBytesSc = 1024 + (size_t)kStages * (kStageA + kStageB) + 256;
-static_assert(kSmemBytesSc <= 232448, "shared memory per CTA");
+constexpr size_t kSmemBytesScPair = 1024 + (size_t)kStagesPair * (kStagePairA + kStagePairB) + 256;
+static_assert(kSmemBytesSc <= 232448 && kSmemBytesScPair <= 232448, "shared memory per CTA");
+
+template <int kMode, bool kCap>
+cudaError_t launch_pair(int units, int num_sms, const CUtensorMap* tmA, const CUtensorMap* tmB, const Dev& dv,
+                        cudaStream_t st) {
+  int pairs = units < num_sms / 2 ? units : num_sms / 2;
+  if (pairs < 1) pairs = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kThreadsLM);
+  cfg.dynamicSmemBytes = kSmemBytesScPair;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_selfcond_pair<kMode, kCap>, *tmA, *tmB, dv);
+}
 
 }  // namespace
 
@@ -321,6 +557,9 @@ cudaError_t selfcond_configure() {
   for (auto k : {k_selfcond<kProbs, false>, k_selfcond<kProbs, true>, k_selfcond<kGemm, false>,
                  k_selfcond<kGemm, true>})
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesSc);
+  for (auto k : {k_selfcond_pair<kProbs, false>, k_selfcond_pair<kProbs, true>, k_selfcond_pair<kGemm, false>})
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesScPair);
   return e;
 }
 
@@ -330,23 +569,34 @@ cudaError_t launch_transpose_w(const void* w, uint16_t* wt, int V, int d, int v_
   return cudaGetLastError();
 }
 
-cudaError_t launch_selfcond(const Dev& dv, const CUtensorMap* tm_h, const CUtensorMap* tm_w, const CUtensorMap* tm_p,
-                            const CUtensorMap* tm_wt, float* out, int num_sms, cudaStream_t st) {
-  const int max_mt = (dv.max_active * dv.L + kBM - 1) / kBM;
+cudaError_t launch_selfcond(const Dev& dv, bool pair, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
+                            const CUtensorMap* tm_p, const CUtensorMap* tm_wt, float* out, int num_sms, cudaStream_t st) {
   const int n_dt = (dv.d + kBN - 1) / kBN;
-  int g1 = max_mt * dv.n_chunks, g2 = max_mt * n_dt * dv.sc_kc;
-  g1 = g1 < num_sms ? g1 : num_sms;
-  g2 = g2 < num_sms ? g2 : num_sms;
   const bool cap = dv.softcap > 0.f;
-  if (cap)
-    k_selfcond<kProbs, true><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
-  else
-    k_selfcond<kProbs, false><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  k_selfcond<kGemm, false><<<g2, kThreadsLM, kSmemBytesSc, st>>>(*tm_p, *tm_wt, dv);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if (pair) {
+    // 256-row tiles on SM pairs; the maps' B boxes are 128 rows (each CTA's half of a tile)
+    const int max_mt = (dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM);
+    e = cap ? launch_pair<kProbs, true>(max_mt * dv.n_chunks, num_sms, tm_h, tm_w, dv, st)
+            : launch_pair<kProbs, false>(max_mt * dv.n_chunks, num_sms, tm_h, tm_w, dv, st);
+    if (e != cudaSuccess) return e;
+    e = launch_pair<kGemm, false>(max_mt * n_dt * dv.sc_kc, num_sms, tm_p, tm_wt, dv, st);
+    if (e != cudaSuccess) return e;
+  } else {
+    const int max_mt = (dv.max_active * dv.L + kBM - 1) / kBM;
+    int g1 = max_mt * dv.n_chunks, g2 = max_mt * n_dt * dv.sc_kc;
+    g1 = g1 < num_sms ? g1 : num_sms;
+    g2 = g2 < num_sms ? g2 : num_sms;
+    if (cap)
+      k_selfcond<kProbs, true><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
+    else
+      k_selfcond<kProbs, false><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_selfcond<kGemm, false><<<g2, kThreadsLM, kSmemBytesSc, st>>>(*tm_p, *tm_wt, dv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const long long work = (long long)dv.max_active * dv.L * (dv.d >> 2);
   long long blocks = (work + 255) / 256;
   if (blocks > 8 * num_sms) blocks = 8 * num_sms;
