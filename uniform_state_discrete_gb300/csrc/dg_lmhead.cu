@@ -541,9 +541,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      // descriptors of stage 0; a stage or K offset adds its 16-byte count to the
-      // start-address field, which stays below 2^14 for any shared-memory address
-      const uint64_t adesc0 = sw128_desc(smem_u32(sA)), bdesc0 = sw128_desc(smem_u32(sB));
+      // descriptors of stage 0; a stage or K offset adds to the low word only (as on pairs)
+      const DescPair dA(sw128_desc(smem_u32(sA))), dB(sw128_desc(smem_u32(sB)));
       uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true, any = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -565,12 +564,12 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
               break;
             }
             tc_fence_after();
-            const uint64_t ad = adesc0 + (uint64_t)((stage * kStageA) >> 4);
-            const uint64_t bd = bdesc0 + (uint64_t)((stage * kStageB) >> 4);
+            const uint32_t alo = dA.lo + (uint32_t)((stage * kStageA) >> 4);
+            const uint32_t blo = dB.lo + (uint32_t)((stage * kStageB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               // advance K by 16 bf16 = 32 bytes inside the swizzled 128-byte row
-              mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), (kb | kk) != 0 ? 1u : 0u);
+              mma_bf16(d_tmem, dA.at(alo + (uint32_t)(kk * 2)), dB.at(blo + (uint32_t)(kk * 2)), (kb | kk) != 0 ? 1u : 0u);
             }
             mma_commit(&empty[stage]);
             any = true;
@@ -870,8 +869,9 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     }
     asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
     if (warp == 2 && lane == 0 && n_rows > (int)blockIdx.x) {
-      __threadfence();  // this CTA's rows are written
-      atomicAdd(dv.rows_ready, (unsigned)((n_rows - 1 - (int)blockIdx.x) / (int)gridDim.x + 1));
+      // this CTA's rows (written by all its epilogue warps, ordered before this thread by the
+      // barrier above) are released with the count, in one reduction
+      red_release_add(dv.rows_ready, (unsigned)((n_rows - 1 - (int)blockIdx.x) / (int)gridDim.x + 1));
     }
   }
 
@@ -955,8 +955,10 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
     // ---------------------------------------------------------- MMA issuer (leader)
     if (lane == 0 && leader) {
       // descriptors of stage 0; a stage or K offset adds its 16-byte count to the
-      // start-address field, which stays below 2^14 for any shared-memory address
-      const uint64_t adesc0 = sw128_desc(smem_u32(sA)), bdesc0 = sw128_desc(smem_u32(sB));
+      // start-address field, which stays below 2^14 for any shared-memory address,
+      // so only the low word changes (32-bit adds: fewer instructions from a warp
+      // whose issue slots the epilogue warps of its sub-partition contend for)
+      const DescPair dA(sw128_desc(smem_u32(sA))), dB(sw128_desc(smem_u32(sB)));
       uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true, any = false;
       for (int u = cid; u < n_units && ok; u += n_clusters) {
@@ -978,11 +980,12 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
               break;
             }
             tc_fence_after();
-            const uint64_t ad = adesc0 + (uint64_t)((stage * kStagePairA) >> 4);
-            const uint64_t bd = bdesc0 + (uint64_t)((stage * kStagePairB) >> 4);
+            const uint32_t alo = dA.lo + (uint32_t)((stage * kStagePairA) >> 4);
+            const uint32_t blo = dB.lo + (uint32_t)((stage * kStagePairB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_bf16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), (kb | kk) != 0 ? 1u : 0u);
+              mma_bf16_pair(d_tmem, dA.at(alo + (uint32_t)(kk * 2)), dB.at(blo + (uint32_t)(kk * 2)),
+                            (kb | kk) != 0 ? 1u : 0u);
             mma_commit_pair(&empty[stage], (uint16_t)0x3);
             any = true;
             if (++stage == (uint32_t)kStagesPair) {

@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint64_t adesc0 = sw128_desc(smem_u32(sA)), bdesc0 = sw128_desc(smem_u32(sB));
+      const DescPair dA(sw128_desc(smem_u32(sA))), dB(sw128_desc(smem_u32(sB)));
       uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true, any = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -202,11 +202,12 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
               break;
             }
             tc_fence_after();
-            const uint64_t ad = adesc0 + (uint64_t)((stage * kStageA) >> 4);
-            const uint64_t bd = bdesc0 + (uint64_t)((stage * kStageB) >> 4);
+            const uint32_t alo = dA.lo + (uint32_t)((stage * kStageA) >> 4);
+            const uint32_t blo = dB.lo + (uint32_t)((stage * kStageB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_bf16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), (kb != kb0 || kk != 0) ? 1u : 0u);
+              mma_bf16(d_tmem, dA.at(alo + (uint32_t)(kk * 2)), dB.at(blo + (uint32_t)(kk * 2)),
+                       (kb != kb0 || kk != 0) ? 1u : 0u);
             mma_commit(&empty[stage]);
             any = true;
             if (++stage == (uint32_t)kStages) {
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer (leader)
     if (lane == 0 && leader) {
-      const uint64_t adesc0 = sw128_desc(smem_u32(sA)), bdesc0 = sw128_desc(smem_u32(sB));
+      const DescPair dA(sw128_desc(smem_u32(sA))), dB(sw128_desc(smem_u32(sB)));
       uint32_t stage = 0, phase = 0, tcount = 0;
       bool ok = true, any = false;
       for (int u = cid; u < n_units && ok; u += n_clusters) {
@@ -404,11 +405,11 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
               break;
             }
             tc_fence_after();
-            const uint64_t ad = adesc0 + (uint64_t)((stage * kStagePairA) >> 4);
-            const uint64_t bd = bdesc0 + (uint64_t)((stage * kStagePairB) >> 4);
+            const uint32_t alo = dA.lo + (uint32_t)((stage * kStagePairA) >> 4);
+            const uint32_t blo = dB.lo + (uint32_t)((stage * kStagePairB) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_bf16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+              mma_bf16_pair(d_tmem, dA.at(alo + (uint32_t)(kk * 2)), dB.at(blo + (uint32_t)(kk * 2)),
                             (kb != kb0 || kk != 0) ? 1u : 0u);
             mma_commit_pair(&empty[stage], (uint16_t)0x3);
             any = true;

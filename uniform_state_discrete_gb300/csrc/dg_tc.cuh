@@ -53,6 +53,11 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
       : "memory");
   return ok != 0;
 }
+// A release reduction at GPU scope: the thread's earlier writes, and those ordered before it by a
+// CTA barrier, are visible before the addition is.
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -138,6 +143,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= (uint64_t)2 << 61;                            // layout: 128-byte swizzle
   return d;
 }
+
+// A descriptor split into its fixed high word and its low word, which holds the start address:
+// stage and K offsets are added to the low word alone (no carry: the 14-bit field holds any
+// shared-memory address).
+struct DescPair {
+  uint64_t hi;
+  uint32_t lo;
+  __device__ __forceinline__ explicit DescPair(uint64_t d) : hi(d & 0xFFFFFFFF00000000ull), lo((uint32_t)d) {}
+  __device__ __forceinline__ uint64_t at(uint32_t low) const { return hi | low; }
+};
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
 constexpr uint32_t kIdesc = (1u << 4)                         // D format fp32
