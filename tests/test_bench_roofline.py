@@ -39,3 +39,25 @@ def test_single_cta_kernel_reads_bf16_rows_instead_of_the_residual():
     # below 256 positions the RMSNorm kernel writes h first: the LM head reads 16 x 128 bf16 rows
     roof, _, _ = bench.lmhead_roofline(2048, 128, 16, False, 5e-6, PEAKS)
     assert roof["algorithmic_bytes_per_launch"] == 2048 * 128 * 2 + 16 * 128 * 2 + 16 * 8 * 32
+
+
+def test_self_conditioning_roofline_counts_both_contractions():
+    # one canvas at model scale: W 262144 x 2816 bf16 once, the bf16 rows h (256 x 2816 x 2 B) and
+    # the fp32 output (256 x 2816 x 4 B); the logits and P W are 2 x 2 x 256 x 262144 x 2816 flops,
+    # 0.398 ms at 1900 TFLOP/s against 0.218 ms for the bytes at 6800 GB/s: tensor-bound
+    V, d, P = 262144, 2816, 256
+    r = bench.self_cond_roofline(V, d, P, 0.56e-3, PEAKS)
+    want_bytes = V * d * 2 + P * d * 2 + P * d * 4
+    flops = 4.0 * P * V * d
+    assert r["algorithmic_bytes_per_call"] == want_bytes and r["algorithmic_flops_per_call"] == flops
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["roofline_time_ms"] == pytest.approx(flops / 1900e12 * 1e3)
+    assert r["frac"] == pytest.approx(flops / 0.56e-3 / 1900e12)
+
+
+def test_self_conditioning_roofline_at_few_positions_is_bound_by_w():
+    # 16 positions: the flops (2 x 2 x 16 x 2048 x 128) take nanoseconds, W 2048 x 128 bf16 microseconds
+    r = bench.self_cond_roofline(2048, 128, 16, 10e-6, PEAKS)
+    want_bytes = 2048 * 128 * 2 + 16 * 128 * 6
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(want_bytes / 10e-6 / 1e9)
