@@ -222,8 +222,9 @@ dg_status dg_vocab_slice(int32_t vocab, int32_t ranks, int32_t rank, int32_t* v_
 
 /*
  * Self-conditioning input of the next step ("The Annotated DiffusionGemma",
- * decode mode: "P @ E computes the expected token embeddings from the previous
- * iteration"; `_forward`'s condition_x before the embedding scale): for every
+ * decode mode: the previous step's probabilities times the embedding matrix
+ * give each position's expected token embedding; `_forward`'s condition_x
+ * before the embedding scale): for every
  * position of the canvases active at the last tick,
  *   out[c, p, :] = sum_v P[v] W[v, :],  P = softmax(z / T) of that tick
  * (after the softcap, at the tick's temperature: the distribution whose

@@ -172,10 +172,10 @@ def softcap(z: np.ndarray, c: float) -> np.ndarray:
 
 def expected_embedding(z: np.ndarray, T, W: np.ndarray, block_rows: int = 8192):
     """Self-conditioning input: e[p, :] = sum_v P[p, v] W[v, :] with P = softmax(z / T) row by row, in
-    fp64 from the bf16 values of W ("The Annotated DiffusionGemma", decode mode: "P @ E computes the
-    expected token embeddings from the previous iteration", P the previous step's post-softmax
-    distribution, which its denoise loop forms as Categorical(logits = model output / t); `_forward`'s
-    condition_x before the embedding scale).  ``z`` are the logits after the final softcap.  Returns
+    fp64 from the bf16 values of W ("The Annotated DiffusionGemma", decode mode: the previous step's
+    probabilities times the embedding matrix give each position's expected token embedding, the
+    probabilities being the categorical distribution its denoise loop forms from the model output
+    divided by the temperature; `_forward`'s condition_x before the embedding scale).  ``z`` are the logits after the final softcap.  Returns
     (e, a): e fp64 [n, d], and a[p, k] = sum_v P[p, v] |W[v, k]|, the scale of each coordinate."""
     z = np.asarray(z, dtype=np.float64)
     T = np.broadcast_to(np.asarray(T, dtype=np.float64), (z.shape[0],))[:, None]

@@ -21,8 +21,8 @@
  *       and one categorical sample.  The sample is drawn by the Gumbel-max
  *       rule (Gumbel 1954; e.g. Maddison, Tarlow, Minka, "A* Sampling", 2014):
  *       y = argmax_v (z_v/T + G_v), G_v = -ln E_v with E_v i.i.d. Exp(1),
- *       which has the law of Categorical(logits = z/T).sample() used in
- *       "Denoise, stage, commit, and generate".
+ *       which has the law of a draw from the categorical distribution with
+ *       logits z/T, the draw "Denoise, stage, commit, and generate" makes.
  *
  *   or_exp_variates -- the Exp(1) variates E_v of one position.  The
  *       vocabulary is cut into groups of 16 entries, j = v >> 4, and each

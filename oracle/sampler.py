@@ -29,7 +29,7 @@ accepted set and commit_step the last step a position was accepted.
 
 Readings where the pages are silent or disagree:
 by default committed positions stay frozen (ComfyUI-DiffusionGemma, "What it
-is": the lowest-entropy positions freeze into place) and only uncommitted
+is": positions committed at low entropy are not revisited) and only uncommitted
 positions enter the per-step sort; the prefix is exclusive and compared with <=; ties in
 H go to the lower position; the early-stop test is skipped at s = 0; the last
 step commits every remaining position to its sample; blocks of one canvas run

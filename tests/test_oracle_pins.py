@@ -496,8 +496,9 @@ def test_multi_commit_regime_low_noise():
 
 
 def test_committed_token_is_a_sample_not_the_argmax():
-    """Accepted positions take Categorical(logits=z/T).sample() ("Denoise, stage, commit, and
-    generate"), not the argmax: over near-uniform distributions on V=2048 the two almost never agree."""
+    """Accepted positions take a draw from the categorical distribution with logits z/T ("Denoise,
+    stage, commit, and generate"), not the argmax: over near-uniform distributions on V=2048 the two
+    almost never agree."""
     cfg = _cfg0(n_canvases=4, seeds=[0, 1, 2, 3])
     W = synth.wvocab(0, cfg.vocab, cfg.hidden)
     hits, total = 0, 0

@@ -1,11 +1,12 @@
 // Self-conditioning input for the next denoising step: the expected token
 // embedding under this step's distribution,
 //   e[p, :] = sum_v P[p, v] W[v, :],  P[p, :] = softmax(z[p, :] / T),
-// "The Annotated DiffusionGemma", decode mode ("P @ E computes the expected
-// token embeddings from the previous iteration, L independent convex sums")
-// and `_forward`'s condition_x, before the embedding scale; P is the same
-// distribution whose entropy the commit uses (the page's denoise loop forms
-// Categorical(logits = model output / t) and passes its probs to the next
+// "The Annotated DiffusionGemma", decode mode (the previous step's
+// probabilities times the embedding matrix, one convex combination of
+// embedding rows per position) and `_forward`'s condition_x, before the
+// embedding scale; P is the same distribution whose entropy the commit uses
+// (the page's denoise loop builds a categorical distribution from the model
+// output divided by the temperature and hands its probabilities to the next
 // decode), cast to bf16 before the contraction as the page casts it to the
 // activation dtype.
 //
