@@ -78,14 +78,38 @@ DEFAULT_WORKLOAD = "stress64x4_v262k"
 SIGMA_HIDDEN = 0.5
 
 
+def strip_comments(src: str) -> str:
+    """C/CUDA source without its comments and blank lines (string literals kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':  # a string literal, escapes included
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_digest() -> str:
-    """Digest of the LM-head kernel sources; a stored ncu traffic figure is valid only for this digest."""
+    """Digest of the LM-head kernel sources, comments left out; a stored ncu traffic figure is valid
+    only for this digest."""
     h = hashlib.sha256()
     for rel in ("uniform_state_discrete_gb300/csrc/dg_lmhead.cu", "uniform_state_discrete_gb300/csrc/dg_internal.cuh",
                 "uniform_state_discrete_gb300/csrc/dg_gumbel.cuh", "uniform_state_discrete_gb300/csrc/dg_norm.cuh",
                 "uniform_state_discrete_gb300/csrc/dg_tc.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

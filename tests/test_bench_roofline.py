@@ -61,3 +61,10 @@ def test_self_conditioning_roofline_at_few_positions_is_bound_by_w():
     want_bytes = 2048 * 128 * 2 + 16 * 128 * 6
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
     assert r["achieved"] == pytest.approx(want_bytes / 10e-6 / 1e9)
+
+
+def test_kernel_digest_ignores_comments_but_not_code():
+    src = 'int a = 1;  // a note\n/* a block\n   note */\nconst char* s = "x // y /* z */";\n\n  b += 2;\n'
+    assert bench.strip_comments(src) == 'int a = 1;\nconst char* s = "x // y /* z */";\n  b += 2;'
+    assert bench.strip_comments(src.replace("a note", "another note")) == bench.strip_comments(src)
+    assert bench.strip_comments(src.replace("b += 2", "b += 3")) != bench.strip_comments(src)

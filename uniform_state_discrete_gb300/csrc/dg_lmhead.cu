@@ -188,9 +188,11 @@ struct BestScore {
 // (global memory).  Each is the score of a real entry, so the row's winner is
 // always scored and the result equals the unscreened maximum.  The walk is
 // started only if its first entry or the second order statistic can pass,
-// tested on the first Philox block alone -- one block for sixteen entries (see
-// below).  Walks run one step per lane per round, all lanes of the warp
-// together.  Equal scores keep the lower index.
+// tested on words of the first Philox block alone -- one block for sixteen
+// entries, drawn before the tile's accumulator is ready (first_blocks).  Walks
+// run one step per lane per round, all lanes of the warp together.  Equal
+// scores keep the lower index.
+
 // The logits of a group as the statistics and the screen take them: capped (kCap), with
 // columns at or beyond V set to -inf (kTail); returns the group's maximum logit in `cmz`, or
 // false when the whole group lies beyond V.
