@@ -215,15 +215,27 @@ __device__ __forceinline__ void pdl_allow_next_after(int v) {
   asm volatile("griddepcontrol.launch_dependents;" ::"r"(v) : "memory");
 }
 
-// Counters that hand data from one kernel of a tick to the next without
-// waiting for the whole previous grid: the writer makes its stores visible
-// (fence after a CTA barrier) and adds to the counter; the reader spins on an
-// acquire load until the count it needs is reached, giving up after
-// kWaitLimitNs.  The planner of the next tick resets them.
+// Counters that hand data from one CTA or kernel of a tick to another without
+// waiting for a whole grid: after a CTA barrier one thread of the writer adds
+// to the counter with release semantics, so the CTA's earlier memory
+// operations are visible before the addition is; the reader acquires it (one
+// thread, followed by a CTA barrier), spinning until the count it needs is
+// reached and giving up after kWaitLimitNs.  The planner of the next tick
+// resets them.  Release and acquire each fold the fence into the one access.
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Both at once, for a counter whose old value elects the CTA that goes on with
+// every contributor's data: returns the value before the addition.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 __device__ __forceinline__ uint64_t now_ns() {
   uint64_t t;

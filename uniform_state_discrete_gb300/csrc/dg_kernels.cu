@@ -34,10 +34,7 @@ __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const float* __restric
                                    dv.h + (size_t)row * dv.d, dv.d, dv.eps, (int)threadIdx.x, red,
                                    [] { __syncthreads(); });
   // the row is written: count it for the LM head, which waits for all rows
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(dv.rows_ready, 1u);
-  }
+  if (threadIdx.x == 0) red_release_add(dv.rows_ready, 1u);
 }
 
 // Finishing kernel of a tick.  Each warp combines the split-vocabulary partial
@@ -53,8 +50,8 @@ static_assert(kFinishRows <= (int)(sizeof(TailScratch::row_canvas) / sizeof(int)
 
 // The planner of k_finish: waits (bounded) until every CTA of the grid has read
 // this tick's plan, then plans the next tick.  `started` says that thread 0
-// already saw every CTA counted (a load the caller ordered by a fence since),
-// so no wait is needed; known_c / known_state pass on a slot the group wrote.
+// already saw every CTA counted, with an acquire load, so no wait is needed;
+// known_c / known_state pass on a slot the group wrote.
 __device__ __forceinline__ void plan_next_tick(const Dev& dv, int tick, const Group& g, TailScratch* sc,
                                                bool started = false, int known_c = -1, int known_state = kDone) {
   if (g.tid == 0 && !started) {
@@ -79,10 +76,7 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   const int tick = __ldcg(&dv.plan->tick);
   if (dv.sc_rows && blockIdx.x == 0 && threadIdx.x == 0) *dv.sc_rows = (uint32_t)n_rows;  // for self-conditioning
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(dv.fin_started, 1u);
-  }
+  if (threadIdx.x == 0) red_release_add(dv.fin_started, 1u);  // after every thread's reads of the plan
   pdl_allow_next();
   if (n_rows == 0) {
     if (blockIdx.x == 0) plan_next_tick(dv, tick, g, &sc);
@@ -141,14 +135,15 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
       }
     }
   }
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    // Release this CTA's rows to the canvas counter; the CTA that completes a canvas
+    // acquires every other CTA's rows of it with the same access.
     int nd = 0;
     for (int a = row0 / dv.L; a * dv.L < row1; ++a) {
       const int lo = max(a * dv.L, row0), hi = min((a + 1) * dv.L, row1);
       const int c = sc.row_canvas[lo - row0];
-      const unsigned old = atomicAdd(&dv.canvas_rows[c], (unsigned)(hi - lo));
+      const unsigned old = atom_add_acq_rel(&dv.canvas_rows[c], (unsigned)(hi - lo));
       if (old + (unsigned)(hi - lo) == (unsigned)dv.L) {
         dv.canvas_rows[c] = 0u;  // every row of this canvas is combined: reset for the next tick
         sc.done_list[nd++] = c;
@@ -161,27 +156,20 @@ __global__ void __launch_bounds__(256) k_finish(const Dev dv) {
   const int na = n_rows / dv.L;  // canvases active this tick
   for (int i = 0; i < nd; ++i) {
     const int c = sc.done_list[i];
-    // whether every CTA of the grid has started (plain load; the fence below
-    // orders it before the plan is rewritten)
-    const bool started = threadIdx.x == 0 && *(volatile const uint32_t*)dv.fin_started >= gridDim.x;
-    __threadfence();  // the rows' results, seen complete through the canvas counter, are read after it
+    // whether every CTA of the grid has started (an acquire: the plan is rewritten after it)
+    const bool started = threadIdx.x == 0 && ld_acquire(dv.fin_started) >= gridDim.x;
     const int state = commit_canvas(dv, c, g, &sc);
-    // With several canvases, the commit's writes are released before the commit
-    // counter and the planner acquires the other commits' slots; alone, this CTA
-    // plans right away from what it wrote itself.
-    if (na > 1) __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-      // the last commit of the tick plans the next; alone, this one is the last
-      sc.flags[1] = (na == 1 || atomicAdd(&dv.plan->commits, 1u) == (unsigned)(na - 1)) ? 1 : 0;
+      // The last commit of the tick plans the next; alone, this one is the last and
+      // plans right away from what it wrote itself.  With several canvases the
+      // commit counter releases this commit's writes and acquires the others'.
+      sc.flags[1] = (na == 1 || atom_add_acq_rel(&dv.plan->commits, 1u) == (unsigned)(na - 1)) ? 1 : 0;
     }
     __syncthreads();
     const int plan_now = sc.flags[1];
     __syncthreads();
-    if (plan_now) {
-      if (na > 1) __threadfence();
-      plan_next_tick(dv, tick, g, &sc, started, c, state);
-    }
+    if (plan_now) plan_next_tick(dv, tick, g, &sc, started, c, state);
   }
 }
 

@@ -714,10 +714,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       }
       if (cg == 0) gbest[rl] = ord_key(-INFINITY);  // the next unit may hold other rows
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-      if (warp == 2 && lane == 0 && mt * kBM < n_rows && !dv.hold_slabs) {
-        __threadfence();  // this unit's partial records of the slab are written
-        atomicAdd(dv.slab_done + mt, 1u);
-      }
+      if (warp == 2 && lane == 0 && mt * kBM < n_rows && !dv.hold_slabs)
+        red_release_add(dv.slab_done + mt, 1u);  // after this unit's partial records of the slab
     }
   }
 
@@ -1130,10 +1128,8 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
         // before that CTA's slab count: once the finishing kernel has seen every slab done it
         // may reset the tick's counters, and a later increment would carry into the next tick.
         if (rank == 0) atomicAdd(dv.units_done, 1u);
-        if ((mt * 2 + (int)rank) * kBM < n_rows && !dv.hold_slabs) {
-          __threadfence();  // this unit's partial records of the slab are written
-          atomicAdd(dv.slab_done + mt * 2 + (int)rank, 1u);
-        }
+        if ((mt * 2 + (int)rank) * kBM < n_rows && !dv.hold_slabs)
+          red_release_add(dv.slab_done + mt * 2 + (int)rank, 1u);  // after the records and the pacing count
       }
     }
   }
