@@ -192,6 +192,45 @@ def expected_embedding(z: np.ndarray, T, W: np.ndarray, block_rows: int = 8192):
     return e, a
 
 
+def expected_embedding_topk(z: np.ndarray, T, W: np.ndarray, k: int):
+    """Top-K self-conditioning input: e[p, :] = sum over the K most probable tokens v of row p of
+    q[p, v] W[v, :], q = softmax(z / T) restricted to those K tokens and renormalised to sum 1.
+
+    TensorSharp's DiffusionGemma doc lists an experimental top-K cutoff of the self-conditioning
+    input (DIFFUSION_SC_TOPK, default 32) beside its on-device sampling; the Annotated page's decode
+    mode describes the input as one convex combination of embedding rows per position, which the
+    renormalisation keeps.  Ranking: larger z / T first, equal values by the lower token index (the
+    tie rule used everywhere else); k >= V keeps every token, giving ``expected_embedding``.  In
+    fp64 from the bf16 values of W; ``z`` are the logits after the final softcap.
+
+    Returns (e, a, gap, sel): e fp64 [n, d]; a[p, k] = sum_v q[p, v] |W[v, k]|; gap[p] = the K-th
+    largest z / T minus the (K+1)-th (inf when k >= V), the margin by which the kept set is
+    decided; sel [n, K] the kept token indices, most probable first."""
+    z = np.asarray(z, dtype=np.float64)
+    n, V = z.shape
+    T = np.broadcast_to(np.asarray(T, dtype=np.float64), (n,))
+    kk = min(int(k), V)
+    d = W.shape[1]
+    e = np.zeros((n, d))
+    a = np.zeros((n, d))
+    gap = np.full(n, np.inf)
+    sel = np.zeros((n, kk), dtype=np.int64)
+    idx = np.arange(V)
+    for p in range(n):
+        u = z[p] / T[p]
+        order = np.lexsort((idx, -u))  # by u descending, then index ascending
+        keep = order[:kk]
+        if kk < V:
+            gap[p] = u[order[kk - 1]] - u[order[kk]]
+        w = np.exp(u[keep] - u[keep].max())
+        q = w / w.sum()
+        Wk = bf16_value(W[keep])
+        e[p] = q @ Wk
+        a[p] = q @ np.abs(Wk)
+        sel[p] = keep
+    return e, a, gap, sel
+
+
 def stats(z: np.ndarray, T, seed, block, step, pos) -> np.ndarray:
     """Per-row temperature softmax statistics and Gumbel-max sample; returns POS_DTYPE [n]."""
     z = np.ascontiguousarray(z, dtype=np.float64)

@@ -324,6 +324,80 @@ def test_expected_embedding_is_a_convex_combination_and_temperature_sharpens_it(
     np.testing.assert_allclose(e0, Wv[np.argmax(z, axis=1)], atol=1e-12)
 
 
+# ------------------------------------------------- top-K self-conditioning input
+def test_topk_embedding_keeping_every_token_is_the_dense_one():
+    """k >= V keeps the whole distribution: the dense expected embedding (itself pinned above)."""
+    W = synth.wvocab(7, 300, 24, sigma_w=0.3)
+    z = np.random.default_rng(8).standard_normal((5, 300))
+    dense, da = oracle.expected_embedding(z, 0.7, W)
+    for k in (300, 1000):
+        e, a, gap, sel = oracle.expected_embedding_topk(z, 0.7, W, k)
+        np.testing.assert_allclose(e, dense, rtol=0, atol=1e-14)
+        np.testing.assert_allclose(a, da, rtol=0, atol=1e-14)
+        assert np.all(np.isinf(gap)) and sel.shape == (5, 300)
+
+
+def test_topk_embedding_of_one_token_is_the_argmax_row_with_ties_to_the_lower_index():
+    W = synth.wvocab(9, 128, 16, sigma_w=0.3)
+    z = np.random.default_rng(10).standard_normal((3, 128))
+    z[0, 17] = 9.0
+    z[1, 90] = z[1, 33] = 9.0  # a tie: the lower index is kept
+    z[2, 127] = 9.0
+    e, _, gap, sel = oracle.expected_embedding_topk(z, 0.5, W, 1)
+    assert list(sel[:, 0]) == [17, 33, 127]
+    np.testing.assert_array_equal(e, oracle.bf16_value(W[[17, 33, 127]]))
+    assert gap[1] == 0.0 and gap[0] > 0 and gap[2] > 0
+
+
+def test_topk_embedding_of_equal_logits_is_the_mean_of_the_first_k_rows():
+    """Every token equally likely: ties go to the lower index, so the first k rows are kept with
+    equal weights."""
+    W = synth.wvocab(11, 200, 12, sigma_w=0.3)
+    for k in (1, 7, 32):
+        e, _, gap, sel = oracle.expected_embedding_topk(np.full((2, 200), -1.25), 0.9, W, k)
+        assert np.all(sel == np.arange(k)) and np.all(gap == 0.0)
+        mean = [sum(float(oracle.bf16_value(W[v, j])) for v in range(k)) / k for j in range(12)]
+        np.testing.assert_allclose(e, np.array([mean, mean]), rtol=0, atol=1e-15)
+
+
+def test_topk_embedding_two_kept_tokens_closed_form():
+    """k = 2 of many tokens: the two largest logits are renormalised between themselves,
+    e = s W_a + (1 - s) W_b with s = sigmoid((z_a - z_b) / T), whatever the other logits are."""
+    W = synth.wvocab(12, 64, 8, sigma_w=0.3)
+    z = np.random.default_rng(13).uniform(-3.0, 0.0, (1, 64))
+    z[0, 50], z[0, 9] = 2.0, 1.4
+    e, _, gap, sel = oracle.expected_embedding_topk(z, 0.8, W, 2)
+    s_ = 1.0 / (1.0 + math.exp(-(2.0 - 1.4) / 0.8))
+    np.testing.assert_allclose(e[0], s_ * oracle.bf16_value(W[50]) + (1 - s_) * oracle.bf16_value(W[9]), atol=1e-15)
+    assert list(sel[0]) == [50, 9]
+    assert abs(gap[0] - (1.4 - np.sort(z[0])[-3]) / 0.8) < 1e-15
+
+
+def test_topk_embedding_matches_brute_force_over_subsets():
+    """The kept set maximises the sum of the kept logits over all k-subsets (unique for distinct
+    logits), and the weights are the softmax restricted to it: the coordinate of W that is 1 for
+    every token gives 1 exactly, and adding a constant to every logit changes nothing."""
+    rng = np.random.default_rng(14)
+    V, d = 9, 6
+    W = synth.wvocab(15, V, d, sigma_w=0.3)
+    Wv = oracle.bf16_value(W)
+    W1 = W.copy()
+    W1[:, 0] = 0x3F80  # bf16 1.0
+    for k in (1, 2, 4, 8):
+        z = rng.standard_normal((3, V))
+        e, _, _, sel = oracle.expected_embedding_topk(z, 0.6, W, k)
+        for p in range(3):
+            best = max(itertools.combinations(range(V), k), key=lambda s: sum(z[p, list(s)]))
+            assert set(sel[p]) == set(best)
+            q = np.exp(z[p, list(best)] / 0.6)
+            q /= q.sum()
+            np.testing.assert_allclose(e[p], q @ Wv[list(best)], rtol=0, atol=1e-14)
+        e1, _, _, _ = oracle.expected_embedding_topk(z, 0.6, W1, k)
+        np.testing.assert_allclose(e1[:, 0], 1.0, rtol=0, atol=1e-15)
+        e2, _, _, _ = oracle.expected_embedding_topk(z + 3.5, 0.6, W, k)
+        np.testing.assert_allclose(e2, e, rtol=0, atol=1e-14)
+
+
 # ----------------------------------------------------------------- commit rule
 def test_acceptance_matches_pages_prefix_expression():
     """The pages' acceptance: sort H, accept where cumsum(sH) - sH <= bound ("Denoise, stage,
