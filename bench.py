@@ -161,6 +161,30 @@ def lmhead_roofline(V: int, d: int, P: int, pair: bool, seconds: float, peaks: d
     return roof, t_hbm, t_tc
 
 
+def self_cond_topk_roofline(V: int, d: int, P: float, K: int, seconds: float, peaks: dict) -> dict:
+    """Roofline of one dg_self_condition_topk call over P positions taking `seconds`: the logits
+    z = h W^T formed again (2 P V d flops) and the K kept rows of W summed per position.
+    Algorithmic bytes: W once, the bf16 rows h, the K gathered bf16 rows of W per position and the
+    fp32 output (the bf16 probabilities the implementation writes and re-reads are not counted)."""
+    k = min(K, V)
+    alg_bytes = V * d * 2 + P * d * (2 + 4) + P * k * d * 2
+    alg_flops = 2.0 * P * V * d
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg_flops / (peaks["bf16_tflops"] * 1e12)
+    r = {"ms_mean": seconds * 1e3, "positions_per_call": P, "top_k": K, "algorithmic_bytes_per_call": alg_bytes,
+         "algorithmic_flops_per_call": alg_flops,
+         "kernels": "k_selfcond (the LM head again, writing P = softmax(z/T) in bf16), k_selfcond_topk (one CTA "
+                    "per position: candidates from P, their logits again in fp32, the K best, the weighted rows)",
+         "timing": "CUDA events around the call on the sampler stream, after a tick, L2 flushed before it"}
+    if t_hbm >= t_tc:
+        r.update(bound="hbm", achieved=alg_bytes / seconds / 1e9, peak=peaks["hbm_gbs"], unit="GB/s")
+    else:
+        r.update(bound="tensor", achieved=alg_flops / seconds / 1e12, peak=peaks["bf16_tflops"], unit="TFLOP/s")
+    r["frac"] = r["achieved"] / r["peak"]
+    r["roofline_time_ms"] = max(t_hbm, t_tc) * 1e3
+    return r
+
+
 def self_cond_roofline(V: int, d: int, P: float, seconds: float, peaks: dict) -> dict:
     """Roofline of one dg_self_condition call over P positions taking `seconds`: the expected
     embedding softmax(z/T) W, with z = h W^T formed again.  Algorithmic bytes: W once, the bf16
@@ -576,7 +600,7 @@ def run_ours(args, wl, world, rank, local):
             per_kernel[k] = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
         s.set_timing_events(None)
         cs2 = canvas_steps(s.sync_info())  # also surfaces a latched device fault
-        sc_ms, sc_rows = [], []
+        sc_ms, sc_rows, sck_ms = [], [], []
         if args.self_cond:
             # the self-conditioning input after a tick (dg_self_condition), timed alone, L2 flushed
             sc_out = torch.empty(B, L, d, dtype=torch.float32, device=dev)
@@ -593,6 +617,14 @@ def run_ours(args, wl, world, rank, local):
                 e1.synchronize()
                 sc_ms.append(e0.elapsed_time(e1))
                 sc_rows.append((canvas_steps(s.sync_info()) - before) * L)
+                if args.self_cond_topk:
+                    # the top-K variant after the same tick (it reads what the tick left), L2 flushed
+                    flush_l2()
+                    e0.record(stream)
+                    s.self_condition_topk(sc_out, args.self_cond_topk)
+                    e1.record(stream)
+                    e1.synchronize()
+                    sck_ms.append(e0.elapsed_time(e1))
     s.sync_info()  # a fault latched by the self-conditioning calls
     device_s = float(tick_ms.sum()) / 1e3
     # positions denoised in the timed ticks, counted from the sampler's own step counters
@@ -690,6 +722,9 @@ def run_ours(args, wl, world, rank, local):
                 "roofline": roof, "e2e": e2e, "clocks": clk}
         if sc_ms:
             line["self_cond"] = self_cond_roofline(V, d, float(np.mean(sc_rows)), float(np.mean(sc_ms)) / 1e3, peaks)
+        if sck_ms:
+            line["self_cond_topk"] = self_cond_topk_roofline(V, d, float(np.mean(sc_rows)), args.self_cond_topk,
+                                                             float(np.mean(sck_ms)) / 1e3, peaks)
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args, wl, W16)
         print(json.dumps(line), flush=True)
@@ -721,6 +756,8 @@ def main():
     ap.add_argument("--kernel-steps", type=int, default=None,
                     help="ticks of the per-kernel timing pass (default: 50 on the model-scale workloads, else 200)")
     ap.add_argument("--clocks-csv", default=None, help="also write the raw clock samples of the timed region here")
+    ap.add_argument("--self-cond-topk", type=int, default=0, metavar="K",
+                    help="with --self-cond, also time dg_self_condition_topk with this K and report its roofline")
     ap.add_argument("--self-cond", action="store_true",
                     help="also time dg_self_condition after the per-kernel pass and report its roofline")
     ap.add_argument("--cpu-one-core", action="store_true", help=argparse.SUPPRESS)

@@ -239,6 +239,31 @@ dg_status dg_vocab_slice(int32_t vocab, int32_t ranks, int32_t rank, int32_t* v_
  */
 dg_status dg_self_condition(dg_sampler* s, float* out);
 
+/*
+ * Top-K variant of the self-conditioning input (TensorSharp's DiffusionGemma
+ * doc: an experimental cutoff of the self-conditioning input, K = 32 by
+ * default).  For every position of the canvases active at the last tick,
+ *   out[c, p, :] = sum over the K most probable tokens v of q[v] W[v, :],
+ * q = softmax(z / T) of that tick restricted to those K tokens and
+ * renormalised to sum 1, which keeps the input a convex combination of
+ * embedding rows as in the Annotated page's decode mode.  Tokens rank by
+ * z / T (after the softcap), equal values by the lower token index; top_k >= V
+ * keeps every token.  The weights come from the kept tokens' logits in fp32
+ * (not from bf16 probabilities) and the sum accumulates in fp32.  Tokens whose
+ * probability is below 2^-126 are never kept (their weights would be below
+ * 2^-108 of the largest), so fewer than K tokens may be kept.
+ *   top_k  1 <= top_k <= DG_SC_TOPK_MAX, else DG_ERR_ARG.
+ *   out    dev, fp32 [B, L, d], 16-byte aligned; rows of canvases not active
+ *          at the last tick are left as they are.
+ * Asynchronous.  Call it after a tick and before the next one; needs a
+ * sampler created with self_cond = 1, else DG_ERR_STATE.  It runs the LM head
+ * once more (its epilogue writes the probabilities in bf16, which only narrow
+ * down the candidates), then one CTA per position recomputes the candidates'
+ * logits and sums the kept rows of W: about one LM head in all.
+ */
+#define DG_SC_TOPK_MAX 256
+dg_status dg_self_condition_topk(dg_sampler* s, int32_t top_k, float* out);
+
 /* Residual supplier for dg_run: the backbone's place in the loop.  Must fill
  * resid_dev [B, L, d] for the active canvases of this tick from their current
  * canvas_dev [B, L] and slots_dev [B], enqueueing work on `stream`.  Returns

@@ -73,6 +73,7 @@ for _ in range(3):
                                          sc.canvas().cpu().numpy()[act])).to("cuda:0")
     sc.step(resid)
     sc.self_condition(out)
+    sc.self_condition_topk(out, 32)
     for s in ranks:
         s.step_partial(resid)
     dg.exchange_partials(ranks)
@@ -82,7 +83,7 @@ for _ in range(3):
     assert all(torch.equal(s.canvas(), sc.canvas()) for s in ranks)
 for s in ranks + [sc]:
     s.debug_check()
-print("split vocabulary and self-conditioning: guards intact, no index check failed", flush=True)
+print("split vocabulary and self-conditioning (dense and top-K): guards intact, no index check failed", flush=True)
 
 # a planted overflow: one byte past the first workspace buffer (the per-canvas slots), from the host
 s = ranks[0]

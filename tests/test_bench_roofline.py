@@ -63,6 +63,21 @@ def test_self_conditioning_roofline_at_few_positions_is_bound_by_w():
     assert r["achieved"] == pytest.approx(want_bytes / 10e-6 / 1e9)
 
 
+def test_topk_self_conditioning_roofline():
+    # one canvas at model scale: 2 x 256 x 262144 x 2816 = 378 GFLOP take 0.2 ms at 1900 TF/s, while W
+    # (1.476 GB) plus the 32 gathered rows per position take 0.22 ms at 6800 GB/s: bound by W
+    r = bench.self_cond_topk_roofline(262144, 2816, 256, 32, 0.5e-3, PEAKS)
+    want = 262144 * 2816 * 2 + 256 * 2816 * 6 + 256 * 32 * 2816 * 2
+    assert r["bound"] == "hbm" and r["algorithmic_bytes_per_call"] == want
+    assert r["frac"] == pytest.approx(want / 0.5e-3 / 6800e9)
+    # K above V keeps V rows
+    assert bench.self_cond_topk_roofline(200, 64, 16, 256, 1e-5, PEAKS)["algorithmic_bytes_per_call"] == \
+        200 * 64 * 2 + 16 * 64 * 6 + 16 * 200 * 64 * 2
+    # sixteen canvases: 6.05 PFLOP take 3.2 ms, 2.28 GB 0.34 ms: the contraction bounds it
+    r = bench.self_cond_topk_roofline(262144, 2816, 4096, 32, 4e-3, PEAKS)
+    assert r["bound"] == "tensor" and r["achieved"] == pytest.approx(2 * 4096 * 262144 * 2816 / 4e-3 / 1e12)
+
+
 def test_kernel_digest_ignores_comments_but_not_code():
     src = 'int a = 1;  // a note\n/* a block\n   note */\nconst char* s = "x // y /* z */";\n\n  b += 2;\n'
     assert bench.strip_comments(src) == 'int a = 1;\nconst char* s = "x // y /* z */";\n  b += 2;'

@@ -75,6 +75,7 @@ _SIGS = {
     "dg_denoise_step_partial": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "dg_denoise_step_finish": (ctypes.c_int, [ctypes.c_void_p]),
     "dg_self_condition": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "dg_self_condition_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     "dg_partial_records": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
                                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
@@ -268,6 +269,12 @@ class Sampler:
         active at the last tick, into ``out`` (fp32 [B, L, d] on the device)."""
         assert out.dtype.itemsize == 4 and out.is_contiguous() and out.numel() == self.B * self.L * self.d
         _check(lib.dg_self_condition(self.handle, ctypes.c_void_p(out.data_ptr())), self.handle)
+
+    def self_condition_topk(self, out, top_k=32):
+        """dg_self_condition_topk: the same input restricted to each position's ``top_k`` most probable
+        tokens, renormalised, into ``out`` (fp32 [B, L, d] on the device)."""
+        assert out.dtype.itemsize == 4 and out.is_contiguous() and out.numel() == self.B * self.L * self.d
+        _check(lib.dg_self_condition_topk(self.handle, int(top_k), ctypes.c_void_p(out.data_ptr())), self.handle)
 
     def step_partial(self, resid):
         """dg_denoise_step_partial: RMSNorm and the LM head over this rank's vocabulary chunks."""

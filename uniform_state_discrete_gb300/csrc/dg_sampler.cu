@@ -15,6 +15,12 @@
 
 #include "dg_internal.cuh"
 
+namespace dg {
+// defined with the other self-conditioning kernels (dg_selfcond.cu)
+cudaError_t launch_selfcond_topk(const Dev& dv, bool pair, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
+                                 const void* w, int top_k, float* out, int num_sms, cudaStream_t st);
+}  // namespace dg
+
 struct dg_sampler {
   dg_config cfg;
   std::vector<uint64_t> seeds;
@@ -22,6 +28,7 @@ struct dg_sampler {
   dg::Dev dv;
   CUtensorMap tmA, tmB;
   CUtensorMap tmP, tmWT;  // self-conditioning: P, and W^T in boxes of the LM head's B rows
+  const void* w_vocab = nullptr;  // the borrowed W rows (the top-K self-conditioning variant reads them directly)
   bool pair;  // LM head on CTA pairs (tcgen05 cta_group::2), chosen when a tick can hold >= 256 rows
   bool split = false;            // the vocabulary is split across ranks (dg_denoise_step_partial / _finish)
   bool partial_pending = false;  // a partial tick waits for its finishing step
@@ -369,6 +376,7 @@ dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const flo
   dg_sampler* s = new (std::nothrow) dg_sampler();
   if (!s) return set_err(g_create_err, "out of host memory"), DG_ERR_ARG;
   s->cfg = *cfg;
+  s->w_vocab = w_vocab;
   const int B = cfg->n_canvases;
   s->seeds.resize(B);
   s->admit.resize(B);
@@ -579,6 +587,20 @@ dg_status dg_self_condition(dg_sampler* s, float* out) {
   DG_CUDA(s->err,
           dg::launch_selfcond(s->dv, s->pair, &s->tmA, &s->tmB, &s->tmP, &s->tmWT, out, s->num_sms, s->stream),
           "launch self-conditioning");
+  return DG_OK;
+}
+
+dg_status dg_self_condition_topk(dg_sampler* s, int32_t top_k, float* out) {
+  if (!s) return DG_ERR_ARG;
+  if (!out) return set_err(s->err, "out is NULL"), DG_ERR_ARG;
+  if (top_k < 1 || top_k > DG_SC_TOPK_MAX)
+    return set_err(s->err, "top_k must be in [1, %d] (got %d)", DG_SC_TOPK_MAX, top_k), DG_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(out) % 16) return set_err(s->err, "out must be 16-byte aligned"), DG_ERR_ALIGN;
+  if (!s->dv.sc_probs) return set_err(s->err, "the sampler was created without self_cond"), DG_ERR_STATE;
+  if (s->partial_pending) return set_err(s->err, "a partial tick is not finished"), DG_ERR_STATE;
+  DG_CUDA(s->err,
+          dg::launch_selfcond_topk(s->dv, s->pair, &s->tmA, &s->tmB, s->w_vocab, top_k, out, s->num_sms, s->stream),
+          "launch top-K self-conditioning");
   return DG_OK;
 }
 

@@ -512,6 +512,222 @@ __global__ void __launch_bounds__(256) k_selfcond_reduce(const Dev dv, float* __
   }
 }
 
+// ------------------------------------------------------------- top-K variant
+// e[p, :] = sum over the K most probable tokens v of position p of q_v W[v, :],
+// q the tick's softmax restricted to those K tokens and renormalised.
+// TensorSharp's DiffusionGemma doc lists this cutoff of the self-conditioning
+// input (experimental, K = 32 by default); the renormalisation keeps the one
+// convex combination of embedding rows per position that the Annotated page's
+// decode mode describes.  Tokens rank by z / T, equal values by the lower
+// index.  One CTA per position, after k_selfcond<kProbs> has written the
+// position's row of P in bf16 (P >= 0, so a bf16 bit pattern orders like its
+// value, and the rounding keeps order):
+//   1. each thread's largest P over its entries; the K-th largest of these
+//      maxima, s, is a lower bound of the K-th largest P (K threads each hold
+//      an entry >= s), so every entry of the top K has P >= s;
+//   2. the entries with P >= s (and P > 0) are the candidates -- about K of
+//      them for any smooth distribution;
+//   3. each candidate's logit again in fp32 (one warp per candidate: h . W[v],
+//      the softcap, the row's temperature factor), and the K best by
+//      (z desc, v asc), which ranks them;
+//   4. q = 2^(u - u_max) / (sum over the K), e = sum_j q_j W[v_j, :] in rank
+//      order (a fixed order: the result does not depend on the schedule).
+// Entries whose P rounds to zero (p < 2^-126) are never kept: their weights
+// would be below 2^-108 of the largest.  When more than kTopKCand entries are
+// candidates (a plateau of equal probabilities at the top, as with equal
+// logits), the row is taken in windows of kTopKWin entries and each window's
+// candidates are merged into the running K best: slower, the same result.
+constexpr int kTopKThreads = 256;
+constexpr int kTopKWarps = kTopKThreads / 32;
+constexpr int kTopKCand = 2048;
+constexpr int kTopKWin = kTopKThreads * 8;  // one 16-byte group of P per thread
+static_assert(kTopKWin <= kTopKCand, "a window's candidates fit the candidate list");
+
+// The 16-bit keys of entries [8 i, 8 i + 8) of a row of P, -1 past V.
+__device__ __forceinline__ void p_keys8(const uint16_t* __restrict__ prow, int i, int V, int (&key)[8]) {
+  const uint4 q = __ldcg(reinterpret_cast<const uint4*>(prow) + i);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int v = 8 * i + j;
+    key[j] = v < V ? (int)((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu) : -1;
+  }
+}
+
+// (u, v) ranks before (u2, v2): larger logit first, equal logits by the lower index.
+__device__ __forceinline__ bool topk_before(float u, int v, float u2, int v2) { return u > u2 || (u == u2 && v < v2); }
+
+// u = z' log2(e) for each of cand[i0, i1): one warp per candidate, fp32 h . W[v] accumulated in
+// a fixed order, then the softcap and the row's factor log2(e) / T (as the tick forms them).
+__device__ __forceinline__ void topk_logits(const Dev& dv, const uint16_t* __restrict__ W,
+                                            const uint16_t* __restrict__ hrow, float scale, const int* cand_v,
+                                            float* cand_u, int i0, int i1) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d8 = dv.d >> 3;
+  for (int i = i0 + warp; i < i1; i += kTopKWarps) {
+    const int v = cand_v[i];
+    const uint4* wr = reinterpret_cast<const uint4*>(W + (size_t)v * dv.d);
+    const uint4* hr = reinterpret_cast<const uint4*>(hrow);
+    float acc = 0.f;
+    for (int k = lane; k < d8; k += 32) {
+      const uint4 a = __ldg(hr + k), b = __ldg(wr + k);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc = fmaf(__uint_as_float(aw[j] << 16), __uint_as_float(bw[j] << 16), acc);
+        acc = fmaf(__uint_as_float(aw[j] & 0xFFFF0000u), __uint_as_float(bw[j] & 0xFFFF0000u), acc);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (lane == 0) {
+      float z = acc;
+      if (dv.softcap > 0.f) z = dv.softcap * tanhf(z * dv.inv_softcap);
+      const float u = z * scale;
+      cand_u[i] = u == u ? u : -INFINITY;  // a non-finite logit ranks last
+    }
+  }
+}
+
+// Keeps the best min(K, n) of cand[0, n) in rank order at cand[0, ...); returns how many.
+__device__ __forceinline__ int topk_select(int* cand_v, float* cand_u, int n, int K, int* sel_v, float* sel_u) {
+  for (int i = threadIdx.x; i < n; i += kTopKThreads) {
+    const float u = cand_u[i];
+    const int v = cand_v[i];
+    int r = 0;
+    for (int j = 0; j < n && r < K; ++j) r += topk_before(cand_u[j], cand_v[j], u, v) ? 1 : 0;
+    if (r < K) {
+      sel_v[r] = v;
+      sel_u[r] = u;
+    }
+  }
+  __syncthreads();
+  const int m = n < K ? n : K;
+  for (int i = threadIdx.x; i < m; i += kTopKThreads) {
+    cand_v[i] = sel_v[i];
+    cand_u[i] = sel_u[i];
+  }
+  __syncthreads();
+  return m;
+}
+
+__global__ void __launch_bounds__(kTopKThreads)
+    k_selfcond_topk(const Dev dv, const uint16_t* __restrict__ W, int top_k, float* __restrict__ out) {
+  __shared__ int tmax[kTopKThreads];
+  __shared__ int cand_v[kTopKCand + DG_SC_TOPK_MAX];
+  __shared__ float cand_u[kTopKCand + DG_SC_TOPK_MAX];
+  __shared__ int sel_v[DG_SC_TOPK_MAX];
+  __shared__ float sel_u[DG_SC_TOPK_MAX];
+  __shared__ int s_thresh, s_count;
+  __shared__ float s_sum;
+
+  const int row = blockIdx.x;
+  const int n_rows = (int)__ldcg(dv.sc_rows);
+  if (row >= n_rows) return;
+  const int tid = threadIdx.x;
+  const int V = dv.V, K = top_k < V ? top_k : V;
+  const int n8 = dv.sc_vpad >> 3;
+  const uint16_t* prow = dv.sc_probs + (size_t)row * dv.sc_vpad;
+  const uint16_t* hrow = dv.h + (size_t)row * dv.d;
+  const float scale = __ldcg(dv.row_scale + row);
+
+  // 1. this thread's largest key; s = the K-th largest of the threads' maxima (ties by thread)
+  int mx = -1;
+#pragma unroll 4
+  for (int i = tid; i < n8; i += kTopKThreads) {
+    int key[8];
+    p_keys8(prow, i, V, key);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mx = max(mx, key[j]);
+  }
+  tmax[tid] = mx;
+  if (tid == 0) s_count = 0;
+  __syncthreads();
+  {
+    int r = 0;
+    for (int j = 0; j < kTopKThreads; ++j) r += (tmax[j] > mx || (tmax[j] == mx && j < tid)) ? 1 : 0;
+    if (r == K - 1) s_thresh = mx > 1 ? mx : 1;  // entries whose P rounds to zero are never kept
+  }
+  __syncthreads();
+  const int s = s_thresh;
+
+  // 2. the candidates: entries with key >= s
+#pragma unroll 4
+  for (int i = tid; i < n8; i += kTopKThreads) {
+    int key[8];
+    p_keys8(prow, i, V, key);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (key[j] >= s) {
+        const int at = atomicAdd(&s_count, 1);
+        if (at < kTopKCand) cand_v[at] = 8 * i + j;
+      }
+  }
+  __syncthreads();
+  const int n_cand = s_count;
+
+  // 3. exact logits of the candidates and the K best
+  int n_keep;
+  if (n_cand <= kTopKCand) {
+    topk_logits(dv, W, hrow, scale, cand_v, cand_u, 0, n_cand);
+    __syncthreads();
+    n_keep = topk_select(cand_v, cand_u, n_cand, K, sel_v, sel_u);
+  } else {
+    // a plateau at the top: windows of kTopKWin entries in index order, each window's
+    // candidates merged into the running K best (held at cand[0, n_keep))
+    n_keep = 0;
+    for (int w0 = 0; w0 < n8; w0 += kTopKThreads) {
+      __syncthreads();
+      if (tid == 0) s_count = 0;
+      __syncthreads();
+      const int i = w0 + tid;
+      if (i < n8) {
+        int key[8];
+        p_keys8(prow, i, V, key);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (key[j] >= s) cand_v[n_keep + atomicAdd(&s_count, 1)] = 8 * i + j;
+      }
+      __syncthreads();
+      const int n_new = s_count;
+      if (n_new == 0) continue;
+      topk_logits(dv, W, hrow, scale, cand_v, cand_u, n_keep, n_keep + n_new);
+      __syncthreads();
+      n_keep = topk_select(cand_v, cand_u, n_keep + n_new, K, sel_v, sel_u);
+    }
+  }
+
+  // 4. the weights, summed in rank order, and the weighted rows of W
+  if (tid == 0) {
+    float S = 0.f;
+    for (int j = 0; j < n_keep; ++j) S += exp2f(cand_u[j] - cand_u[0]);
+    s_sum = S;
+  }
+  __syncthreads();
+  for (int j = tid; j < n_keep; j += kTopKThreads) sel_u[j] = exp2f(cand_u[j] - cand_u[0]) / s_sum;
+  __syncthreads();
+  const int a = row / dv.L, p = row - a * dv.L;
+  const int c = __ldcg(dv.row_canvas + a);
+  if (!DG_IN_BOUNDS(dv.plan, c >= 0 && c < dv.B && row < dv.rows_cap, 10, c)) return;
+  float* orow = out + ((size_t)c * dv.L + p) * dv.d;
+  for (int k8 = tid; k8 < (dv.d >> 3); k8 += kTopKThreads) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < n_keep; ++j) {
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(W + (size_t)cand_v[j] * dv.d) + k8);
+      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+      const float q = sel_u[j];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        acc[2 * t] = fmaf(q, __uint_as_float(bw[t] << 16), acc[2 * t]);
+        acc[2 * t + 1] = fmaf(q, __uint_as_float(bw[t] & 0xFFFF0000u), acc[2 * t + 1]);
+      }
+    }
+    float4* o = reinterpret_cast<float4*>(orow + 8 * k8);
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
 // W [V, d] -> W^T [d, V_pad], zero past V, through 32 x 32 tiles in shared memory.
 __global__ void __launch_bounds__(256) k_transpose_w(const uint16_t* __restrict__ W, uint16_t* __restrict__ WT, int V,
                                                      int d, int v_pad) {
@@ -552,6 +768,26 @@ cudaError_t launch_pair(int units, int num_sms, const CUtensorMap* tmA, const CU
   return cudaLaunchKernelEx(&cfg, k_selfcond_pair<kMode, kCap>, *tmA, *tmB, dv);
 }
 
+// The LM head again, its epilogue writing P in bf16 (the first kernel of either variant).
+cudaError_t launch_probs(const Dev& dv, bool pair, const CUtensorMap* tm_h, const CUtensorMap* tm_w, int num_sms,
+                         cudaStream_t st) {
+  const bool cap = dv.softcap > 0.f;
+  if (pair) {
+    // 256-row tiles on SM pairs; the maps' B boxes are 128 rows (each CTA's half of a tile)
+    const int max_mt = (dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM);
+    return cap ? launch_pair<kProbs, true>(max_mt * dv.n_chunks, num_sms, tm_h, tm_w, dv, st)
+               : launch_pair<kProbs, false>(max_mt * dv.n_chunks, num_sms, tm_h, tm_w, dv, st);
+  }
+  const int max_mt = (dv.max_active * dv.L + kBM - 1) / kBM;
+  int g1 = max_mt * dv.n_chunks;
+  g1 = g1 < num_sms ? g1 : num_sms;
+  if (cap)
+    k_selfcond<kProbs, true><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
+  else
+    k_selfcond<kProbs, false><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t selfcond_configure() {
@@ -574,27 +810,16 @@ cudaError_t launch_transpose_w(const void* w, uint16_t* wt, int V, int d, int v_
 cudaError_t launch_selfcond(const Dev& dv, bool pair, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
                             const CUtensorMap* tm_p, const CUtensorMap* tm_wt, float* out, int num_sms, cudaStream_t st) {
   const int n_dt = (dv.d + kBN - 1) / kBN;
-  const bool cap = dv.softcap > 0.f;
-  cudaError_t e;
+  cudaError_t e = launch_probs(dv, pair, tm_h, tm_w, num_sms, st);
+  if (e != cudaSuccess) return e;
   if (pair) {
-    // 256-row tiles on SM pairs; the maps' B boxes are 128 rows (each CTA's half of a tile)
     const int max_mt = (dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM);
-    e = cap ? launch_pair<kProbs, true>(max_mt * dv.n_chunks, num_sms, tm_h, tm_w, dv, st)
-            : launch_pair<kProbs, false>(max_mt * dv.n_chunks, num_sms, tm_h, tm_w, dv, st);
-    if (e != cudaSuccess) return e;
     e = launch_pair<kGemm, false>(max_mt * n_dt * dv.sc_kc, num_sms, tm_p, tm_wt, dv, st);
     if (e != cudaSuccess) return e;
   } else {
     const int max_mt = (dv.max_active * dv.L + kBM - 1) / kBM;
-    int g1 = max_mt * dv.n_chunks, g2 = max_mt * n_dt * dv.sc_kc;
-    g1 = g1 < num_sms ? g1 : num_sms;
+    int g2 = max_mt * n_dt * dv.sc_kc;
     g2 = g2 < num_sms ? g2 : num_sms;
-    if (cap)
-      k_selfcond<kProbs, true><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
-    else
-      k_selfcond<kProbs, false><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     k_selfcond<kGemm, false><<<g2, kThreadsLM, kSmemBytesSc, st>>>(*tm_p, *tm_wt, dv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -603,6 +828,15 @@ cudaError_t launch_selfcond(const Dev& dv, bool pair, const CUtensorMap* tm_h, c
   long long blocks = (work + 255) / 256;
   if (blocks > 8 * num_sms) blocks = 8 * num_sms;
   k_selfcond_reduce<<<(int)(blocks > 0 ? blocks : 1), 256, 0, st>>>(dv, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selfcond_topk(const Dev& dv, bool pair, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
+                                 const void* w, int top_k, float* out, int num_sms, cudaStream_t st) {
+  cudaError_t e = launch_probs(dv, pair, tm_h, tm_w, num_sms, st);
+  if (e != cudaSuccess) return e;
+  const int rows = dv.max_active * dv.L;  // CTAs past the tick's rows return at once
+  k_selfcond_topk<<<rows > 0 ? rows : 1, kTopKThreads, 0, st>>>(dv, static_cast<const uint16_t*>(w), top_k, out);
   return cudaGetLastError();
 }
 
