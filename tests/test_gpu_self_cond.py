@@ -84,6 +84,9 @@ def test_self_condition_needs_the_option():
 # 2^-12 a_k + 1e-7 of the oracle's, a_k = sum_j q_j |W_jk| over the kept tokens -- sixteen times
 # tighter than the dense input's bf16 bound.  Where the oracle's K-th and (K+1)-th largest z / T
 # differ by less than 1e-4 the kept set is a near-tie: such positions are counted, not compared.
+# K at most the number of 256-wide vocabulary chunks (V / 256, at most 74) takes the path where the
+# LM head lists the candidates; a larger K, and a row with too many candidates (the plateau), the
+# path that ranks them from the bf16 probabilities: the cases cover both.
 TOPK_GAP = 1e-4
 
 
@@ -140,10 +143,10 @@ def _check_topk(case, ticks, ks, resid_fn=None, expect=None):
     pytest.param(Case(vocab=1000, hidden=200, canvas_len=37, n_canvases=3, steps=5, seeds=(5, 6, 7), admit=(0, 1, 1),
                       gen_blocks=2), 3, (32, 100), id="ragged-staggered"),
     pytest.param(Case(vocab=200, hidden=64, canvas_len=16, steps=4), 1, (256,), id="k-above-vocab"),
-    pytest.param(Case(vocab=4096, hidden=256, canvas_len=256, n_canvases=2, steps=4, seeds=(3, 4)), 1, (32,),
+    pytest.param(Case(vocab=4096, hidden=256, canvas_len=256, n_canvases=2, steps=4, seeds=(3, 4)), 1, (8, 32),
                  id="pair-256-rows"),
     pytest.param(Case(vocab=2048, hidden=128, canvas_len=32, steps=6, softcap=2.0, sigma_w=0.2, w_seed=4,
-                      t_max=1.5, t_min=0.1), 2, (32,), id="softcap"),
+                      t_max=1.5, t_min=0.1), 2, (4, 32), id="softcap"),
     pytest.param(Case(vocab=32768, hidden=1024, canvas_len=256, steps=4, sigma=0.1, t_max=0.1, t_min=0.05), 1, (32,),
                  id="peaked-rows"),
     pytest.param(Case(vocab=262144, hidden=2816, canvas_len=256, steps=48), 1, (32,), id="model-scale"),

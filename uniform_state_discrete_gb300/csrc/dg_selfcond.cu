@@ -34,7 +34,30 @@
 namespace dg {
 namespace {
 
-enum : int { kProbs = 0, kGemm = 1 };
+// kProbs: the LM head again, writing P.  kCands: the same, also listing each row's top-K
+// candidates with their logits (the top-K variant, below).  kGemm: P W^T.
+enum : int { kProbs = 0, kGemm = 1, kCands = 2 };
+
+// The top-K variant's candidate lists live in the dense variant's per-chunk shares (which it does
+// not use), one region of sc_kc * d floats per row: a 16-byte header {count, bound, dense, -} and
+// then (token, u) pairs.  `bound` is the row's lower bound of the K-th largest u = z log2(e)/T;
+// `dense` marks a row whose bound is not known (K above the number of vocabulary chunks).
+constexpr int kTopKCand = 2048;  // candidates a row can list, at most
+struct CandHeader {
+  uint32_t count;
+  float bound;
+  uint32_t dense;
+  uint32_t pad;
+};
+static_assert(sizeof(CandHeader) == 16, "candidate header is 16 bytes");
+__device__ __forceinline__ CandHeader* cand_header(const Dev& dv, int row) {
+  return reinterpret_cast<CandHeader*>(dv.sc_part + (size_t)row * dv.sc_kc * dv.d);
+}
+__device__ __forceinline__ int2* cand_list(const Dev& dv, int row) { return reinterpret_cast<int2*>(cand_header(dv, row) + 1); }
+__device__ __forceinline__ uint32_t cand_capacity(const Dev& dv) {
+  const size_t pairs = ((size_t)dv.sc_kc * dv.d * 4 - sizeof(CandHeader)) / 8;
+  return (uint32_t)(pairs < (size_t)kTopKCand ? pairs : (size_t)kTopKCand);
+}
 
 // The units of one launch: kProbs (row tile, vocabulary chunk) with the chunk's
 // vocabulary tiles as N tiles and the hidden dimension as K; kGemm (row tile,
@@ -43,12 +66,12 @@ enum : int { kProbs = 0, kGemm = 1 };
 struct ScUnits {
   int n_mt, n_dt, KB;
   __device__ __forceinline__ int units(const Dev& dv, int mode) const {
-    return mode == kProbs ? n_mt * dv.n_chunks : n_mt * n_dt * dv.sc_kc;
+    return mode != kGemm ? n_mt * dv.n_chunks : n_mt * n_dt * dv.sc_kc;
   }
   // first/last N tile and first/last K block of unit u, and its row tile
   __device__ __forceinline__ void at(const Dev& dv, int mode, int u, int& mt, int& t0, int& t1, int& kb0,
                                      int& kb1) const {
-    if (mode == kProbs) {
+    if (mode != kGemm) {
       const int chunk = u / n_mt;
       mt = u - chunk * n_mt;
       t0 = chunk * dv.tiles_per_chunk;
@@ -68,12 +91,13 @@ struct ScUnits {
 };
 
 // An epilogue's 16 accumulator columns [c0, c0 + 16) of `row`: kProbs writes P = 2^(u - log2 Z),
-// u = z log2(e)/T, rounded to bf16 (zero past V); kGemm writes the vocabulary chunk's share of e
-// for hidden columns [c0, c0 + 16).
+// u = z log2(e)/T, rounded to bf16 (zero past V); kCands also lists the columns whose u reaches
+// the row's bound `cand` (with u as the tick forms its maxima: the capped logit times log2(e)/T);
+// kGemm writes the vocabulary chunk's share of e for hidden columns [c0, c0 + 16).
 template <int kMode, bool kCap>
 __device__ __forceinline__ void store_cols(const Dev& dv, const float (&acc)[16], int row, int c0, int kb0,
-                                           float scale, float l2z) {
-  if (kMode == kProbs) {
+                                           float scale, float l2z, float cand) {
+  if (kMode != kGemm) {
     uint32_t pk[8];
 #pragma unroll
     for (int j = 0; j < 16; j += 2) {
@@ -81,6 +105,22 @@ __device__ __forceinline__ void store_cols(const Dev& dv, const float (&acc)[16]
       if (kCap) {
         z0 = dv.softcap * tanhf(z0 * dv.inv_softcap);
         z1 = dv.softcap * tanhf(z1 * dv.inv_softcap);
+      }
+      if (kMode == kCands) {
+        const float u0 = z0 * scale, u1 = z1 * scale;
+        const bool t0 = c0 + j < dv.V && u0 >= cand, t1 = c0 + j + 1 < dv.V && u1 >= cand;
+        if (t0 || t1) {
+          CandHeader* hd = cand_header(dv, row);
+          const uint32_t cap = cand_capacity(dv);
+          if (t0) {
+            const uint32_t at = atomicAdd(&hd->count, 1u);
+            if (at < cap) cand_list(dv, row)[at] = make_int2(c0 + j, __float_as_int(u0));
+          }
+          if (t1) {
+            const uint32_t at = atomicAdd(&hd->count, 1u);
+            if (at < cap) cand_list(dv, row)[at] = make_int2(c0 + j + 1, __float_as_int(u1));
+          }
+        }
       }
       const float p0 = c0 + j < dv.V ? ex2_approx(fmaf(z0, scale, -l2z)) : 0.f;
       const float p1 = c0 + j + 1 < dv.V ? ex2_approx(fmaf(z1, scale, -l2z)) : 0.f;
@@ -239,8 +279,9 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       su.at(dv, kMode, u, mt, t0, t1, kb0, kb1);
       const int row = mt * kBM + q * 32 + lane;
       const bool valid = row < n_rows;
-      const float scale = valid && kMode == kProbs ? __ldcg(dv.row_scale + row) : 0.f;
-      const float l2z = valid && kMode == kProbs ? __ldcg(dv.row_log2z + row) : 0.f;
+      const float scale = valid && kMode != kGemm ? __ldcg(dv.row_scale + row) : 0.f;
+      const float l2z = valid && kMode != kGemm ? __ldcg(dv.row_log2z + row) : 0.f;
+      const float cand = valid && kMode == kCands ? __ldcg(&cand_header(dv, row)->bound) : INFINITY;
       for (int t = t0; t < t1; ++t, ++tcount) {
         if (aborted) continue;
         const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
@@ -265,7 +306,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             if (lane == 0) mbar_arrive(&tempty[ab]);
           }
           if (!valid) continue;
-          store_cols<kMode, kCap>(dv, acc, row, t * kBN + cg * kColsPerWarp + cc * 16, kb0, scale, l2z);
+          store_cols<kMode, kCap>(dv, acc, row, t * kBN + cg * kColsPerWarp + cc * 16, kb0, scale, l2z, cand);
         }
       }
     }
@@ -444,8 +485,9 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
       su.at(dv, kMode, u, mt, t0, t1, kb0, kb1);
       const int row = mt * 2 * kBM + (int)rank * kBM + q * 32 + lane;
       const bool valid = row < n_rows;
-      const float scale = valid && kMode == kProbs ? __ldcg(dv.row_scale + row) : 0.f;
-      const float l2z = valid && kMode == kProbs ? __ldcg(dv.row_log2z + row) : 0.f;
+      const float scale = valid && kMode != kGemm ? __ldcg(dv.row_scale + row) : 0.f;
+      const float l2z = valid && kMode != kGemm ? __ldcg(dv.row_log2z + row) : 0.f;
+      const float cand = valid && kMode == kCands ? __ldcg(&cand_header(dv, row)->bound) : INFINITY;
       for (int t = t0; t < t1; ++t, ++tcount) {
         if (aborted) continue;
         const uint32_t ab = tcount & 1u, aph = (tcount >> 1) & 1u;
@@ -473,7 +515,7 @@ __global__ void __launch_bounds__(kThreadsLM, 1)
             if (lane == 0) mbar_arrive_cluster(tempty_leader[ab]);
           }
           if (!valid) continue;
-          store_cols<kMode, kCap>(dv, acc, row, t * kBN + cg * kColsPerWarp + cc * 16, kb0, scale, l2z);
+          store_cols<kMode, kCap>(dv, acc, row, t * kBN + cg * kColsPerWarp + cc * 16, kb0, scale, l2z, cand);
         }
       }
     }
@@ -519,9 +561,21 @@ __global__ void __launch_bounds__(256) k_selfcond_reduce(const Dev dv, float* __
 // input (experimental, K = 32 by default); the renormalisation keeps the one
 // convex combination of embedding rows per position that the Annotated page's
 // decode mode describes.  Tokens rank by z / T, equal values by the lower
-// index.  One CTA per position, after k_selfcond<kProbs> has written the
-// position's row of P in bf16 (P >= 0, so a bf16 bit pattern orders like its
-// value, and the rounding keeps order):
+// index.
+//
+// The tick's partial records hold each vocabulary chunk's largest u = z
+// log2(e)/T of every row: when K is at most the number of chunks, the K-th
+// largest of those maxima is a lower bound of the K-th largest u (K chunks
+// each hold an entry at least as large).  k_topk_prep writes that bound (less
+// a margin) into each row's candidate header, k_selfcond<kCands> -- the LM
+// head again -- lists every entry that reaches it with its fp32 u from the
+// accumulator, and k_selfcond_topk ranks the row's list (about K entries for a
+// smooth distribution).  A row with more candidates than its list holds, or K
+// above the number of chunks, takes the path below instead, from the bf16 P
+// that the same launch wrote.
+//
+// That path takes one CTA per position (P >= 0, so a bf16 bit pattern orders
+// like its value, and the rounding keeps order):
 //   1. each thread's largest P over its entries; the K-th largest of these
 //      maxima, s, is a lower bound of the K-th largest P (K threads each hold
 //      an entry >= s), so every entry of the top K has P >= s;
@@ -539,7 +593,6 @@ __global__ void __launch_bounds__(256) k_selfcond_reduce(const Dev dv, float* __
 // candidates are merged into the running K best: slower, the same result.
 constexpr int kTopKThreads = 256;
 constexpr int kTopKWarps = kTopKThreads / 32;
-constexpr int kTopKCand = 2048;
 constexpr int kTopKWin = kTopKThreads * 8;  // one 16-byte group of P per thread
 static_assert(kTopKWin <= kTopKCand, "a window's candidates fit the candidate list");
 
@@ -611,25 +664,49 @@ __device__ __forceinline__ int topk_select(int* cand_v, float* cand_u, int n, in
   return m;
 }
 
-__global__ void __launch_bounds__(kTopKThreads)
-    k_selfcond_topk(const Dev dv, const uint16_t* __restrict__ W, int top_k, float* __restrict__ out) {
-  __shared__ int tmax[kTopKThreads];
-  __shared__ int cand_v[kTopKCand + DG_SC_TOPK_MAX];
-  __shared__ float cand_u[kTopKCand + DG_SC_TOPK_MAX];
-  __shared__ int sel_v[DG_SC_TOPK_MAX];
-  __shared__ float sel_u[DG_SC_TOPK_MAX];
-  __shared__ int s_thresh, s_count;
-  __shared__ float s_sum;
-
-  const int row = blockIdx.x;
+// One warp per row: the row's bound -- the K-th largest of its chunk maxima (ties by chunk), less
+// a margin of 2^-12 (|bound| + 1), and no lower than log2 Z - 126, below which P rounds to zero --
+// and an empty candidate list.
+__global__ void __launch_bounds__(256) k_topk_prep(const Dev dv, int top_k) {
+  __shared__ float m_s[8][kChunkTarget];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
   const int n_rows = (int)__ldcg(dv.sc_rows);
   if (row >= n_rows) return;
+  const int nc = dv.n_chunks, K = top_k < dv.V ? top_k : dv.V;
+  CandHeader* hd = cand_header(dv, row);
+  if (K > nc || nc > kChunkTarget) {
+    if (lane == 0) *hd = CandHeader{0u, INFINITY, 1u, 0u};
+    return;
+  }
+  for (int c = lane; c < nc; c += 32) {
+    const float m = __ldcg(&dv.part[(size_t)row * dv.n_sub + c].m);
+    m_s[warp][c] = m == m ? m : -INFINITY;
+  }
+  __syncwarp();
+  for (int c = lane; c < nc; c += 32) {
+    const float m = m_s[warp][c];
+    int r = 0;
+    for (int j = 0; j < nc; ++j) r += (m_s[warp][j] > m || (m_s[warp][j] == m && j < c)) ? 1 : 0;
+    if (r == K - 1) {
+      const float floor_u = __ldcg(dv.row_log2z + row) - 126.f;
+      const float b = m - 0x1p-12f * (fabsf(m) + 1.f);
+      *hd = CandHeader{0u, b > floor_u ? b : floor_u, 0u, 0u};
+    }
+  }
+}
+
+// The K best of a row from its bf16 probabilities (the path described above); they are left in
+// rank order at cand[0, n_keep).
+__device__ __noinline__ int topk_from_probs(const Dev& dv, const uint16_t* __restrict__ W,
+                                            const uint16_t* __restrict__ prow, const uint16_t* __restrict__ hrow,
+                                            float scale, int K, int* tmax, int* cand_v, float* cand_u, int* sel_v,
+                                            float* sel_u, int* s_thresh_p, int* s_count_p) {
+  int& s_thresh = *s_thresh_p;
+  int& s_count = *s_count_p;
   const int tid = threadIdx.x;
-  const int V = dv.V, K = top_k < V ? top_k : V;
+  const int V = dv.V;
   const int n8 = dv.sc_vpad >> 3;
-  const uint16_t* prow = dv.sc_probs + (size_t)row * dv.sc_vpad;
-  const uint16_t* hrow = dv.h + (size_t)row * dv.d;
-  const float scale = __ldcg(dv.row_scale + row);
 
   // 1. this thread's largest key; s = the K-th largest of the threads' maxima (ties by thread)
   int mx = -1;
@@ -697,7 +774,16 @@ __global__ void __launch_bounds__(kTopKThreads)
     }
   }
 
-  // 4. the weights, summed in rank order, and the weighted rows of W
+  return n_keep;
+}
+
+// 4. the weights of the kept cand[0, n_keep) (rank order, largest u first), summed in rank order,
+// and the weighted rows of W, written where the row's canvas keeps its positions.
+__device__ __noinline__ void topk_write(const Dev& dv, const uint16_t* __restrict__ W, int row, int n_keep,
+                                        const int* cand_v, const float* cand_u, float* sel_u, float* s_sum_p,
+                                        float* __restrict__ out) {
+  float& s_sum = *s_sum_p;
+  const int tid = threadIdx.x;
   if (tid == 0) {
     float S = 0.f;
     for (int j = 0; j < n_keep; ++j) S += exp2f(cand_u[j] - cand_u[0]);
@@ -726,6 +812,45 @@ __global__ void __launch_bounds__(kTopKThreads)
     o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
+}
+
+__global__ void __launch_bounds__(kTopKThreads)
+    k_selfcond_topk(const Dev dv, const uint16_t* __restrict__ W, int top_k, float* __restrict__ out) {
+  __shared__ int tmax[kTopKThreads];
+  __shared__ int cand_v[kTopKCand + DG_SC_TOPK_MAX];
+  __shared__ float cand_u[kTopKCand + DG_SC_TOPK_MAX];
+  __shared__ int sel_v[DG_SC_TOPK_MAX];
+  __shared__ float sel_u[DG_SC_TOPK_MAX];
+  __shared__ int s_thresh, s_count;
+  __shared__ float s_sum;
+
+  const int row = blockIdx.x;
+  const int n_rows = (int)__ldcg(dv.sc_rows);
+  if (row >= n_rows) return;
+  const int tid = threadIdx.x;
+  const int K = top_k < dv.V ? top_k : dv.V;
+  const uint16_t* prow = dv.sc_probs + (size_t)row * dv.sc_vpad;
+  const uint16_t* hrow = dv.h + (size_t)row * dv.d;
+  const float scale = __ldcg(dv.row_scale + row);
+
+  int n_keep;
+  const uint4 hd = __ldcg(reinterpret_cast<const uint4*>(cand_header(dv, row)));  // {count, bound, dense, -}
+  if (hd.z == 0u && hd.x >= 1u && hd.x <= cand_capacity(dv)) {
+    // the row's candidates as the LM head listed them, with their fp32 u
+    const int2* lst = cand_list(dv, row);
+    const int n = (int)hd.x;
+    for (int i = tid; i < n; i += kTopKThreads) {
+      const int2 e = __ldcg(lst + i);
+      cand_v[i] = e.x;
+      const float u = __int_as_float(e.y);
+      cand_u[i] = u == u ? u : -INFINITY;
+    }
+    __syncthreads();
+    n_keep = topk_select(cand_v, cand_u, n, K, sel_v, sel_u);
+  } else {
+    n_keep = topk_from_probs(dv, W, prow, hrow, scale, K, tmax, cand_v, cand_u, sel_v, sel_u, &s_thresh, &s_count);
+  }
+  topk_write(dv, W, row, n_keep, cand_v, cand_u, sel_u, &s_sum, out);
 }
 
 // W [V, d] -> W^T [d, V_pad], zero past V, through 32 x 32 tiles in shared memory.
@@ -768,23 +893,25 @@ cudaError_t launch_pair(int units, int num_sms, const CUtensorMap* tmA, const CU
   return cudaLaunchKernelEx(&cfg, k_selfcond_pair<kMode, kCap>, *tmA, *tmB, dv);
 }
 
-// The LM head again, its epilogue writing P in bf16 (the first kernel of either variant).
+// The LM head again, its epilogue writing P in bf16 (the first kernel of either variant; kMode
+// kCands also lists the top-K candidates).
+template <int kMode>
 cudaError_t launch_probs(const Dev& dv, bool pair, const CUtensorMap* tm_h, const CUtensorMap* tm_w, int num_sms,
                          cudaStream_t st) {
   const bool cap = dv.softcap > 0.f;
   if (pair) {
     // 256-row tiles on SM pairs; the maps' B boxes are 128 rows (each CTA's half of a tile)
     const int max_mt = (dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM);
-    return cap ? launch_pair<kProbs, true>(max_mt * dv.n_chunks, num_sms, tm_h, tm_w, dv, st)
-               : launch_pair<kProbs, false>(max_mt * dv.n_chunks, num_sms, tm_h, tm_w, dv, st);
+    return cap ? launch_pair<kMode, true>(max_mt * dv.n_chunks, num_sms, tm_h, tm_w, dv, st)
+               : launch_pair<kMode, false>(max_mt * dv.n_chunks, num_sms, tm_h, tm_w, dv, st);
   }
   const int max_mt = (dv.max_active * dv.L + kBM - 1) / kBM;
   int g1 = max_mt * dv.n_chunks;
   g1 = g1 < num_sms ? g1 : num_sms;
   if (cap)
-    k_selfcond<kProbs, true><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
+    k_selfcond<kMode, true><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
   else
-    k_selfcond<kProbs, false><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
+    k_selfcond<kMode, false><<<g1, kThreadsLM, kSmemBytesSc, st>>>(*tm_h, *tm_w, dv);
   return cudaGetLastError();
 }
 
@@ -793,9 +920,10 @@ cudaError_t launch_probs(const Dev& dv, bool pair, const CUtensorMap* tm_h, cons
 cudaError_t selfcond_configure() {
   cudaError_t e = cudaSuccess;
   for (auto k : {k_selfcond<kProbs, false>, k_selfcond<kProbs, true>, k_selfcond<kGemm, false>,
-                 k_selfcond<kGemm, true>})
+                 k_selfcond<kGemm, true>, k_selfcond<kCands, false>, k_selfcond<kCands, true>})
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesSc);
-  for (auto k : {k_selfcond_pair<kProbs, false>, k_selfcond_pair<kProbs, true>, k_selfcond_pair<kGemm, false>})
+  for (auto k : {k_selfcond_pair<kProbs, false>, k_selfcond_pair<kProbs, true>, k_selfcond_pair<kGemm, false>,
+                 k_selfcond_pair<kCands, false>, k_selfcond_pair<kCands, true>})
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesScPair);
   return e;
@@ -810,7 +938,7 @@ cudaError_t launch_transpose_w(const void* w, uint16_t* wt, int V, int d, int v_
 cudaError_t launch_selfcond(const Dev& dv, bool pair, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
                             const CUtensorMap* tm_p, const CUtensorMap* tm_wt, float* out, int num_sms, cudaStream_t st) {
   const int n_dt = (dv.d + kBN - 1) / kBN;
-  cudaError_t e = launch_probs(dv, pair, tm_h, tm_w, num_sms, st);
+  cudaError_t e = launch_probs<kProbs>(dv, pair, tm_h, tm_w, num_sms, st);
   if (e != cudaSuccess) return e;
   if (pair) {
     const int max_mt = (dv.max_active * dv.L + 2 * kBM - 1) / (2 * kBM);
@@ -833,9 +961,12 @@ cudaError_t launch_selfcond(const Dev& dv, bool pair, const CUtensorMap* tm_h, c
 
 cudaError_t launch_selfcond_topk(const Dev& dv, bool pair, const CUtensorMap* tm_h, const CUtensorMap* tm_w,
                                  const void* w, int top_k, float* out, int num_sms, cudaStream_t st) {
-  cudaError_t e = launch_probs(dv, pair, tm_h, tm_w, num_sms, st);
-  if (e != cudaSuccess) return e;
   const int rows = dv.max_active * dv.L;  // CTAs past the tick's rows return at once
+  k_topk_prep<<<(rows + 7) / 8 > 0 ? (rows + 7) / 8 : 1, 256, 0, st>>>(dv, top_k);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_probs<kCands>(dv, pair, tm_h, tm_w, num_sms, st);
+  if (e != cudaSuccess) return e;
   k_selfcond_topk<<<rows > 0 ? rows : 1, kTopKThreads, 0, st>>>(dv, static_cast<const uint16_t*>(w), top_k, out);
   return cudaGetLastError();
 }
