@@ -173,8 +173,9 @@ def self_cond_topk_roofline(V: int, d: int, P: float, K: int, seconds: float, pe
     t_tc = alg_flops / (peaks["bf16_tflops"] * 1e12)
     r = {"ms_mean": seconds * 1e3, "positions_per_call": P, "top_k": K, "algorithmic_bytes_per_call": alg_bytes,
          "algorithmic_flops_per_call": alg_flops,
-         "kernels": "k_selfcond (the LM head again, writing P = softmax(z/T) in bf16), k_selfcond_topk (one CTA "
-                    "per position: candidates from P, their logits again in fp32, the K best, the weighted rows)",
+         "kernels": "k_topk_prep (each row's bound from the tick's chunk maxima), k_selfcond (the LM head again, "
+                    "writing P = softmax(z/T) in bf16 and listing each row's candidates with their logits), "
+                    "k_selfcond_topk (one CTA per position: the K best of the list, their weights and rows)",
          "timing": "CUDA events around the call on the sampler stream, after a tick, L2 flushed before it"}
     if t_hbm >= t_tc:
         r.update(bound="hbm", achieved=alg_bytes / seconds / 1e9, peak=peaks["hbm_gbs"], unit="GB/s")
