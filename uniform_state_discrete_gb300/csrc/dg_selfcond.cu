@@ -23,6 +23,11 @@
 //                       chunks kc so the grid fills the GPU;
 //   k_selfcond_reduce   e = sum over kc in order (deterministic), written to
 //                       the caller's [B, L, d] array at each row's canvas.
+// The top-K variant (further down) keeps each position's K most probable
+// tokens only: k_topk_prep bounds each row's K-th largest logit from the
+// tick's chunk maxima, k_selfcond<kCands> is the LM head again listing the
+// entries that reach the bound (and writing P), and k_selfcond_topk ranks a
+// row's list and sums the kept rows of W.
 // Producer (warp 0), MMA issuer (warp 1) and 16 epilogue warps as in the LM
 // head; every wait is bounded (1 s) and latches DG_ERR_TIMEOUT.
 #include <cuda_bf16.h>
