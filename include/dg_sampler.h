@@ -345,6 +345,16 @@ dg_status dg_set_state(dg_sampler* s, const dg_state* host);
  * dg_set_state (which also clears the latch) makes it usable again. */
 dg_status dg_debug_hold_slabs(dg_sampler* s, int on);
 
+/* Test hook for failure detection, process-wide: after `after` more CUDA
+ * calls that the library checks (0: the next one), one is not made and is
+ * reported as failed with cudaErrorLaunchFailure, as the real call would
+ * report a failure -- the entry point returns DG_ERR_CUDA with the call named
+ * in dg_last_error.  The hook then turns itself off; after = -1 turns it off
+ * at once.  Nothing reaches the GPU.  A failure between the kernels of a tick
+ * leaves the sampler's state undefined, as a real one would; dg_set_state
+ * makes it usable again.  DG_ERR_ARG for after < -1. */
+dg_status dg_debug_fail_cuda_call(int32_t after);
+
 /*
  * Race and bounds checks of the debug build (the library compiled with
  * DG_DEBUG_CHECKS; the release build returns DG_ERR_UNSUPPORTED).  In that

@@ -339,6 +339,55 @@ def test_bounded_wait_runs_out_and_sampler_recovers(canvas_len, vocab):
         assert torch.equal(getattr(s, view)(), getattr(fresh, view)())
 
 
+@pytest.mark.parametrize("canvas_len,vocab", [(16, 2048), (256, 4096)])
+def test_failed_cuda_call_is_reported_and_sampler_recovers(canvas_len, vocab):
+    """Failure detection with a fake of the failing call, on the host: the library's next checked CUDA
+    call is not made and reports a failure.  A step whose first launch fails returns DG_ERR_CUDA
+    naming the launch and changes nothing, so retrying it gives a fresh sampler's tick; one that
+    fails between the kernels of a tick is brought back by dg_set_state."""
+    import torch
+    import uniform_state_discrete_gb300 as dg
+    case = Case(vocab=vocab, hidden=128, canvas_len=canvas_len, steps=6, seeds=(4,))
+    W = weights(case)
+    dev = torch.device("cuda:0")
+    w_dev = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    ocfg = case.oracle_cfg()
+    fresh = dg.Sampler(case.gpu_cfg(), w_dev)
+    st0 = fresh.get_state()
+    r = torch.from_numpy(resid_slots(case, ocfg, W, np.array([0]), np.array([0]), np.array([0]),
+                                     st0["tokens"][:1])).to(dev)
+    fresh.step(r)
+    fresh.sync_info()
+    s = dg.Sampler(case.gpu_cfg(), w_dev)
+    try:
+        # the first checked call of the step fails: nothing was launched
+        assert dg.lib.dg_debug_fail_cuda_call(0) == dg.DG_OK
+        with pytest.raises(dg.DGError) as err:
+            s.step(r)
+        assert err.value.status == dg.DG_ERR_CUDA and "cudaErrorLaunchFailure" in str(err.value)
+        assert "launch" in str(err.value)
+        s.step(r)  # the hook turned itself off
+        s.sync_info()
+        for view in ("canvas", "entropy", "sample"):
+            assert torch.equal(getattr(s, view)(), getattr(fresh, view)())
+        # the second checked call fails: the tick is cut between its kernels
+        s.set_state(st0)
+        assert dg.lib.dg_debug_fail_cuda_call(1) == dg.DG_OK
+        with pytest.raises(dg.DGError) as err:
+            s.step(r)
+        assert err.value.status == dg.DG_ERR_CUDA
+        s.set_state(st0)
+        s.step(r)
+        s.sync_info()
+        for view in ("canvas", "entropy", "sample"):
+            assert torch.equal(getattr(s, view)(), getattr(fresh, view)())
+        assert dg.lib.dg_debug_fail_cuda_call(-2) == dg.DG_ERR_ARG
+    finally:
+        dg.lib.dg_debug_fail_cuda_call(-1)
+        s.close()
+        fresh.close()
+
+
 def test_batched_model_scale_sampled_rows():
     """16 canvases x 256 positions at V=2^18, d=2816 (the batched configuration with every canvas
     active: 16 row tiles of the SM-pair LM head per vocabulary chunk), one tick; sampled positions

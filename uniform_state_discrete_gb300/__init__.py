@@ -76,6 +76,7 @@ _SIGS = {
     "dg_denoise_step_finish": (ctypes.c_int, [ctypes.c_void_p]),
     "dg_self_condition": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "dg_self_condition_topk": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
+    "dg_debug_fail_cuda_call": (ctypes.c_int, [ctypes.c_int32]),
     "dg_partial_records": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
                                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),

@@ -9,9 +9,12 @@
 #include <cstdarg>
 #include <cstdio>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <new>
 #include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "dg_internal.cuh"
 
@@ -218,11 +221,33 @@ dg_status cuda_fail(char* buf, cudaError_t e, const char* what) {
   return DG_ERR_CUDA;
 }
 
-#define DG_CUDA(s, call, what)                               \
-  do {                                                       \
-    cudaError_t e_ = (call);                                 \
-    if (e_ != cudaSuccess) return cuda_fail((s), e_, (what)); \
+// dg_debug_fail_cuda_call: how many more checked CUDA calls run before one is
+// replaced by a reported failure (-1: none).
+std::atomic<int> g_fail_after{-1};
+
+// Whether this checked CUDA call is the one to fail (it is then not made).
+bool injected_failure() {
+  int v = g_fail_after.load();
+  while (v >= 0) {
+    if (g_fail_after.compare_exchange_weak(v, v - 1)) return v == 0;
+  }
+  return false;
+}
+
+#define DG_CUDA(s, call, what)                                                          \
+  do {                                                                                  \
+    if (injected_failure()) return cuda_fail((s), cudaErrorLaunchFailure, (what));     \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess) return cuda_fail((s), e_, (what));                           \
   } while (0)
+
+// An NVTX range over one entry point (shown by profilers that collect NVTX; free otherwise).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode(char* why) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -344,6 +369,7 @@ size_t dg_workspace_size(const dg_config* cfg) {
 
 dg_status dg_sampler_create(const dg_config* cfg, const void* w_vocab, const float* norm_w, void* workspace,
                             size_t ws_bytes, dg_stream_t stream, dg_sampler** out) {
+  NvtxRange nvtx_("dg_sampler_create");
   g_create_err[0] = 0;
   if (!out) return set_err(g_create_err, "out is NULL"), DG_ERR_ARG;
   *out = nullptr;
@@ -539,6 +565,7 @@ static dg_status refuse_split(dg_sampler* s) {
 }
 
 dg_status dg_denoise_step_partial(dg_sampler* s, const float* resid) {
+  NvtxRange nvtx_("dg_denoise_step_partial");
   if (!s) return DG_ERR_ARG;
   if (!resid) return set_err(s->err, "resid is NULL"), DG_ERR_ARG;
   if (reinterpret_cast<uintptr_t>(resid) % 16) return set_err(s->err, "resid must be 16-byte aligned"), DG_ERR_ALIGN;
@@ -550,6 +577,7 @@ dg_status dg_denoise_step_partial(dg_sampler* s, const float* resid) {
 }
 
 dg_status dg_denoise_step_finish(dg_sampler* s) {
+  NvtxRange nvtx_("dg_denoise_step_finish");
   if (!s) return DG_ERR_ARG;
   if (!s->partial_pending) return set_err(s->err, "no partial tick to finish"), DG_ERR_STATE;
   s->partial_pending = false;
@@ -579,6 +607,7 @@ dg_status dg_vocab_slice(int32_t vocab, int32_t ranks, int32_t rank, int32_t* v_
 }
 
 dg_status dg_self_condition(dg_sampler* s, float* out) {
+  NvtxRange nvtx_("dg_self_condition");
   if (!s) return DG_ERR_ARG;
   if (!out) return set_err(s->err, "out is NULL"), DG_ERR_ARG;
   if (reinterpret_cast<uintptr_t>(out) % 16) return set_err(s->err, "out must be 16-byte aligned"), DG_ERR_ALIGN;
@@ -591,6 +620,7 @@ dg_status dg_self_condition(dg_sampler* s, float* out) {
 }
 
 dg_status dg_self_condition_topk(dg_sampler* s, int32_t top_k, float* out) {
+  NvtxRange nvtx_("dg_self_condition_topk");
   if (!s) return DG_ERR_ARG;
   if (!out) return set_err(s->err, "out is NULL"), DG_ERR_ARG;
   if (top_k < 1 || top_k > DG_SC_TOPK_MAX)
@@ -605,6 +635,7 @@ dg_status dg_self_condition_topk(dg_sampler* s, int32_t top_k, float* out) {
 }
 
 dg_status dg_denoise_step(dg_sampler* s, const float* resid) {
+  NvtxRange nvtx_("dg_denoise_step");
   if (!s) return DG_ERR_ARG;
   if (s->split) return refuse_split(s);
   if (!resid) return set_err(s->err, "resid is NULL"), DG_ERR_ARG;
@@ -613,6 +644,7 @@ dg_status dg_denoise_step(dg_sampler* s, const float* resid) {
 }
 
 dg_status dg_denoise_step_host(dg_sampler* s, const float* resid_host, int32_t* canvas_host, float* entropy_host) {
+  NvtxRange nvtx_("dg_denoise_step_host");
   if (!s) return DG_ERR_ARG;
   if (s->split) return refuse_split(s);
   if (!resid_host) return set_err(s->err, "resid_host is NULL"), DG_ERR_ARG;
@@ -665,6 +697,7 @@ dg_status dg_sync_info(dg_sampler* s, dg_slot* slots_host) {
 
 dg_status dg_run(dg_sampler* s, dg_resid_fn fn, void* user, float* resid_dev, int32_t* tokens_host,
                  dg_slot* slots_host) {
+  NvtxRange nvtx_("dg_run");
   if (!s || !fn) return DG_ERR_ARG;
   if (s->split) return refuse_split(s);
   float* resid = resid_dev ? resid_dev : s->dv.resid_stage;
@@ -713,6 +746,7 @@ dg_status dg_get_state(dg_sampler* s, dg_state* h) {
 }
 
 dg_status dg_set_state(dg_sampler* s, const dg_state* h) {
+  NvtxRange nvtx_("dg_set_state");
   if (!s || !h || !h->slots || !h->tokens || !h->committed || !h->commit_step || !h->prev_argmax)
     return DG_ERR_ARG;
   if (h->tick < 0) return set_err(s->err, "tick must be >= 0"), DG_ERR_ARG;
@@ -755,6 +789,12 @@ void dg_destroy(dg_sampler* s) {
   if (!s) return;
   cudaStreamSynchronize(s->stream);
   delete s;
+}
+
+dg_status dg_debug_fail_cuda_call(int32_t after) {
+  if (after < -1) return DG_ERR_ARG;
+  g_fail_after.store(after);
+  return DG_OK;
 }
 
 dg_status dg_debug_hold_slabs(dg_sampler* s, int on) {
