@@ -149,7 +149,7 @@ def _check_topk(case, ticks, ks, resid_fn=None, expect=None):
                       t_max=1.5, t_min=0.1), 2, (4, 32), id="softcap"),
     pytest.param(Case(vocab=32768, hidden=1024, canvas_len=256, steps=4, sigma=0.1, t_max=0.1, t_min=0.05), 1, (32,),
                  id="peaked-rows"),
-    pytest.param(Case(vocab=262144, hidden=2816, canvas_len=256, steps=48), 1, (32,), id="model-scale"),
+    pytest.param(Case(vocab=262144, hidden=2816, canvas_len=256, steps=48), 1, (32, 256), id="model-scale"),
 ])
 def test_self_condition_topk_matches_oracle(case, ticks, ks):
     worst, flagged, checked = _check_topk(case, ticks, ks)
