@@ -194,7 +194,9 @@ def all_gather_partials(records, chunk_ranges, rank: int, group=None) -> None:
     """The exchange of a vocabulary-parallel tick across processes (torch.distributed): ``records`` is
     this rank's [rows_cap, n_chunks, 8] record array (a view of the workspace, or any tensor of that
     layout), ``chunk_ranges`` every rank's (chunk_begin, chunk_end).  Each rank's columns are packed,
-    all-gathered and written into every rank's array in place."""
+    all-gathered and written into every rank's array in place.  The collective and the copies run on
+    torch's current stream: call it under ``torch.cuda.stream(sampler.stream)`` (or after synchronizing
+    the sampler's stream) so that they follow the partial tick, and before dg_denoise_step_finish."""
     import torch
     import torch.distributed as dist
     b, e = chunk_ranges[rank]
