@@ -243,6 +243,28 @@ def test_idle_ticks_before_admission_pair_kernel():
     assert np.array_equal(info["steps_used"], o.steps_used)
 
 
+@pytest.mark.parametrize("canvas_len", [16, 256], ids=["single-cta", "pair"])
+def test_maximum_hidden_size(canvas_len):
+    """The largest hidden size the ABI takes (d = 16384): rows longer than the RMSNorm forms keep in
+    registers (they loop over the row), 256 K stages per LM-head tile, on both LM-head kernels."""
+    case = Case(vocab=1024, hidden=16384, canvas_len=canvas_len, steps=3, seeds=(8,))
+    _assert_report(teacher_forced(case), f"d16384-L{canvas_len}")
+
+
+def test_idle_ticks_before_admission_single_cta_kernels():
+    """16 positions of two canvases admitted at ticks 2 and 3: the RMSNorm, single-CTA LM head and
+    finishing kernels run ticks with no active canvas (and then with one) before both run; the free
+    run must match the oracle's."""
+    case = Case(vocab=2048, hidden=128, canvas_len=16, n_canvases=2, steps=4, seeds=(6, 7), admit=(2, 3))
+    W = weights(case)
+    o = oracle.OracleSampler(case.oracle_cfg(), W)
+    o.run(oracle.sampler.synth_resid_fn(case.oracle_cfg(), W, case.sigma))
+    s, tok, info = _gpu_free_run(case, W)
+    assert np.array_equal(tok, o.tokens_out)
+    assert np.array_equal(s.commit_steps_out().cpu().numpy(), o.commit_steps_out)
+    assert np.array_equal(info["steps_used"], o.steps_used)
+
+
 def test_batch_and_admission_invariance_bitwise():
     """A canvas gives the same tokens and entropies alone or inside a staggered batch
     (TensorSharp doc, "7. Test coverage": batched decode equals per-sequence decode)."""
