@@ -265,6 +265,38 @@ def test_idle_ticks_before_admission_single_cta_kernels():
     assert np.array_equal(info["steps_used"], o.steps_used)
 
 
+def _random_cases(n, seed=2026):
+    """Small configurations drawn at random (fixed seed): every knob of the ABI varied together."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        B = int(rng.integers(1, 4))
+        L = int(rng.choice([1, 7, 16, 33, 100, 256, 300]))
+        t_max = float(rng.choice([0.5, 0.8, 1.5]))
+        out.append(Case(vocab=int(rng.choice([2, 37, 256, 1000, 2048, 4099])),
+                        hidden=int(rng.choice([8, 64, 120, 256, 520])),
+                        canvas_len=L, n_canvases=B, gen_blocks=int(rng.integers(1, 3)),
+                        steps=int(rng.integers(2, 6)), t_max=t_max, t_min=float(t_max * rng.choice([0.2, 0.5, 1.0])),
+                        bound=float(rng.choice([0.0, 0.1, 2.0, 50.0])), conf=float(rng.choice([0.0, 0.005, 0.5])),
+                        sigma=float(rng.choice([0.05, 0.5, 2.0])), sigma_w=float(rng.choice([0.02, 0.2])),
+                        w_seed=int(rng.integers(0, 100)), seeds=tuple(int(x) for x in rng.integers(0, 2**63, B)),
+                        admit=tuple(int(x) for x in rng.integers(0, 3, B)),
+                        max_active=int(rng.integers(0, B + 1)),
+                        mode=str(rng.choice(["freeze", "reaccept"])), softcap=float(rng.choice([0.0, 0.0, 3.0])),
+                        stability=int(rng.integers(1, 3))))
+    return out
+
+
+@pytest.mark.parametrize("case", _random_cases(16), ids=[f"random{i}" for i in range(16)])
+def test_randomized_configurations_teacher_forced(case):
+    """Sixteen small configurations with every knob drawn at random (vocabulary and hidden sizes
+    including ragged and minimal ones, canvas counts and lengths on both LM-head kernels, staggered
+    admission under a slot limit, both commit modes, softcap, stability, temperatures, budgets and
+    confidence thresholds including 0), each teacher-forced on every tick against the oracle."""
+    _assert_report(teacher_forced(case), f"V{case.vocab} d{case.hidden} L{case.canvas_len} B{case.n_canvases} "
+                   f"{case.mode} cap{case.softcap}")
+
+
 def test_batch_and_admission_invariance_bitwise():
     """A canvas gives the same tokens and entropies alone or inside a staggered batch
     (TensorSharp doc, "7. Test coverage": batched decode equals per-sequence decode)."""
