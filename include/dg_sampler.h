@@ -241,8 +241,8 @@ dg_status dg_self_condition(dg_sampler* s, float* out);
 
 /*
  * Top-K variant of the self-conditioning input (TensorSharp's DiffusionGemma
- * doc: an experimental cutoff of the self-conditioning input, K = 32 by
- * default).  For every position of the canvases active at the last tick,
+ * doc, "5. Acceleration status", its toggles: an experimental cutoff of the
+ * self-conditioning input, K = 32 by default).  For every position of the canvases active at the last tick,
  *   out[c, p, :] = sum over the K most probable tokens v of q[v] W[v, :],
  * q = softmax(z / T) of that tick restricted to those K tokens and
  * renormalised to sum 1, which keeps the input a convex combination of

@@ -196,10 +196,10 @@ def expected_embedding_topk(z: np.ndarray, T, W: np.ndarray, k: int):
     """Top-K self-conditioning input: e[p, :] = sum over the K most probable tokens v of row p of
     q[p, v] W[v, :], q = softmax(z / T) restricted to those K tokens and renormalised to sum 1.
 
-    TensorSharp's DiffusionGemma doc lists an experimental top-K cutoff of the self-conditioning
-    input (DIFFUSION_SC_TOPK, default 32) beside its on-device sampling; the Annotated page's decode
-    mode describes the input as one convex combination of embedding rows per position, which the
-    renormalisation keeps.  Ranking: larger z / T first, equal values by the lower token index (the
+    TensorSharp's DiffusionGemma doc ("5. Acceleration status", its toggles) lists an experimental
+    top-K cutoff of the self-conditioning input (DIFFUSION_SC_TOPK, default 32) beside its on-device
+    sampling; the Annotated page's decode mode describes the input as one convex combination of
+    embedding rows per position, which the renormalisation keeps.  Ranking: larger z / T first, equal values by the lower token index (the
     tie rule used everywhere else); k >= V keeps every token, giving ``expected_embedding``.  In
     fp64 from the bf16 values of W; ``z`` are the logits after the final softcap.
 

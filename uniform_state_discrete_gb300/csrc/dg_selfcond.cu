@@ -562,8 +562,9 @@ __global__ void __launch_bounds__(256) k_selfcond_reduce(const Dev dv, float* __
 // ------------------------------------------------------------- top-K variant
 // e[p, :] = sum over the K most probable tokens v of position p of q_v W[v, :],
 // q the tick's softmax restricted to those K tokens and renormalised.
-// TensorSharp's DiffusionGemma doc lists this cutoff of the self-conditioning
-// input (experimental, K = 32 by default); the renormalisation keeps the one
+// TensorSharp's DiffusionGemma doc ("5. Acceleration status", its toggles)
+// lists this cutoff of the self-conditioning input (experimental, K = 32 by
+// default); the renormalisation keeps the one
 // convex combination of embedding rows per position that the Annotated page's
 // decode mode describes.  Tokens rank by z / T, equal values by the lower
 // index.
